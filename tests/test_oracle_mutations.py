@@ -1,0 +1,54 @@
+"""The oracle's pins must fail on plausible mistakes planted in the oracle.
+
+Each case writes a copy of oracle.c with one planted mistake into a temporary
+directory, compiles it with gcc (CPU only) and runs the pin suite against it
+through the CF_ORACLE_LIB override; the suite must fail.  The committed
+oracle itself is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTATIONS = {
+    "eps_outside_sqrt": ("sqrt(sum_sq / (double)H + eps)", "(sqrt(sum_sq / (double)H) + eps)"),
+    "sum_not_mean": ("sum_sq / (double)H + eps", "sum_sq + eps"),
+    "drop_ln_weight": ("n[i] = (x[i] / rms) * g[i];", "n[i] = (x[i] / rms);"),
+    "rope_sign_first": ("u[i] = a * c - b * s;", "u[i] = a * c + b * s;"),
+    "rope_sign_second": ("u[i + half] = b * c + a * s;", "u[i + half] = b * c - a * s;"),
+    "rope_frequency": ("pow(theta, -2.0 * (double)i / (double)d)",
+                       "pow(theta, -1.0 * (double)i / (double)d)"),
+    "no_score_scale": ("const double scale = 1.0 / sqrt((double)d);\n  double* s =",
+                       "const double scale = 1.0;\n  double* s ="),
+    "gqa_modulo_grouping": ("const int j = h / group;", "const int j = h % nkv;"),
+    "drop_new_token": ("orc_attention(d, pos + 1,", "orc_attention(d, pos,"),
+    "drop_residual": ("out[i] = x[i] + proj[i];", "out[i] = proj[i];"),
+    "q_from_wrong_columns": ("double* q = y;", "double* q = y + (size_t)nkv * d;"),
+    "no_rope_on_q": ("for (int h = 0; h < nq; ++h) orc_rope(", "for (int h = 0; h < 0; ++h) orc_rope("),
+    "no_rope_on_k": ("for (int j = 0; j < nkv; ++j) orc_rope(", "for (int j = 0; j < 0; ++j) orc_rope("),
+    "split_without_rescale": ("double r = exp(mc[c] - m);", "double r = 1.0;"),
+    "transposed_weight": (
+        "const double* row = W + (size_t)i * (size_t)N;\n    for (int j = 0; j < N; ++j) y[j] += xi * row[j];",
+        "for (int j = 0; j < N; ++j) y[j] += xi * W[(size_t)j * (size_t)K + i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    src = open(SRC).read()
+    old, new = MUTATIONS[name]
+    assert old in src, f"mutation anchor for {name} no longer present"
+    cpath = tmp_path / f"{name}.c"
+    cpath.write_text(src.replace(old, new, 1))
+    so = tmp_path / f"{name}.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-I", os.path.dirname(SRC), "-fPIC",
+                           "-shared", str(cpath), "-o", str(so), "-lm"])
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=dict(os.environ, CF_ORACLE_LIB=str(so)),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"pins did not catch '{name}':\n{r.stdout[-2000:]}"

@@ -1,0 +1,334 @@
+"""Pins of the float64 oracle to facts fixed by the pages and by mathematics.
+
+Nothing here compares the oracle with a retyped copy of its own formula: each
+test uses a closed form, a hand-worked value, an invariant, a special case
+that reduces to a library routine (numpy), or brute force on a tiny input.
+Each is chosen so that a plausible slip in the oracle (eps outside the sqrt,
+a dropped ln_weight, a transposed weight, interleaved instead of rotate-half
+RoPE, a wrong frequency exponent or sign, a missing 1/sqrt(d), a wrong GQA
+grouping, an off-by-one in the attended positions, a wrong head order in the
+output projection, a dropped residual) fails at least one of them.
+
+Pages: [CF] "ClusterFusion框架深度解析" (devpress.csdn.net);
+[LNA] "大模型推理中的算子融合优化：LayerNorm + Attention" (asdsk.com).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- RMSNorm --
+def test_rmsnorm_constant_vector_closed_form():
+    # [LNA §三 stage 1]: x = c*1 gives n_i = g_i * c / sqrt(c^2 + eps).  A large
+    # eps separates "inside the sqrt" from "added to the rms".
+    H, c, eps = 8, -1.5, 0.25
+    g = RNG.normal(size=H)
+    n = oracle.rmsnorm(np.full(H, c), g, eps)
+    np.testing.assert_allclose(n, g * c / math.sqrt(c * c + eps), rtol=1e-14)
+
+
+def test_rmsnorm_hand_example():
+    # x = (3, 4): mean square = 12.5 (mean over H = 2, not the sum 25).
+    n = oracle.rmsnorm([3.0, 4.0], [1.0, 2.0], 0.0)
+    r = math.sqrt(12.5)
+    np.testing.assert_allclose(n, [3.0 / r, 8.0 / r], rtol=1e-15)
+
+
+def test_rmsnorm_scale_invariance():
+    x = RNG.normal(size=64)
+    g = RNG.normal(size=64)
+    np.testing.assert_allclose(oracle.rmsnorm(7.0 * x, g, 0.0),
+                               oracle.rmsnorm(x, g, 0.0), rtol=1e-13)
+
+
+# ----------------------------------------------------------------- matvec --
+def test_matvec_matches_numpy_on_nonsquare():
+    # x . W with W [K, N] row-major; K != N so a transposed read cannot pass.
+    x = RNG.normal(size=7)
+    W = RNG.normal(size=(7, 5))
+    np.testing.assert_allclose(oracle.matvec(x, W), x @ W, rtol=1e-13, atol=1e-14)
+
+
+def test_matvec_brute_force_integers():
+    x = np.arange(1, 4, dtype=np.float64)             # [1,2,3]
+    W = np.arange(6, dtype=np.float64).reshape(3, 2)  # [[0,1],[2,3],[4,5]]
+    # y_0 = 1*0 + 2*2 + 3*4 = 16; y_1 = 1*1 + 2*3 + 3*5 = 22.
+    np.testing.assert_array_equal(oracle.matvec(x, W), [16.0, 22.0])
+
+
+# ------------------------------------------------------------------- RoPE --
+def test_rope_position_zero_is_identity():
+    u = RNG.normal(size=128)
+    np.testing.assert_array_equal(oracle.rope(u, 0, 1e4), u)
+
+
+def test_rope_d2_direction():
+    # d = 2: one pair (0, 1), frequency theta^0 = 1, angle = pos.
+    np.testing.assert_allclose(oracle.rope([1.0, 0.0], 1, 1e4),
+                               [math.cos(1.0), math.sin(1.0)], rtol=1e-15)
+    np.testing.assert_allclose(oracle.rope([0.0, 1.0], 1, 1e4),
+                               [-math.sin(1.0), math.cos(1.0)], rtol=1e-15)
+
+
+def test_rope_rotate_half_pairing_and_frequency():
+    # d = 4: pairs (0,2) and (1,3); pair 1 turns at theta^(-2/4) = 0.01 rad per
+    # position, so pos = 100 turns it by exactly 1 rad.  Interleaved pairing
+    # would move e_1 into index 0; theta^(-i/d) would turn it by 10 rad.
+    u = oracle.rope([0.0, 1.0, 0.0, 0.0], 100, 1e4)
+    np.testing.assert_allclose(u, [0.0, math.cos(1.0), 0.0, math.sin(1.0)],
+                               atol=1e-13)
+    u = oracle.rope([1.0, 0.0, 0.0, 0.0], 100, 1e4)
+    np.testing.assert_allclose(u, [math.cos(100.0), 0.0, math.sin(100.0), 0.0],
+                               atol=1e-13)
+
+
+def test_rope_preserves_pair_norms():
+    d = 64
+    u = RNG.normal(size=d)
+    r = oracle.rope(u, 777, 5e5)
+    h = d // 2
+    np.testing.assert_allclose(r[:h] ** 2 + r[h:] ** 2, u[:h] ** 2 + u[h:] ** 2,
+                               rtol=1e-12)
+
+
+def test_rope_relative_position_property():
+    d = 128
+    q, k = RNG.normal(size=d), RNG.normal(size=d)
+    a = oracle.rope(q, 300, 1e4) @ oracle.rope(k, 120, 1e4)
+    b = oracle.rope(q, 1300, 1e4) @ oracle.rope(k, 1120, 1e4)
+    assert abs(a - b) < 1e-10 * max(1.0, abs(a))
+
+
+# -------------------------------------------------------------- attention --
+def test_attention_single_token_returns_its_value():
+    d = 64
+    q, k, v = RNG.normal(size=d), RNG.normal(size=(1, d)), RNG.normal(size=(1, d))
+    o, w = oracle.attention(q, k, v)
+    np.testing.assert_allclose(o, v[0], rtol=1e-15)
+    np.testing.assert_array_equal(w, [1.0])
+
+
+def test_attention_identical_keys_average_values():
+    d, n = 32, 17
+    key = RNG.normal(size=d)
+    K = np.tile(key, (n, 1))
+    V = RNG.normal(size=(n, d))
+    o, w = oracle.attention(RNG.normal(size=d), K, V)
+    np.testing.assert_allclose(w, np.full(n, 1.0 / n), rtol=1e-14)
+    np.testing.assert_allclose(o, V.mean(axis=0), rtol=1e-12, atol=1e-14)
+
+
+def test_attention_two_key_hand_example_fixes_scale():
+    # d = 4, q = (1,1,1,1), k_0 = 0, k_1 = (1,1,1,1): s_0 = 0, s_1 = 4/sqrt(4) = 2.
+    # v_0 = 0, v_1 = 1 -> o = e^2 / (1 + e^2) in every coordinate.
+    q = np.ones(4)
+    K = np.array([np.zeros(4), np.ones(4)])
+    V = np.array([np.zeros(4), np.ones(4)])
+    o, w = oracle.attention(q, K, V)
+    w1 = math.exp(2.0) / (1.0 + math.exp(2.0))
+    np.testing.assert_allclose(w, [1.0 - w1, w1], rtol=1e-15)
+    np.testing.assert_allclose(o, np.full(4, w1), rtol=1e-15)
+
+
+def test_attention_weights_sum_to_one_and_follow_score_order():
+    d, n = 64, 200
+    q = RNG.normal(size=d)
+    K = RNG.normal(size=(n, d))
+    o, w = oracle.attention(q, K, RNG.normal(size=(n, d)))
+    assert abs(w.sum() - 1.0) < 1e-13
+    assert np.all(w > 0)
+    np.testing.assert_array_equal(np.argsort(w, kind="stable"),
+                                  np.argsort(K @ q, kind="stable"))
+
+
+@pytest.mark.parametrize("ends", [
+    [5, 200], [1, 2, 3, 200], [0, 0, 100, 100, 200], [64, 128, 192, 200],
+    list(range(1, 201))])
+def test_split_kv_equals_two_pass(ends):
+    d, n = 64, 200
+    q = RNG.normal(size=d) * 3.0
+    K = RNG.normal(size=(n, d))
+    V = RNG.normal(size=(n, d))
+    o, _ = oracle.attention(q, K, V)
+    np.testing.assert_allclose(oracle.attention_split(q, K, V, ends), o,
+                               rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------- whole decode block --
+def _tiny(nq=4, nkv=4, d=16, H=48, S=9, theta=1e4, eps=1e-6):
+    return dict(hidden=H, n_q_heads=nq, n_kv_heads=nkv, head_dim=d, s_max=S,
+                rope_theta=theta, rms_eps=eps)
+
+
+def _draw(cfg, rng):
+    H, nq, nkv, d, S = (cfg[k] for k in ("hidden", "n_q_heads", "n_kv_heads",
+                                         "head_dim", "s_max"))
+    C = (nq + 2 * nkv) * d
+    return dict(x=rng.normal(size=H), g=1 + 0.1 * rng.normal(size=H),
+                wqkv=0.2 * rng.normal(size=(H, C)), wo=0.2 * rng.normal(size=(nq * d, H)),
+                kc=rng.normal(size=(S, nkv, d)), vc=rng.normal(size=(S, nkv, d)))
+
+
+def test_decode_zero_output_projection_returns_residual_exactly():
+    cfg = _tiny()
+    t = _draw(cfg, np.random.default_rng(0))
+    t["wo"][:] = 0.0
+    r = oracle.decode_row(cfg, t["x"], t["g"], t["wqkv"], t["wo"], t["kc"], t["vc"], 5)
+    np.testing.assert_array_equal(r["out"], t["x"])
+
+
+@pytest.mark.parametrize("nq,nkv", [(4, 4), (4, 2), (6, 2)])
+def test_decode_zero_query_gives_uniform_attention(nq, nkv):
+    # W_q = 0 makes every score 0, so o_h is the plain mean of the values at
+    # positions 0..pos (the appended token included) of KV head h // (nq/nkv).
+    # Expected values are built from numpy matmuls and means only.
+    cfg = _tiny(nq=nq, nkv=nkv)
+    H, d, pos = cfg["hidden"], cfg["head_dim"], 6
+    t = _draw(cfg, np.random.default_rng(1))
+    t["wqkv"][:, : nq * d] = 0.0
+    kc0, vc0 = t["kc"].copy(), t["vc"].copy()
+    r = oracle.decode_row(cfg, t["x"], t["g"], t["wqkv"], t["wo"], t["kc"], t["vc"], pos)
+    n = oracle.rmsnorm(t["x"], t["g"], cfg["rms_eps"])
+    y = n @ t["wqkv"]
+    v_new = y[(nq + nkv) * d:].reshape(nkv, d)
+    k_new = y[nq * d:(nq + nkv) * d].reshape(nkv, d)
+    vals = vc0.copy()
+    vals[pos] = v_new
+    group = nq // nkv
+    o_exp = np.concatenate([vals[: pos + 1, h // group].mean(axis=0) for h in range(nq)])
+    np.testing.assert_allclose(r["o"], o_exp, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["proj"], o_exp @ t["wo"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(r["out"], t["x"] + o_exp @ t["wo"], rtol=1e-11, atol=1e-12)
+    # Only slot pos changed; it holds v_new and RoPE(k_new, pos).
+    changed = np.any(t["kc"] != kc0, axis=(1, 2)) | np.any(t["vc"] != vc0, axis=(1, 2))
+    assert changed.tolist() == [s == pos for s in range(cfg["s_max"])]
+    np.testing.assert_allclose(t["vc"][pos], v_new, rtol=1e-13)
+    k_rot = np.stack([oracle.rope(k_new[j], pos, cfg["rope_theta"]) for j in range(nkv)])
+    np.testing.assert_allclose(t["kc"][pos], k_rot, rtol=1e-12, atol=1e-13)
+
+
+def test_decode_position_zero_attends_to_new_token_only():
+    cfg = _tiny(nq=4, nkv=2)
+    t = _draw(cfg, np.random.default_rng(2))
+    r = oracle.decode_row(cfg, t["x"], t["g"], t["wqkv"], t["wo"], t["kc"], t["vc"], 0)
+    n = oracle.rmsnorm(t["x"], t["g"], cfg["rms_eps"])
+    y = n @ t["wqkv"]
+    nq, nkv, d = 4, 2, cfg["head_dim"]
+    v_new = y[(nq + nkv) * d:].reshape(nkv, d)
+    np.testing.assert_allclose(r["o"].reshape(nq, d), v_new[[0, 0, 1, 1]], rtol=1e-12)
+    # RoPE at position 0 is the identity, so the cached key is the raw projection.
+    np.testing.assert_allclose(t["kc"][0], y[nq * d:(nq + nkv) * d].reshape(nkv, d),
+                               rtol=1e-12)
+
+
+def test_decode_query_heads_rotated_by_position():
+    cfg = _tiny(nq=2, nkv=1, d=8, H=32, S=40)
+    t = _draw(cfg, np.random.default_rng(3))
+    pos = 33
+    r = oracle.decode_row(cfg, t["x"], t["g"], t["wqkv"], t["wo"], t["kc"], t["vc"], pos)
+    y = oracle.rmsnorm(t["x"], t["g"], cfg["rms_eps"]) @ t["wqkv"]
+    q = y[: 2 * 8].reshape(2, 8)
+    for h in range(2):
+        np.testing.assert_allclose(r["q"][h * 8:(h + 1) * 8],
+                                   oracle.rope(q[h], pos, cfg["rope_theta"]), rtol=1e-12)
+
+
+def test_gqa_equals_mha_with_repeat_interleaved_kv_heads():
+    # Consecutive grouping [LNA §三]: query head h reads KV head h // (nq/nkv).
+    nq, nkv, d, H, S = 6, 2, 8, 32, 12
+    cfg_g = _tiny(nq=nq, nkv=nkv, d=d, H=H, S=S)
+    cfg_m = _tiny(nq=nq, nkv=nq, d=d, H=H, S=S)
+    t = _draw(cfg_g, np.random.default_rng(4))
+    grp = nq // nkv
+    wq = t["wqkv"][:, : nq * d]
+    wk = t["wqkv"][:, nq * d:(nq + nkv) * d].reshape(H, nkv, d)
+    wv = t["wqkv"][:, (nq + nkv) * d:].reshape(H, nkv, d)
+    wqkv_m = np.concatenate([wq, np.repeat(wk, grp, axis=1).reshape(H, nq * d),
+                             np.repeat(wv, grp, axis=1).reshape(H, nq * d)], axis=1)
+    kc_m = np.ascontiguousarray(np.repeat(t["kc"], grp, axis=1))
+    vc_m = np.ascontiguousarray(np.repeat(t["vc"], grp, axis=1))
+    rg = oracle.decode_row(cfg_g, t["x"], t["g"], t["wqkv"], t["wo"], t["kc"], t["vc"], 7)
+    rm = oracle.decode_row(cfg_m, t["x"], t["g"], wqkv_m, t["wo"], kc_m, vc_m, 7)
+    np.testing.assert_allclose(rg["out"], rm["out"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(rg["o"], rm["o"], rtol=1e-13, atol=1e-14)
+
+
+def test_decode_matches_brute_force_triple_loop_on_tiny_shape():
+    # Brute force: every sum written as an explicit Python loop (tiny sizes).
+    cfg = _tiny(nq=2, nkv=1, d=4, H=6, S=4, theta=10.0, eps=1e-3)
+    t = _draw(cfg, np.random.default_rng(5))
+    pos = 2
+    x, g, W, Wo = t["x"], t["g"], t["wqkv"], t["wo"]
+    kc, vc = t["kc"].copy(), t["vc"].copy()
+    r = oracle.decode_row(cfg, x, g, W, Wo, t["kc"], t["vc"], pos)
+    H, d = 6, 4
+    ms = sum(x[i] * x[i] for i in range(H)) / H
+    n = [x[i] / math.sqrt(ms + 1e-3) * g[i] for i in range(H)]
+    y = [sum(n[i] * W[i][j] for i in range(H)) for j in range(W.shape[1])]
+
+    def rot(u):
+        out = list(u)
+        for i in range(d // 2):
+            ang = pos * 10.0 ** (-2.0 * i / d)
+            out[i] = u[i] * math.cos(ang) - u[i + d // 2] * math.sin(ang)
+            out[i + d // 2] = u[i + d // 2] * math.cos(ang) + u[i] * math.sin(ang)
+        return out
+
+    qs = [rot(y[0:4]), rot(y[4:8])]
+    k_new, v_new = rot(y[8:12]), y[12:16]
+    keys = [list(kc[t_, 0]) for t_ in range(pos)] + [k_new]
+    vals = [list(vc[t_, 0]) for t_ in range(pos)] + [v_new]
+    o = []
+    for qh in qs:
+        s = [sum(qh[i] * kk[i] for i in range(d)) / math.sqrt(d) for kk in keys]
+        e = [math.exp(si) for si in s]
+        z = sum(e)
+        o += [sum(e[t_] / z * vals[t_][i] for t_ in range(pos + 1)) for i in range(d)]
+    out = [x[j] + sum(o[k] * Wo[k][j] for k in range(2 * d)) for j in range(H)]
+    np.testing.assert_allclose(r["o"], o, rtol=1e-12)
+    np.testing.assert_allclose(r["out"], out, rtol=1e-12)
+
+
+def test_decode_rejects_position_outside_cache():
+    cfg = _tiny()
+    t = _draw(cfg, np.random.default_rng(6))
+    for bad in (-1, cfg["s_max"]):
+        with pytest.raises(ValueError):
+            oracle.decode_row(cfg, t["x"], t["g"], t["wqkv"], t["wo"], t["kc"], t["vc"], bad)
+
+
+def test_decode_batch_rows_are_independent():
+    cfg = _tiny(S=20)
+    rng = np.random.default_rng(7)
+    B = 3
+    X = rng.normal(size=(B, cfg["hidden"]))
+    t = _draw(cfg, rng)
+    KC = rng.normal(size=(B, 20, 4, 16))
+    VC = rng.normal(size=(B, 20, 4, 16))
+    pos = [3, 19, 0]
+    full = oracle.decode(cfg, X, t["g"], t["wqkv"], t["wo"], KC.copy(), VC.copy(), pos)
+    perm = [2, 0, 1]
+    permd = oracle.decode(cfg, X[perm], t["g"], t["wqkv"], t["wo"], KC[perm].copy(),
+                          VC[perm].copy(), [pos[i] for i in perm])
+    np.testing.assert_array_equal(permd["out"], full["out"][perm])
+
+
+def test_oracle_regression_fixture():
+    # Guards against accidental edits of the oracle (fixture written by
+    # tests/golden/gen_oracle_regression.py, which calls only oracle/).
+    import os
+    import sys
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    import gen_oracle_regression as gen
+    r = gen.compute()
+    with open(os.path.join(here, "tiny_oracle_regression.txt")) as fh:
+        rows = [ln.split() for ln in fh if not ln.startswith("#")]
+    stored = {row[0]: np.array([float(v) for v in row[1:]]) for row in rows}
+    np.testing.assert_allclose(r["out"][0], stored["out"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["o"][0], stored["o"], rtol=1e-12, atol=1e-13)
