@@ -1,0 +1,240 @@
+"""ctypes binding of libcf.so (include/cf.h, include/cf_test.h).
+
+Argument marshalling only: every step of the decode block runs in the CUDA
+library.  There is no fallback of any kind -- if the library is missing or
+was not built, ``lib()`` raises.  Tensors may be passed as torch tensors
+(their ``data_ptr()`` is used) or as raw integer addresses.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+CF_OK = 0
+CF_ERR_INVALID_ARG = -1
+CF_ERR_UNSUPPORTED = -2
+CF_ERR_ALIAS = -3
+CF_ERR_CLUSTER = -4
+CF_ERR_CUDA = -5
+CF_ERR_DEVICE_POS_RANGE = -6
+CF_ERR_DEVICE_TIMEOUT = -7
+
+CF_F32, CF_F16, CF_BF16 = 0, 1, 2
+
+
+class CfConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "hidden", "n_q_heads", "n_kv_heads", "head_dim", "max_batch", "s_max")] + [
+        ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)] + [
+        (n, ctypes.c_int32) for n in (
+            "dtype", "cluster_size", "batch_tile", "stage_bytes", "ctas_per_sm")]
+
+
+class CfLaunchInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "cluster_size", "batch_tile", "group", "rows_per_wtile", "pos_per_ktile",
+        "wo_rows_per_tile", "wo_cols_per_tile", "stages", "stage_bytes", "smem_bytes",
+        "threads", "max_active_clusters", "sm_count")]
+
+
+class CfError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})" if what else
+                         f"{strerror(code)} ({code})")
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+
+# Exported symbols, with (restype, argtypes).
+SIGNATURES = {
+    "cf_create": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.POINTER(_vp)]),
+    "cf_decode_attn_block": (ctypes.c_int, [_vp, ctypes.c_int32] + [_vp] * 9),
+    "cf_get_status": (ctypes.c_int, [_vp]),
+    "cf_set_debug": (ctypes.c_int, [_vp, _vp]),
+    "cf_get_launch_info": (ctypes.c_int, [_vp, ctypes.POINTER(CfLaunchInfo)]),
+    "cf_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "cf_destroy": (None, [_vp]),
+    "cf_test_cluster_allreduce": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 _vp, _vp, _vp, _vp]),
+    "cf_test_cluster_reduce_scatter": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                                      _vp, _vp]),
+    "cf_test_cluster_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp]),
+    "cf_bench_cluster_collective": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   _vp, _vp, _vp, _vp, _vp]),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = True):
+    """Load libcf.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing and _build.is_stale():
+                _build.build()
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library {path} is missing; run "
+                                   "attention_block_gb300.build.build() (needs nvcc)")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().cf_strerror(int(code)).decode()
+    except Exception:  # message lookup must never mask the original error
+        return f"error {code}"
+
+
+def make_config(hidden, n_q_heads, n_kv_heads, head_dim, max_batch, s_max, rope_theta=1e4,
+                rms_eps=1e-6, dtype=CF_F16, cluster_size=0, batch_tile=0, stage_bytes=0,
+                ctas_per_sm=0) -> CfConfig:
+    if isinstance(dtype, str):
+        dtype = {"f32": CF_F32, "f16": CF_F16, "bf16": CF_BF16}[dtype]
+    return CfConfig(int(hidden), int(n_q_heads), int(n_kv_heads), int(head_dim),
+                    int(max_batch), int(s_max), float(rope_theta), float(rms_eps), int(dtype),
+                    int(cluster_size), int(batch_tile), int(stage_bytes), int(ctas_per_sm))
+
+
+def cf_create(cfg: CfConfig) -> int:
+    h = _vp()
+    rc = lib().cf_create(ctypes.byref(cfg), ctypes.byref(h))
+    if rc != CF_OK:
+        raise CfError(rc, "cf_create")
+    return h.value
+
+
+def cf_create_rc(cfg: CfConfig | None) -> tuple[int, int | None]:
+    """Return code and handle without raising (boundary tests)."""
+    h = _vp()
+    rc = lib().cf_create(ctypes.byref(cfg) if cfg is not None else None, ctypes.byref(h))
+    return rc, h.value
+
+
+def cf_decode_attn_block(handle, batch, hidden_states, ln_weight, w_qkv, w_o, k_cache, v_cache,
+                         positions, out, stream=None) -> int:
+    return lib().cf_decode_attn_block(handle, int(batch), _ptr(hidden_states), _ptr(ln_weight),
+                                      _ptr(w_qkv), _ptr(w_o), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(positions), _ptr(out), _stream(stream))
+
+
+def cf_get_status(handle) -> int:
+    return lib().cf_get_status(handle)
+
+
+def cf_set_debug(handle, dbg) -> int:
+    return lib().cf_set_debug(handle, _ptr(dbg))
+
+
+def cf_get_launch_info(handle) -> dict:
+    info = CfLaunchInfo()
+    rc = lib().cf_get_launch_info(handle, ctypes.byref(info))
+    if rc != CF_OK:
+        raise CfError(rc, "cf_get_launch_info")
+    return {n: getattr(info, n) for n, _ in CfLaunchInfo._fields_}
+
+
+def cf_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def cf_destroy(handle) -> None:
+    lib().cf_destroy(handle)
+
+
+def cf_test_cluster_allreduce(cluster_size, op, n, inp, out, errflag, stream=None) -> int:
+    return lib().cf_test_cluster_allreduce(int(cluster_size), int(op), int(n), _ptr(inp),
+                                           _ptr(out), _ptr(errflag), _stream(stream))
+
+
+def cf_test_cluster_reduce_scatter(cluster_size, n, inp, out, errflag, stream=None) -> int:
+    return lib().cf_test_cluster_reduce_scatter(int(cluster_size), int(n), _ptr(inp), _ptr(out),
+                                                _ptr(errflag), _stream(stream))
+
+
+def cf_test_cluster_gather(cluster_size, n, inp, out, errflag, stream=None) -> int:
+    return lib().cf_test_cluster_gather(int(cluster_size), int(n), _ptr(inp), _ptr(out),
+                                        _ptr(errflag), _stream(stream))
+
+
+def cf_bench_cluster_collective(kind, cluster_size, n, inp, out, errflag, cycles,
+                                stream=None) -> int:
+    return lib().cf_bench_cluster_collective(int(kind), int(cluster_size), int(n), _ptr(inp),
+                                             _ptr(out), _ptr(errflag), _ptr(cycles),
+                                             _stream(stream))
+
+
+class DecodeAttnBlock:
+    """Owns one cf_handle; calling it enqueues one fused decode step.
+
+    Raises CfError on any non-zero return code.  ``status()`` synchronizes
+    the current device and reads (and clears) the device error flag.
+    """
+
+    def __init__(self, **cfg):
+        self.cfg = make_config(**cfg)
+        self.handle = cf_create(self.cfg)
+
+    def __call__(self, batch, hidden_states, ln_weight, w_qkv, w_o, k_cache, v_cache, positions,
+                 out, stream=None):
+        rc = cf_decode_attn_block(self.handle, batch, hidden_states, ln_weight, w_qkv, w_o,
+                                  k_cache, v_cache, positions, out, stream)
+        if rc != CF_OK:
+            raise CfError(rc, "cf_decode_attn_block")
+        return out
+
+    def launch_info(self) -> dict:
+        return cf_get_launch_info(self.handle)
+
+    def set_debug(self, dbg) -> None:
+        rc = cf_set_debug(self.handle, dbg)
+        if rc != CF_OK:
+            raise CfError(rc, "cf_set_debug")
+
+    def status(self) -> int:
+        import torch
+        torch.cuda.synchronize()
+        return cf_get_status(self.handle)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            cf_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,534 @@
+// cf_api.cu -- host side of the C ABI declared in include/cf.h: argument
+// validation, kernel-instance choice, shared-memory planning, TMA tensor-map
+// encoding (cached per pointer), the handle's device workspace and the
+// cluster launch.  No allocation, synchronization or host copy happens on the
+// cf_decode_attn_block path, so it can be captured in a CUDA graph.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "cf.h"
+#include "cf_params.h"
+#include "cf_registry.h"
+
+using namespace cf;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+int esize(int dt) { return dt == CF_F32 ? 4 : 2; }
+
+CUtensorMapDataType tm_type(int dt) {
+  return dt == CF_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                      : (dt == CF_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+int pow2_floor(int v) {
+  int p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+// Largest power of two <= cap that divides v (v > 0).
+int pow2_divisor(int v, int cap) {
+  int p = 1;
+  while (p * 2 <= cap && v % (p * 2) == 0) p *= 2;
+  return p;
+}
+int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+const KernelEntry* find_entry(int dtype, int D, int G, int BT) {
+  const KernelEntry* e = nullptr;
+  int n = dtype == CF_F32 ? registry_f32(&e) : (dtype == CF_F16 ? registry_f16(&e) : registry_bf16(&e));
+  for (int i = 0; i < n; ++i)
+    if (e[i].D == D && e[i].G == G && e[i].BT == BT) return &e[i];
+  return nullptr;
+}
+
+// Largest compiled batch tile <= want for (dtype, D, G); 0 if none.
+int best_batch_tile(int dtype, int D, int G, int want) {
+  const KernelEntry* e = nullptr;
+  int n = dtype == CF_F32 ? registry_f32(&e) : (dtype == CF_F16 ? registry_f16(&e) : registry_bf16(&e));
+  int best = 0;
+  for (int i = 0; i < n; ++i)
+    if (e[i].D == D && e[i].G == G && e[i].BT <= want && e[i].BT > best) best = e[i].BT;
+  return best;
+}
+
+// Small per-handle cache of encoded tensor maps keyed by (pointer, extent).
+struct MapCache {
+  static constexpr int kSlots = 64;
+  const void* ptr[kSlots] = {};
+  int extent[kSlots] = {};
+  CUtensorMap map[kSlots];
+  int next = 0;
+  const CUtensorMap* find(const void* p, int e) const {
+    for (int i = 0; i < kSlots; ++i)
+      if (ptr[i] == p && extent[i] == e && p != nullptr) return &map[i];
+    return nullptr;
+  }
+  CUtensorMap* insert(const void* p, int e) {
+    const int i = next;
+    next = (next + 1) % kSlots;
+    ptr[i] = p;
+    extent[i] = e;
+    return &map[i];
+  }
+};
+
+struct Plan {
+  int N, BT, G, Rw, Rt, Ro, Co, stages, stage_bytes, ctas_per_sm;
+  SmemLayout L;
+};
+
+// Shared-memory plan for one (config, N, BT, stage size, CTAs/SM).  Returns
+// false when not even two ring stages fit.
+bool make_plan(const cf_config& c, int N, int BT, int stage_req, int ctas_per_sm,
+               const cudaDeviceProp& prop, Plan& pl) {
+  const int es = esize(c.dtype), D = c.head_dim, H = c.hidden;
+  const int G = c.n_q_heads / c.n_kv_heads, NSEG = G + 2;
+  const int P = D / (2 * N), SE = BT * NSEG * 2 * P;
+  const int Hc = H / N;
+  const int nrounds = __builtin_ctz((unsigned)N);
+  pl.N = N;
+  pl.BT = BT;
+  pl.G = G;
+  pl.Co = pow2_divisor(Hc, 256);
+  pl.Rw = pow2_divisor(Hc, std::min(256, std::max(1, stage_req / (NSEG * D * es))));
+  pl.Rt = std::min(256, pow2_floor(std::max(1, stage_req / (2 * D * es))));
+  pl.Ro = pow2_divisor(G * D, std::min(256, std::max(1, stage_req / (pl.Co * es))));
+  const int item = std::max(NSEG * pl.Rw * D * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
+  pl.stage_bytes = round_up(item, 1024);
+
+  const int MXP = (BT * G + 3) & ~3;
+  const int SMP = BT * G * (D + 4);
+  int off = 0;
+  SmemLayout& L = pl.L;
+  auto take = [&](int bytes) {
+    const int o = off;
+    off += round_up(bytes, 128);
+    return o;
+  };
+  L.bars = take(BarIdx::count * 8);
+  L.xn = take(BT * Hc * 4);
+  L.red = take(N * SE * 4);
+  L.scratch = take(std::max(std::max((N - 1) * SE, kConsumerWarps * G * (D + 4)), BT * pl.Co) * 4);
+  L.qkv = take(BT * NSEG * D * 4);
+  L.mx = take(MXP * 4 * (1 + nrounds));
+  L.sm = take(SMP * 4 * (1 + nrounds));
+  L.mloc = take(MXP * 4);
+  L.rope = take(BT * P * 2 * 4);
+  L.misc = take((BT + 4 + BT + kConsumerWarps * BT) * 4);
+  const int extras = round_up(off, 1024);
+
+  const int per_sm = (int)prop.sharedMemPerMultiprocessor;
+  const int per_block_max = (int)prop.sharedMemPerBlockOptin;
+  int budget = std::min(per_block_max, per_sm / ctas_per_sm - (int)prop.reservedSharedMemPerBlock);
+  budget -= 1024;  // alignment slack of the dynamic base
+  int stages = (budget - extras) / pl.stage_bytes;
+  stages = std::min(stages, kMaxStages);
+  if (stages < 2) return false;
+  pl.stages = stages;
+  pl.ctas_per_sm = ctas_per_sm;
+  // ring first, then the other regions (all offsets from the 1024-aligned base)
+  const int ring = stages * pl.stage_bytes;
+  L.ring = 0;
+  L.bars += ring;
+  L.xn += ring;
+  L.red += ring;
+  L.scratch += ring;
+  L.qkv += ring;
+  L.mx += ring;
+  L.sm += ring;
+  L.mloc += ring;
+  L.rope += ring;
+  L.misc += ring;
+  L.total = ring + extras + 1024;
+  return true;
+}
+
+}  // namespace
+
+struct cf_handle {
+  cf_config cfg;
+  int device = 0, sm_count = 0;
+  Plan plan;
+  const void* fn = nullptr;
+  int max_active_clusters = 0;
+  void* ws = nullptr;       // one allocation: acc | counters | errflag
+  float* acc = nullptr;
+  int* counters = nullptr;
+  int* errflag = nullptr;
+  float* dbg = nullptr;
+  double inv_freq[64];
+  MapCache m_wqkv, m_wo, m_k, m_v;
+};
+
+namespace {
+
+int validate_config(const cf_config* c) {
+  if (c == nullptr) return CF_ERR_INVALID_ARG;
+  if (c->hidden <= 0 || c->hidden % 64 != 0) return CF_ERR_INVALID_ARG;
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads != 0)
+    return CF_ERR_INVALID_ARG;
+  if (c->head_dim <= 0 || c->head_dim % 2 != 0) return CF_ERR_INVALID_ARG;
+  if (c->max_batch <= 0 || c->s_max <= 0) return CF_ERR_INVALID_ARG;
+  if (c->dtype < CF_F32 || c->dtype > CF_BF16) return CF_ERR_INVALID_ARG;
+  if (!(c->rope_theta > 0.f) || !std::isfinite(c->rope_theta)) return CF_ERR_INVALID_ARG;
+  if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps)) return CF_ERR_INVALID_ARG;
+  const int N = c->cluster_size;
+  if (N != 0 && !(N == 1 || N == 2 || N == 4 || N == 8 || N == 16)) return CF_ERR_INVALID_ARG;
+  if (c->batch_tile < 0 || c->stage_bytes < 0) return CF_ERR_INVALID_ARG;
+  if (c->stage_bytes != 0 && (c->stage_bytes < 2048 || c->stage_bytes > 131072))
+    return CF_ERR_INVALID_ARG;
+  if (c->ctas_per_sm < 0 || c->ctas_per_sm > 2) return CF_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return CF_ERR_UNSUPPORTED;
+  if (N != 0 && N > c->head_dim / 4) return CF_ERR_INVALID_ARG;
+  if (N != 0 && ((c->hidden / N) * esize(c->dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
+  // The 4D KV map's extents must fit its index range.
+  if ((long long)c->s_max * c->n_kv_heads * c->head_dim > (1LL << 40)) return CF_ERR_INVALID_ARG;
+  return CF_OK;
+}
+
+bool encode(CUtensorMap* m, int dtype, int rank, const void* base, const uint64_t* dims,
+            const uint64_t* strides_bytes, const uint32_t* box) {
+  uint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, tm_type(dtype), (cuuint32_t)rank, const_cast<void*>(base),
+                        (const cuuint64_t*)dims, (const cuuint64_t*)strides_bytes,
+                        (const cuuint32_t*)box, (const cuuint32_t*)estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cf_strerror(int code) {
+  switch (code) {
+    case CF_OK: return "ok";
+    case CF_ERR_INVALID_ARG: return "invalid argument";
+    case CF_ERR_UNSUPPORTED: return "unsupported configuration (no kernel built for it)";
+    case CF_ERR_ALIAS: return "output overlaps an input";
+    case CF_ERR_CLUSTER: return "thread-block cluster shape cannot be resident on this device";
+    case CF_ERR_CUDA: return "CUDA runtime or driver error";
+    case CF_ERR_DEVICE_POS_RANGE: return "a positions[] value was outside [0, s_max)";
+    case CF_ERR_DEVICE_TIMEOUT: return "an in-kernel wait timed out";
+    default: return "unknown error code";
+  }
+}
+
+int cf_create(const cf_config* cfg, cf_handle** out) {
+  if (out == nullptr) return CF_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc != CF_OK) return rc;
+  const cf_config c = *cfg;
+  const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
+
+  // Batch tile: requested, else the largest compiled one <= max_batch.
+  int BT = c.batch_tile;
+  if (BT == 0) {
+    BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 4));
+    if (G > 1) BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 2));
+  }
+  if (BT <= 0) return CF_ERR_UNSUPPORTED;
+  const KernelEntry* ke = find_entry(c.dtype, D, G, BT);
+  if (ke == nullptr) return CF_ERR_UNSUPPORTED;
+  if (!get_encode()) return CF_ERR_CUDA;
+
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CF_ERR_CUDA;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return CF_ERR_CUDA;
+
+  // Cluster size: requested, else the smallest power of two >= 2 that gives
+  // about two blocks per SM over the whole grid (capped by head_dim/4 and by
+  // the hidden size's 16-byte column bands).
+  const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
+  int N = c.cluster_size;
+  if (N == 0) {
+    N = 2;
+    while (N < 16 && N * 2 <= D / 4 && ((c.hidden / (N * 2)) * esize(c.dtype)) % 16 == 0 &&
+           (long long)clusters * N * 2 <= 2LL * prop.multiProcessorCount)
+      N *= 2;
+  }
+  if (N > D / 4 || ((c.hidden / N) * esize(c.dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
+
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
+  int cps = c.ctas_per_sm;
+  if (cps == 0) {
+    const bool regs_ok = fa.numRegs * kThreads * 2 <= prop.regsPerMultiprocessor;
+    cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
+  }
+  const int stage_req = c.stage_bytes ? c.stage_bytes : 32768;
+  Plan pl;
+  if (!make_plan(c, N, BT, stage_req, cps, prop, pl)) {
+    if (cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)) {
+      // fall back to one block per SM
+    } else {
+      return CF_ERR_UNSUPPORTED;
+    }
+  }
+
+  // The attribute is per function: only ever raise it, so a later handle with
+  // a smaller plan cannot break an earlier handle's launches.
+  {
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    cudaFuncAttributes cur;
+    if (cudaFuncGetAttributes(&cur, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
+    if (cur.maxDynamicSharedSizeBytes < pl.L.total &&
+        cudaFuncSetAttribute(ke->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.L.total) !=
+            cudaSuccess)
+      return CF_ERR_CUDA;
+  }
+  if (N > 8 && cudaFuncSetAttribute(ke->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                   cudaSuccess)
+    return CF_ERR_CLUSTER;
+
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = N;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3(N * clusters, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = pl.L.total;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, ke->fn, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CLUSTER;
+  }
+  if (nclusters <= 0) return CF_ERR_CLUSTER;
+
+  cf_handle* h = new (std::nothrow) cf_handle();
+  if (h == nullptr) return CF_ERR_CUDA;
+  h->cfg = c;
+  h->device = dev;
+  h->sm_count = prop.multiProcessorCount;
+  h->plan = pl;
+  h->fn = ke->fn;
+  h->max_active_clusters = nclusters;
+  for (int i = 0; i < 64; ++i)
+    h->inv_freq[i] = (i < D / 2) ? std::pow((double)c.rope_theta, -2.0 * i / (double)D) : 0.0;
+
+  const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
+  const size_t cnt_bytes = (size_t)((c.max_batch + BT - 1) / BT) * N * sizeof(int);
+  const size_t total = acc_bytes + cnt_bytes + 256;
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
+    delete h;
+    return CF_ERR_CUDA;
+  }
+  if (cudaMemset(h->ws, 0, total) != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return CF_ERR_CUDA;
+  }
+  h->acc = static_cast<float*>(h->ws);
+  h->counters = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes);
+  h->errflag = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes + cnt_bytes);
+  *out = h;
+  return CF_OK;
+}
+
+int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
+                         const void* ln_weight, const void* w_qkv, const void* w_o,
+                         void* k_cache, void* v_cache, const int32_t* positions, void* out,
+                         void* stream) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  const cf_config& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return CF_ERR_INVALID_ARG;
+  if (batch == 0) return CF_OK;
+  const void* ptrs[] = {hidden_states, ln_weight, w_qkv, w_o, k_cache, v_cache, positions, out};
+  for (const void* p : ptrs)
+    if (p == nullptr || ((uintptr_t)p & 15u) != 0) return CF_ERR_INVALID_ARG;
+
+  const int es = esize(c.dtype), D = c.head_dim, H = c.hidden;
+  const int nq = c.n_q_heads, nkv = c.n_kv_heads, S = c.s_max;
+  const int C = (nq + 2 * nkv) * D;
+  const size_t out_bytes = (size_t)batch * H * es;
+  const size_t cache_bytes = (size_t)batch * S * nkv * D * es;
+  if (overlaps(out, out_bytes, hidden_states, (size_t)batch * H * es) ||
+      overlaps(out, out_bytes, ln_weight, (size_t)H * es) ||
+      overlaps(out, out_bytes, w_qkv, (size_t)H * C * es) ||
+      overlaps(out, out_bytes, w_o, (size_t)nq * D * H * es) ||
+      overlaps(out, out_bytes, k_cache, cache_bytes) ||
+      overlaps(out, out_bytes, v_cache, cache_bytes) ||
+      overlaps(out, out_bytes, positions, (size_t)batch * 4))
+    return CF_ERR_ALIAS;
+
+  const Plan& pl = h->plan;
+  KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  // Tensor maps (encoded on the host, cached per pointer).
+  {
+    const CUtensorMap* m = h->m_wqkv.find(w_qkv, 0);
+    if (!m) {
+      CUtensorMap* n = h->m_wqkv.insert(w_qkv, 0);
+      const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H};
+      const uint64_t str[1] = {(uint64_t)C * es};
+      const uint32_t box[2] = {(uint32_t)D, (uint32_t)pl.Rw};
+      if (!encode(n, c.dtype, 2, w_qkv, dims, str, box)) {
+        h->m_wqkv.ptr[(h->m_wqkv.next + MapCache::kSlots - 1) % MapCache::kSlots] = nullptr;
+        return CF_ERR_CUDA;
+      }
+      m = n;
+    }
+    kp.tm_wqkv = *m;
+  }
+  {
+    const CUtensorMap* m = h->m_wo.find(w_o, 0);
+    if (!m) {
+      CUtensorMap* n = h->m_wo.insert(w_o, 0);
+      const uint64_t dims[2] = {(uint64_t)H, (uint64_t)nq * D};
+      const uint64_t str[1] = {(uint64_t)H * es};
+      const uint32_t box[2] = {(uint32_t)pl.Co, (uint32_t)pl.Ro};
+      if (!encode(n, c.dtype, 2, w_o, dims, str, box)) {
+        h->m_wo.ptr[(h->m_wo.next + MapCache::kSlots - 1) % MapCache::kSlots] = nullptr;
+        return CF_ERR_CUDA;
+      }
+      m = n;
+    }
+    kp.tm_wo = *m;
+  }
+  for (int which = 0; which < 2; ++which) {
+    MapCache& mc = which == 0 ? h->m_k : h->m_v;
+    const void* base = which == 0 ? k_cache : v_cache;
+    const CUtensorMap* m = mc.find(base, batch);
+    if (!m) {
+      CUtensorMap* n = mc.insert(base, batch);
+      const uint64_t dims[4] = {(uint64_t)D, (uint64_t)nkv, (uint64_t)S, (uint64_t)batch};
+      const uint64_t str[3] = {(uint64_t)D * es, (uint64_t)nkv * D * es, (uint64_t)S * nkv * D * es};
+      const uint32_t box[4] = {(uint32_t)D, 1u, (uint32_t)pl.Rt, 1u};
+      if (!encode(n, c.dtype, 4, base, dims, str, box)) {
+        mc.ptr[(mc.next + MapCache::kSlots - 1) % MapCache::kSlots] = nullptr;
+        return CF_ERR_CUDA;
+      }
+      m = n;
+    }
+    (which == 0 ? kp.tm_k : kp.tm_v) = *m;
+  }
+
+  kp.hidden = hidden_states;
+  kp.ln_w = ln_weight;
+  kp.k_cache = k_cache;
+  kp.v_cache = v_cache;
+  kp.positions = positions;
+  kp.out = out;
+  kp.acc = h->acc;
+  kp.counters = h->counters;
+  kp.errflag = h->errflag;
+  kp.dbg = h->dbg;
+  kp.B = batch;
+  kp.H = H;
+  kp.nq = nq;
+  kp.nkv = nkv;
+  kp.S = S;
+  kp.N = pl.N;
+  kp.nbt = (batch + pl.BT - 1) / pl.BT;
+  kp.Rw = pl.Rw;
+  kp.Rt = pl.Rt;
+  kp.Ro = pl.Ro;
+  kp.Co = pl.Co;
+  kp.stages = pl.stages;
+  kp.stage_bytes = pl.stage_bytes;
+  kp.eps = c.rms_eps;
+  kp.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  kp.L = pl.L;
+  for (int i = 0; i < 64; ++i) kp.inv_freq[i] = h->inv_freq[i];
+
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.N;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3(pl.N * nkv * kp.nbt, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = pl.L.total;
+  lc.stream = static_cast<cudaStream_t>(stream);
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  void* args[] = {&kp};
+  if (cudaLaunchKernelExC(&lc, h->fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
+  return CF_OK;
+}
+
+int cf_get_status(cf_handle* h) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  int flag = 0;
+  if (cudaMemcpy(&flag, h->errflag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CF_ERR_CUDA;
+  if (flag != 0 && cudaMemset(h->errflag, 0, sizeof(int)) != cudaSuccess) return CF_ERR_CUDA;
+  if (flag & kDevErrTimeout) return CF_ERR_DEVICE_TIMEOUT;
+  if (flag & kDevErrPosRange) return CF_ERR_DEVICE_POS_RANGE;
+  return CF_OK;
+}
+
+int cf_set_debug(cf_handle* h, float* dbg) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  h->dbg = dbg;
+  return CF_OK;
+}
+
+int cf_get_launch_info(const cf_handle* h, cf_launch_info* info) {
+  if (h == nullptr || info == nullptr) return CF_ERR_INVALID_ARG;
+  const Plan& pl = h->plan;
+  info->cluster_size = pl.N;
+  info->batch_tile = pl.BT;
+  info->group = pl.G;
+  info->rows_per_wtile = pl.Rw;
+  info->pos_per_ktile = pl.Rt;
+  info->wo_rows_per_tile = pl.Ro;
+  info->wo_cols_per_tile = pl.Co;
+  info->stages = pl.stages;
+  info->stage_bytes = pl.stage_bytes;
+  info->smem_bytes = pl.L.total;
+  info->threads = kThreads;
+  info->max_active_clusters = h->max_active_clusters;
+  info->sm_count = h->sm_count;
+  return CF_OK;
+}
+
+void cf_destroy(cf_handle* h) {
+  if (h == nullptr) return;
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+}
+
+}  // extern "C"

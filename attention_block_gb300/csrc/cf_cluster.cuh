@@ -1,0 +1,110 @@
+// cf_cluster.cuh -- cluster collectives over distributed shared memory.
+//
+// ClusterReduce [CF §3.1.1, Alg. 1] and ClusterGather [CF §3.1.2, Alg. 2],
+// page "ClusterFusion框架深度解析" (devpress.csdn.net), written for sm_103a:
+//
+//  * every round is a butterfly exchange with partner = rank ^ stride, where
+//    rank is the block's rank inside its cluster (%cluster_ctarank);
+//  * data is PUSHED: each thread writes its 16-byte pieces straight into the
+//    partner's shared memory with st.async, which also signals the
+//    partner's per-round mbarrier (complete_tx); the receiver waits on its
+//    own mbarrier, so there is no cluster-wide barrier per round and threads
+//    outside the collective (the TMA producer warp) never stall;
+//  * each round of each collective owns its receive buffer and mbarrier, so a
+//    buffer is written once per launch and no write-after-read hazard exists
+//    between rounds (the page's double buffering, taken one step further).
+//
+// The collectives run on the NT consumer threads of a block, which
+// synchronize with the named barrier kBar.  Every mbarrier is initialized
+// with count 1 and armed once by the block itself (arrive.expect_tx with the
+// byte count of its round) before the cluster's start barrier; it completes a
+// single phase (parity 0) per launch.  All sizes are multiples of 4 floats.
+#pragma once
+
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+struct OpSum {
+  static __device__ __forceinline__ float apply(float a, float b) { return a + b; }
+};
+struct OpMax {
+  static __device__ __forceinline__ float apply(float a, float b) { return fmaxf(a, b); }
+};
+
+// Bytes one round of each collective receives (what its mbarrier expects).
+__host__ __device__ constexpr int allreduce_round_bytes(int n) { return n * 4; }
+__host__ __device__ constexpr int reduce_scatter_round_bytes(int N, int r, int se) {
+  return (N >> (r + 1)) * se * 4;
+}
+__host__ __device__ constexpr int gather_round_bytes(int r, int se) { return (1 << r) * se * 4; }
+
+// Push n floats (n % 4 == 0) from local shared memory `src` to the same-offset
+// location `dst_local` (an address in this block's window) of block `peer`,
+// signalling that block's mbarrier at `bar_local`.
+template <int NT>
+__device__ __forceinline__ void push_to_peer(const float* src, const float* dst_local, int n,
+                                             uint64_t* bar_local, uint32_t peer, int tid) {
+  const uint32_t raddr = mapa(smem_u32(dst_local), peer);
+  const uint32_t rbar = mapa(smem_u32(bar_local), peer);
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+  for (int i = tid; i < n / 4; i += NT) st_async_v4(raddr + 16u * i, s4[i], rbar);
+}
+
+// ClusterReduce, all-reduce form (recursive doubling): afterwards every block
+// holds op-reduced data[0..n).  rbuf holds log2(N) receive buffers of n
+// floats; rbar log2(N) mbarriers.  The two operands of each round are
+// combined as op(own, partner) -- for sum and max this equals
+// op(partner, own) bit for bit, so all blocks finish with identical data.
+template <class Op, int NT, int kBar>
+__device__ void cluster_allreduce(float* data, int n, float* rbuf, uint64_t* rbar, int rank,
+                                  int N, int tid, int* err) {
+  int r = 0;
+  for (int s = 1; s < N; s <<= 1, ++r) {
+    float* rb = rbuf + r * n;
+    push_to_peer<NT>(data, rb, n, &rbar[r], rank ^ s, tid);
+    mbar_wait_cluster(&rbar[r], 0, err);
+    for (int i = tid; i < n; i += NT) data[i] = Op::apply(data[i], rb[i]);
+    named_sync(kBar, NT);
+  }
+}
+
+// ClusterReduce, reduce-scatter form (recursive halving, sum): data holds N
+// slices of se floats; afterwards slice `rank` holds the cluster-wide sum of
+// that slice (other slices are left partially reduced).  rbuf holds the
+// rounds' receive buffers back to back ((N-1)*se floats in total).
+template <int NT, int kBar>
+__device__ void cluster_reduce_scatter(float* data, int se, float* rbuf, uint64_t* rbar,
+                                       int rank, int N, int tid, int* err) {
+  int lo = 0, r = 0;
+  float* rb = rbuf;
+  for (int s = N >> 1; s >= 1; s >>= 1, ++r) {
+    const int keep = (rank & s) ? lo + s : lo;
+    const int send = (rank & s) ? lo : lo + s;
+    push_to_peer<NT>(data + send * se, rb, s * se, &rbar[r], rank ^ s, tid);
+    mbar_wait_cluster(&rbar[r], 0, err);
+    float* dst = data + keep * se;
+    for (int i = tid; i < s * se; i += NT) dst[i] += rb[i];
+    named_sync(kBar, NT);
+    lo = keep;
+    rb += s * se;
+  }
+}
+
+// ClusterGather (recursive doubling, [CF §3.1.2]: the data moved per round
+// doubles): data holds N slices of se floats of which slice `rank` is
+// filled; afterwards every block holds all N slices.  Received blocks land
+// directly in their final place in `data` (each slice is written once).
+template <int NT, int kBar>
+__device__ void cluster_gather(float* data, int se, uint64_t* gbar, int rank, int N, int tid,
+                               int* err) {
+  int r = 0;
+  for (int s = 1; s < N; s <<= 1, ++r) {
+    const int blk = rank & ~(s - 1);
+    push_to_peer<NT>(data + blk * se, data + blk * se, s * se, &gbar[r], rank ^ s, tid);
+    mbar_wait_cluster(&gbar[r], 0, err);
+  }
+  named_sync(kBar, NT);
+}
+
+}  // namespace cf

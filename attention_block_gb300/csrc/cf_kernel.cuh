@@ -1,0 +1,750 @@
+// cf_kernel.cuh -- the fused single-token decode attention block for sm_103a.
+//
+// Pages cited by title and section:
+//   [CF]  "ClusterFusion框架深度解析：LLM推理优化的集群级通信革命" (devpress.csdn.net)
+//   [LNA] "大模型推理中的算子融合优化：LayerNorm + Attention 的 CUDA Kernel 手写与验证"
+//         (asdsk.com)
+//
+// One launch computes, for every batch row, RMSNorm -> merged QKV projection
+// -> RoPE -> KV-cache append -> split-KV online-softmax attention -> output
+// projection + residual ([CF §3.2] fused_qkv_attention_out, [LNA §一]).
+//
+// Mapping [CF §3.2 空间映射策略]: one thread-block cluster per (KV head g,
+// batch tile of BT rows); for GQA the cluster serves the G = nq/nkv query
+// heads of its KV head, so each K/V byte is read once.  The N blocks of a
+// cluster split
+//   * the hidden (reduction) dimension of the QKV projection: block c owns
+//     rows [c*H/N, (c+1)*H/N) of W_qkv's head columns; the partial q/k/v are
+//     combined by ClusterReduce (reduce-scatter form), which leaves block c
+//     owning head-dim slice c (the RoPE pairs (i, i+d/2) with i in
+//     [c*P, (c+1)*P), P = d/(2N)); block c rotates and appends its slice, and
+//     ClusterGather then gives every block the full q', k', v [CF §3.1.2,
+//     "QKV向量共享"];
+//   * the KV sequence of the attention: block c takes its share of the
+//     position tiles and produces online-softmax partials (m, l, o); these
+//     are combined with ClusterReduce(max) and a rescaled ClusterReduce(sum)
+//     [CF §3.2 在线softmax, §3.1.1];
+//   * the output columns of the O projection: block c multiplies o by its
+//     column band of W_o and adds into an fp32 accumulator with atomics
+//     [CF §3.2 原子写合并]; the last block to finish a (batch tile, band)
+//     adds the residual, rounds to the storage type and writes `out`.
+//
+// Data movement: one producer warp streams every byte the block needs
+// (W_qkv tiles, then K/V tiles, then W_o tiles) through a ring of
+// shared-memory stages with TMA tensor copies (evict-first in L2), running
+// ahead of the 8 consumer warps across phase boundaries, so HBM stays busy
+// while the consumers are in a cluster exchange ([CF §4.2] "通信-计算重叠",
+// done with TMA instead of cuda::memcpy_async).  Intermediates never touch
+// HBM: normed hidden, q/k/v, softmax statistics and partial outputs live in
+// shared memory and move between blocks over DSMEM.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "cf_cluster.cuh"
+#include "cf_params.h"
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+// ------------------------------------------------------------ conversions --
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static __device__ __forceinline__ float to_f(float v) { return v; }
+  static __device__ __forceinline__ float from_f(float v) { return v; }
+  static __device__ __forceinline__ void words(const uint32_t* w, int nw, float* f) {
+    for (int i = 0; i < nw; ++i) f[i] = __uint_as_float(w[i]);
+  }
+};
+template <>
+struct Elem<__half> {
+  static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+  static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+  static __device__ __forceinline__ void words(const uint32_t* w, int nw, float* f) {
+    for (int i = 0; i < nw; ++i) {
+      float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+  static __device__ __forceinline__ void words(const uint32_t* w, int nw, float* f) {
+    for (int i = 0; i < nw; ++i) {
+      float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+
+// Load NE contiguous elements (NE*sizeof(T) in {4, 8, 16} bytes, naturally
+// aligned) and widen them to fp32.
+template <typename T, int NE>
+__device__ __forceinline__ void load_cvt(const T* p, float* f) {
+  constexpr int B = NE * (int)sizeof(T);
+  static_assert(B == 4 || B == 8 || B == 16, "vector width");
+  if constexpr (B == 16) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    Elem<T>::words(w, 4, f);
+  } else if constexpr (B == 8) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    uint32_t w[2] = {u.x, u.y};
+    Elem<T>::words(w, 2, f);
+  } else {
+    uint32_t w[1] = {*reinterpret_cast<const uint32_t*>(p)};
+    Elem<T>::words(w, 1, f);
+  }
+}
+
+// Store 4 consecutive elements from fp32 (round to nearest even).
+template <typename T>
+__device__ __forceinline__ void store4(T* p, const float* f) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  } else {
+    T t[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) t[e] = Elem<T>::from_f(f[e]);
+    *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(t);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Position tiles [t0, t1) of the cached keys 0..pos-1 handled by block `rank`
+// (balanced split of ceil(pos/Rt) tiles over N blocks).  pos < 0 marks an
+// invalid row; pos == 0 has no cached key (only the new token).
+__device__ __forceinline__ void kv_tile_range(int pos, int Rt, int rank, int N, int& t0,
+                                              int& t1) {
+  if (pos <= 0) {
+    t0 = t1 = 0;
+    return;
+  }
+  const int nt = (pos + Rt - 1) / Rt;
+  t0 = (int)(((long long)rank * nt) / N);
+  t1 = (int)(((long long)(rank + 1) * nt) / N);
+}
+
+constexpr int kBarConsumers = 1;  // named barrier id of the 256 consumer threads
+
+template <typename T, int D, int G, int BT>
+__global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_constant__ KParams p) {
+  constexpr int NSEG = G + 2;          // q heads of the group, k, v
+  constexpr int CPL = D / 32;          // projection columns per lane per segment
+  // attention: LPP lanes share one position; each lane owns DPL head dims
+  constexpr int LPP = (4 * G < 8) ? 8 : ((4 * G > 32) ? 32 : 4 * G);
+  constexpr int NGRP = 32 / LPP;
+  constexpr int DPL = D / LPP;
+  constexpr int PB = (DPL * (int)sizeof(T) < 16) ? DPL * (int)sizeof(T) : 16;
+  constexpr int EP = PB / (int)sizeof(T);  // elements per load piece
+  constexpr int NPC = DPL / EP;            // pieces per lane
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(DPL % EP == 0 && NPC >= 1, "lane split");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int N = p.N;
+  const int rank = (int)cluster_ctarank();
+  const int cid = blockIdx.x / N;
+  const int g = cid / p.nbt;  // KV head
+  const int bt = cid % p.nbt; // batch tile
+  const int b0 = bt * BT;
+  const int P = D / (2 * N);            // RoPE pairs per head-dim slice
+  const int SE = BT * NSEG * 2 * P;     // floats per slice
+  const int Hc = p.H / N;               // K band rows == O-proj column band
+  const int k0 = rank * Hc;
+  const int nrounds = __ffs(N) - 1;
+  const int MXP = (BT * G + 3) & ~3;
+  const int SMP = BT * G * (D + 4);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.L.bars);
+  uint64_t* full = bars + BarIdx::full;
+  uint64_t* empty = bars + BarIdx::empty;
+  uint8_t* ring = sm + p.L.ring;
+  float* xn = reinterpret_cast<float*>(sm + p.L.xn);
+  float* red = reinterpret_cast<float*>(sm + p.L.red);
+  float* scratch = reinterpret_cast<float*>(sm + p.L.scratch);
+  float* qkv = reinterpret_cast<float*>(sm + p.L.qkv);
+  float* mx = reinterpret_cast<float*>(sm + p.L.mx);
+  float* smx = reinterpret_cast<float*>(sm + p.L.sm);
+  float* mloc = reinterpret_cast<float*>(sm + p.L.mloc);
+  float* rope = reinterpret_cast<float*>(sm + p.L.rope);
+  int* s_pos = reinterpret_cast<int*>(sm + p.L.misc);
+  int* s_flag = s_pos + BT;
+  float* s_rinv = reinterpret_cast<float*>(s_flag + 4);
+
+  // ---------------------------------------------------------------- setup --
+  if (tid < BT) {
+    const int b = b0 + tid;
+    int pos = -1;
+    if (b < p.B) {
+      pos = p.positions[b];
+      if (pos < 0 || pos >= p.S) {
+        if (rank == 0 && g == 0) atomicOr(p.errflag, kDevErrPosRange);
+        pos = -1;
+      }
+    }
+    s_pos[tid] = pos;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    for (int r = 0; r < nrounds; ++r) {
+      mbar_init(&bars[BarIdx::rs + r], 1);
+      mbar_init(&bars[BarIdx::ga + r], 1);
+      mbar_init(&bars[BarIdx::mx + r], 1);
+      mbar_init(&bars[BarIdx::sm + r], 1);
+    }
+    fence_mbar_init_cluster();
+    for (int r = 0; r < nrounds; ++r) {
+      mbar_arrive_expect_tx(&bars[BarIdx::rs + r], reduce_scatter_round_bytes(N, r, SE));
+      mbar_arrive_expect_tx(&bars[BarIdx::ga + r], gather_round_bytes(r, SE));
+      mbar_arrive_expect_tx(&bars[BarIdx::mx + r], allreduce_round_bytes(MXP));
+      mbar_arrive_expect_tx(&bars[BarIdx::sm + r], allreduce_round_bytes(SMP));
+    }
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&p.tm_wqkv);
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+    prefetch_tensormap(&p.tm_wo);
+  }
+  __syncthreads();
+  cluster_sync_all();  // peers' barriers are initialized before any DSMEM traffic
+
+  const int nkt = Hc / p.Rw;
+  const int ncb = Hc / p.Co;
+  const int nrt = G * D / p.Ro;
+
+  if (warp == kConsumerWarps) {
+    // ============================================== TMA producer warp ====
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int it = 0;
+      auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
+        const int s = it % p.stages;
+        if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+        bar = &full[s];
+        mbar_arrive_expect_tx(bar, bytes);
+        return ring + (size_t)s * p.stage_bytes;
+      };
+      // Phase 1: W_qkv row tiles of this block's K band, G+2 head slices each.
+      const uint32_t seg_bytes = (uint32_t)(p.Rw * D * sizeof(T));
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        uint64_t* bar;
+        uint8_t* dst = slot(NSEG * seg_bytes, bar);
+        const int y = k0 + kt * p.Rw;
+        for (int j = 0; j < G; ++j)
+          tma_load_2d(dst + j * seg_bytes, &p.tm_wqkv, (g * G + j) * D, y, bar, pol);
+        tma_load_2d(dst + G * seg_bytes, &p.tm_wqkv, (p.nq + g) * D, y, bar, pol);
+        tma_load_2d(dst + (G + 1) * seg_bytes, &p.tm_wqkv, (p.nq + p.nkv + g) * D, y, bar, pol);
+      }
+      // Phase 2: K and V tiles of this block's share of each row's positions.
+      const uint32_t kv_bytes = (uint32_t)(p.Rt * D * sizeof(T));
+      for (int bb = 0; bb < BT; ++bb) {
+        int t0, t1;
+        kv_tile_range(s_pos[bb], p.Rt, rank, N, t0, t1);
+        for (int t = t0; t < t1; ++t, ++it) {
+          uint64_t* bar;
+          uint8_t* dst = slot(2 * kv_bytes, bar);
+          tma_load_4d(dst, &p.tm_k, 0, g, t * p.Rt, b0 + bb, bar, pol);
+          tma_load_4d(dst + kv_bytes, &p.tm_v, 0, g, t * p.Rt, b0 + bb, bar, pol);
+        }
+      }
+      // Phase 3: W_o tiles: rows of the group's heads x this block's column band.
+      const uint32_t wo_bytes = (uint32_t)(p.Ro * p.Co * sizeof(T));
+      for (int cb = 0; cb < ncb; ++cb)
+        for (int rt = 0; rt < nrt; ++rt, ++it) {
+          uint64_t* bar;
+          uint8_t* dst = slot(wo_bytes, bar);
+          tma_load_2d(dst, &p.tm_wo, k0 + cb * p.Co, g * G * D + rt * p.Ro, bar, pol);
+        }
+    }
+    __syncwarp();
+  } else {
+    // ============================================== consumer warps =======
+    const T* __restrict__ hidden = reinterpret_cast<const T*>(p.hidden);
+    const T* __restrict__ lnw = reinterpret_cast<const T*>(p.ln_w);
+    int it = 0;
+
+    // ---- Phase 0: RMSNorm of the tile's rows [LNA §三 stage 1] ----------
+    for (int i = tid; i < N * SE; i += kConsumers) red[i] = 0.f;
+    for (int i = tid; i < MXP; i += kConsumers) mx[i] = 0.f;
+    for (int i = tid; i < SMP; i += kConsumers) smx[i] = 0.f;
+    {
+      constexpr int EV = 16 / (int)sizeof(T);
+      float ss[BT];
+#pragma unroll
+      for (int bb = 0; bb < BT; ++bb) {
+        ss[bb] = 0.f;
+        if (b0 + bb < p.B) {
+          const T* x = hidden + (size_t)(b0 + bb) * p.H;
+          for (int i = tid * EV; i < p.H; i += kConsumers * EV) {
+            float f[EV];
+            load_cvt<T, EV>(x + i, f);
+#pragma unroll
+            for (int e = 0; e < EV; ++e) ss[bb] = fmaf(f[e], f[e], ss[bb]);
+          }
+        }
+        ss[bb] = warp_sum(ss[bb]);
+      }
+      // [8 warps][BT] partial sums; its own region, because `scratch` is the
+      // reduce-scatter receive area that peers may start writing at any time.
+      float* wred = s_rinv + BT;
+      if (lane == 0)
+#pragma unroll
+        for (int bb = 0; bb < BT; ++bb) wred[warp * BT + bb] = ss[bb];
+      named_sync(kBarConsumers, kConsumers);
+      if (tid < BT) {
+        float tot = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) tot += wred[w * BT + tid];
+        s_rinv[tid] = 1.0f / sqrtf(tot / (float)p.H + p.eps);
+      }
+      // cos/sin of this block's RoPE pairs, in float64 then rounded [LNA §三]
+      for (int idx = tid; idx < BT * P; idx += kConsumers) {
+        const int bb = idx / P, j = idx % P;
+        const int pos = s_pos[bb];
+        float c = 1.f, s = 0.f;
+        if (pos >= 0) {
+          double sd, cd;
+          sincos((double)pos * p.inv_freq[rank * P + j], &sd, &cd);
+          c = (float)cd;
+          s = (float)sd;
+        }
+        rope[2 * idx] = c;
+        rope[2 * idx + 1] = s;
+      }
+      named_sync(kBarConsumers, kConsumers);
+      for (int idx = tid; idx < BT * Hc; idx += kConsumers) {
+        const int bb = idx / Hc, i = idx % Hc;
+        float v = 0.f;
+        if (b0 + bb < p.B)
+          v = Elem<T>::to_f(hidden[(size_t)(b0 + bb) * p.H + k0 + i]) * s_rinv[bb] *
+              Elem<T>::to_f(lnw[k0 + i]);
+        xn[idx] = v;
+      }
+      named_sync(kBarConsumers, kConsumers);
+    }
+
+    // ---- Phase 1: merged QKV projection over this block's K band --------
+    {
+      float acc[BT][NSEG][CPL];
+#pragma unroll
+      for (int bb = 0; bb < BT; ++bb)
+#pragma unroll
+        for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+          for (int e = 0; e < CPL; ++e) acc[bb][sg][e] = 0.f;
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        const int s = it % p.stages;
+        mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
+        for (int r = warp; r < p.Rw; r += kConsumerWarps) {
+          float nv[BT];
+#pragma unroll
+          for (int bb = 0; bb < BT; ++bb) nv[bb] = xn[bb * Hc + kt * p.Rw + r];
+#pragma unroll
+          for (int sg = 0; sg < NSEG; ++sg) {
+            float w[CPL];
+            load_cvt<T, CPL>(tile + ((size_t)sg * p.Rw + r) * D + lane * CPL, w);
+#pragma unroll
+            for (int bb = 0; bb < BT; ++bb)
+#pragma unroll
+              for (int e = 0; e < CPL; ++e) acc[bb][sg][e] = fmaf(nv[bb], w[e], acc[bb][sg][e]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      // Sum the 8 warps' partials into the slice-ordered buffer: column i of
+      // a segment belongs to slice c = (i mod d/2) / P, so each RoPE pair
+      // (i, i + d/2) stays inside one slice.
+#pragma unroll
+      for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) {
+          const int col = lane * CPL + e;
+          const int hi = col / (D / 2), il = col % (D / 2);
+          const int c = il / P, j = il % P;
+#pragma unroll
+          for (int bb = 0; bb < BT; ++bb)
+            atomicAdd(&red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j], acc[bb][sg][e]);
+        }
+      named_sync(kBarConsumers, kConsumers);
+    }
+
+    // ---- ClusterReduce (reduce-scatter): block `rank` owns slice `rank` --
+    cluster_reduce_scatter<kConsumers, kBarConsumers>(red, SE, scratch, &bars[BarIdx::rs], rank,
+                                                      N, tid, p.errflag);
+
+    // ---- RoPE on the own slice, then append K/V [LNA §三 stage 3] -------
+    {
+      float* my = red + rank * SE;
+      T* kc = reinterpret_cast<T*>(p.k_cache);
+      T* vc = reinterpret_cast<T*>(p.v_cache);
+      for (int idx = tid; idx < BT * NSEG * P; idx += kConsumers) {
+        const int bb = idx / (NSEG * P), rem = idx % (NSEG * P);
+        const int sg = rem / P, j = rem % P;
+        const int pos = s_pos[bb];
+        if (pos < 0) continue;
+        float* lo = my + ((bb * NSEG + sg) * 2) * P + j;
+        float* hi = lo + P;
+        float a = *lo, bv = *hi;
+        if (sg <= G) {  // query heads and the key: rotate-half
+          const float c = rope[2 * (bb * P + j)], sn = rope[2 * (bb * P + j) + 1];
+          const float ra = a * c - bv * sn;
+          const float rb = bv * c + a * sn;
+          a = ra;
+          bv = rb;
+        }
+        if (sg >= G) {  // key and value: round to storage and append
+          const T ta = Elem<T>::from_f(a), tb = Elem<T>::from_f(bv);
+          a = Elem<T>::to_f(ta);
+          bv = Elem<T>::to_f(tb);
+          T* cache = (sg == G) ? kc : vc;
+          const size_t base = (((size_t)(b0 + bb) * p.S + pos) * p.nkv + g) * D;
+          cache[base + rank * P + j] = ta;
+          cache[base + D / 2 + rank * P + j] = tb;
+        }
+        *lo = a;
+        *hi = bv;
+      }
+      named_sync(kBarConsumers, kConsumers);
+    }
+
+    // ---- ClusterGather of the q'/k'/v slices [CF §3.1.2] -----------------
+    cluster_gather<kConsumers, kBarConsumers>(red, SE, &bars[BarIdx::ga], rank, N, tid, p.errflag);
+    for (int idx = tid; idx < BT * NSEG * D; idx += kConsumers) {
+      const int bb = idx / (NSEG * D), rem = idx % (NSEG * D);
+      const int sg = rem / D, dim = rem % D;
+      const int hi = dim / (D / 2), il = dim % (D / 2);
+      const int c = il / P, j = il % P;
+      qkv[idx] = red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j];
+    }
+    named_sync(kBarConsumers, kConsumers);
+    if (p.dbg != nullptr && rank == 0) {
+      float* dq = p.dbg;
+      float* dk = dq + (size_t)p.B * p.nq * D;
+      float* dv = dk + (size_t)p.B * p.nkv * D;
+      for (int idx = tid; idx < BT * NSEG * D; idx += kConsumers) {
+        const int bb = idx / (NSEG * D), rem = idx % (NSEG * D);
+        const int sg = rem / D, dim = rem % D;
+        const int b = b0 + bb;
+        if (b >= p.B || s_pos[bb] < 0) continue;
+        if (sg < G) dq[((size_t)b * p.nq + g * G + sg) * D + dim] = qkv[idx];
+        else if (sg == G) dk[((size_t)b * p.nkv + g) * D + dim] = qkv[idx];
+        else dv[((size_t)b * p.nkv + g) * D + dim] = qkv[idx];
+      }
+    }
+
+    // ---- Phase 2: split-KV online-softmax attention [CF §3.2] ------------
+    {
+      const int grp = lane / LPP, kl = lane % LPP;
+      float* wst = scratch;  // [8 warps][G][D+4]: o[D], m, l
+      for (int bb = 0; bb < BT; ++bb) {
+        const int pos = s_pos[bb];
+        float q[G][DPL], o[G][DPL], m[G], l[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          m[h] = -INFINITY;
+          l[h] = 0.f;
+#pragma unroll
+          for (int i = 0; i < NPC; ++i)
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+              const int dim = (kl + i * LPP) * EP + e;
+              q[h][i * EP + e] = qkv[(bb * NSEG + h) * D + dim] * p.qk_scale_log2;
+              o[h][i * EP + e] = 0.f;
+            }
+        }
+        // One position's contribution to this lane group's running state.
+        auto consume = [&](const T* krow, const T* vrow, bool valid) {
+          float kf[DPL], vf[DPL];
+#pragma unroll
+          for (int i = 0; i < NPC; ++i) load_cvt<T, EP>(krow + (kl + i * LPP) * EP, kf + i * EP);
+          float sc[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) s = fmaf(q[h][e], kf[e], s);
+            sc[h] = s;
+          }
+#pragma unroll
+          for (int off = LPP / 2; off >= 1; off >>= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+#pragma unroll
+          for (int i = 0; i < NPC; ++i) load_cvt<T, EP>(vrow + (kl + i * LPP) * EP, vf + i * EP);
+          if (valid) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float mn = fmaxf(m[h], sc[h]);
+              const float alpha = exp2f(m[h] - mn);
+              const float pe = exp2f(sc[h] - mn);
+              l[h] = fmaf(l[h], alpha, pe);
+#pragma unroll
+              for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(o[h][e], alpha, pe * vf[e]);
+              m[h] = mn;
+            }
+          }
+        };
+        int t0, t1;
+        kv_tile_range(pos, p.Rt, rank, N, t0, t1);
+        for (int t = t0; t < t1; ++t, ++it) {
+          const int s = it % p.stages;
+          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+          const T* Kt = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
+          const T* Vt = Kt + (size_t)p.Rt * D;
+          const int lim = min(p.Rt, pos - t * p.Rt);  // cached positions < pos only
+          for (int pb = warp * NGRP; pb < lim; pb += kConsumerWarps * NGRP) {
+            const int pp = pb + grp;
+            const bool valid = pp < lim;
+            const int row = valid ? pp : pb;
+            consume(Kt + (size_t)row * D, Vt + (size_t)row * D, valid);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        // The new token (position pos) comes from shared memory, not the
+        // cache; the last block of the cluster folds it in.
+        if (rank == N - 1 && warp == 0 && pos >= 0) {
+          const float* kn = qkv + (bb * NSEG + G) * D;
+          const float* vn = qkv + (bb * NSEG + G + 1) * D;
+          float kf[DPL], vf[DPL];
+#pragma unroll
+          for (int i = 0; i < NPC; ++i)
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+              kf[i * EP + e] = kn[(kl + i * LPP) * EP + e];
+              vf[i * EP + e] = vn[(kl + i * LPP) * EP + e];
+            }
+          float sc[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) s = fmaf(q[h][e], kf[e], s);
+            sc[h] = s;
+          }
+#pragma unroll
+          for (int off = LPP / 2; off >= 1; off >>= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+          if (grp == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float mn = fmaxf(m[h], sc[h]);
+              const float alpha = exp2f(m[h] - mn);
+              const float pe = exp2f(sc[h] - mn);
+              l[h] = fmaf(l[h], alpha, pe);
+#pragma unroll
+              for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(o[h][e], alpha, pe * vf[e]);
+              m[h] = mn;
+            }
+          }
+        }
+        // Merge the lane groups of the warp.
+#pragma unroll
+        for (int off = LPP; off < 32; off <<= 1)
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
+            const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
+            const float mn = fmaxf(m[h], mo);
+            const float a = (mn == -INFINITY) ? 0.f : exp2f(m[h] - mn);
+            const float b = (mn == -INFINITY) ? 0.f : exp2f(mo - mn);
+            l[h] = l[h] * a + lo * b;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) {
+              const float oo = __shfl_xor_sync(0xffffffffu, o[h][e], off);
+              o[h][e] = o[h][e] * a + oo * b;
+            }
+            m[h] = mn;
+          }
+        if (grp == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float* st = wst + (warp * G + h) * (D + 4);
+#pragma unroll
+            for (int i = 0; i < NPC; ++i)
+#pragma unroll
+              for (int e = 0; e < EP; ++e) st[(kl + i * LPP) * EP + e] = o[h][i * EP + e];
+            if (kl == 0) {
+              st[D] = m[h];
+              st[D + 1] = l[h];
+            }
+          }
+        }
+        named_sync(kBarConsumers, kConsumers);
+        // Merge the 8 warps into this block's partial (m, l, o) of row bb.
+        for (int idx = tid; idx < G * D; idx += kConsumers) {
+          const int h = idx / D, dim = idx % D;
+          float M = -INFINITY;
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wst[(w * G + h) * (D + 4) + D]);
+          float O = 0.f, L = 0.f;
+          if (M != -INFINITY) {
+            for (int w = 0; w < kConsumerWarps; ++w) {
+              const float* st = wst + (w * G + h) * (D + 4);
+              const float f = exp2f(st[D] - M);
+              O = fmaf(f, st[dim], O);
+              L = fmaf(f, st[D + 1], L);
+            }
+          }
+          float* dst = smx + (bb * G + h) * (D + 4);
+          dst[dim] = O;
+          if (dim == 0) {
+            dst[D] = L;
+            mx[bb * G + h] = M;
+            mloc[bb * G + h] = M;
+          }
+        }
+        named_sync(kBarConsumers, kConsumers);
+      }
+    }
+
+    // ---- ClusterReduce(max), rescale, ClusterReduce(sum) [CF §3.1.1] -----
+    cluster_allreduce<OpMax, kConsumers, kBarConsumers>(mx, MXP, mx + MXP, &bars[BarIdx::mx],
+                                                        rank, N, tid, p.errflag);
+    for (int idx = tid; idx < BT * G * (D + 4); idx += kConsumers) {
+      const int row = idx / (D + 4);
+      const float ml = mloc[row];
+      smx[idx] *= (ml == -INFINITY) ? 0.f : exp2f(ml - mx[row]);
+    }
+    named_sync(kBarConsumers, kConsumers);
+    cluster_allreduce<OpSum, kConsumers, kBarConsumers>(smx, SMP, smx + SMP, &bars[BarIdx::sm],
+                                                        rank, N, tid, p.errflag);
+    // Final attention output o = (sum o_c e^{m_c-m}) / (sum l_c e^{m_c-m}),
+    // written over the (no longer needed) q' of the same head.
+    for (int idx = tid; idx < BT * G * D; idx += kConsumers) {
+      const int bb = idx / (G * D), rem = idx % (G * D);
+      const int h = rem / D, dim = rem % D;
+      const float* src = smx + (bb * G + h) * (D + 4);
+      const float L = src[D];
+      qkv[(bb * NSEG + h) * D + dim] = (L > 0.f) ? src[dim] / L : 0.f;
+    }
+    for (int i = tid; i < BT * p.Co; i += kConsumers) scratch[i] = 0.f;
+    named_sync(kBarConsumers, kConsumers);
+    if (p.dbg != nullptr && rank == 0) {
+      float* dob = p.dbg + (size_t)p.B * (p.nq + 2 * p.nkv) * D;
+      for (int idx = tid; idx < BT * G * D; idx += kConsumers) {
+        const int bb = idx / (G * D), rem = idx % (G * D);
+        const int h = rem / D, dim = rem % D;
+        const int b = b0 + bb;
+        if (b >= p.B || s_pos[bb] < 0) continue;
+        dob[((size_t)b * p.nq + g * G + h) * D + dim] = qkv[(bb * NSEG + h) * D + dim];
+      }
+    }
+
+    // ---- Phase 3: O projection of this block's column band [CF §3.2] -----
+    {
+      const int CQ = p.Co / 4;
+      const int RG = kConsumers / CQ;
+      const int colq = tid % CQ, rg = tid / CQ;
+      float* ob = scratch;  // [BT][Co]
+      for (int cb = 0; cb < ncb; ++cb) {
+        float a[BT][4];
+#pragma unroll
+        for (int bb = 0; bb < BT; ++bb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a[bb][e] = 0.f;
+        for (int rt = 0; rt < nrt; ++rt, ++it) {
+          const int s = it % p.stages;
+          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+          const T* W = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
+          if (rg < RG) {
+            for (int r = rg; r < p.Ro; r += RG) {
+              float w[4];
+              load_cvt<T, 4>(W + (size_t)r * p.Co + colq * 4, w);
+              const int row = rt * p.Ro + r;
+              const int h = row / D, dim = row % D;
+#pragma unroll
+              for (int bb = 0; bb < BT; ++bb) {
+                const float ov = qkv[(bb * NSEG + h) * D + dim];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a[bb][e] = fmaf(ov, w[e], a[bb][e]);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (rg < RG)
+#pragma unroll
+          for (int bb = 0; bb < BT; ++bb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) atomicAdd(&ob[bb * p.Co + colq * 4 + e], a[bb][e]);
+        named_sync(kBarConsumers, kConsumers);
+        for (int i4 = tid; i4 < BT * CQ; i4 += kConsumers) {
+          const int bb = i4 / CQ, cq = i4 % CQ;
+          float4* src = reinterpret_cast<float4*>(ob) + i4;
+          const float4 v = *src;
+          *src = make_float4(0.f, 0.f, 0.f, 0.f);
+          const int b = b0 + bb;
+          if (b < p.B && s_pos[bb] >= 0)
+            atomicAdd(reinterpret_cast<float4*>(p.acc + (size_t)b * p.H + k0 + cb * p.Co + cq * 4),
+                      v);
+        }
+        named_sync(kBarConsumers, kConsumers);
+      }
+    }
+
+    // ---- Residual + finalize by the last block of each (tile, band) ------
+    __threadfence();
+    named_sync(kBarConsumers, kConsumers);
+    if (tid == 0) {
+      const int ticket = atomicAdd(&p.counters[bt * N + rank], 1);
+      const int last = (ticket == p.nkv - 1);
+      if (last) __threadfence();
+      s_flag[0] = last;
+    }
+    named_sync(kBarConsumers, kConsumers);
+    if (s_flag[0]) {
+      T* out = reinterpret_cast<T*>(p.out);
+      float* dproj = p.dbg ? p.dbg + (size_t)p.B * (2 * p.nq + 2 * p.nkv) * D : nullptr;
+      const int C4 = Hc / 4;
+      for (int i4 = tid; i4 < BT * C4; i4 += kConsumers) {
+        const int bb = i4 / C4, c4 = i4 % C4;
+        const int b = b0 + bb;
+        if (b >= p.B) continue;
+        const size_t off = (size_t)b * p.H + k0 + c4 * 4;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
+        __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
+        float xf[4];
+        load_cvt<T, 4>(hidden + off, xf);
+        const float r[4] = {xf[0] + v.x, xf[1] + v.y, xf[2] + v.z, xf[3] + v.w};
+        store4<T>(out + off, r);
+        if (dproj) {
+          dproj[off + 0] = v.x;
+          dproj[off + 1] = v.y;
+          dproj[off + 2] = v.z;
+          dproj[off + 3] = v.w;
+        }
+      }
+      if (tid == 0) p.counters[bt * N + rank] = 0;
+    }
+  }
+
+  // No block leaves while a peer may still write into its shared memory.
+  __syncwarp();
+  cluster_sync_all();
+}
+
+}  // namespace cf

@@ -1,0 +1,508 @@
+"""Benchmark of the fused decode attention block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--cluster-size C] [--batch-tile B]
+                    [--stage-bytes S] [--ctas-per-sm X] [--no-graph]
+
+One step = one decode attention-block call (RMSNorm, QKV, RoPE, KV append,
+split-KV attention, O projection + residual) over one batch of synthetic
+inputs; for the 32-layer long-context workload one step is the 32-layer
+chain.  Inputs live in HBM before timing starts; between steps the next of R
+independently seeded replicas is used, with R chosen so the replicas span at
+least 4x the L2 size (L2 never serves a step's weights or KV).
+
+Prints ONE JSON line (rank 0).  ``value`` is the achieved HBM throughput in
+GB/s (algorithmic bytes of all ranks' steps / max-over-ranks time);
+``us_per_step`` is the step latency.  N > 1 runs independent replicas, one
+per GPU (the path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attention-block µs/step and achieved HBM GB/s (fraction of GB300 peak)"
+DEFAULT_WORKLOAD = "llama2_7b_layer_b1_p1024_f16"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_L2_BYTES = 129 * 1024 * 1024
+KERNEL_NAME = "cf_decode_kernel"
+
+
+# ------------------------------------------------------------ host helpers --
+def algorithmic_bytes(w, positions) -> int:
+    """Bytes one decode step must move at minimum: weights, ln_weight, the KV
+    read over positions [0, p_b) of every row, the new K/V written, hidden
+    read, out written, positions read."""
+    es = 4 if w.dtype == "f32" else 2
+    d, nq, nkv, H, B = w.head_dim, w.n_q_heads, w.n_kv_heads, w.hidden, w.batch
+    weights = H * w.qkv_cols * es + nq * d * H * es + H * es
+    kv_read = sum(2 * int(p) * nkv * d * es for p in positions)
+    kv_write = 2 * B * nkv * d * es
+    io = 2 * B * H * es + 4 * B
+    return weights + kv_read + kv_write + io
+
+
+def flops_per_step(w, positions) -> int:
+    d, nq, H, B = w.head_dim, w.n_q_heads, w.hidden, w.batch
+    proj = 2 * B * H * w.qkv_cols + 2 * B * nq * d * H
+    attn = sum(4 * (int(p) + 1) * nq * d for p in positions)
+    return proj + attn
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            v = float(json.load(fh)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_block_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+        ent = rec.get(workload)
+        if ent and ent.get("kernel_src_sha") == kernel_source_hash():
+            return int(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def parse_clocks(lines):
+    """Parse nvidia-smi CSV samples -> clocks dict for the JSON line."""
+    sm, mx, reasons, loaded = [], 0.0, set(), []
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 9 or not parts[1].split()[0].replace(".", "").isdigit():
+            continue
+        try:
+            cur = float(parts[1].split()[0])
+            mx = max(mx, float(parts[2].split()[0]))
+            pw = float(parts[3].split()[0])
+        except ValueError:
+            continue
+        sm.append(cur)
+        loaded.append((cur, pw))
+        for name, val in zip(names, parts[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    under = [c for c, p in loaded if p > 200.0] or sm
+    return {"sm_mhz": statistics.median(under) if under else None,
+            "sm_max_mhz": mx or None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+        return False
+
+    def result(self):
+        return parse_clocks(self.lines)
+
+
+def allgather_rows(mine, world: int, device):
+    """All ranks' float rows (one list per rank), via torch.distributed."""
+    import torch
+    import torch.distributed as dist
+    if world == 1:
+        return [list(mine)]
+    t = torch.tensor([list(mine)], dtype=torch.float64, device=device)
+    gathered = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(gathered, t)
+    return [g[0].tolist() for g in gathered]
+
+
+def aggregate(per_rank):
+    """Combine per-rank (bytes, seconds, steps) -> whole-job numbers: total
+    bytes over the max time (the slowest rank bounds the job)."""
+    tot_bytes = sum(r[0] for r in per_rank)
+    t = max(r[1] for r in per_rank)
+    return {"gbs": tot_bytes / t / 1e9, "seconds": t}
+
+
+# ---------------------------------------------------------------- oracle --
+def time_oracle(w, layer_cpu, budget_s: float, max_steps: int | None = None):
+    """Run the float64 oracle over batch rows of one step until budget_s is
+    spent (at least one row).  Returns (seconds per full step, rows done)."""
+    import numpy as np
+    import oracle
+    from attention_block_gb300 import synth
+
+    f = {k: synth.to_f64(layer_cpu[k]) for k in ("hidden", "ln_weight", "w_qkv", "w_o")}
+    pos = layer_cpu["positions"].numpy()
+    cfg = w.oracle_cfg()
+    rows_done, t_rows = 0, 0.0
+    t0 = time.perf_counter()
+    b = 0
+    while True:
+        kc = np.ascontiguousarray(synth.to_f64(layer_cpu["k_cache"][b]))
+        vc = np.ascontiguousarray(synth.to_f64(layer_cpu["v_cache"][b]))
+        s = time.perf_counter()
+        oracle.decode_row(cfg, f["hidden"][b], f["ln_weight"], f["w_qkv"], f["w_o"], kc, vc,
+                          int(pos[b]))
+        t_rows += time.perf_counter() - s
+        rows_done += 1
+        b = (b + 1) % w.batch
+        if time.perf_counter() - t0 >= budget_s or (max_steps and rows_done >= max_steps):
+            break
+    per_row = t_rows / rows_done
+    return per_row * w.batch * w.layers, rows_done
+
+
+# ------------------------------------------------------------------ main --
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cluster-size", type=int, default=int(os.environ.get("CF_CLUSTER_SIZE", 0)))
+    ap.add_argument("--batch-tile", type=int, default=int(os.environ.get("CF_BATCH_TILE", 0)))
+    ap.add_argument("--stage-bytes", type=int, default=int(os.environ.get("CF_STAGE_BYTES", 0)))
+    ap.add_argument("--ctas-per-sm", type=int, default=int(os.environ.get("CF_CTAS_PER_SM", 0)))
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    import torch
+
+    from attention_block_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch.distributed as dist
+    from attention_block_gb300 import binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or FALLBACK_L2_BYTES
+
+    # ---- inputs: R replicas (or the 32-layer chain), all resident in HBM
+    layer0 = synth.make_layer(w, seed=0, device=dev)
+    pos0 = layer0["positions"].tolist()
+    step_bytes = algorithmic_bytes(w, pos0) * w.layers
+    if w.layers > 1:
+        reps = [[layer0] + [synth.make_layer(w, seed=l, device=dev) for l in range(1, w.layers)]]
+    else:
+        n_rep = max(1, -(-4 * l2 // algorithmic_bytes(w, pos0)))
+        reps = [[layer0]] + [[synth.make_layer(w, seed=r, device=dev)] for r in range(1, n_rep)]
+    R = len(reps)
+    footprint = sum(sum(t.numel() * t.element_size() for t in L.values())
+                    for rep in reps for L in rep)
+    blk = binding.DecodeAttnBlock(
+        hidden=w.hidden, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
+        max_batch=w.batch, s_max=w.s_max, rope_theta=w.rope_theta, rms_eps=w.rms_eps,
+        dtype=w.dtype, cluster_size=args.cluster_size, batch_tile=args.batch_tile,
+        stage_bytes=args.stage_bytes, ctas_per_sm=args.ctas_per_sm)
+    info = blk.launch_info()
+    outs = [[torch.empty_like(L["hidden"]) for L in rep] for rep in reps]
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def run_step(r):
+        x = reps[r][0]["hidden"]
+        for l, L in enumerate(reps[r]):
+            blk(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"], L["v_cache"],
+                L["positions"], outs[r][l], stream)
+            x = outs[r][l]
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            run_step(i % R)
+    stream.synchronize()
+    st = blk.status()
+    if st != binding.CF_OK:
+        raise RuntimeError(f"device status after warm-up: {binding.strerror(st)}")
+
+    # ---- per-launch kernel durations (eager, CUDA events on the launch stream)
+    n_lat = min(args.steps, 4 * R if w.layers == 1 else 4)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_lat * w.layers)]
+    with torch.cuda.stream(stream):
+        k = 0
+        for i in range(n_lat):
+            r = i % R
+            x = reps[r][0]["hidden"]
+            for l, L in enumerate(reps[r]):
+                evs[k][0].record(stream)
+                blk(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"],
+                    L["v_cache"], L["positions"], outs[r][l], stream)
+                evs[k][1].record(stream)
+                x = outs[r][l]
+                k += 1
+    stream.synchronize()
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    launch_ms_avg = sum(launch_ms) / len(launch_ms)
+
+    # ---- the timed region: graph-captured steps (one graph per replica)
+    use_graph = not args.no_graph
+    graphs = []
+    if use_graph:
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                run_step(r)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                graphs[i % R].replay()
+        stream.synchronize()
+
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(args.steps):
+                if use_graph:
+                    graphs[i % R].replay()
+                else:
+                    run_step(i % R)
+            t_end.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    elapsed_s = t_start.elapsed_time(t_end) / 1e3
+    st = blk.status()
+    if st != binding.CF_OK:
+        raise RuntimeError(f"device status after timed steps: {binding.strerror(st)}")
+
+    # ---- end to end through the public API with host buffers
+    B, H = w.batch, w.hidden
+    h_in = [torch.empty_like(reps[r][0]["hidden"], device="cpu").pin_memory() for r in range(R)]
+    p_in = [torch.empty_like(reps[r][0]["positions"], device="cpu").pin_memory()
+            for r in range(R)]
+    for r in range(R):
+        h_in[r].copy_(reps[r][0]["hidden"])
+        p_in[r].copy_(reps[r][0]["positions"])
+    h_out = torch.empty_like(h_in[0]).pin_memory()
+    x_dev = [torch.empty_like(reps[r][0]["hidden"]) for r in range(R)]
+    p_dev = [torch.empty_like(reps[r][0]["positions"]) for r in range(R)]
+    e2e_steps = max(args.e2e_steps, 3)
+
+    def e2e_step(i):
+        r = i % R
+        x_dev[r].copy_(h_in[r], non_blocking=True)
+        p_dev[r].copy_(p_in[r], non_blocking=True)
+        x = x_dev[r]
+        for l, L in enumerate(reps[r]):
+            blk(B, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"], L["v_cache"],
+                p_dev[r], outs[r][l], stream)
+            x = outs[r][l]
+        h_out.copy_(outs[r][-1], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    h2d = B * H * h_in[0].element_size() + 4 * B
+    d2h = B * H * h_out.element_size()
+
+    # ---- whole-job aggregation (max time over ranks)
+    mine = [float(step_bytes * args.steps), elapsed_s, float(args.steps)]
+    mine_e2e = [float(step_bytes * e2e_steps), e2e_s, float(e2e_steps)]
+    rows = allgather_rows(mine + mine_e2e, world, dev)
+    per_rank = [r[:3] for r in rows]
+    per_rank_e2e = [r[3:] for r in rows]
+    agg = aggregate(per_rank)
+    agg_e2e = aggregate(per_rank_e2e)
+
+    if rank == 0:
+        peak, peak_kind = measured_peak_hbm()
+        per_launch_bytes = algorithmic_bytes(w, pos0)
+        achieved = per_launch_bytes / (launch_ms_avg / 1e3) / 1e9
+        us_step = elapsed_s / args.steps * 1e6
+        cpu = None
+        if world == 1:
+            lay_cpu = {k: v.cpu() for k, v in reps[0][0].items()}
+            t_cpu, rows = time_oracle(w, lay_cpu, args.cpu_budget)
+            cpu = {"value": step_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": 1,
+                   "kind": "oracle", "us_per_step": t_cpu * 1e6,
+                   "sample": (f"{rows} batch row(s) of layer 0 of this workload through the "
+                              f"float64 single-threaded C oracle; per-step time = per-row time "
+                              f"x {w.batch} rows x {w.layers} layer(s)"),
+                   "host_cpus": os.cpu_count()}
+        line = {
+            "metric": METRIC,
+            "value": round(agg["gbs"], 2),
+            "unit": "GB/s",
+            "us_per_step": round(us_step, 3),
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(elapsed_s / args.steps * 1e3, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": w.name, "hidden": w.hidden, "q_heads": w.n_q_heads,
+                "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "batch": w.batch,
+                "positions": w.positions, "layers_per_step": w.layers,
+                "storage_dtype": w.dtype, "accumulate": "f32",
+                "algorithmic_bytes_per_step": step_bytes,
+                "flops_per_step": flops_per_step(w, pos0) * w.layers,
+                "l2_defeat": (f"inputs larger than L2: {R} independently seeded replica(s) "
+                              f"rotated, {footprint / 1e9:.2f} GB resident vs L2 "
+                              f"{l2 / 1e6:.0f} MB"),
+                "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
+                "launch": info,
+            },
+            "roofline": {
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "traffic": recorded_traffic(w.name),
+                "kernel": KERNEL_NAME,
+                "launch_us_avg": round(launch_ms_avg * 1e3, 3),
+                "launch_us_min": round(min(launch_ms) * 1e3, 3),
+                "bytes_per_launch": per_launch_bytes,
+                "frac_of_nominal_7_9TBs": round(achieved / 7900.0, 4),
+            },
+            "e2e": {"value": round(agg_e2e["gbs"], 2), "unit": "GB/s",
+                    "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": args.steps * w.layers,
+            "clocks": clk.result(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    blk.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args, w, rank, world):
+    """The float64 oracle as the reference arm, on the host cores, rank 0 only."""
+    if rank != 0:
+        return 0
+    import torch
+
+    from attention_block_gb300 import synth
+
+    layer = synth.make_layer(w, seed=0, device="cpu")
+    pos = layer["positions"].tolist()
+    step_bytes = algorithmic_bytes(w, pos) * w.layers
+    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(w, layer, 0.0, max_steps=1)
+    times, rows_total = [], 0
+    for _ in range(args.steps):
+        t_step, rows = time_oracle(w, layer, budget)
+        times.append(t_step)
+        rows_total += rows
+    t = sum(times) / len(times)
+    val = step_bytes / t / 1e9
+    sample = (f"each step: batch rows of layer 0 through the float64 single-threaded C oracle "
+              f"for ~{budget:.1f} s; per-step time = per-row time x {w.batch} rows x "
+              f"{w.layers} layer(s); {rows_total} rows in total")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+        "us_per_step": round(t * 1e6, 1), "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "hidden": w.hidden, "q_heads": w.n_q_heads,
+                   "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "batch": w.batch,
+                   "positions": w.positions, "layers_per_step": w.layers,
+                   "storage_dtype": w.dtype, "algorithmic_bytes_per_step": step_bytes},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "host_cpus": os.cpu_count()},
+        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,50 @@
+/*
+ * cf_test.h -- test and measurement exports of the cluster collectives used
+ * inside the fused decode kernel.  Not part of the decode API.
+ *
+ * ClusterReduce [CF §3.1.1, Alg. 1] and ClusterGather [CF §3.1.2, Alg. 2] of
+ * "ClusterFusion框架深度解析：LLM推理优化的集群级通信革命" (devpress.csdn.net):
+ * butterfly rounds with partner = rank ^ stride over distributed shared
+ * memory.  Every call launches ONE thread-block cluster of `cluster_size`
+ * blocks (1, 2, 4, 8 or 16) on `stream` and returns without waiting.
+ *
+ * All buffers are device float arrays, row r belonging to cluster block r;
+ * n is a positive multiple of 4; errflag is a device int that receives bit 2
+ * if an in-kernel wait timed out (it is only ever OR-ed).
+ * Errors: CF_ERR_INVALID_ARG (sizes, NULLs, shared memory over 200 KB),
+ * CF_ERR_CLUSTER, CF_ERR_CUDA.
+ */
+#ifndef CF_TEST_H
+#define CF_TEST_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* All-reduce: in, out [cluster_size][n]; every out row = op over in rows
+ * (op 0 = sum, 1 = max).  All rows of out are bitwise identical. */
+int cf_test_cluster_allreduce(int cluster_size, int op, int n, const float* in, float* out,
+                              int* errflag, void* stream);
+
+/* Reduce-scatter: in [cluster_size][cluster_size*n] (row r holds block r's N
+ * slices of n floats); out [cluster_size][n]: out row r = sum over blocks of
+ * slice r. */
+int cf_test_cluster_reduce_scatter(int cluster_size, int n, const float* in, float* out,
+                                   int* errflag, void* stream);
+
+/* All-gather: in [cluster_size][n] (block r's slice); out
+ * [cluster_size][cluster_size*n]: every row = concatenation of all slices. */
+int cf_test_cluster_gather(int cluster_size, int n, const float* in, float* out, int* errflag,
+                           void* stream);
+
+/* Same collectives (kind 0 sum all-reduce, 1 max all-reduce, 2 reduce-scatter,
+ * 3 gather) with the SM cycles each block spent inside the collective written
+ * to cycles[cluster_size] (device long long).  Buffer shapes as above. */
+int cf_bench_cluster_collective(int kind, int cluster_size, int n, const float* in, float* out,
+                                int* errflag, long long* cycles, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CF_TEST_H */

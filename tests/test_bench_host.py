@@ -1,0 +1,71 @@
+"""Host logic of bench.py, no GPU: algorithmic bytes, clock parsing, the
+max-over-ranks aggregation, and the N>1 gather over a 2-rank gloo group."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from attention_block_gb300 import synth
+
+
+def test_algorithmic_bytes_llama2_layer():
+    # W_qkv 4096x12288 + W_o 4096x4096 + ln 4096 (fp16) + KV read 2x1024x32x128
+    # + KV write 2x32x128 (fp16) + hidden + out (fp16) + one int32 position.
+    w = synth.WORKLOADS[synth.LLAMA2_1K]
+    expect = (4096 * 12288 + 4096 * 4096 + 4096 + 2 * 1024 * 32 * 128 + 2 * 32 * 128
+              + 2 * 4096) * 2 + 4
+    assert bench.algorithmic_bytes(w, [1024]) == expect == 151_035_908
+
+
+def test_algorithmic_bytes_counts_each_rows_own_positions():
+    w = synth.WORKLOADS[synth.SMALL_HEAD_B64]
+    a = bench.algorithmic_bytes(w, [1024] * 64)
+    b = bench.algorithmic_bytes(w, [1024] * 63 + [2048])
+    assert b - a == 2 * 1024 * 32 * 64 * 2
+
+
+def test_parse_clocks():
+    lines = [
+        "0, 1965 MHz, 2070 MHz, 900.12 W, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1900 MHz, 2070 MHz, 1000.0 W, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 345 MHz, 2070 MHz, 120.0 W, 0x1, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+    ]
+    c = bench.parse_clocks(lines)
+    assert c["sm_max_mhz"] == 2070.0
+    assert c["sm_mhz"] == pytest.approx(1932.5)
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def test_aggregate_uses_slowest_rank():
+    agg = bench.aggregate([[100e9, 1.0, 10], [100e9, 2.0, 10]])
+    assert agg["seconds"] == 2.0 and agg["gbs"] == pytest.approx(100.0)
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rows = bench.allgather_rows([float(rank + 1) * 1e9, 1.0 + rank, 5.0], world, "cpu")
+    q.put((rank, rows, bench.aggregate(rows)))
+    dist.destroy_process_group()
+
+
+def test_two_rank_gather_and_aggregate_over_gloo():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, rows, agg in res:
+        assert rows == [[1e9, 1.0, 5.0], [2e9, 2.0, 5.0]]
+        assert agg["seconds"] == 2.0 and agg["gbs"] == pytest.approx(1.5)

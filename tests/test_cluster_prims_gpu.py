@@ -1,0 +1,88 @@
+"""GPU unit tests of the DSMEM collectives (ClusterReduce all-reduce and
+reduce-scatter forms, ClusterGather) through the test exports of libcf.so.
+
+Inputs are small integers stored as floats, so every sum is exact and the
+results are compared bit for bit with host-computed values.
+"""
+import pytest
+import torch
+
+from attention_block_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [1, 2, 4, 8, 16]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    binding.lib()
+
+
+def _ints(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(-1000, 1000, shape, generator=g).float().cuda()
+
+
+@pytest.mark.parametrize("N", SIZES)
+@pytest.mark.parametrize("n", [4, 132, 1024])
+def test_allreduce_sum_and_max(N, n):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = _ints((N, n), N * 1000 + n)
+    for op, ref in ((0, x.sum(0)), (1, x.max(0).values)):
+        out = torch.full_like(x, float("nan"))
+        assert binding.cf_test_cluster_allreduce(N, op, n, x, out, err) == binding.CF_OK
+        torch.cuda.synchronize()
+        for r in range(N):
+            assert torch.equal(out[r], ref), (N, n, op, r)
+    assert int(err.item()) == 0
+
+
+def test_allreduce_max_with_ties_and_negative_infinity():
+    N, n = 8, 8
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = torch.full((N, n), float("-inf"), device="cuda")
+    x[3, :4] = 5.0
+    x[6, :4] = 5.0
+    out = torch.empty_like(x)
+    assert binding.cf_test_cluster_allreduce(N, 1, n, x, out, err) == binding.CF_OK
+    torch.cuda.synchronize()
+    ref = x.max(0).values
+    for r in range(N):
+        assert torch.equal(out[r], ref)
+
+
+@pytest.mark.parametrize("N", SIZES)
+@pytest.mark.parametrize("n", [4, 96])
+def test_reduce_scatter(N, n):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = _ints((N, N * n), 7 * N + n)
+    out = torch.full((N, n), float("nan"), device="cuda")
+    assert binding.cf_test_cluster_reduce_scatter(N, n, x, out, err) == binding.CF_OK
+    torch.cuda.synchronize()
+    total = x.sum(0).view(N, n)
+    assert torch.equal(out, total)
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("N", SIZES)
+@pytest.mark.parametrize("n", [4, 48, 400])
+def test_gather(N, n):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = _ints((N, n), 11 * N + n)
+    out = torch.full((N, N * n), float("nan"), device="cuda")
+    assert binding.cf_test_cluster_gather(N, n, x, out, err) == binding.CF_OK
+    torch.cuda.synchronize()
+    for r in range(N):
+        assert torch.equal(out[r], x.reshape(-1))
+    assert int(err.item()) == 0
+
+
+def test_bad_arguments_rejected_without_launch():
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = torch.zeros(64, device="cuda")
+    assert binding.cf_test_cluster_allreduce(3, 0, 4, x, x, err) == binding.CF_ERR_INVALID_ARG
+    assert binding.cf_test_cluster_allreduce(2, 0, 6, x, x, err) == binding.CF_ERR_INVALID_ARG
+    assert binding.cf_test_cluster_gather(2, 4, None, x, err) == binding.CF_ERR_INVALID_ARG
