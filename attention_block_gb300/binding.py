@@ -30,7 +30,8 @@ class CfConfig(ctypes.Structure):
         "hidden", "n_q_heads", "n_kv_heads", "head_dim", "max_batch", "s_max")] + [
         ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)] + [
         (n, ctypes.c_int32) for n in (
-            "dtype", "cluster_size", "batch_tile", "stage_bytes", "ctas_per_sm")]
+            "dtype", "cluster_size", "batch_tile", "stage_bytes", "ctas_per_sm",
+            "prefetch_ahead", "prefetch_late", "pdl", "max_stages")]
 
 
 class CfLaunchInfo(ctypes.Structure):
@@ -67,7 +68,15 @@ SIGNATURES = {
     "cf_test_cluster_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp]),
     "cf_bench_cluster_collective": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    _vp, _vp, _vp, _vp, _vp]),
+    "cf_set_timeline": (ctypes.c_int, [_vp, _vp]),
+    "cf_bench_tma_stream": (ctypes.c_int, [ctypes.c_int] * 8 + [_vp, _vp, _vp]),
 }
+
+TIMELINE_SLOTS = 24
+TIMELINE_NAMES = ["start", "norm", "proj", "reduce_scatter", "gather", "attn", "merge", "sum",
+                  "oproj", "final", "prod_w", "prod_kv", "prod_all", "end", "proj_loop",
+                  "proj_loop_last_warp", "rinv", "attn_first_tile", "oproj_first_tile",
+                  "oproj_loop", "ticket"]
 
 
 def lib_path() -> str:
@@ -120,12 +129,14 @@ def strerror(code: int) -> str:
 
 def make_config(hidden, n_q_heads, n_kv_heads, head_dim, max_batch, s_max, rope_theta=1e4,
                 rms_eps=1e-6, dtype=CF_F16, cluster_size=0, batch_tile=0, stage_bytes=0,
-                ctas_per_sm=0) -> CfConfig:
+                ctas_per_sm=0, prefetch_ahead=0, prefetch_late=0, pdl=0,
+                max_stages=0) -> CfConfig:
     if isinstance(dtype, str):
         dtype = {"f32": CF_F32, "f16": CF_F16, "bf16": CF_BF16}[dtype]
     return CfConfig(int(hidden), int(n_q_heads), int(n_kv_heads), int(head_dim),
                     int(max_batch), int(s_max), float(rope_theta), float(rms_eps), int(dtype),
-                    int(cluster_size), int(batch_tile), int(stage_bytes), int(ctas_per_sm))
+                    int(cluster_size), int(batch_tile), int(stage_bytes), int(ctas_per_sm),
+                    int(prefetch_ahead), int(prefetch_late), int(pdl), int(max_stages))
 
 
 def cf_create(cfg: CfConfig) -> int:
@@ -164,6 +175,10 @@ def cf_get_launch_info(handle) -> dict:
     if rc != CF_OK:
         raise CfError(rc, "cf_get_launch_info")
     return {n: getattr(info, n) for n, _ in CfLaunchInfo._fields_}
+
+
+def cf_set_timeline(handle, stamps) -> int:
+    return lib().cf_set_timeline(handle, _ptr(stamps))
 
 
 def cf_strerror(code: int) -> str:

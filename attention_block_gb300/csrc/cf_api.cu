@@ -16,6 +16,7 @@
 #include "cf.h"
 #include "cf_params.h"
 #include "cf_registry.h"
+#include "cf_test.h"
 
 using namespace cf;
 
@@ -118,10 +119,13 @@ bool make_plan(const cf_config& c, int N, int BT, int stage_req, int ctas_per_sm
   pl.Rw = pow2_divisor(Hc, std::min(256, std::max(1, stage_req / (NSEG * D * es))));
   pl.Rt = std::min(256, pow2_floor(std::max(1, stage_req / (2 * D * es))));
   pl.Ro = pow2_divisor(G * D, std::min(256, std::max(1, stage_req / (pl.Co * es))));
-  const int item = std::max(NSEG * pl.Rw * D * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
+  int item = std::max(NSEG * pl.Rw * D * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
+  // A held stage also serves as the buffer of the projection's cross-warp
+  // tree (at least 4 slots of BT*NSEG*(D/32) floats per lane) and of the
+  // O projection's row-group partials ([RG][BT][Co] floats, RG*Co = 1024).
+  item = std::max(item, std::max(4 * BT * NSEG * (D / 32) * 32 * 4, 1024 * BT * 4));
   pl.stage_bytes = round_up(item, 1024);
 
-  const int MXP = (BT * G + 3) & ~3;
   const int SMP = BT * G * (D + 4);
   int off = 0;
   SmemLayout& L = pl.L;
@@ -133,11 +137,10 @@ bool make_plan(const cf_config& c, int N, int BT, int stage_req, int ctas_per_sm
   L.bars = take(BarIdx::count * 8);
   L.xn = take(BT * Hc * 4);
   L.red = take(N * SE * 4);
-  L.scratch = take(std::max(std::max((N - 1) * SE, kConsumerWarps * G * (D + 4)), BT * pl.Co) * 4);
+  L.scratch = take(std::max((N - 1) * SE, kConsumerWarps * G * (D + 4)) * 4);
   L.qkv = take(BT * NSEG * D * 4);
-  L.mx = take(MXP * 4 * (1 + nrounds));
   L.sm = take(SMP * 4 * (1 + nrounds));
-  L.mloc = take(MXP * 4);
+  L.scale = take(BT * G * 2 * 4);
   L.rope = take(BT * P * 2 * 4);
   L.misc = take((BT + 4 + BT + kConsumerWarps * BT) * 4);
   const int extras = round_up(off, 1024);
@@ -148,6 +151,7 @@ bool make_plan(const cf_config& c, int N, int BT, int stage_req, int ctas_per_sm
   budget -= 1024;  // alignment slack of the dynamic base
   int stages = (budget - extras) / pl.stage_bytes;
   stages = std::min(stages, kMaxStages);
+  if (c.max_stages > 0) stages = std::min(stages, c.max_stages);
   if (stages < 2) return false;
   pl.stages = stages;
   pl.ctas_per_sm = ctas_per_sm;
@@ -159,9 +163,8 @@ bool make_plan(const cf_config& c, int N, int BT, int stage_req, int ctas_per_sm
   L.red += ring;
   L.scratch += ring;
   L.qkv += ring;
-  L.mx += ring;
   L.sm += ring;
-  L.mloc += ring;
+  L.scale += ring;
   L.rope += ring;
   L.misc += ring;
   L.total = ring + extras + 1024;
@@ -181,7 +184,10 @@ struct cf_handle {
   int* counters = nullptr;
   int* errflag = nullptr;
   float* dbg = nullptr;
-  double inv_freq[64];
+  unsigned long long* timeline = nullptr;
+  int prefetch_ahead = 0, prefetch_late = 0;
+  bool pdl = true;
+  float turn_hi[64], turn_lo[64];  // RoPE turn rates as float pairs (see KParams)
   MapCache m_wqkv, m_wo, m_k, m_v;
 };
 
@@ -203,6 +209,11 @@ int validate_config(const cf_config* c) {
   if (c->stage_bytes != 0 && (c->stage_bytes < 2048 || c->stage_bytes > 131072))
     return CF_ERR_INVALID_ARG;
   if (c->ctas_per_sm < 0 || c->ctas_per_sm > 2) return CF_ERR_INVALID_ARG;
+  if (c->prefetch_ahead < -1 || c->prefetch_ahead > 64) return CF_ERR_INVALID_ARG;
+  if (c->prefetch_late < -1 || c->prefetch_late > 2) return CF_ERR_INVALID_ARG;
+  if (c->pdl < -1 || c->pdl > 1) return CF_ERR_INVALID_ARG;
+  if (c->max_stages < 0 || c->max_stages == 1 || c->max_stages > kMaxStages)
+    return CF_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return CF_ERR_UNSUPPORTED;
   if (N != 0 && N > c->head_dim / 4) return CF_ERR_INVALID_ARG;
   if (N != 0 && ((c->hidden / N) * esize(c->dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
@@ -341,8 +352,19 @@ int cf_create(const cf_config* cfg, cf_handle** out) {
   h->plan = pl;
   h->fn = ke->fn;
   h->max_active_clusters = nclusters;
-  for (int i = 0; i < 64; ++i)
-    h->inv_freq[i] = (i < D / 2) ? std::pow((double)c.rope_theta, -2.0 * i / (double)D) : 0.0;
+  // Both L2 prefetches measured slower on the B = 1 Llama2 layer (they compete
+  // with the W_qkv stream), so they are off unless asked for.
+  h->prefetch_ahead = std::max(0, c.prefetch_ahead);
+  h->prefetch_late = std::max(0, c.prefetch_late);
+  h->pdl = c.pdl != -1;
+  for (int i = 0; i < 64; ++i) {
+    // turns per position: theta^(-2i/d) / (2 pi), split into hi + lo floats
+    const double two_pi = 6.283185307179586476925286766559;
+    const double rate = (i < D / 2) ? std::pow((double)c.rope_theta, -2.0 * i / (double)D) / two_pi
+                                    : 0.0;
+    h->turn_hi[i] = (float)rate;
+    h->turn_lo[i] = (float)(rate - (double)h->turn_hi[i]);
+  }
 
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
   const size_t cnt_bytes = (size_t)((c.max_batch + BT - 1) / BT) * N * sizeof(int);
@@ -451,6 +473,9 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
   kp.counters = h->counters;
   kp.errflag = h->errflag;
   kp.dbg = h->dbg;
+  kp.timeline = h->timeline;
+  kp.prefetch_ahead = h->prefetch_ahead;
+  kp.prefetch_late = h->prefetch_late;
   kp.B = batch;
   kp.H = H;
   kp.nq = nq;
@@ -467,20 +492,28 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
   kp.eps = c.rms_eps;
   kp.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   kp.L = pl.L;
-  for (int i = 0; i < 64; ++i) kp.inv_freq[i] = h->inv_freq[i];
+  for (int i = 0; i < 64; ++i) {
+    kp.turn_hi[i] = h->turn_hi[i];
+    kp.turn_lo[i] = h->turn_lo[i];
+  }
 
   cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = pl.N;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: the kernel may be scheduled while the
+  // previous kernel on the stream drains; it waits for that kernel's
+  // completion (griddepcontrol.wait) before reading any global memory.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.gridDim = dim3(pl.N * nkv * kp.nbt, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = pl.L.total;
   lc.stream = static_cast<cudaStream_t>(stream);
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = h->pdl ? 2 : 1;
   void* args[] = {&kp};
   if (cudaLaunchKernelExC(&lc, h->fn, args) != cudaSuccess) {
     cudaGetLastError();
@@ -503,6 +536,12 @@ int cf_get_status(cf_handle* h) {
 int cf_set_debug(cf_handle* h, float* dbg) {
   if (h == nullptr) return CF_ERR_INVALID_ARG;
   h->dbg = dbg;
+  return CF_OK;
+}
+
+int cf_set_timeline(cf_handle* h, unsigned long long* stamps) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  h->timeline = stamps;
   return CF_OK;
 }
 

@@ -69,6 +69,43 @@ __device__ void cluster_allreduce(float* data, int n, float* rbuf, uint64_t* rba
   }
 }
 
+// ClusterReduce with the online-softmax combine ([CF §3.2] 在线softmax; the
+// page's ClusterReduce(max) followed by the rescaled ClusterReduce(sum), done
+// in one butterfly).  data holds nrec records [o(D) | m | l | 2 pad] of
+// partial attention states (m in log2 units, o unnormalized); afterwards every
+// block holds, per record, m = max_c m_c, l = sum_c l_c 2^(m_c - m) and
+// o = sum_c o_c 2^(m_c - m).  `scale` is 2*nrec floats of scratch.  Products
+// and sums are rounded one by one (no fused multiply-add), so both sides of
+// each exchange compute bit-identical records.
+template <int NT, int kBar>
+__device__ void cluster_allreduce_softmax(float* data, int nrec, int D, float* rbuf,
+                                          uint64_t* rbar, float* scale, int rank, int N,
+                                          int tid, int* err) {
+  const int W = D + 4, n = nrec * W;
+  int r = 0;
+  for (int s = 1; s < N; s <<= 1, ++r) {
+    float* rb = rbuf + r * n;
+    push_to_peer<NT>(data, rb, n, &rbar[r], rank ^ s, tid);
+    mbar_wait_cluster(&rbar[r], 0, err);
+    for (int i = tid; i < nrec; i += NT) {
+      const float ma = data[i * W + D], mb = rb[i * W + D];
+      const float mm = fmaxf(ma, mb);
+      scale[2 * i] = (mm == -INFINITY) ? 0.f : exp2f(ma - mm);
+      scale[2 * i + 1] = (mm == -INFINITY) ? 0.f : exp2f(mb - mm);
+    }
+    named_sync(kBar, NT);
+    for (int i = tid; i < n; i += NT) {
+      const int rec = i / W, e = i - rec * W;
+      if (e == D) {
+        data[i] = fmaxf(data[i], rb[i]);
+      } else if (e < D || e == D + 1) {
+        data[i] = __fadd_rn(__fmul_rn(data[i], scale[2 * rec]), __fmul_rn(rb[i], scale[2 * rec + 1]));
+      }
+    }
+    named_sync(kBar, NT);
+  }
+}
+
 // ClusterReduce, reduce-scatter form (recursive halving, sum): data holds N
 // slices of se floats; afterwards slice `rank` holds the cluster-wide sum of
 // that slice (other slices are left partially reduced).  rbuf holds the

@@ -137,6 +137,25 @@ __device__ __forceinline__ void kv_tile_range(int pos, int Rt, int rank, int N, 
   t1 = (int)(((long long)(rank + 1) * nt) / N);
 }
 
+// cos and sin of the RoPE angle pos * theta^(-2i/d) [LNA §三] without FP64
+// (GB300's double-precision path is slow and this sits between two cluster
+// exchanges).  The angle is reduced to a fraction of a turn exactly: the turn
+// rate c = theta^(-2i/d) / (2 pi) comes from the host (computed in float64)
+// as an unevaluated pair hi + lo of floats; pos < 2^24 is exact in fp32;
+// pos*hi is split into its rounded value and exact error with one FMA
+// (Dekker's two-product); subtracting the nearest integer is exact
+// (Sterbenz).  The remaining fraction t, |t| <= 1/2 + 2^-20, goes to
+// sincospif(2t) = (sin, cos)(2 pi t); the angle error stays below 1e-7 rad
+// for every pos < 2^24.
+__device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float& c, float& s) {
+  const float pf = (float)pos;
+  const float ph = pf * hi;
+  const float pe = fmaf(pf, hi, -ph);
+  const float fr = ph - rintf(ph);
+  const float t = fr + fmaf(pf, lo, pe);
+  sincospif(2.0f * t, &s, &c);
+}
+
 constexpr int kBarConsumers = 1;  // named barrier id of the 256 consumer threads
 
 template <typename T, int D, int G, int BT>
@@ -169,7 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
   const int Hc = p.H / N;               // K band rows == O-proj column band
   const int k0 = rank * Hc;
   const int nrounds = __ffs(N) - 1;
-  const int MXP = (BT * G + 3) & ~3;
   const int SMP = BT * G * (D + 4);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.L.bars);
@@ -180,15 +198,46 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
   float* red = reinterpret_cast<float*>(sm + p.L.red);
   float* scratch = reinterpret_cast<float*>(sm + p.L.scratch);
   float* qkv = reinterpret_cast<float*>(sm + p.L.qkv);
-  float* mx = reinterpret_cast<float*>(sm + p.L.mx);
   float* smx = reinterpret_cast<float*>(sm + p.L.sm);
-  float* mloc = reinterpret_cast<float*>(sm + p.L.mloc);
+  float* mscale = reinterpret_cast<float*>(sm + p.L.scale);
   float* rope = reinterpret_cast<float*>(sm + p.L.rope);
   int* s_pos = reinterpret_cast<int*>(sm + p.L.misc);
   int* s_flag = s_pos + BT;
   float* s_rinv = reinterpret_cast<float*>(s_flag + 4);
 
   // ---------------------------------------------------------------- setup --
+  // Programmatic dependent launch: let the next kernel in the stream start
+  // its own set-up as our blocks retire; it waits (griddepcontrol.wait
+  // below) for this grid to finish before it reads global memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    for (int r = 0; r < nrounds; ++r) {
+      mbar_init(&bars[BarIdx::rs + r], 1);
+      mbar_init(&bars[BarIdx::ga + r], 1);
+      mbar_init(&bars[BarIdx::sm + r], 1);
+    }
+    fence_mbar_init_cluster();
+    for (int r = 0; r < nrounds; ++r) {
+      mbar_arrive_expect_tx(&bars[BarIdx::rs + r], reduce_scatter_round_bytes(N, r, SE));
+      mbar_arrive_expect_tx(&bars[BarIdx::ga + r], gather_round_bytes(r, SE));
+      mbar_arrive_expect_tx(&bars[BarIdx::sm + r], allreduce_round_bytes(SMP));
+    }
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&p.tm_wqkv);
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+    prefetch_tensormap(&p.tm_wo);
+  }
+  __syncthreads();
+  cluster_sync_all();  // peers' barriers are initialized before any DSMEM traffic
+  // Everything above touched only shared memory; from here on global memory
+  // may hold a preceding kernel's results (e.g. the previous layer's out).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid < BT) {
     const int b = b0 + tid;
     int pos = -1;
@@ -201,33 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
     }
     s_pos[tid] = pos;
   }
-  if (tid == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    for (int r = 0; r < nrounds; ++r) {
-      mbar_init(&bars[BarIdx::rs + r], 1);
-      mbar_init(&bars[BarIdx::ga + r], 1);
-      mbar_init(&bars[BarIdx::mx + r], 1);
-      mbar_init(&bars[BarIdx::sm + r], 1);
-    }
-    fence_mbar_init_cluster();
-    for (int r = 0; r < nrounds; ++r) {
-      mbar_arrive_expect_tx(&bars[BarIdx::rs + r], reduce_scatter_round_bytes(N, r, SE));
-      mbar_arrive_expect_tx(&bars[BarIdx::ga + r], gather_round_bytes(r, SE));
-      mbar_arrive_expect_tx(&bars[BarIdx::mx + r], allreduce_round_bytes(MXP));
-      mbar_arrive_expect_tx(&bars[BarIdx::sm + r], allreduce_round_bytes(SMP));
-    }
-  }
-  if (warp == kConsumerWarps && lane == 0) {
-    prefetch_tensormap(&p.tm_wqkv);
-    prefetch_tensormap(&p.tm_k);
-    prefetch_tensormap(&p.tm_v);
-    prefetch_tensormap(&p.tm_wo);
-  }
   __syncthreads();
-  cluster_sync_all();  // peers' barriers are initialized before any DSMEM traffic
+  // Optional phase timeline (tuning aid): thread 0 stamps consumer phases,
+  // the producer lane its own milestones.
+  auto stamp = [&](int slot) {
+    if (p.timeline != nullptr && tid == 0)
+      p.timeline[blockIdx.x * kTimelineSlots + slot] = globaltimer_ns();
+  };
+  auto stamp_last_warp = [&](int slot) {  // latest over the consumer warps
+    if (p.timeline != nullptr && lane == 0)
+      atomicMax(&p.timeline[blockIdx.x * kTimelineSlots + slot], globaltimer_ns());
+  };
+  stamp(kTlStart);
 
   const int nkt = Hc / p.Rw;
   const int ncb = Hc / p.Co;
@@ -237,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
     // ============================================== TMA producer warp ====
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
       int it = 0;
       auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
         const int s = it % p.stages;
@@ -245,8 +280,31 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
         mbar_arrive_expect_tx(bar, bytes);
         return ring + (size_t)s * p.stage_bytes;
       };
+      // L2 prefetch of the K/V and W_o boxes this block will need after its
+      // cluster exchanges, so HBM streams them while the block is still in
+      // the projection (the later TMA loads then hit L2).
+      auto prefetch_late = [&]() {
+        for (int bb = 0; bb < BT; ++bb) {
+          int t0, t1;
+          kv_tile_range(s_pos[bb], p.Rt, rank, N, t0, t1);
+          for (int t = t0; t < t1; ++t) {
+            tma_prefetch_4d(&p.tm_k, 0, g, t * p.Rt, b0 + bb, pol_keep);
+            tma_prefetch_4d(&p.tm_v, 0, g, t * p.Rt, b0 + bb, pol_keep);
+          }
+        }
+        for (int cb = 0; cb < ncb; ++cb)
+          for (int rt = 0; rt < nrt; ++rt)
+            tma_prefetch_2d(&p.tm_wo, k0 + cb * p.Co, g * G * D + rt * p.Ro, pol_keep);
+      };
+      auto prefetch_w = [&](int kt) {
+        const int y = k0 + kt * p.Rw;
+        for (int j = 0; j < G; ++j) tma_prefetch_2d(&p.tm_wqkv, (g * G + j) * D, y, pol);
+        tma_prefetch_2d(&p.tm_wqkv, (p.nq + g) * D, y, pol);
+        tma_prefetch_2d(&p.tm_wqkv, (p.nq + p.nkv + g) * D, y, pol);
+      };
       // Phase 1: W_qkv row tiles of this block's K band, G+2 head slices each.
       const uint32_t seg_bytes = (uint32_t)(p.Rw * D * sizeof(T));
+      const int fill = min(p.stages, nkt);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         uint64_t* bar;
         uint8_t* dst = slot(NSEG * seg_bytes, bar);
@@ -255,7 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           tma_load_2d(dst + j * seg_bytes, &p.tm_wqkv, (g * G + j) * D, y, bar, pol);
         tma_load_2d(dst + G * seg_bytes, &p.tm_wqkv, (p.nq + g) * D, y, bar, pol);
         tma_load_2d(dst + (G + 1) * seg_bytes, &p.tm_wqkv, (p.nq + p.nkv + g) * D, y, bar, pol);
+        if (p.prefetch_ahead > 0) {
+          // keep a window of prefetch_ahead tiles beyond the ring in flight
+          if (kt == fill - 1)
+            for (int k2 = fill; k2 < min(nkt, fill + p.prefetch_ahead); ++k2) prefetch_w(k2);
+          else if (kt >= fill && kt + p.prefetch_ahead < nkt)
+            prefetch_w(kt + p.prefetch_ahead);
+        }
+        if (kt == fill - 1 && p.prefetch_late == 2) prefetch_late();
       }
+      // Default: queue the late prefetches behind the whole W_qkv stream, so
+      // they fill HBM's idle time during the cluster exchanges.
+      if (p.prefetch_late == 1) prefetch_late();
+      if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdW] = globaltimer_ns();
       // Phase 2: K and V tiles of this block's share of each row's positions.
       const uint32_t kv_bytes = (uint32_t)(p.Rt * D * sizeof(T));
       for (int bb = 0; bb < BT; ++bb) {
@@ -268,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           tma_load_4d(dst + kv_bytes, &p.tm_v, 0, g, t * p.Rt, b0 + bb, bar, pol);
         }
       }
+      if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdKV] = globaltimer_ns();
       // Phase 3: W_o tiles: rows of the group's heads x this block's column band.
       const uint32_t wo_bytes = (uint32_t)(p.Ro * p.Co * sizeof(T));
       for (int cb = 0; cb < ncb; ++cb)
@@ -276,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           uint8_t* dst = slot(wo_bytes, bar);
           tma_load_2d(dst, &p.tm_wo, k0 + cb * p.Co, g * G * D + rt * p.Ro, bar, pol);
         }
+      if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdAll] = globaltimer_ns();
     }
     __syncwarp();
   } else {
@@ -284,65 +356,53 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
     const T* __restrict__ lnw = reinterpret_cast<const T*>(p.ln_w);
     int it = 0;
 
-    // ---- Phase 0: RMSNorm of the tile's rows [LNA §三 stage 1] ----------
+    // ---- Phase 0: x * ln_weight over the own K band [LNA §三 stage 1] ----
+    // RMSNorm is n = x * g * r with one scalar r = 1/sqrt(mean(x^2) + eps)
+    // per row; r commutes with the projection, so it is applied to the
+    // partial sums after the W_qkv loop and the full-row reduction stays off
+    // the path to the first weight tile.
     for (int i = tid; i < N * SE; i += kConsumers) red[i] = 0.f;
-    for (int i = tid; i < MXP; i += kConsumers) mx[i] = 0.f;
     for (int i = tid; i < SMP; i += kConsumers) smx[i] = 0.f;
+    // One pass over each row: the sum of squares of the whole row (for r)
+    // and x*g for the 16-byte chunks inside the own K band.
+    float* wred = s_rinv + BT;  // [8 warps][BT] partial sums of squares
     {
       constexpr int EV = 16 / (int)sizeof(T);
-      float ss[BT];
 #pragma unroll
       for (int bb = 0; bb < BT; ++bb) {
-        ss[bb] = 0.f;
+        float ss = 0.f;
         if (b0 + bb < p.B) {
           const T* x = hidden + (size_t)(b0 + bb) * p.H;
           for (int i = tid * EV; i < p.H; i += kConsumers * EV) {
             float f[EV];
             load_cvt<T, EV>(x + i, f);
 #pragma unroll
-            for (int e = 0; e < EV; ++e) ss[bb] = fmaf(f[e], f[e], ss[bb]);
-          }
-        }
-        ss[bb] = warp_sum(ss[bb]);
-      }
-      // [8 warps][BT] partial sums; its own region, because `scratch` is the
-      // reduce-scatter receive area that peers may start writing at any time.
-      float* wred = s_rinv + BT;
-      if (lane == 0)
+            for (int e = 0; e < EV; ++e) ss = fmaf(f[e], f[e], ss);
+            if (i >= k0 && i < k0 + Hc) {
+              float gw[EV];
+              load_cvt<T, EV>(lnw + i, gw);
 #pragma unroll
-        for (int bb = 0; bb < BT; ++bb) wred[warp * BT + bb] = ss[bb];
-      named_sync(kBarConsumers, kConsumers);
-      if (tid < BT) {
-        float tot = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) tot += wred[w * BT + tid];
-        s_rinv[tid] = 1.0f / sqrtf(tot / (float)p.H + p.eps);
+              for (int e = 0; e < EV; ++e) xn[bb * Hc + (i - k0) + e] = f[e] * gw[e];
+            }
+          }
+        } else {
+          for (int i = tid; i < Hc; i += kConsumers) xn[bb * Hc + i] = 0.f;
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) wred[warp * BT + bb] = ss;
       }
-      // cos/sin of this block's RoPE pairs, in float64 then rounded [LNA §三]
+      // cos/sin of this block's own RoPE pairs
       for (int idx = tid; idx < BT * P; idx += kConsumers) {
         const int bb = idx / P, j = idx % P;
         const int pos = s_pos[bb];
-        float c = 1.f, s = 0.f;
-        if (pos >= 0) {
-          double sd, cd;
-          sincos((double)pos * p.inv_freq[rank * P + j], &sd, &cd);
-          c = (float)cd;
-          s = (float)sd;
-        }
+        float c = 1.f, sn = 0.f;
+        if (pos >= 0) rope_cos_sin(pos, p.turn_hi[rank * P + j], p.turn_lo[rank * P + j], c, sn);
         rope[2 * idx] = c;
-        rope[2 * idx + 1] = s;
+        rope[2 * idx + 1] = sn;
       }
-      named_sync(kBarConsumers, kConsumers);
-      for (int idx = tid; idx < BT * Hc; idx += kConsumers) {
-        const int bb = idx / Hc, i = idx % Hc;
-        float v = 0.f;
-        if (b0 + bb < p.B)
-          v = Elem<T>::to_f(hidden[(size_t)(b0 + bb) * p.H + k0 + i]) * s_rinv[bb] *
-              Elem<T>::to_f(lnw[k0 + i]);
-        xn[idx] = v;
-      }
-      named_sync(kBarConsumers, kConsumers);
     }
-
+    named_sync(kBarConsumers, kConsumers);
+    stamp(kTlNorm);
     // ---- Phase 1: merged QKV projection over this block's K band --------
     {
       float acc[BT][NSEG][CPL];
@@ -371,29 +431,81 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        // The last tile's stage is kept from the producer: it becomes the
+        // buffer of the cross-warp reduction below and is released after it.
+        if (lane == 0 && kt < nkt - 1) mbar_arrive(&empty[s]);
       }
-      // Sum the 8 warps' partials into the slice-ordered buffer: column i of
-      // a segment belongs to slice c = (i mod d/2) / P, so each RoPE pair
-      // (i, i + d/2) stays inside one slice.
+      stamp(kTlProjLoop);
+      stamp_last_warp(kTlProjLoopLast);
+      // RMSNorm scale r = 1/sqrt(mean(x^2) + eps) of each row from the warp
+      // partials of phase 0 (warp shuffles, then one cross-warp step [LNA §五]).
+      if (tid < BT) {
+        float tot = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) tot += wred[w * BT + tid];
+        s_rinv[tid] = (b0 + tid < p.B) ? 1.0f / sqrtf(tot / (float)p.H + p.eps) : 0.f;
+      }
+      // Tree sum of the 8 warps' partials (8 -> 4 -> 2 -> 1) through the held
+      // stage, [slot][value][lane] so every access is conflict-free; no
+      // atomics, and the summation order is fixed.
+      {
+        const int s_last = (it - 1) % p.stages;
+        float* tb = reinterpret_cast<float*>(ring + (size_t)s_last * p.stage_bytes);
+        constexpr int PW = BT * NSEG * CPL;
+        const bool disjoint = 7 * PW * 32 * 4 <= p.stage_bytes;  // one region per step
+        int base = 0;
+        named_sync(kBarConsumers, kConsumers);  // every warp is done reading the tile
+        for (int half = kConsumerWarps / 2; half >= 1; half >>= 1) {
+          if (warp >= half && warp < 2 * half) {
+            float* dst = tb + (base + warp - half) * PW * 32 + lane;
 #pragma unroll
-      for (int sg = 0; sg < NSEG; ++sg)
+            for (int bb = 0; bb < BT; ++bb)
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-          const int col = lane * CPL + e;
-          const int hi = col / (D / 2), il = col % (D / 2);
-          const int c = il / P, j = il % P;
+              for (int sg = 0; sg < NSEG; ++sg)
 #pragma unroll
-          for (int bb = 0; bb < BT; ++bb)
-            atomicAdd(&red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j], acc[bb][sg][e]);
+                for (int e = 0; e < CPL; ++e) dst[((bb * NSEG + sg) * CPL + e) * 32] = acc[bb][sg][e];
+          }
+          named_sync(kBarConsumers, kConsumers);
+          if (warp < half) {
+            const float* src = tb + (base + warp) * PW * 32 + lane;
+#pragma unroll
+            for (int bb = 0; bb < BT; ++bb)
+#pragma unroll
+              for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+                for (int e = 0; e < CPL; ++e) acc[bb][sg][e] += src[((bb * NSEG + sg) * CPL + e) * 32];
+          }
+          if (disjoint) base += half;
+          else named_sync(kBarConsumers, kConsumers);
         }
-      named_sync(kBarConsumers, kConsumers);
+        // Warp 0 holds the block's partial sums: scale by r and store them
+        // slice-ordered -- column i of a segment belongs to slice
+        // c = (i mod d/2) / P, so each RoPE pair (i, i + d/2) stays in one slice.
+        if (warp == 0) {
+#pragma unroll
+          for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) {
+              const int col = lane * CPL + e;
+              const int hi = col / (D / 2), il = col % (D / 2);
+              const int c = il / P, j = il % P;
+#pragma unroll
+              for (int bb = 0; bb < BT; ++bb)
+                red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j] = acc[bb][sg][e] * s_rinv[bb];
+            }
+        }
+        fence_proxy_async_smem();  // our stores into the stage precede the next TMA write
+        named_sync(kBarConsumers, kConsumers);
+        if (lane == 0) mbar_arrive(&empty[s_last]);  // hand the stage back
+      }
+      stamp(kTlRinv);
     }
 
+    stamp(kTlProj);
     // ---- ClusterReduce (reduce-scatter): block `rank` owns slice `rank` --
     cluster_reduce_scatter<kConsumers, kBarConsumers>(red, SE, scratch, &bars[BarIdx::rs], rank,
                                                       N, tid, p.errflag);
 
+    stamp(kTlReduceScatter);
     // ---- RoPE on the own slice, then append K/V [LNA §三 stage 3] -------
     {
       float* my = red + rank * SE;
@@ -414,10 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           a = ra;
           bv = rb;
         }
-        if (sg >= G) {  // key and value: round to storage and append
+        if (sg >= G) {  // key and value: append (rounded to storage); the
+                        // attention below keeps using the fp32 on-chip values
           const T ta = Elem<T>::from_f(a), tb = Elem<T>::from_f(bv);
-          a = Elem<T>::to_f(ta);
-          bv = Elem<T>::to_f(tb);
           T* cache = (sg == G) ? kc : vc;
           const size_t base = (((size_t)(b0 + bb) * p.S + pos) * p.nkv + g) * D;
           cache[base + rank * P + j] = ta;
@@ -454,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
       }
     }
 
+    stamp(kTlGather);
     // ---- Phase 2: split-KV online-softmax attention [CF §3.2] ------------
     {
       const int grp = lane / LPP, kl = lane % LPP;
@@ -511,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
         for (int t = t0; t < t1; ++t, ++it) {
           const int s = it % p.stages;
           mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+          if (bb == 0 && t == t0) stamp(kTlAttnFirst);
           const T* Kt = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
           const T* Vt = Kt + (size_t)p.Rt * D;
           const int lim = min(p.Rt, pos - t * p.Rt);  // cached positions < pos only
@@ -611,36 +724,30 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           float* dst = smx + (bb * G + h) * (D + 4);
           dst[dim] = O;
           if (dim == 0) {
-            dst[D] = L;
-            mx[bb * G + h] = M;
-            mloc[bb * G + h] = M;
+            dst[D] = M;
+            dst[D + 1] = L;
           }
         }
         named_sync(kBarConsumers, kConsumers);
       }
     }
 
-    // ---- ClusterReduce(max), rescale, ClusterReduce(sum) [CF §3.1.1] -----
-    cluster_allreduce<OpMax, kConsumers, kBarConsumers>(mx, MXP, mx + MXP, &bars[BarIdx::mx],
-                                                        rank, N, tid, p.errflag);
-    for (int idx = tid; idx < BT * G * (D + 4); idx += kConsumers) {
-      const int row = idx / (D + 4);
-      const float ml = mloc[row];
-      smx[idx] *= (ml == -INFINITY) ? 0.f : exp2f(ml - mx[row]);
-    }
-    named_sync(kBarConsumers, kConsumers);
-    cluster_allreduce<OpSum, kConsumers, kBarConsumers>(smx, SMP, smx + SMP, &bars[BarIdx::sm],
-                                                        rank, N, tid, p.errflag);
+    stamp(kTlAttn);
+    // ---- ClusterReduce of the softmax partials [CF §3.1.1, §3.2]: max of
+    // the statistics and the rescaled sum of (o, l) in one butterfly ---------
+    cluster_allreduce_softmax<kConsumers, kBarConsumers>(smx, BT * G, D, smx + SMP,
+                                                         &bars[BarIdx::sm], mscale, rank, N, tid,
+                                                         p.errflag);
+    stamp(kTlMax);
     // Final attention output o = (sum o_c e^{m_c-m}) / (sum l_c e^{m_c-m}),
     // written over the (no longer needed) q' of the same head.
     for (int idx = tid; idx < BT * G * D; idx += kConsumers) {
       const int bb = idx / (G * D), rem = idx % (G * D);
       const int h = rem / D, dim = rem % D;
       const float* src = smx + (bb * G + h) * (D + 4);
-      const float L = src[D];
+      const float L = src[D + 1];
       qkv[(bb * NSEG + h) * D + dim] = (L > 0.f) ? src[dim] / L : 0.f;
     }
-    for (int i = tid; i < BT * p.Co; i += kConsumers) scratch[i] = 0.f;
     named_sync(kBarConsumers, kConsumers);
     if (p.dbg != nullptr && rank == 0) {
       float* dob = p.dbg + (size_t)p.B * (p.nq + 2 * p.nkv) * D;
@@ -653,12 +760,12 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
       }
     }
 
+    stamp(kTlSum);
     // ---- Phase 3: O projection of this block's column band [CF §3.2] -----
     {
       const int CQ = p.Co / 4;
       const int RG = kConsumers / CQ;
       const int colq = tid % CQ, rg = tid / CQ;
-      float* ob = scratch;  // [BT][Co]
       for (int cb = 0; cb < ncb; ++cb) {
         float a[BT][4];
 #pragma unroll
@@ -668,6 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
         for (int rt = 0; rt < nrt; ++rt, ++it) {
           const int s = it % p.stages;
           mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+          if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
           const T* W = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
           if (rg < RG) {
             for (int r = rg; r < p.Ro; r += RG) {
@@ -684,28 +792,45 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
+          // the box's last tile stage is held for the row-group reduction
+          if (lane == 0 && rt < nrt - 1) mbar_arrive(&empty[s]);
         }
+        if (cb == ncb - 1) stamp(kTlOprojLoop);
+        // Row-group partials [RG][BT][Co] into the held stage, then each
+        // float4 of the box summed over the groups in a fixed order and added
+        // to the accumulator with one vector atomic.
+        const int s_last = (it - 1) % p.stages;
+        float* pb = reinterpret_cast<float*>(ring + (size_t)s_last * p.stage_bytes);
+        named_sync(kBarConsumers, kConsumers);  // every warp is done reading the tile
         if (rg < RG)
 #pragma unroll
           for (int bb = 0; bb < BT; ++bb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) atomicAdd(&ob[bb * p.Co + colq * 4 + e], a[bb][e]);
+            *reinterpret_cast<float4*>(pb + ((size_t)rg * BT + bb) * p.Co + colq * 4) =
+                make_float4(a[bb][0], a[bb][1], a[bb][2], a[bb][3]);
         named_sync(kBarConsumers, kConsumers);
         for (int i4 = tid; i4 < BT * CQ; i4 += kConsumers) {
           const int bb = i4 / CQ, cq = i4 % CQ;
-          float4* src = reinterpret_cast<float4*>(ob) + i4;
-          const float4 v = *src;
-          *src = make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int gq = 0; gq < RG; ++gq) {
+            const float4 u =
+                *reinterpret_cast<const float4*>(pb + ((size_t)gq * BT + bb) * p.Co + cq * 4);
+            v.x += u.x;
+            v.y += u.y;
+            v.z += u.z;
+            v.w += u.w;
+          }
           const int b = b0 + bb;
           if (b < p.B && s_pos[bb] >= 0)
             atomicAdd(reinterpret_cast<float4*>(p.acc + (size_t)b * p.H + k0 + cb * p.Co + cq * 4),
                       v);
         }
+        fence_proxy_async_smem();  // our stores into the stage precede the next TMA write
         named_sync(kBarConsumers, kConsumers);
+        if (lane == 0) mbar_arrive(&empty[s_last]);
       }
     }
 
+    stamp(kTlOproj);
     // ---- Residual + finalize by the last block of each (tile, band) ------
     __threadfence();
     named_sync(kBarConsumers, kConsumers);
@@ -716,6 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
       s_flag[0] = last;
     }
     named_sync(kBarConsumers, kConsumers);
+    stamp(kTlTicket);
     if (s_flag[0]) {
       T* out = reinterpret_cast<T*>(p.out);
       float* dproj = p.dbg ? p.dbg + (size_t)p.B * (2 * p.nq + 2 * p.nkv) * D : nullptr;
@@ -742,9 +868,11 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
     }
   }
 
+  stamp(kTlFinal);
   // No block leaves while a peer may still write into its shared memory.
   __syncwarp();
   cluster_sync_all();
+  stamp(kTlEnd);
 }
 
 }  // namespace cf

@@ -18,6 +18,32 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxRounds = 4;                     // log2(kMaxCluster)
 constexpr int kMaxStages = 32;
 
+// Phase stamps of the optional timeline (one row of kTimelineSlots per block).
+enum TimelineSlot {
+  kTlStart = 0,       // after the start-up cluster barrier
+  kTlNorm = 1,        // RMSNorm done
+  kTlProj = 2,        // last W_qkv tile consumed and partials summed
+  kTlReduceScatter = 3,
+  kTlGather = 4,
+  kTlAttn = 5,        // all rows' attention partials merged inside the block
+  kTlMax = 6,
+  kTlSum = 7,         // final o available
+  kTlOproj = 8,
+  kTlFinal = 9,
+  kTlProdW = 10,      // producer: last W_qkv tile issued
+  kTlProdKV = 11,     // producer: last K/V tile issued
+  kTlProdAll = 12,    // producer: last W_o tile issued
+  kTlEnd = 13,
+  kTlProjLoop = 14,   // last W_qkv tile consumed by warp 0 (before the norm scale)
+  kTlProjLoopLast = 15,  // same, slowest consumer warp (atomic max)
+  kTlRinv = 16,       // norm scale ready
+  kTlAttnFirst = 17,  // first K/V tile in hand
+  kTlOprojFirst = 18, // first W_o tile in hand
+  kTlOprojLoop = 19,  // last W_o tile consumed
+  kTlTicket = 20,     // accumulator fence + ticket done
+  kTimelineSlots = 24
+};
+
 // Byte offsets of the shared-memory regions (from a 1024-aligned base).
 struct SmemLayout {
   int ring;      // stages * stage_bytes       TMA ring
@@ -26,9 +52,8 @@ struct SmemLayout {
   int red;       // [N][SE] f32                projection partials / gathered slices
   int scratch;   // reduce-scatter receive buffers, later warp states, later O-proj buffer
   int qkv;       // [BT][NSEG][D] f32          full q', k', v (q' reused for o)
-  int mx;        // [MXP] f32 + log2N receive  softmax max statistics
-  int sm;        // [SMP] f32 + log2N receive  rescaled (o, l) partials
-  int mloc;      // [MXP] f32                  local max copy
+  int sm;        // [BT*G][D+4] f32 + log2N receive: partial (o, m, l) records
+  int scale;     // [BT*G][2] f32              combine factors of one round
   int rope;      // [BT][P][2] f32             cos/sin of own pairs
   int misc;      // positions [BT] i32, flags [4] i32, rinv [BT] f32, RMS partials [8][BT] f32
   int total;     // bytes incl. 1024 alignment slack
@@ -40,8 +65,7 @@ struct BarIdx {
   static constexpr int empty = kMaxStages;             // [kMaxStages]
   static constexpr int rs = 2 * kMaxStages;            // [kMaxRounds] reduce-scatter
   static constexpr int ga = rs + kMaxRounds;           // [kMaxRounds] gather
-  static constexpr int mx = ga + kMaxRounds;           // [kMaxRounds] max all-reduce
-  static constexpr int sm = mx + kMaxRounds;           // [kMaxRounds] sum all-reduce
+  static constexpr int sm = ga + kMaxRounds;           // [kMaxRounds] softmax-merge all-reduce
   static constexpr int count = sm + kMaxRounds;
 };
 
@@ -60,6 +84,10 @@ struct KParams {  // 128-byte aligned through its CUtensorMap members
   int* counters;         // [nbt * N] completion counters, zero between launches
   int* errflag;          // device error bits
   float* dbg;            // optional intermediate dump (NULL = off)
+  unsigned long long* timeline;  // optional [grid][kTimelineSlots] globaltimer stamps (NULL = off)
+  int prefetch_ahead;    // W_qkv tiles prefetched into L2 ahead of the ring (0 = off)
+  int prefetch_late;     // L2 prefetch of the block's K/V and W_o boxes: 0 off,
+                         // 1 after the last W_qkv tile is issued, 2 at the start
   int B, H, nq, nkv, S;
   int N;                 // cluster size
   int nbt;               // batch tiles
@@ -68,7 +96,8 @@ struct KParams {  // 128-byte aligned through its CUtensorMap members
   float eps;
   float qk_scale_log2;   // log2(e) / sqrt(D)
   SmemLayout L;
-  double inv_freq[64];   // theta^(-2i/D), i < D/2, computed in float64
+  float turn_hi[64];     // RoPE turn rate theta^(-2i/D) / (2 pi), i < D/2, as an
+  float turn_lo[64];     // unevaluated float pair hi + lo computed in float64
 };
 
 }  // namespace cf

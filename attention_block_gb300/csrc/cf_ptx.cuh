@@ -123,6 +123,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   return mbar_wait_slow<true>(a, parity, errflag);
 }
 
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------ TMA loads --
 // Tiled tensor copies global -> this CTA's shared memory, completing on `bar`
 // with complete_tx of the box's byte count.  The innermost coordinate x is
@@ -147,10 +153,40 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm,
       : "memory");
 }
 
+// L2-only prefetch of one tensor box (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(tm),
+      "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* tm, int x, int y, int z, int w,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3, %4}], %5;" ::"l"(
+          tm),
+      "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {

@@ -130,20 +130,29 @@ class ClockSampler:
         self.lines = []
 
     def __enter__(self):
+        self.stamped = []      # (host time, line)
+        self.window = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader", "-lms", "100"],
+                 "--format=csv,noheader", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.stamped and time.time() - t0 < 10.0:
+                time.sleep(0.01)  # first sample in hand before timing starts
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln)
+            self.stamped.append((time.time(), ln))
+
+    def mark(self, t_begin: float, t_end: float):
+        """Host times bracketing the timed region."""
+        self.window = (t_begin, t_end)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -156,7 +165,21 @@ class ClockSampler:
         return False
 
     def result(self):
-        return parse_clocks(self.lines)
+        """Samples inside the timed window; if the window is shorter than the
+        sampling period, the samples just before and after it (flagged)."""
+        if self.window is None:
+            return parse_clocks([ln for _, ln in self.stamped])
+        a, b = self.window
+        inside = [ln for t, ln in self.stamped if a <= t <= b]
+        if inside:
+            res = parse_clocks(inside)
+            res["window"] = "timed region"
+            return res
+        before = [ln for t, ln in self.stamped if t < a][-2:]
+        after = [ln for t, ln in self.stamped if t > b][:2]
+        res = parse_clocks(before + after)
+        res["window"] = "samples bracketing a timed region shorter than the sampling period"
+        return res
 
 
 def allgather_rows(mine, world: int, device):
@@ -177,6 +200,50 @@ def aggregate(per_rank):
     tot_bytes = sum(r[0] for r in per_rank)
     t = max(r[1] for r in per_rank)
     return {"gbs": tot_bytes / t / 1e9, "seconds": t}
+
+
+def phase_timeline(blk, binding, w, reps, outs, stream, dev, info, R, launches=4):
+    """Per-phase block stamps of a few eager launches: for each phase the
+    median and max over blocks of (stamp - earliest block start), in us."""
+    import torch
+    grid = info["cluster_size"] * w.n_kv_heads * (-(-w.batch // info["batch_tile"]))
+    bufs = [torch.zeros(grid * binding.TIMELINE_SLOTS, dtype=torch.int64, device=dev)
+            for _ in range(launches)]
+    per = {n: [] for n in binding.TIMELINE_NAMES}
+    gaps = []
+    try:
+        # back-to-back launches (no host sync in between), one stamp buffer each
+        with torch.cuda.stream(stream):
+            for i in range(launches):
+                r = i % R
+                L = reps[r][0]
+                binding.cf_set_timeline(blk.handle, bufs[i])
+                blk(w.batch, L["hidden"], L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"],
+                    L["v_cache"], L["positions"], outs[r][0], stream)
+        stream.synchronize()
+    finally:
+        binding.cf_set_timeline(blk.handle, None)
+    prev_end = None
+    for buf in bufs:
+        st = buf.view(grid, binding.TIMELINE_SLOTS)[:, :len(binding.TIMELINE_NAMES)]
+        st = st.cpu().double()
+        t0 = st[:, 0].min()
+        if prev_end is not None:
+            gaps.append(float(t0 - prev_end) / 1e3)
+        prev_end = st[:, binding.TIMELINE_NAMES.index("end")].max()
+        for j, n in enumerate(binding.TIMELINE_NAMES):
+            col = st[:, j]
+            col = col[col > 0]
+            if len(col):
+                rel = (col - t0) / 1e3
+                per[n].append((float(rel.median()), float(rel.max())))
+    res = {n: {"median": round(statistics.median(v[0] for v in vals), 2),
+               "max": round(statistics.median(v[1] for v in vals), 2)}
+           for n, vals in per.items() if vals}
+    if gaps:
+        res["gap_to_next_launch"] = {"median": round(statistics.median(gaps), 2),
+                                     "max": round(max(gaps), 2)}
+    return res
 
 
 # ---------------------------------------------------------------- oracle --
@@ -212,14 +279,22 @@ def time_oracle(w, layer_cpu, budget_s: float, max_steps: int | None = None):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cluster-size", type=int, default=int(os.environ.get("CF_CLUSTER_SIZE", 0)))
     ap.add_argument("--batch-tile", type=int, default=int(os.environ.get("CF_BATCH_TILE", 0)))
     ap.add_argument("--stage-bytes", type=int, default=int(os.environ.get("CF_STAGE_BYTES", 0)))
     ap.add_argument("--ctas-per-sm", type=int, default=int(os.environ.get("CF_CTAS_PER_SM", 0)))
+    ap.add_argument("--prefetch-ahead", type=int,
+                    default=int(os.environ.get("CF_PREFETCH_AHEAD", 0)))
+    ap.add_argument("--prefetch-late", type=int, default=int(os.environ.get("CF_PREFETCH_LATE", 0)))
+    ap.add_argument("--max-stages", type=int, default=int(os.environ.get("CF_MAX_STAGES", 0)))
+    ap.add_argument("--pdl", type=int, default=int(os.environ.get("CF_PDL", 0)),
+                    help="programmatic dependent launch: 0 default (on), -1 off")
+    ap.add_argument("--timeline", action="store_true",
+                    help="add per-phase block timings (globaltimer) of a few launches")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -266,7 +341,9 @@ def main(argv=None):
         hidden=w.hidden, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
         max_batch=w.batch, s_max=w.s_max, rope_theta=w.rope_theta, rms_eps=w.rms_eps,
         dtype=w.dtype, cluster_size=args.cluster_size, batch_tile=args.batch_tile,
-        stage_bytes=args.stage_bytes, ctas_per_sm=args.ctas_per_sm)
+        stage_bytes=args.stage_bytes, ctas_per_sm=args.ctas_per_sm,
+        prefetch_ahead=args.prefetch_ahead, prefetch_late=args.prefetch_late, pdl=args.pdl,
+        max_stages=args.max_stages)
     info = blk.launch_info()
     outs = [[torch.empty_like(L["hidden"]) for L in rep] for rep in reps]
 
@@ -307,18 +384,29 @@ def main(argv=None):
     launch_ms = [a.elapsed_time(b) for a, b in evs]
     launch_ms_avg = sum(launch_ms) / len(launch_ms)
 
-    # ---- the timed region: graph-captured steps (one graph per replica)
+    timeline = None
+    if args.timeline:
+        timeline = phase_timeline(blk, binding, w, reps, outs, stream, dev, info, R)
+
+    # ---- the timed region: graph-captured steps.  One graph holds all R
+    # replica steps back to back (so consecutive kernels can overlap their
+    # launch through programmatic dependent launch); one-step graphs cover a
+    # step count that is not a multiple of R.
     use_graph = not args.no_graph
-    graphs = []
+    single, full = [], None
     if use_graph:
         for r in range(R):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 run_step(r)
-            graphs.append(g)
+            single.append(g)
+        full = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(full, stream=stream):
+            for r in range(R):
+                run_step(r)
         with torch.cuda.stream(stream):
-            for i in range(args.warmup):
-                graphs[i % R].replay()
+            for i in range(-(-args.warmup // R)):
+                full.replay()
         stream.synchronize()
 
     t_start = torch.cuda.Event(enable_timing=True)
@@ -327,15 +415,20 @@ def main(argv=None):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        h0 = time.time()
         with torch.cuda.stream(stream):
             t_start.record(stream)
-            for i in range(args.steps):
-                if use_graph:
-                    graphs[i % R].replay()
-                else:
+            if use_graph:
+                for _ in range(args.steps // R):
+                    full.replay()
+                for r in range(args.steps % R):
+                    single[r].replay()
+            else:
+                for i in range(args.steps):
                     run_step(i % R)
             t_end.record(stream)
         stream.synchronize()
+        clk.mark(h0, time.time())
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -451,6 +544,7 @@ def main(argv=None):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
             "gpu_launches": args.steps * w.layers,
+            **({"timeline_us": timeline} if timeline else {}),
             "clocks": clk.result(),
             "cpu_baseline": cpu,
         }

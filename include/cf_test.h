@@ -43,6 +43,27 @@ int cf_test_cluster_gather(int cluster_size, int n, const float* in, float* out,
 int cf_bench_cluster_collective(int kind, int cluster_size, int n, const float* in, float* out,
                                 int* errflag, long long* cycles, void* stream);
 
+/* Bare TMA streaming rate of the decode kernel's W_qkv access pattern: one
+ * launch of cluster_size * n_kv_heads blocks (no cluster attribute; any
+ * cluster_size dividing hidden), each streaming its K band of the three
+ * head_dim-wide column slices of head g of the fp16 matrix w [hidden,
+ * (nq+2nkv)*head_dim] in tiles of rows_per_tile rows through `stages`
+ * shared-memory stages, with shared memory padded so that ctas_per_sm blocks
+ * fit per SM.  No compute.  Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
+int cf_bench_tma_stream(int hidden, int n_q_heads, int n_kv_heads, int head_dim,
+                        int cluster_size, int rows_per_tile, int stages, int ctas_per_sm,
+                        const void* w, int* errflag, void* stream);
+
+/* Phase timeline of later cf_decode_attn_block calls of handle h (a tuning
+ * aid): when `stamps` is a device buffer of grid_blocks * 16 unsigned 64-bit
+ * values, every block writes %globaltimer (ns) at its phase boundaries (slot
+ * order: start, norm, proj, reduce-scatter, gather, attention, max, sum,
+ * o-proj, final, producer-W, producer-KV, producer-all, end).  The grid has
+ * cluster_size * n_kv_heads * ceil(batch / batch_tile) blocks.  NULL turns it
+ * off.  Returns CF_OK or CF_ERR_INVALID_ARG. */
+struct cf_handle;
+int cf_set_timeline(struct cf_handle* h, unsigned long long* stamps);
+
 #ifdef __cplusplus
 }
 #endif
