@@ -72,11 +72,12 @@ SIGNATURES = {
     "cf_bench_tma_stream": (ctypes.c_int, [ctypes.c_int] * 8 + [_vp, _vp, _vp]),
 }
 
-TIMELINE_SLOTS = 24
+TIMELINE_SLOTS = 32
 TIMELINE_NAMES = ["start", "norm", "proj", "reduce_scatter", "gather", "attn", "merge", "sum",
                   "oproj", "final", "prod_w", "prod_kv", "prod_all", "end", "proj_loop",
                   "proj_loop_last_warp", "rinv", "attn_first_tile", "oproj_first_tile",
-                  "oproj_loop", "ticket"]
+                  "oproj_loop", "ticket", "oproj_tile1", "oproj_tile2", "oproj_tile3",
+                  "attn_loop", "attn_warps"]
 
 
 def lib_path() -> str:

@@ -122,8 +122,9 @@ bool make_plan(const cf_config& c, int N, int BT, int stage_req, int ctas_per_sm
   int item = std::max(NSEG * pl.Rw * D * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
   // A held stage also serves as the buffer of the projection's cross-warp
   // tree (at least 4 slots of BT*NSEG*(D/32) floats per lane) and of the
-  // O projection's row-group partials ([RG][BT][Co] floats, RG*Co = 1024).
-  item = std::max(item, std::max(4 * BT * NSEG * (D / 32) * 32 * 4, 1024 * BT * 4));
+  // O projection's row-group partials ([RG][BT][Co] floats, RG*Co = 256 *
+  // (16 / element size)).
+  item = std::max(item, std::max(4 * BT * NSEG * (D / 32) * 32 * 4, 256 * (16 / es) * BT * 4));
   pl.stage_bytes = round_up(item, 1024);
 
   const int SMP = BT * G * (D + 4);
@@ -210,7 +211,7 @@ int validate_config(const cf_config* c) {
     return CF_ERR_INVALID_ARG;
   if (c->ctas_per_sm < 0 || c->ctas_per_sm > 2) return CF_ERR_INVALID_ARG;
   if (c->prefetch_ahead < -1 || c->prefetch_ahead > 64) return CF_ERR_INVALID_ARG;
-  if (c->prefetch_late < -1 || c->prefetch_late > 2) return CF_ERR_INVALID_ARG;
+  if (c->prefetch_late < -1 || c->prefetch_late > 3) return CF_ERR_INVALID_ARG;
   if (c->pdl < -1 || c->pdl > 1) return CF_ERR_INVALID_ARG;
   if (c->max_stages < 0 || c->max_stages == 1 || c->max_stages > kMaxStages)
     return CF_ERR_INVALID_ARG;
@@ -297,7 +298,9 @@ int cf_create(const cf_config* cfg, cf_handle** out) {
   if (cudaFuncGetAttributes(&fa, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
   int cps = c.ctas_per_sm;
   if (cps == 0) {
-    const bool regs_ok = fa.numRegs * kThreads * 2 <= prop.regsPerMultiprocessor;
+    // registers are allocated per thread in multiples of 8
+    const int regs = (fa.numRegs + 7) / 8 * 8;
+    const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
     cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
   }
   const int stage_req = c.stage_bytes ? c.stage_bytes : 32768;

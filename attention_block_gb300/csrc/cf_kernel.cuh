@@ -158,8 +158,10 @@ __device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float&
 
 constexpr int kBarConsumers = 1;  // named barrier id of the 256 consumer threads
 
-template <typename T, int D, int G, int BT>
-__global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_constant__ KParams p) {
+// MINB: blocks per SM the register allocation must allow (2 for the
+// small-state instances, so two 288-thread blocks fit in 64K registers).
+template <typename T, int D, int G, int BT, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_constant__ KParams p) {
   constexpr int NSEG = G + 2;          // q heads of the group, k, v
   constexpr int CPL = D / 32;          // projection columns per lane per segment
   // attention: LPP lanes share one position; each lane owns DPL head dims
@@ -497,6 +499,14 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
         named_sync(kBarConsumers, kConsumers);
         if (lane == 0) mbar_arrive(&empty[s_last]);  // hand the stage back
       }
+      // Optional: pull this block's W_o band into L2 now that its own W_qkv
+      // stream is done, so the O-projection tiles later come from L2.
+      if (p.prefetch_late == 3 && tid == 0) {
+        const uint64_t keep = policy_evict_last();
+        for (int cb = 0; cb < ncb; ++cb)
+          for (int rt = 0; rt < nrt; ++rt)
+            tma_prefetch_2d(&p.tm_wo, k0 + cb * p.Co, g * G * D + rt * p.Ro, keep);
+      }
       stamp(kTlRinv);
     }
 
@@ -586,40 +596,62 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
               o[h][i * EP + e] = 0.f;
             }
         }
-        // One position's contribution to this lane group's running state.
-        auto consume = [&](const T* krow, const T* vrow, bool valid) {
-          float kf[DPL], vf[DPL];
+        // Two positions' contribution to this lane group's running state: the
+        // two dot products, reductions and exponentials are independent
+        // (instruction-level parallelism); the state is rescaled once.
+        auto score = [&](const T* krow, float (&sc)[G]) {
+          float kf[DPL];
 #pragma unroll
           for (int i = 0; i < NPC; ++i) load_cvt<T, EP>(krow + (kl + i * LPP) * EP, kf + i * EP);
-          float sc[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            float s = 0.f;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) s = fmaf(q[h][e], kf[e], s);
-            sc[h] = s;
+            for (int e = 0; e < DPL; e += 2) {
+              s0 = fmaf(q[h][e], kf[e], s0);
+              s1 = fmaf(q[h][e + 1], kf[e + 1], s1);
+            }
+            sc[h] = s0 + s1;
           }
+        };
+        auto consume2 = [&](const T* kA, const T* vA, bool okA, const T* kB, const T* vB,
+                            bool okB) {
+          float sa[G], sb[G];
+          score(kA, sa);
+          score(kB, sb);
 #pragma unroll
           for (int off = LPP / 2; off >= 1; off >>= 1)
 #pragma unroll
-            for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+            for (int h = 0; h < G; ++h) {
+              sa[h] += __shfl_xor_sync(0xffffffffu, sa[h], off);
+              sb[h] += __shfl_xor_sync(0xffffffffu, sb[h], off);
+            }
+          if (okA || okB) {
+            float va[DPL], vb[DPL];
 #pragma unroll
-          for (int i = 0; i < NPC; ++i) load_cvt<T, EP>(vrow + (kl + i * LPP) * EP, vf + i * EP);
-          if (valid) {
+            for (int i = 0; i < NPC; ++i) {
+              load_cvt<T, EP>(vA + (kl + i * LPP) * EP, va + i * EP);
+              load_cvt<T, EP>(vB + (kl + i * LPP) * EP, vb + i * EP);
+            }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              const float mn = fmaxf(m[h], sc[h]);
+              float mn = m[h];
+              if (okA) mn = fmaxf(mn, sa[h]);
+              if (okB) mn = fmaxf(mn, sb[h]);
               const float alpha = exp2f(m[h] - mn);
-              const float pe = exp2f(sc[h] - mn);
-              l[h] = fmaf(l[h], alpha, pe);
+              const float pa = okA ? exp2f(sa[h] - mn) : 0.f;
+              const float pb2 = okB ? exp2f(sb[h] - mn) : 0.f;
+              l[h] = fmaf(l[h], alpha, pa + pb2);
 #pragma unroll
-              for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(o[h][e], alpha, pe * vf[e]);
+              for (int e = 0; e < DPL; ++e)
+                o[h][e] = fmaf(o[h][e], alpha, fmaf(pa, va[e], pb2 * vb[e]));
               m[h] = mn;
             }
           }
         };
         int t0, t1;
         kv_tile_range(pos, p.Rt, rank, N, t0, t1);
+        constexpr int kStep = kConsumerWarps * NGRP;  // positions per warp-wide pass
         for (int t = t0; t < t1; ++t, ++it) {
           const int s = it % p.stages;
           mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
@@ -627,11 +659,12 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           const T* Kt = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
           const T* Vt = Kt + (size_t)p.Rt * D;
           const int lim = min(p.Rt, pos - t * p.Rt);  // cached positions < pos only
-          for (int pb = warp * NGRP; pb < lim; pb += kConsumerWarps * NGRP) {
-            const int pp = pb + grp;
-            const bool valid = pp < lim;
-            const int row = valid ? pp : pb;
-            consume(Kt + (size_t)row * D, Vt + (size_t)row * D, valid);
+          for (int pb = warp * NGRP; pb < lim; pb += 2 * kStep) {
+            const int pa = pb + grp, pbb = pb + kStep + grp;
+            const bool okA = pa < lim, okB = pbb < lim;
+            const int ra = okA ? pa : pb, rb = okB ? pbb : pb;
+            consume2(Kt + (size_t)ra * D, Vt + (size_t)ra * D, okA, Kt + (size_t)rb * D,
+                     Vt + (size_t)rb * D, okB);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
@@ -674,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
             }
           }
         }
+        if (bb == 0) stamp(kTlAttnLoop);
         // Merge the lane groups of the warp.
 #pragma unroll
         for (int off = LPP; off < 32; off <<= 1)
@@ -707,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
           }
         }
         named_sync(kBarConsumers, kConsumers);
+        if (bb == 0) stamp(kTlAttnWarps);
         // Merge the 8 warps into this block's partial (m, l, o) of row bb.
         for (int idx = tid; idx < G * D; idx += kConsumers) {
           const int h = idx / D, dim = idx % D;
@@ -763,31 +798,36 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
     stamp(kTlSum);
     // ---- Phase 3: O projection of this block's column band [CF §3.2] -----
     {
+      // Each thread owns one 16-byte column chunk (CW columns) of a tile row
+      // and every RG-th row; a warp reads whole rows with 16-byte loads.
+      constexpr int CW = 16 / (int)sizeof(T);
+      const int CC = p.Co / CW;  // chunks per tile row
+      const int RG = kConsumers / CC;
+      const int cc = tid % CC, rg = tid / CC;
       const int CQ = p.Co / 4;
-      const int RG = kConsumers / CQ;
-      const int colq = tid % CQ, rg = tid / CQ;
       for (int cb = 0; cb < ncb; ++cb) {
-        float a[BT][4];
+        float a[BT][CW];
 #pragma unroll
         for (int bb = 0; bb < BT; ++bb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) a[bb][e] = 0.f;
+          for (int e = 0; e < CW; ++e) a[bb][e] = 0.f;
         for (int rt = 0; rt < nrt; ++rt, ++it) {
           const int s = it % p.stages;
           mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
           if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
+          else if (cb * nrt + rt < 4) stamp(kTlOprojTile1 - 1 + cb * nrt + rt);
           const T* W = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
           if (rg < RG) {
             for (int r = rg; r < p.Ro; r += RG) {
-              float w[4];
-              load_cvt<T, 4>(W + (size_t)r * p.Co + colq * 4, w);
+              float w[CW];
+              load_cvt<T, CW>(W + (size_t)r * p.Co + cc * CW, w);
               const int row = rt * p.Ro + r;
               const int h = row / D, dim = row % D;
 #pragma unroll
               for (int bb = 0; bb < BT; ++bb) {
                 const float ov = qkv[(bb * NSEG + h) * D + dim];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) a[bb][e] = fmaf(ov, w[e], a[bb][e]);
+                for (int e = 0; e < CW; ++e) a[bb][e] = fmaf(ov, w[e], a[bb][e]);
               }
             }
           }
@@ -805,8 +845,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_decode_kernel(const __grid_con
         if (rg < RG)
 #pragma unroll
           for (int bb = 0; bb < BT; ++bb)
-            *reinterpret_cast<float4*>(pb + ((size_t)rg * BT + bb) * p.Co + colq * 4) =
-                make_float4(a[bb][0], a[bb][1], a[bb][2], a[bb][3]);
+#pragma unroll
+            for (int e4 = 0; e4 < CW; e4 += 4)
+              *reinterpret_cast<float4*>(pb + ((size_t)rg * BT + bb) * p.Co + cc * CW + e4) =
+                  make_float4(a[bb][e4], a[bb][e4 + 1], a[bb][e4 + 2], a[bb][e4 + 3]);
         named_sync(kBarConsumers, kConsumers);
         for (int i4 = tid; i4 < BT * CQ; i4 += kConsumers) {
           const int bb = i4 / CQ, cq = i4 % CQ;

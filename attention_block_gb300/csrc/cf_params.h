@@ -41,7 +41,10 @@ enum TimelineSlot {
   kTlOprojFirst = 18, // first W_o tile in hand
   kTlOprojLoop = 19,  // last W_o tile consumed
   kTlTicket = 20,     // accumulator fence + ticket done
-  kTimelineSlots = 24
+  kTlOprojTile1 = 21, // W_o tiles 1..3 in hand (slots 21..23)
+  kTlAttnLoop = 24,   // last K/V tile and the new token consumed (row 0)
+  kTlAttnWarps = 25,  // warp states written (row 0)
+  kTimelineSlots = 32
 };
 
 // Byte offsets of the shared-memory regions (from a 1024-aligned base).

@@ -488,7 +488,11 @@ def main(argv=None):
     if rank == 0:
         peak, peak_kind = measured_peak_hbm()
         per_launch_bytes = algorithmic_bytes(w, pos0)
-        achieved = per_launch_bytes / (launch_ms_avg / 1e3) / 1e9
+        # The kernel's average launch duration inside the timed region: one
+        # kernel per layer, launched back to back on one stream, timed with
+        # CUDA events on that stream.
+        launch_s_timed = elapsed_s / (args.steps * w.layers)
+        achieved = per_launch_bytes / launch_s_timed / 1e9
         us_step = elapsed_s / args.steps * 1e6
         cpu = None
         if world == 1:
@@ -534,8 +538,10 @@ def main(argv=None):
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": recorded_traffic(w.name),
                 "kernel": KERNEL_NAME,
-                "launch_us_avg": round(launch_ms_avg * 1e3, 3),
-                "launch_us_min": round(min(launch_ms) * 1e3, 3),
+                "launch_us_avg": round(launch_s_timed * 1e6, 3),
+                "launch_timing": "timed region (graph replays) / launches",
+                "isolated_launch_us_avg": round(launch_ms_avg * 1e3, 3),
+                "isolated_launch_us_min": round(min(launch_ms) * 1e3, 3),
                 "bytes_per_launch": per_launch_bytes,
                 "frac_of_nominal_7_9TBs": round(achieved / 7900.0, 4),
             },

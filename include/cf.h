@@ -71,9 +71,11 @@ typedef struct cf_config {
   int32_t ctas_per_sm;  /* 0 = default, else 1 or 2 (shared-memory split)    */
   int32_t prefetch_ahead; /* W_qkv tiles prefetched into L2 beyond the ring:
                              0 or -1 = none (default), else that many        */
-  int32_t prefetch_late;  /* L2 prefetch of each block's K/V and W_o tiles:
-                             0 or -1 = off (default), 1 = after the block's
-                             last W_qkv tile is issued, 2 = at kernel start  */
+  int32_t prefetch_late;  /* L2 prefetch of each block's later tiles:
+                             0 or -1 = off (default); K/V and W_o tiles
+                             1 = after the block's last W_qkv tile is issued,
+                             2 = at kernel start; W_o tiles only 3 = once the
+                             block's projection is complete                   */
   int32_t pdl;            /* programmatic dependent launch: 0 = default (on),
                              -1 = off                                         */
   int32_t max_stages;     /* 0 = as many ring stages as fit, else at most this

@@ -55,12 +55,12 @@ int cf_bench_tma_stream(int hidden, int n_q_heads, int n_kv_heads, int head_dim,
                         const void* w, int* errflag, void* stream);
 
 /* Phase timeline of later cf_decode_attn_block calls of handle h (a tuning
- * aid): when `stamps` is a device buffer of grid_blocks * 16 unsigned 64-bit
- * values, every block writes %globaltimer (ns) at its phase boundaries (slot
- * order: start, norm, proj, reduce-scatter, gather, attention, max, sum,
- * o-proj, final, producer-W, producer-KV, producer-all, end).  The grid has
- * cluster_size * n_kv_heads * ceil(batch / batch_tile) blocks.  NULL turns it
- * off.  Returns CF_OK or CF_ERR_INVALID_ARG. */
+ * aid): when `stamps` is a zeroed device buffer of grid_blocks * 32 unsigned
+ * 64-bit values, every block writes %globaltimer (ns) at its phase
+ * boundaries into its row of 32 slots (slot meanings: the TimelineSlot enum
+ * of the kernel sources, listed in order by the Python binding).  The grid
+ * has cluster_size * n_kv_heads * ceil(batch / batch_tile) blocks.  NULL
+ * turns it off.  Returns CF_OK or CF_ERR_INVALID_ARG. */
 struct cf_handle;
 int cf_set_timeline(struct cf_handle* h, unsigned long long* stamps);
 
