@@ -70,6 +70,8 @@ SIGNATURES = {
                                                    _vp, _vp, _vp, _vp, _vp]),
     "cf_set_timeline": (ctypes.c_int, [_vp, _vp]),
     "cf_bench_tma_stream": (ctypes.c_int, [ctypes.c_int] * 8 + [_vp, _vp, _vp]),
+    "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
+                                     + [_vp] * 9),
 }
 
 TIMELINE_SLOTS = 32
@@ -160,6 +162,14 @@ def cf_decode_attn_block(handle, batch, hidden_states, ln_weight, w_qkv, w_o, k_
     return lib().cf_decode_attn_block(handle, int(batch), _ptr(hidden_states), _ptr(ln_weight),
                                       _ptr(w_qkv), _ptr(w_o), _ptr(k_cache), _ptr(v_cache),
                                       _ptr(positions), _ptr(out), _stream(stream))
+
+
+def cf_decode_attn_block_noalloc(cfg: CfConfig, batch, hidden_states, ln_weight, w_qkv, w_o,
+                                 k_cache, v_cache, positions, out, stream=None) -> int:
+    """Allocation-free decode step (no handle; scratch in a static device array)."""
+    return lib().cf_decode_attn_block_noalloc(
+        ctypes.byref(cfg), int(batch), _ptr(hidden_states), _ptr(ln_weight), _ptr(w_qkv),
+        _ptr(w_o), _ptr(k_cache), _ptr(v_cache), _ptr(positions), _ptr(out), _stream(stream))
 
 
 def cf_get_status(handle) -> int:

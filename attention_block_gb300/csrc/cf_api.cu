@@ -574,3 +574,164 @@ void cf_destroy(cf_handle* h) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc at all: code running inside a CUDA
+// graph capture region that must not allocate, custom allocators that own all
+// device memory, or embeddings in runtimes that forbid allocation after
+// start-up.  cf_decode_attn_block_noalloc serves them: it needs no handle, and
+// its scratch -- the fp32 output accumulator, the completion counters and the
+// error flag that cf_create would otherwise allocate -- lives in the
+// file-scope device array below, which every GPU that loads this library
+// holds until the process exits.  Its planning state lives in static host
+// storage, one slot per device, so no host heap is touched either.
+// ===========================================================================
+namespace {
+
+constexpr size_t kNoAllocAccFloats = size_t(1) << 19;  // 2 MiB: batch * hidden <= 524288
+constexpr size_t kNoAllocCounters = 8192;
+constexpr size_t kNoAllocBytes = kNoAllocAccFloats * 4 + kNoAllocCounters * 4 + 256;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocSlot {
+  bool ready = false;        // device address of the scratch obtained
+  unsigned char* scratch = nullptr;
+  bool planned = false;      // `h` prepared for `cfg`
+  cf_config cfg;
+  cf_handle h;
+};
+NoAllocSlot g_noalloc[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// The planning half of cf_create (kernel instance, cluster size, shared-memory
+// plan, function attributes) with the handle's workspace pointed at the
+// static scratch instead of a fresh allocation.
+int noalloc_prepare(const cf_config& c, unsigned char* scratch, cf_handle& h) {
+  const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
+  int BT = c.batch_tile;
+  if (BT == 0) {
+    BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 4));
+    if (G > 1) BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 2));
+  }
+  if (BT <= 0) return CF_ERR_UNSUPPORTED;
+  const KernelEntry* ke = find_entry(c.dtype, D, G, BT);
+  if (ke == nullptr) return CF_ERR_UNSUPPORTED;
+  if (!get_encode()) return CF_ERR_CUDA;
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CF_ERR_CUDA;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return CF_ERR_CUDA;
+  const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
+  int N = c.cluster_size;
+  if (N == 0) {
+    N = 2;
+    while (N < 16 && N * 2 <= D / 4 && ((c.hidden / (N * 2)) * esize(c.dtype)) % 16 == 0 &&
+           (long long)clusters * N * 2 <= 2LL * prop.multiProcessorCount)
+      N *= 2;
+  }
+  if (N > D / 4 || ((c.hidden / N) * esize(c.dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
+  if ((size_t)((c.max_batch + BT - 1) / BT) * N > kNoAllocCounters) return CF_ERR_INVALID_ARG;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
+  int cps = c.ctas_per_sm;
+  if (cps == 0) {
+    const int regs = (fa.numRegs + 7) / 8 * 8;
+    const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
+    cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
+  }
+  const int stage_req = c.stage_bytes ? c.stage_bytes : 32768;
+  Plan pl;
+  if (!make_plan(c, N, BT, stage_req, cps, prop, pl) &&
+      !(cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)))
+    return CF_ERR_UNSUPPORTED;
+  if (fa.maxDynamicSharedSizeBytes < pl.L.total &&
+      cudaFuncSetAttribute(ke->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.L.total) !=
+          cudaSuccess)
+    return CF_ERR_CUDA;
+  if (N > 8 && cudaFuncSetAttribute(ke->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                   cudaSuccess)
+    return CF_ERR_CLUSTER;
+  h.cfg = c;
+  h.device = dev;
+  h.sm_count = prop.multiProcessorCount;
+  h.plan = pl;
+  h.fn = ke->fn;
+  h.max_active_clusters = 0;
+  h.ws = nullptr;  // nothing to free: the workspace is the static scratch
+  h.acc = reinterpret_cast<float*>(scratch);
+  h.counters = reinterpret_cast<int*>(scratch + kNoAllocAccFloats * 4);
+  h.errflag = reinterpret_cast<int*>(scratch + kNoAllocAccFloats * 4 + kNoAllocCounters * 4);
+  h.dbg = nullptr;
+  h.timeline = nullptr;
+  h.prefetch_ahead = std::max(0, c.prefetch_ahead);
+  h.prefetch_late = std::max(0, c.prefetch_late);
+  h.pdl = c.pdl != -1;
+  for (int i = 0; i < 64; ++i) {
+    const double two_pi = 6.283185307179586476925286766559;
+    const double rate = (i < D / 2) ? std::pow((double)c.rope_theta, -2.0 * i / (double)D) / two_pi
+                                    : 0.0;
+    h.turn_hi[i] = (float)rate;
+    h.turn_lo[i] = (float)(rate - (double)h.turn_hi[i]);
+  }
+  for (MapCache* mc : {&h.m_wqkv, &h.m_wo, &h.m_k, &h.m_v}) {
+    for (int i = 0; i < MapCache::kSlots; ++i) mc->ptr[i] = nullptr;
+    mc->next = 0;
+  }
+  return CF_OK;
+}
+
+}  // namespace
+
+extern "C" int cf_decode_attn_block_noalloc(const cf_config* cfg, int32_t batch,
+                                            const void* hidden_states, const void* ln_weight,
+                                            const void* w_qkv, const void* w_o, void* k_cache,
+                                            void* v_cache, const int32_t* positions, void* out,
+                                            void* stream) {
+  int rc = validate_config(cfg);
+  if (rc != CF_OK) return rc;
+  if (batch < 0 || batch > cfg->max_batch) return CF_ERR_INVALID_ARG;
+  if ((size_t)cfg->max_batch * (size_t)cfg->hidden > kNoAllocAccFloats) return CF_ERR_INVALID_ARG;
+  if (batch == 0) return CF_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CF_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return CF_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocSlot& s = g_noalloc[dev];
+  if (!s.ready) {
+    // Once per device, with that device current: the host-side name of the
+    // array is only a stand-in, so fetch its real device address.
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return CF_ERR_CUDA;
+    }
+    s.scratch = static_cast<unsigned char*>(p);
+    s.ready = true;
+  }
+  if (!s.planned || std::memcmp(&s.cfg, cfg, sizeof(cf_config)) != 0) {
+    s.planned = false;
+    rc = noalloc_prepare(*cfg, s.scratch, s.h);
+    if (rc != CF_OK) return rc;
+    s.cfg = *cfg;
+    s.planned = true;
+  }
+  // The kernel leaves the accumulator and counters at zero, but the array
+  // keeps whatever the previous call left (e.g. one stopped by an error), so
+  // the regions this call uses are cleared first, on the same stream.
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t acc_bytes = (size_t)batch * cfg->hidden * sizeof(float);
+  const size_t cnt_bytes =
+      (size_t)((batch + s.h.plan.BT - 1) / s.h.plan.BT) * s.h.plan.N * sizeof(int);
+  if (cudaMemsetAsync(s.h.acc, 0, acc_bytes, st) != cudaSuccess ||
+      cudaMemsetAsync(s.h.counters, 0, cnt_bytes, st) != cudaSuccess ||
+      cudaMemsetAsync(s.h.errflag, 0, sizeof(int), st) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
+  return cf_decode_attn_block(&s.h, batch, hidden_states, ln_weight, w_qkv, w_o, k_cache, v_cache,
+                              positions, out, stream);
+}

@@ -149,6 +149,31 @@ const char* cf_strerror(int code);
 /* Free the handle and its workspace.  NULL is a no-op. */
 void cf_destroy(cf_handle* h);
 
+/* The same decode step for callers that cannot allocate device memory at all
+ * -- for example code that runs while a CUDA graph is being captured under a
+ * no-allocation policy, or runtimes whose own allocator owns all device
+ * memory.  The pages have no counterpart of this entry point.
+ *
+ * It takes the configuration directly (no handle) and calls no cudaMalloc,
+ * cudaFree or other allocating routine.  Its scratch (fp32 output
+ * accumulator, completion counters, error flag) is a fixed file-scope device
+ * array of about 2 MiB that every GPU which loads this library keeps until
+ * the process exits; calls are rejected with CF_ERR_INVALID_ARG when
+ * cfg->max_batch * cfg->hidden exceeds 524288.  The first call on each
+ * device looks up that array's device address (cudaGetSymbolAddress) and
+ * sets kernel attributes, so make the first call on a device before any
+ * stream capture.  Each call first clears, on `stream`, the part of the
+ * array it uses.  All calls share the one array: calls whose work overlaps
+ * on the GPU (different streams, or different host threads) race and give
+ * wrong results -- serialize them.  Device-detected errors (out-of-range
+ * positions) are not reported (there is no handle to read them from); such
+ * rows are left as described for cf_decode_attn_block.  Arguments, layouts
+ * and other return codes are those of cf_create + cf_decode_attn_block. */
+int cf_decode_attn_block_noalloc(const cf_config* cfg, int32_t batch, const void* hidden_states,
+                                 const void* ln_weight, const void* w_qkv, const void* w_o,
+                                 void* k_cache, void* v_cache, const int32_t* positions,
+                                 void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
