@@ -101,7 +101,71 @@ struct MapCache {
 struct Plan {
   int N, BT, G, Rw, Rt, Ro, Co, stages, stage_bytes, ctas_per_sm;
   SmemLayout L;
+  int mode = 0;  // 0 sequence-split kernel, 1 batched row-split kernel
+  int RPC = 0;   // rows per block (mode 1)
 };
+
+// Shared-memory plan of the batched row-split kernel (one block per SM):
+// N = BT / RPC blocks per cluster, K band Hc = H / N.  Returns false when the
+// shape does not fit (the caller reports CF_ERR_UNSUPPORTED).
+bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cudaDeviceProp& prop,
+                    Plan& pl) {
+  const int es = esize(c.dtype), D = c.head_dim, H = c.hidden;
+  const int G = c.n_q_heads / c.n_kv_heads, NSEG = G + 2, NC = NSEG * D, GD = G * D;
+  const int N = BT / RPC;
+  if (N < 1 || N > kMaxCluster || (N & (N - 1)) != 0 || H % (64 * N) != 0) return false;
+  const int Hc = H / N;
+  const int nrounds = __builtin_ctz((unsigned)N);
+  pl.mode = 1;
+  pl.RPC = RPC;
+  pl.N = N;
+  pl.BT = BT;
+  pl.G = G;
+  pl.ctas_per_sm = 1;
+  pl.Co = (Hc % 256 == 0) ? 256 : ((Hc % 128 == 0) ? 128 : 64);
+  // W_qkv tile: Rw rows of the NC group columns plus the [BT x Rw] slice of x
+  int rw = 16;
+  while (rw * 2 <= 256 && Hc % (rw * 2) == 0 && (rw * 2) * (NC + BT) * es <= stage_req) rw *= 2;
+  pl.Rw = rw;
+  pl.Rt = std::min(256, pow2_floor(std::max(16, stage_req / (2 * D * es))));
+  int ro = 16;
+  while (ro * 2 <= 256 && GD % (ro * 2) == 0 && (ro * 2) * pl.Co * es <= stage_req) ro *= 2;
+  pl.Ro = ro;
+  const int item = std::max((NC + BT) * pl.Rw * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
+  pl.stage_bytes = round_up(item, 1024);
+
+  const int SE = RPC * NC;
+  int off = 0;
+  SmemLayout& L = pl.L;
+  auto take = [&](int bytes) {
+    const int o = off;
+    off += round_up(bytes, 128);
+    return o;
+  };
+  L.bars = take(BarIdx::count * 8);
+  L.red = take(BT * NC * 4);                                       // partials / O-proj A
+  L.scratch = take(std::max((N - 1) * SE, kConsumerWarps * G * (D + 4)) * 4);
+  L.qkv = take(BT * GD * 4);                                       // gathered o
+  L.sm = take(G * (D + 4) * 4);                                    // attention record
+  L.xn = take(4 * BT * (pl.Rw + 8) * 2);                           // A staging (2 x hi/lo)
+  L.scale = take(Hc * 4);                                          // ln_weight band
+  L.rope = take(RPC * (D / 2) * 2 * 4);
+  L.misc = take((BT + 4 + RPC + kConsumerWarps * RPC) * 4);
+  const int extras = round_up(off, 1024);
+  int budget = std::min((int)prop.sharedMemPerBlockOptin,
+                        (int)prop.sharedMemPerMultiprocessor - (int)prop.reservedSharedMemPerBlock);
+  budget -= 1024;
+  int stages = std::min((budget - extras) / pl.stage_bytes, kMaxStages);
+  if (c.max_stages > 0) stages = std::min(stages, c.max_stages);
+  if (stages < 2) return false;
+  pl.stages = stages;
+  const int ring = stages * pl.stage_bytes;
+  L.ring = 0;
+  for (int* f : {&L.bars, &L.red, &L.scratch, &L.qkv, &L.sm, &L.xn, &L.scale, &L.rope, &L.misc})
+    *f += ring;
+  L.total = ring + extras + 1024;
+  return true;
+}
 
 // Shared-memory plan for one (config, N, BT, stage size, CTAs/SM).  Returns
 // false when not even two ring stages fit.
@@ -189,7 +253,7 @@ struct cf_handle {
   int prefetch_ahead = 0, prefetch_late = 0;
   bool pdl = true;
   float turn_hi[64], turn_lo[64];  // RoPE turn rates as float pairs (see KParams)
-  MapCache m_wqkv, m_wo, m_k, m_v;
+  MapCache m_wqkv, m_wo, m_k, m_v, m_x;
 };
 
 namespace {
@@ -224,12 +288,13 @@ int validate_config(const cf_config* c) {
 }
 
 bool encode(CUtensorMap* m, int dtype, int rank, const void* base, const uint64_t* dims,
-            const uint64_t* strides_bytes, const uint32_t* box) {
+            const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128 = false) {
   uint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(m, tm_type(dtype), (cuuint32_t)rank, const_cast<void*>(base),
                         (const cuuint64_t*)dims, (const cuuint64_t*)strides_bytes,
                         (const cuuint32_t*)box, (const cuuint32_t*)estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -237,6 +302,140 @@ bool encode(CUtensorMap* m, int dtype, int rank, const void* base, const uint64_
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return x < y + nb && y < x + na;
+}
+
+// The batched row-split instance for c with its plan, or nullptr when c takes
+// the sequence-split kernel: fp32 storage, batch tiles under 16 rows, or no
+// instance built (or fitting shared memory) for the shape.
+const KernelEntry* pick_rows_entry(const cf_config& c, int stage_req, const cudaDeviceProp& prop,
+                                   Plan& pl) {
+  if (c.dtype == CF_F32) return nullptr;
+  if (c.batch_tile > 0 && c.batch_tile < 16) return nullptr;
+  if (c.batch_tile == 0 && c.max_batch < 16) return nullptr;
+  const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
+  const KernelEntry* e = nullptr;
+  const int n = registry_rows(&e);
+  const KernelEntry* best = nullptr;
+  for (int i = 0; i < n; ++i) {
+    const KernelEntry& k = e[i];
+    if (k.dtype != c.dtype || k.D != D || k.G != G) continue;
+    if (c.batch_tile > 0 && k.BT != c.batch_tile) continue;
+    if (c.rows_per_block > 0 && k.RPC != c.rows_per_block) continue;
+    if (c.batch_tile == 0 && k.BT > std::max(16, c.max_batch)) continue;
+    Plan trial;
+    if (!make_plan_rows(c, k.BT, k.RPC, stage_req, prop, trial)) continue;
+    // largest batch tile (weights read once per tile), then fewest rows per
+    // block (more blocks streaming)
+    if (best == nullptr || k.BT > best->BT || (k.BT == best->BT && k.RPC < best->RPC)) {
+      best = &k;
+      pl = trial;
+    }
+  }
+  return best;
+}
+
+// Kernel instance, launch shape and shared-memory plan of config c on the
+// current device, written into h (all but the workspace pointers).
+int plan_handle(const cf_config& c, cf_handle& h) {
+  const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
+  if (!get_encode()) return CF_ERR_CUDA;
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CF_ERR_CUDA;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return CF_ERR_CUDA;
+  const int stage_req = c.stage_bytes ? c.stage_bytes : 32768;
+  Plan pl;
+  const KernelEntry* ke = pick_rows_entry(c, stage_req, prop, pl);
+  if (ke == nullptr) {
+    if (c.batch_tile >= 16) return CF_ERR_UNSUPPORTED;
+    // Batch tile: requested, else the largest compiled one <= max_batch.
+    int BT = c.batch_tile;
+    if (BT == 0) {
+      BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 4));
+      if (G > 1) BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 2));
+    }
+    if (BT <= 0) return CF_ERR_UNSUPPORTED;
+    ke = find_entry(c.dtype, D, G, BT);
+    if (ke == nullptr) return CF_ERR_UNSUPPORTED;
+    // Cluster size: requested, else the smallest power of two >= 2 that gives
+    // about two blocks per SM over the whole grid (capped by head_dim/4 and by
+    // the hidden size's 16-byte column bands).
+    const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
+    int N = c.cluster_size;
+    if (N == 0) {
+      N = 2;
+      while (N < 16 && N * 2 <= D / 4 && ((c.hidden / (N * 2)) * esize(c.dtype)) % 16 == 0 &&
+             (long long)clusters * N * 2 <= 2LL * prop.multiProcessorCount)
+        N *= 2;
+    }
+    if (N > D / 4 || ((c.hidden / N) * esize(c.dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
+    int cps = c.ctas_per_sm;
+    if (cps == 0) {
+      // registers are allocated per thread in multiples of 8
+      const int regs = (fa.numRegs + 7) / 8 * 8;
+      const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
+      cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
+    }
+    if (!make_plan(c, N, BT, stage_req, cps, prop, pl) &&
+        !(cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)))
+      return CF_ERR_UNSUPPORTED;
+  }
+  const int N = pl.N, BT = pl.BT;
+  const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
+  // The attribute is per function: only ever raise it, so a later handle with
+  // a smaller plan cannot break an earlier handle's launches.
+  {
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    cudaFuncAttributes cur;
+    if (cudaFuncGetAttributes(&cur, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
+    if (cur.maxDynamicSharedSizeBytes < pl.L.total &&
+        cudaFuncSetAttribute(ke->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.L.total) !=
+            cudaSuccess)
+      return CF_ERR_CUDA;
+  }
+  if (N > 8 && cudaFuncSetAttribute(ke->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                   cudaSuccess)
+    return CF_ERR_CLUSTER;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = N;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3(N * clusters, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = pl.L.total;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, ke->fn, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CLUSTER;
+  }
+  if (nclusters <= 0) return CF_ERR_CLUSTER;
+  h.cfg = c;
+  h.device = dev;
+  h.sm_count = prop.multiProcessorCount;
+  h.plan = pl;
+  h.fn = ke->fn;
+  h.max_active_clusters = nclusters;
+  // Both L2 prefetches measured slower on the B = 1 Llama2 layer (they compete
+  // with the W_qkv stream), so they are off unless asked for.
+  h.prefetch_ahead = std::max(0, c.prefetch_ahead);
+  h.prefetch_late = std::max(0, c.prefetch_late);
+  h.pdl = c.pdl != -1;
+  for (int i = 0; i < 64; ++i) {
+    // turns per position: theta^(-2i/d) / (2 pi), split into hi + lo floats
+    const double two_pi = 6.283185307179586476925286766559;
+    const double rate = (i < D / 2) ? std::pow((double)c.rope_theta, -2.0 * i / (double)D) / two_pi
+                                    : 0.0;
+    h.turn_hi[i] = (float)rate;
+    h.turn_lo[i] = (float)(rate - (double)h.turn_hi[i]);
+  }
+  return CF_OK;
 }
 
 }  // namespace
@@ -263,112 +462,14 @@ int cf_create(const cf_config* cfg, cf_handle** out) {
   int rc = validate_config(cfg);
   if (rc != CF_OK) return rc;
   const cf_config c = *cfg;
-  const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
-
-  // Batch tile: requested, else the largest compiled one <= max_batch.
-  int BT = c.batch_tile;
-  if (BT == 0) {
-    BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 4));
-    if (G > 1) BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 2));
-  }
-  if (BT <= 0) return CF_ERR_UNSUPPORTED;
-  const KernelEntry* ke = find_entry(c.dtype, D, G, BT);
-  if (ke == nullptr) return CF_ERR_UNSUPPORTED;
-  if (!get_encode()) return CF_ERR_CUDA;
-
-  int dev = 0;
-  cudaDeviceProp prop;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CF_ERR_CUDA;
-  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return CF_ERR_CUDA;
-
-  // Cluster size: requested, else the smallest power of two >= 2 that gives
-  // about two blocks per SM over the whole grid (capped by head_dim/4 and by
-  // the hidden size's 16-byte column bands).
-  const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
-  int N = c.cluster_size;
-  if (N == 0) {
-    N = 2;
-    while (N < 16 && N * 2 <= D / 4 && ((c.hidden / (N * 2)) * esize(c.dtype)) % 16 == 0 &&
-           (long long)clusters * N * 2 <= 2LL * prop.multiProcessorCount)
-      N *= 2;
-  }
-  if (N > D / 4 || ((c.hidden / N) * esize(c.dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
-
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
-  int cps = c.ctas_per_sm;
-  if (cps == 0) {
-    // registers are allocated per thread in multiples of 8
-    const int regs = (fa.numRegs + 7) / 8 * 8;
-    const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
-    cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
-  }
-  const int stage_req = c.stage_bytes ? c.stage_bytes : 32768;
-  Plan pl;
-  if (!make_plan(c, N, BT, stage_req, cps, prop, pl)) {
-    if (cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)) {
-      // fall back to one block per SM
-    } else {
-      return CF_ERR_UNSUPPORTED;
-    }
-  }
-
-  // The attribute is per function: only ever raise it, so a later handle with
-  // a smaller plan cannot break an earlier handle's launches.
-  {
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    cudaFuncAttributes cur;
-    if (cudaFuncGetAttributes(&cur, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
-    if (cur.maxDynamicSharedSizeBytes < pl.L.total &&
-        cudaFuncSetAttribute(ke->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.L.total) !=
-            cudaSuccess)
-      return CF_ERR_CUDA;
-  }
-  if (N > 8 && cudaFuncSetAttribute(ke->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                   cudaSuccess)
-    return CF_ERR_CLUSTER;
-
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = N;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  lc.gridDim = dim3(N * clusters, 1, 1);
-  lc.blockDim = dim3(kThreads, 1, 1);
-  lc.dynamicSmemBytes = pl.L.total;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  int nclusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&nclusters, ke->fn, &lc) != cudaSuccess) {
-    cudaGetLastError();
-    return CF_ERR_CLUSTER;
-  }
-  if (nclusters <= 0) return CF_ERR_CLUSTER;
-
   cf_handle* h = new (std::nothrow) cf_handle();
   if (h == nullptr) return CF_ERR_CUDA;
-  h->cfg = c;
-  h->device = dev;
-  h->sm_count = prop.multiProcessorCount;
-  h->plan = pl;
-  h->fn = ke->fn;
-  h->max_active_clusters = nclusters;
-  // Both L2 prefetches measured slower on the B = 1 Llama2 layer (they compete
-  // with the W_qkv stream), so they are off unless asked for.
-  h->prefetch_ahead = std::max(0, c.prefetch_ahead);
-  h->prefetch_late = std::max(0, c.prefetch_late);
-  h->pdl = c.pdl != -1;
-  for (int i = 0; i < 64; ++i) {
-    // turns per position: theta^(-2i/d) / (2 pi), split into hi + lo floats
-    const double two_pi = 6.283185307179586476925286766559;
-    const double rate = (i < D / 2) ? std::pow((double)c.rope_theta, -2.0 * i / (double)D) / two_pi
-                                    : 0.0;
-    h->turn_hi[i] = (float)rate;
-    h->turn_lo[i] = (float)(rate - (double)h->turn_hi[i]);
+  rc = plan_handle(c, *h);
+  if (rc != CF_OK) {
+    delete h;
+    return rc;
   }
-
+  const int BT = h->plan.BT, N = h->plan.N;
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
   const size_t cnt_bytes = (size_t)((c.max_batch + BT - 1) / BT) * N * sizeof(int);
   const size_t total = acc_bytes + cnt_bytes + 256;
@@ -417,53 +518,52 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
   const Plan& pl = h->plan;
   KParams kp;
   std::memset(&kp, 0, sizeof(kp));
-  // Tensor maps (encoded on the host, cached per pointer).
-  {
-    const CUtensorMap* m = h->m_wqkv.find(w_qkv, 0);
+  // Tensor maps (encoded on the host, cached per pointer and extent).
+  auto get_map = [&](MapCache& mc, const void* base, int key, int rank, const uint64_t* dims,
+                     const uint64_t* str, const uint32_t* box, bool swz,
+                     CUtensorMap& dst) -> bool {
+    const CUtensorMap* m = mc.find(base, key);
     if (!m) {
-      CUtensorMap* n = h->m_wqkv.insert(w_qkv, 0);
-      const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H};
-      const uint64_t str[1] = {(uint64_t)C * es};
-      const uint32_t box[2] = {(uint32_t)D, (uint32_t)pl.Rw};
-      if (!encode(n, c.dtype, 2, w_qkv, dims, str, box)) {
-        h->m_wqkv.ptr[(h->m_wqkv.next + MapCache::kSlots - 1) % MapCache::kSlots] = nullptr;
-        return CF_ERR_CUDA;
+      CUtensorMap* n = mc.insert(base, key);
+      if (!encode(n, c.dtype, rank, base, dims, str, box, swz)) {
+        mc.ptr[(mc.next + MapCache::kSlots - 1) % MapCache::kSlots] = nullptr;
+        return false;
       }
       m = n;
     }
-    kp.tm_wqkv = *m;
+    dst = *m;
+    return true;
+  };
+  // The batched kernel reads weights as 64-column boxes (128 bytes) with the
+  // 128-byte swizzle, and x as [BT x Rw] tiles.
+  const bool rows = pl.mode == 1;
+  {
+    const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H};
+    const uint64_t str[1] = {(uint64_t)C * es};
+    const uint32_t box[2] = {(uint32_t)(rows ? 64 : D), (uint32_t)pl.Rw};
+    if (!get_map(h->m_wqkv, w_qkv, 0, 2, dims, str, box, rows, kp.tm_wqkv)) return CF_ERR_CUDA;
   }
   {
-    const CUtensorMap* m = h->m_wo.find(w_o, 0);
-    if (!m) {
-      CUtensorMap* n = h->m_wo.insert(w_o, 0);
-      const uint64_t dims[2] = {(uint64_t)H, (uint64_t)nq * D};
-      const uint64_t str[1] = {(uint64_t)H * es};
-      const uint32_t box[2] = {(uint32_t)pl.Co, (uint32_t)pl.Ro};
-      if (!encode(n, c.dtype, 2, w_o, dims, str, box)) {
-        h->m_wo.ptr[(h->m_wo.next + MapCache::kSlots - 1) % MapCache::kSlots] = nullptr;
-        return CF_ERR_CUDA;
-      }
-      m = n;
-    }
-    kp.tm_wo = *m;
+    const uint64_t dims[2] = {(uint64_t)H, (uint64_t)nq * D};
+    const uint64_t str[1] = {(uint64_t)H * es};
+    const uint32_t box[2] = {(uint32_t)(rows ? 64 : pl.Co), (uint32_t)pl.Ro};
+    if (!get_map(h->m_wo, w_o, 0, 2, dims, str, box, rows, kp.tm_wo)) return CF_ERR_CUDA;
   }
   for (int which = 0; which < 2; ++which) {
-    MapCache& mc = which == 0 ? h->m_k : h->m_v;
     const void* base = which == 0 ? k_cache : v_cache;
-    const CUtensorMap* m = mc.find(base, batch);
-    if (!m) {
-      CUtensorMap* n = mc.insert(base, batch);
-      const uint64_t dims[4] = {(uint64_t)D, (uint64_t)nkv, (uint64_t)S, (uint64_t)batch};
-      const uint64_t str[3] = {(uint64_t)D * es, (uint64_t)nkv * D * es, (uint64_t)S * nkv * D * es};
-      const uint32_t box[4] = {(uint32_t)D, 1u, (uint32_t)pl.Rt, 1u};
-      if (!encode(n, c.dtype, 4, base, dims, str, box)) {
-        mc.ptr[(mc.next + MapCache::kSlots - 1) % MapCache::kSlots] = nullptr;
-        return CF_ERR_CUDA;
-      }
-      m = n;
-    }
-    (which == 0 ? kp.tm_k : kp.tm_v) = *m;
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)nkv, (uint64_t)S, (uint64_t)batch};
+    const uint64_t str[3] = {(uint64_t)D * es, (uint64_t)nkv * D * es, (uint64_t)S * nkv * D * es};
+    const uint32_t box[4] = {(uint32_t)D, 1u, (uint32_t)pl.Rt, 1u};
+    if (!get_map(which == 0 ? h->m_k : h->m_v, base, batch, 4, dims, str, box, false,
+                 which == 0 ? kp.tm_k : kp.tm_v))
+      return CF_ERR_CUDA;
+  }
+  if (rows) {
+    const uint64_t dims[2] = {(uint64_t)H, (uint64_t)batch};
+    const uint64_t str[1] = {(uint64_t)H * es};
+    const uint32_t box[2] = {(uint32_t)pl.Rw, (uint32_t)pl.BT};
+    if (!get_map(h->m_x, hidden_states, batch, 2, dims, str, box, false, kp.tm_x))
+      return CF_ERR_CUDA;
   }
 
   kp.hidden = hidden_states;
@@ -564,6 +664,8 @@ int cf_get_launch_info(const cf_handle* h, cf_launch_info* info) {
   info->threads = kThreads;
   info->max_active_clusters = h->max_active_clusters;
   info->sm_count = h->sm_count;
+  info->mode = pl.mode;
+  info->rows_per_block = pl.RPC;
   return CF_OK;
 }
 
@@ -611,73 +713,17 @@ std::mutex g_noalloc_mu;
 // plan, function attributes) with the handle's workspace pointed at the
 // static scratch instead of a fresh allocation.
 int noalloc_prepare(const cf_config& c, unsigned char* scratch, cf_handle& h) {
-  const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
-  int BT = c.batch_tile;
-  if (BT == 0) {
-    BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 4));
-    if (G > 1) BT = best_batch_tile(c.dtype, D, G, std::min(c.max_batch, 2));
-  }
-  if (BT <= 0) return CF_ERR_UNSUPPORTED;
-  const KernelEntry* ke = find_entry(c.dtype, D, G, BT);
-  if (ke == nullptr) return CF_ERR_UNSUPPORTED;
-  if (!get_encode()) return CF_ERR_CUDA;
-  int dev = 0;
-  cudaDeviceProp prop;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CF_ERR_CUDA;
-  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return CF_ERR_CUDA;
-  const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
-  int N = c.cluster_size;
-  if (N == 0) {
-    N = 2;
-    while (N < 16 && N * 2 <= D / 4 && ((c.hidden / (N * 2)) * esize(c.dtype)) % 16 == 0 &&
-           (long long)clusters * N * 2 <= 2LL * prop.multiProcessorCount)
-      N *= 2;
-  }
-  if (N > D / 4 || ((c.hidden / N) * esize(c.dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
-  if ((size_t)((c.max_batch + BT - 1) / BT) * N > kNoAllocCounters) return CF_ERR_INVALID_ARG;
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
-  int cps = c.ctas_per_sm;
-  if (cps == 0) {
-    const int regs = (fa.numRegs + 7) / 8 * 8;
-    const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
-    cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
-  }
-  const int stage_req = c.stage_bytes ? c.stage_bytes : 32768;
-  Plan pl;
-  if (!make_plan(c, N, BT, stage_req, cps, prop, pl) &&
-      !(cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)))
-    return CF_ERR_UNSUPPORTED;
-  if (fa.maxDynamicSharedSizeBytes < pl.L.total &&
-      cudaFuncSetAttribute(ke->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.L.total) !=
-          cudaSuccess)
-    return CF_ERR_CUDA;
-  if (N > 8 && cudaFuncSetAttribute(ke->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                   cudaSuccess)
-    return CF_ERR_CLUSTER;
-  h.cfg = c;
-  h.device = dev;
-  h.sm_count = prop.multiProcessorCount;
-  h.plan = pl;
-  h.fn = ke->fn;
-  h.max_active_clusters = 0;
+  const int rc = plan_handle(c, h);
+  if (rc != CF_OK) return rc;
+  if ((size_t)((c.max_batch + h.plan.BT - 1) / h.plan.BT) * h.plan.N > kNoAllocCounters)
+    return CF_ERR_INVALID_ARG;
   h.ws = nullptr;  // nothing to free: the workspace is the static scratch
   h.acc = reinterpret_cast<float*>(scratch);
   h.counters = reinterpret_cast<int*>(scratch + kNoAllocAccFloats * 4);
   h.errflag = reinterpret_cast<int*>(scratch + kNoAllocAccFloats * 4 + kNoAllocCounters * 4);
   h.dbg = nullptr;
   h.timeline = nullptr;
-  h.prefetch_ahead = std::max(0, c.prefetch_ahead);
-  h.prefetch_late = std::max(0, c.prefetch_late);
-  h.pdl = c.pdl != -1;
-  for (int i = 0; i < 64; ++i) {
-    const double two_pi = 6.283185307179586476925286766559;
-    const double rate = (i < D / 2) ? std::pow((double)c.rope_theta, -2.0 * i / (double)D) / two_pi
-                                    : 0.0;
-    h.turn_hi[i] = (float)rate;
-    h.turn_lo[i] = (float)(rate - (double)h.turn_hi[i]);
-  }
-  for (MapCache* mc : {&h.m_wqkv, &h.m_wo, &h.m_k, &h.m_v}) {
+  for (MapCache* mc : {&h.m_wqkv, &h.m_wo, &h.m_k, &h.m_v, &h.m_x}) {
     for (int i = 0; i < MapCache::kSlots; ++i) mc->ptr[i] = nullptr;
     mc->next = 0;
   }

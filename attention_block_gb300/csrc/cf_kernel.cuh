@@ -42,121 +42,14 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "cf_attention.cuh"
 #include "cf_cluster.cuh"
+#include "cf_common.cuh"
 #include "cf_params.h"
 #include "cf_ptx.cuh"
 
 namespace cf {
 
-// ------------------------------------------------------------ conversions --
-template <typename T>
-struct Elem;
-template <>
-struct Elem<float> {
-  static __device__ __forceinline__ float to_f(float v) { return v; }
-  static __device__ __forceinline__ float from_f(float v) { return v; }
-  static __device__ __forceinline__ void words(const uint32_t* w, int nw, float* f) {
-    for (int i = 0; i < nw; ++i) f[i] = __uint_as_float(w[i]);
-  }
-};
-template <>
-struct Elem<__half> {
-  static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
-  static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
-  static __device__ __forceinline__ void words(const uint32_t* w, int nw, float* f) {
-    for (int i = 0; i < nw; ++i) {
-      float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    }
-  }
-};
-template <>
-struct Elem<__nv_bfloat16> {
-  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
-  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
-  static __device__ __forceinline__ void words(const uint32_t* w, int nw, float* f) {
-    for (int i = 0; i < nw; ++i) {
-      float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    }
-  }
-};
-
-// Load NE contiguous elements (NE*sizeof(T) in {4, 8, 16} bytes, naturally
-// aligned) and widen them to fp32.
-template <typename T, int NE>
-__device__ __forceinline__ void load_cvt(const T* p, float* f) {
-  constexpr int B = NE * (int)sizeof(T);
-  static_assert(B == 4 || B == 8 || B == 16, "vector width");
-  if constexpr (B == 16) {
-    uint4 u = *reinterpret_cast<const uint4*>(p);
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    Elem<T>::words(w, 4, f);
-  } else if constexpr (B == 8) {
-    uint2 u = *reinterpret_cast<const uint2*>(p);
-    uint32_t w[2] = {u.x, u.y};
-    Elem<T>::words(w, 2, f);
-  } else {
-    uint32_t w[1] = {*reinterpret_cast<const uint32_t*>(p)};
-    Elem<T>::words(w, 1, f);
-  }
-}
-
-// Store 4 consecutive elements from fp32 (round to nearest even).
-template <typename T>
-__device__ __forceinline__ void store4(T* p, const float* f) {
-  if constexpr (sizeof(T) == 4) {
-    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
-  } else {
-    T t[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) t[e] = Elem<T>::from_f(f[e]);
-    *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(t);
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Position tiles [t0, t1) of the cached keys 0..pos-1 handled by block `rank`
-// (balanced split of ceil(pos/Rt) tiles over N blocks).  pos < 0 marks an
-// invalid row; pos == 0 has no cached key (only the new token).
-__device__ __forceinline__ void kv_tile_range(int pos, int Rt, int rank, int N, int& t0,
-                                              int& t1) {
-  if (pos <= 0) {
-    t0 = t1 = 0;
-    return;
-  }
-  const int nt = (pos + Rt - 1) / Rt;
-  t0 = (int)(((long long)rank * nt) / N);
-  t1 = (int)(((long long)(rank + 1) * nt) / N);
-}
-
-// cos and sin of the RoPE angle pos * theta^(-2i/d) [LNA §三] without FP64
-// (GB300's double-precision path is slow and this sits between two cluster
-// exchanges).  The angle is reduced to a fraction of a turn exactly: the turn
-// rate c = theta^(-2i/d) / (2 pi) comes from the host (computed in float64)
-// as an unevaluated pair hi + lo of floats; pos < 2^24 is exact in fp32;
-// pos*hi is split into its rounded value and exact error with one FMA
-// (Dekker's two-product); subtracting the nearest integer is exact
-// (Sterbenz).  The remaining fraction t, |t| <= 1/2 + 2^-20, goes to
-// sincospif(2t) = (sin, cos)(2 pi t); the angle error stays below 1e-7 rad
-// for every pos < 2^24.
-__device__ __forceinline__ void rope_cos_sin(int pos, float hi, float lo, float& c, float& s) {
-  const float pf = (float)pos;
-  const float ph = pf * hi;
-  const float pe = fmaf(pf, hi, -ph);
-  const float fr = ph - rintf(ph);
-  const float t = fr + fmaf(pf, lo, pe);
-  sincospif(2.0f * t, &s, &c);
-}
-
-constexpr int kBarConsumers = 1;  // named barrier id of the 256 consumer threads
 
 // MINB: blocks per SM the register allocation must allow (2 for the
 // small-state instances, so two 288-thread blocks fit in 64K registers).
@@ -164,15 +57,7 @@ template <typename T, int D, int G, int BT, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_constant__ KParams p) {
   constexpr int NSEG = G + 2;          // q heads of the group, k, v
   constexpr int CPL = D / 32;          // projection columns per lane per segment
-  // attention: LPP lanes share one position; each lane owns DPL head dims
-  constexpr int LPP = (4 * G < 8) ? 8 : ((4 * G > 32) ? 32 : 4 * G);
-  constexpr int NGRP = 32 / LPP;
-  constexpr int DPL = D / LPP;
-  constexpr int PB = (DPL * (int)sizeof(T) < 16) ? DPL * (int)sizeof(T) : 16;
-  constexpr int EP = PB / (int)sizeof(T);  // elements per load piece
-  constexpr int NPC = DPL / EP;            // pieces per lane
   static_assert(D == 64 || D == 128, "head_dim");
-  static_assert(DPL % EP == 0 && NPC >= 1, "lane split");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -577,194 +462,15 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
 
     stamp(kTlGather);
     // ---- Phase 2: split-KV online-softmax attention [CF §3.2] ------------
-    {
-      const int grp = lane / LPP, kl = lane % LPP;
-      float* wst = scratch;  // [8 warps][G][D+4]: o[D], m, l
-      for (int bb = 0; bb < BT; ++bb) {
-        const int pos = s_pos[bb];
-        float q[G][DPL], o[G][DPL], m[G], l[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          m[h] = -INFINITY;
-          l[h] = 0.f;
-#pragma unroll
-          for (int i = 0; i < NPC; ++i)
-#pragma unroll
-            for (int e = 0; e < EP; ++e) {
-              const int dim = (kl + i * LPP) * EP + e;
-              q[h][i * EP + e] = qkv[(bb * NSEG + h) * D + dim] * p.qk_scale_log2;
-              o[h][i * EP + e] = 0.f;
-            }
-        }
-        // Two positions' contribution to this lane group's running state: the
-        // two dot products, reductions and exponentials are independent
-        // (instruction-level parallelism); the state is rescaled once.
-        auto score = [&](const T* krow, float (&sc)[G]) {
-          float kf[DPL];
-#pragma unroll
-          for (int i = 0; i < NPC; ++i) load_cvt<T, EP>(krow + (kl + i * LPP) * EP, kf + i * EP);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < DPL; e += 2) {
-              s0 = fmaf(q[h][e], kf[e], s0);
-              s1 = fmaf(q[h][e + 1], kf[e + 1], s1);
-            }
-            sc[h] = s0 + s1;
-          }
-        };
-        auto consume2 = [&](const T* kA, const T* vA, bool okA, const T* kB, const T* vB,
-                            bool okB) {
-          float sa[G], sb[G];
-          score(kA, sa);
-          score(kB, sb);
-#pragma unroll
-          for (int off = LPP / 2; off >= 1; off >>= 1)
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              sa[h] += __shfl_xor_sync(0xffffffffu, sa[h], off);
-              sb[h] += __shfl_xor_sync(0xffffffffu, sb[h], off);
-            }
-          if (okA || okB) {
-            float va[DPL], vb[DPL];
-#pragma unroll
-            for (int i = 0; i < NPC; ++i) {
-              load_cvt<T, EP>(vA + (kl + i * LPP) * EP, va + i * EP);
-              load_cvt<T, EP>(vB + (kl + i * LPP) * EP, vb + i * EP);
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float mn = m[h];
-              if (okA) mn = fmaxf(mn, sa[h]);
-              if (okB) mn = fmaxf(mn, sb[h]);
-              const float alpha = exp2f(m[h] - mn);
-              const float pa = okA ? exp2f(sa[h] - mn) : 0.f;
-              const float pb2 = okB ? exp2f(sb[h] - mn) : 0.f;
-              l[h] = fmaf(l[h], alpha, pa + pb2);
-#pragma unroll
-              for (int e = 0; e < DPL; ++e)
-                o[h][e] = fmaf(o[h][e], alpha, fmaf(pa, va[e], pb2 * vb[e]));
-              m[h] = mn;
-            }
-          }
-        };
-        int t0, t1;
-        kv_tile_range(pos, p.Rt, rank, N, t0, t1);
-        constexpr int kStep = kConsumerWarps * NGRP;  // positions per warp-wide pass
-        for (int t = t0; t < t1; ++t, ++it) {
-          const int s = it % p.stages;
-          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
-          if (bb == 0 && t == t0) stamp(kTlAttnFirst);
-          const T* Kt = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
-          const T* Vt = Kt + (size_t)p.Rt * D;
-          const int lim = min(p.Rt, pos - t * p.Rt);  // cached positions < pos only
-          for (int pb = warp * NGRP; pb < lim; pb += 2 * kStep) {
-            const int pa = pb + grp, pbb = pb + kStep + grp;
-            const bool okA = pa < lim, okB = pbb < lim;
-            const int ra = okA ? pa : pb, rb = okB ? pbb : pb;
-            consume2(Kt + (size_t)ra * D, Vt + (size_t)ra * D, okA, Kt + (size_t)rb * D,
-                     Vt + (size_t)rb * D, okB);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
-        }
-        // The new token (position pos) comes from shared memory, not the
-        // cache; the last block of the cluster folds it in.
-        if (rank == N - 1 && warp == 0 && pos >= 0) {
-          const float* kn = qkv + (bb * NSEG + G) * D;
-          const float* vn = qkv + (bb * NSEG + G + 1) * D;
-          float kf[DPL], vf[DPL];
-#pragma unroll
-          for (int i = 0; i < NPC; ++i)
-#pragma unroll
-            for (int e = 0; e < EP; ++e) {
-              kf[i * EP + e] = kn[(kl + i * LPP) * EP + e];
-              vf[i * EP + e] = vn[(kl + i * LPP) * EP + e];
-            }
-          float sc[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float s = 0.f;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) s = fmaf(q[h][e], kf[e], s);
-            sc[h] = s;
-          }
-#pragma unroll
-          for (int off = LPP / 2; off >= 1; off >>= 1)
-#pragma unroll
-            for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
-          if (grp == 0) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const float mn = fmaxf(m[h], sc[h]);
-              const float alpha = exp2f(m[h] - mn);
-              const float pe = exp2f(sc[h] - mn);
-              l[h] = fmaf(l[h], alpha, pe);
-#pragma unroll
-              for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(o[h][e], alpha, pe * vf[e]);
-              m[h] = mn;
-            }
-          }
-        }
-        if (bb == 0) stamp(kTlAttnLoop);
-        // Merge the lane groups of the warp.
-#pragma unroll
-        for (int off = LPP; off < 32; off <<= 1)
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m[h], off);
-            const float lo = __shfl_xor_sync(0xffffffffu, l[h], off);
-            const float mn = fmaxf(m[h], mo);
-            const float a = (mn == -INFINITY) ? 0.f : exp2f(m[h] - mn);
-            const float b = (mn == -INFINITY) ? 0.f : exp2f(mo - mn);
-            l[h] = l[h] * a + lo * b;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) {
-              const float oo = __shfl_xor_sync(0xffffffffu, o[h][e], off);
-              o[h][e] = o[h][e] * a + oo * b;
-            }
-            m[h] = mn;
-          }
-        if (grp == 0) {
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float* st = wst + (warp * G + h) * (D + 4);
-#pragma unroll
-            for (int i = 0; i < NPC; ++i)
-#pragma unroll
-              for (int e = 0; e < EP; ++e) st[(kl + i * LPP) * EP + e] = o[h][i * EP + e];
-            if (kl == 0) {
-              st[D] = m[h];
-              st[D + 1] = l[h];
-            }
-          }
-        }
-        named_sync(kBarConsumers, kConsumers);
-        if (bb == 0) stamp(kTlAttnWarps);
-        // Merge the 8 warps into this block's partial (m, l, o) of row bb.
-        for (int idx = tid; idx < G * D; idx += kConsumers) {
-          const int h = idx / D, dim = idx % D;
-          float M = -INFINITY;
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wst[(w * G + h) * (D + 4) + D]);
-          float O = 0.f, L = 0.f;
-          if (M != -INFINITY) {
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              const float* st = wst + (w * G + h) * (D + 4);
-              const float f = exp2f(st[D] - M);
-              O = fmaf(f, st[dim], O);
-              L = fmaf(f, st[D + 1], L);
-            }
-          }
-          float* dst = smx + (bb * G + h) * (D + 4);
-          dst[dim] = O;
-          if (dim == 0) {
-            dst[D] = M;
-            dst[D + 1] = L;
-          }
-        }
-        named_sync(kBarConsumers, kConsumers);
-      }
+    // Block `rank` takes its share of each row's position tiles; the last
+    // block of the cluster also folds in the new token.
+    for (int bb = 0; bb < BT; ++bb) {
+      const float* qb = qkv + bb * NSEG * D;
+      attend_row<T, D, G>(p, qb, qb + G * D, qb + (G + 1) * D, s_pos[bb], rank, N, rank == N - 1,
+                          ring, full, empty, it, scratch, smx + bb * G * (D + 4),
+                          (p.timeline != nullptr && bb == 0)
+                              ? p.timeline + blockIdx.x * kTimelineSlots
+                              : nullptr);
     }
 
     stamp(kTlAttn);

@@ -1,0 +1,512 @@
+// cf_kernel_rows.cuh -- the fused decode attention block for batched decode
+// (16 to 64 rows per cluster) on sm_103a.
+//
+// Pages cited by title and section:
+//   [CF]  "ClusterFusion框架深度解析：LLM推理优化的集群级通信革命" (devpress.csdn.net)
+//   [LNA] "大模型推理中的算子融合优化：LayerNorm + Attention 的 CUDA Kernel 手写与验证"
+//         (asdsk.com)
+//
+// Same computation as cf_kernel.cuh ([CF §3.2] fused_qkv_attention_out,
+// [LNA §一]); the mapping changes with the batch.  One thread-block cluster
+// serves one KV head g and a tile of BT batch rows, so every weight byte of
+// the head group is read once per tile; its N = BT / RPC blocks
+//   * split the hidden (reduction) dimension of the QKV projection, now a
+//     real [BT x H] x [H x (G+2)d] contraction done on the tensor cores
+//     (mma.sync m16n8k16, fp32 accumulation; the fp32 activations enter as a
+//     pair of 16-bit values hi + lo, so the product keeps ~fp32 accuracy);
+//   * combine the partial products with ClusterReduce in reduce-scatter form
+//     over BATCH ROWS [CF §3.1.1]: block c ends up owning rows
+//     [c*RPC, (c+1)*RPC) of the tile, applies the RMSNorm scale, RoPE and
+//     the KV append to them, and runs their attention over the whole
+//     sequence (no cross-block softmax merge is needed);
+//   * exchange the attention outputs with ClusterGather [CF §3.1.2] so that
+//     every block holds o for all BT rows, then split the output projection
+//     by columns (tensor cores again) and merge heads with fp32 atomics
+//     [CF §3.2 原子写合并]; the last block per (tile, column band) adds the
+//     residual and writes `out`.
+// Weight tiles arrive through TMA with the 128-byte swizzle so that the
+// ldmatrix fragment loads are free of bank conflicts; the batch rows of x
+// arrive with each weight tile.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "cf_attention.cuh"
+#include "cf_cluster.cuh"
+#include "cf_common.cuh"
+#include "cf_mma.cuh"
+#include "cf_params.h"
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+template <typename T, int D, int G, int BT, int RPC>
+__global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_constant__ KParams p) {
+  constexpr int NSEG = G + 2;        // q heads of the group, k, v
+  constexpr int NC = NSEG * D;       // projection columns of the group
+  constexpr int MT = BT / 16;        // MMA row tiles
+  constexpr int NTW = NC / 8 / kConsumerWarps;  // projection n-tiles per warp
+  constexpr int GD = G * D;          // O-projection reduction size
+  static_assert(BT % 16 == 0 && BT % RPC == 0, "batch tile");
+  static_assert(NC % (8 * kConsumerWarps) == 0, "projection columns per warp");
+  static_assert(D % 64 == 0, "head_dim in 64-column swizzle boxes");
+  using MK = MmaKind<T>;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int N = p.N;  // == BT / RPC
+  const int rank = (int)cluster_ctarank();
+  const int cid = blockIdx.x / N;
+  const int g = cid / p.nbt;
+  const int bt = cid % p.nbt;
+  const int b0 = bt * BT;
+  const int Hc = p.H / N;  // K band rows == O-proj column band
+  const int k0 = rank * Hc;
+  const int nrounds = __ffs(N) - 1;
+  const int SE = RPC * NC;  // reduce-scatter slice (RPC rows)
+  const int SEo = RPC * GD; // gather slice of o
+  const int r0 = rank * RPC;  // first owned row of the tile
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.L.bars);
+  uint64_t* full = bars + BarIdx::full;
+  uint64_t* empty = bars + BarIdx::empty;
+  uint8_t* ring = sm + p.L.ring;
+  float* red = reinterpret_cast<float*>(sm + p.L.red);          // [BT][NC] partials
+  float* rsrecv = reinterpret_cast<float*>(sm + p.L.scratch);   // RS receive, then warp states
+  float* ogath = reinterpret_cast<float*>(sm + p.L.qkv);        // [BT][GD] o of every row
+  float* rec = reinterpret_cast<float*>(sm + p.L.sm);           // [G][D+4] attention record
+  uint8_t* abuf = sm + p.L.xn;                                  // A operand staging
+  float* gband = reinterpret_cast<float*>(sm + p.L.scale);      // ln_weight band [Hc]
+  float* rope = reinterpret_cast<float*>(sm + p.L.rope);        // [RPC][D/2][2]
+  int* s_pos = reinterpret_cast<int*>(sm + p.L.misc);           // [BT]
+  int* s_flag = s_pos + BT;
+  float* s_rinv = reinterpret_cast<float*>(s_flag + 4);          // [RPC]
+  float* wred = s_rinv + RPC;                                    // [8][RPC]
+
+  // ---------------------------------------------------------------- setup --
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    for (int r = 0; r < nrounds; ++r) {
+      mbar_init(&bars[BarIdx::rs + r], 1);
+      mbar_init(&bars[BarIdx::ga + r], 1);
+    }
+    fence_mbar_init_cluster();
+    for (int r = 0; r < nrounds; ++r) {
+      mbar_arrive_expect_tx(&bars[BarIdx::rs + r], reduce_scatter_round_bytes(N, r, SE));
+      mbar_arrive_expect_tx(&bars[BarIdx::ga + r], gather_round_bytes(r, SEo));
+    }
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&p.tm_wqkv);
+    prefetch_tensormap(&p.tm_x);
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+    prefetch_tensormap(&p.tm_wo);
+  }
+  __syncthreads();
+  cluster_sync_all();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = tid; i < BT; i += kThreads) {
+    const int b = b0 + i;
+    int pos = -1;
+    if (b < p.B) {
+      pos = p.positions[b];
+      if (pos < 0 || pos >= p.S) {
+        if (rank == 0 && g == 0) atomicOr(p.errflag, kDevErrPosRange);
+        pos = -1;
+      }
+    }
+    s_pos[i] = pos;
+  }
+  __syncthreads();
+  auto stamp = [&](int slot) {
+    if (p.timeline != nullptr && tid == 0)
+      p.timeline[blockIdx.x * kTimelineSlots + slot] = globaltimer_ns();
+  };
+  stamp(kTlStart);
+
+  const int nkt = Hc / p.Rw;
+  const int ncb = Hc / p.Co;
+  const int nrt = GD / p.Ro;
+  const int wboxes = NC / 64;                        // 64-column boxes per W_qkv tile
+  const uint32_t wbox_bytes = (uint32_t)(p.Rw * 128);
+  const uint32_t x_bytes = (uint32_t)(BT * p.Rw * 2);
+  const int obox = p.Co / 64;                        // 64-column boxes per W_o tile
+  const uint32_t obox_bytes = (uint32_t)(p.Ro * 128);
+
+  if (warp == kConsumerWarps) {
+    // ============================================== TMA producer warp ====
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int it = 0;
+      auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
+        const int s = it % p.stages;
+        if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+        bar = &full[s];
+        mbar_arrive_expect_tx(bar, bytes);
+        return ring + (size_t)s * p.stage_bytes;
+      };
+      // Phase 1: W_qkv tiles (G+2 head slices, 64-column swizzled boxes) of the
+      // K band, each followed by the matching [BT x Rw] slice of x.
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        uint64_t* bar;
+        uint8_t* dst = slot(wboxes * wbox_bytes + x_bytes, bar);
+        const int y = k0 + kt * p.Rw;
+        for (int bx = 0; bx < wboxes; ++bx) {
+          const int col = bx * 64;  // column inside the group's NC columns
+          const int sg = col / D, cin = col % D;
+          const int gx = (sg < G) ? ((g * G + sg) * D + cin)
+                                  : ((sg == G ? p.nq + g : p.nq + p.nkv + g) * D + cin);
+          tma_load_2d(dst + bx * wbox_bytes, &p.tm_wqkv, gx, y, bar, pol);
+        }
+        tma_load_2d(dst + wboxes * wbox_bytes, &p.tm_x, y, b0, bar, pol);
+      }
+      if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdW] = globaltimer_ns();
+      // Phase 2: K/V tiles of the owned rows, whole sequence each.
+      const uint32_t kv_bytes = (uint32_t)(p.Rt * D * sizeof(T));
+      for (int r = 0; r < RPC; ++r) {
+        int t0, t1;
+        kv_tile_range(s_pos[r0 + r], p.Rt, 0, 1, t0, t1);
+        for (int t = t0; t < t1; ++t, ++it) {
+          uint64_t* bar;
+          uint8_t* dst = slot(2 * kv_bytes, bar);
+          tma_load_4d(dst, &p.tm_k, 0, g, t * p.Rt, b0 + r0 + r, bar, pol);
+          tma_load_4d(dst + kv_bytes, &p.tm_v, 0, g, t * p.Rt, b0 + r0 + r, bar, pol);
+        }
+      }
+      if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdKV] = globaltimer_ns();
+      // Phase 3: W_o tiles (swizzled 64-column boxes) of the column band.
+      for (int cb = 0; cb < ncb; ++cb)
+        for (int rt = 0; rt < nrt; ++rt, ++it) {
+          uint64_t* bar;
+          uint8_t* dst = slot(obox * obox_bytes, bar);
+          for (int bx = 0; bx < obox; ++bx)
+            tma_load_2d(dst + bx * obox_bytes, &p.tm_wo, k0 + cb * p.Co + bx * 64,
+                        g * GD + rt * p.Ro, bar, pol);
+        }
+      if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdAll] = globaltimer_ns();
+    }
+    __syncwarp();
+  } else {
+    // ============================================== consumer warps =======
+    const T* __restrict__ hidden = reinterpret_cast<const T*>(p.hidden);
+    const T* __restrict__ lnw = reinterpret_cast<const T*>(p.ln_w);
+    int it = 0;
+
+    // ---- Phase 0: ln_weight band, sums of squares of the owned rows, the
+    // owned rows' RoPE factors [LNA §三 stage 1] --------------------------
+    for (int i = tid; i < Hc; i += kConsumers) gband[i] = Elem<T>::to_f(lnw[k0 + i]);
+    {
+      constexpr int EV = 16 / (int)sizeof(T);
+      for (int r = 0; r < RPC; ++r) {
+        float ss = 0.f;
+        const int b = b0 + r0 + r;
+        if (b < p.B) {
+          const T* x = hidden + (size_t)b * p.H;
+          for (int i = tid * EV; i < p.H; i += kConsumers * EV) {
+            float f[EV];
+            load_cvt<T, EV>(x + i, f);
+#pragma unroll
+            for (int e = 0; e < EV; ++e) ss = fmaf(f[e], f[e], ss);
+          }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) wred[warp * RPC + r] = ss;
+      }
+      for (int idx = tid; idx < RPC * (D / 2); idx += kConsumers) {
+        const int r = idx / (D / 2), j = idx % (D / 2);
+        const int pos = s_pos[r0 + r];
+        float c = 1.f, sn = 0.f;
+        if (pos >= 0) rope_cos_sin(pos, p.turn_hi[j], p.turn_lo[j], c, sn);
+        rope[2 * idx] = c;
+        rope[2 * idx + 1] = sn;
+      }
+    }
+    named_sync(kBarConsumers, kConsumers);
+    stamp(kTlNorm);
+
+    // ---- Phase 1: [BT x Hc] x [Hc x NC] on the tensor cores ---------------
+    {
+      float acc[MT][NTW][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
+      const int apitch = (p.Rw + 8) * 2;  // bytes per A row (odd multiple of 16)
+      const int abytes = BT * apitch;
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        const int s = it % p.stages;
+        mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        uint8_t* st = ring + (size_t)s * p.stage_bytes;
+        const T* xt = reinterpret_cast<const T*>(st + wboxes * wbox_bytes);  // [BT][Rw]
+        // x * g of this K slice as hi + lo 16-bit pairs (double-buffered)
+        uint8_t* ahi = abuf + (size_t)(kt & 1) * 2 * abytes;
+        uint8_t* alo = ahi + abytes;
+        for (int i2 = tid; i2 < BT * p.Rw / 2; i2 += kConsumers) {
+          const int row = (2 * i2) / p.Rw, k = (2 * i2) % p.Rw;
+          float f[2];
+          load_cvt<T, 2>(xt + row * p.Rw + k, f);
+          const float v0 = f[0] * gband[kt * p.Rw + k], v1 = f[1] * gband[kt * p.Rw + k + 1];
+          uint32_t hi, lo;
+          MK::split2(v0, v1, hi, lo);
+          *reinterpret_cast<uint32_t*>(ahi + row * apitch + k * 2) = hi;
+          *reinterpret_cast<uint32_t*>(alo + row * apitch + k * 2) = lo;
+        }
+        named_sync(kBarConsumers, kConsumers);
+        for (int ks = 0; ks < p.Rw / 16; ++ks) {
+          uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            ldmatrix_a(ah[mt], ahi + mt * 16 * apitch + ks * 32, apitch, lane);
+            ldmatrix_a(al[mt], alo + mt * 16 * apitch + ks * 32, apitch, lane);
+          }
+#pragma unroll
+          for (int j = 0; j < NTW; ++j) {
+            const int n = (warp * NTW + j) * 8;  // column in [0, NC)
+            uint32_t b0r, b1r;
+            ldmatrix_b_sw128(b0r, b1r, st + (n / 64) * wbox_bytes, ks * 16, n % 64, lane);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              MK::mma(acc[mt][j], ah[mt], b0r, b1r);
+              MK::mma(acc[mt][j], al[mt], b0r, b1r);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+      stamp(kTlProjLoop);
+      // partial sums -> red [BT][NC] (row-major, so the owned rows of block c
+      // form the contiguous slice c of the reduce-scatter)
+      const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < NTW; ++j) {
+          const int n = (warp * NTW + j) * 8 + 2 * tq;
+          const int row = mt * 16 + gq;
+          *reinterpret_cast<float2*>(red + row * NC + n) = make_float2(acc[mt][j][0], acc[mt][j][1]);
+          *reinterpret_cast<float2*>(red + (row + 8) * NC + n) =
+              make_float2(acc[mt][j][2], acc[mt][j][3]);
+        }
+      if (tid < RPC) {
+        float tot = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) tot += wred[w * RPC + tid];
+        s_rinv[tid] = (b0 + r0 + tid < p.B) ? 1.0f / sqrtf(tot / (float)p.H + p.eps) : 0.f;
+      }
+      named_sync(kBarConsumers, kConsumers);
+    }
+    stamp(kTlProj);
+
+    // ---- ClusterReduce (reduce-scatter over rows): block `rank` owns rows
+    // [rank*RPC, (rank+1)*RPC) of the tile, fully summed ----------------------
+    cluster_reduce_scatter<kConsumers, kBarConsumers>(red, SE, rsrecv, &bars[BarIdx::rs], rank, N,
+                                                      tid, p.errflag);
+    stamp(kTlReduceScatter);
+
+    // ---- RMSNorm scale, RoPE, KV append of the owned rows [LNA §三] -------
+    float* own = red + rank * SE;  // [RPC][NSEG][D]
+    {
+      T* kc = reinterpret_cast<T*>(p.k_cache);
+      T* vc = reinterpret_cast<T*>(p.v_cache);
+      for (int idx = tid; idx < RPC * NSEG * (D / 2); idx += kConsumers) {
+        const int r = idx / (NSEG * (D / 2)), rem = idx % (NSEG * (D / 2));
+        const int sg = rem / (D / 2), i = rem % (D / 2);
+        const int pos = s_pos[r0 + r];
+        float* u = own + (r * NSEG + sg) * D;
+        float a = u[i] * s_rinv[r], bv = u[i + D / 2] * s_rinv[r];
+        if (sg <= G && pos >= 0) {
+          const float c = rope[2 * (r * (D / 2) + i)], sn = rope[2 * (r * (D / 2) + i) + 1];
+          const float ra = a * c - bv * sn;
+          const float rb = bv * c + a * sn;
+          a = ra;
+          bv = rb;
+        }
+        if (sg >= G && pos >= 0) {
+          T* cache = (sg == G) ? kc : vc;
+          const size_t base = (((size_t)(b0 + r0 + r) * p.S + pos) * p.nkv + g) * D;
+          cache[base + i] = Elem<T>::from_f(a);
+          cache[base + D / 2 + i] = Elem<T>::from_f(bv);
+        }
+        u[i] = a;
+        u[i + D / 2] = bv;
+      }
+      named_sync(kBarConsumers, kConsumers);
+      if (p.dbg != nullptr) {
+        float* dq = p.dbg;
+        float* dk = dq + (size_t)p.B * p.nq * D;
+        float* dv = dk + (size_t)p.B * p.nkv * D;
+        for (int idx = tid; idx < RPC * NC; idx += kConsumers) {
+          const int r = idx / NC, rem = idx % NC, sg = rem / D, dim = rem % D;
+          const int b = b0 + r0 + r;
+          if (b >= p.B || s_pos[r0 + r] < 0) continue;
+          if (sg < G) dq[((size_t)b * p.nq + g * G + sg) * D + dim] = own[idx];
+          else if (sg == G) dk[((size_t)b * p.nkv + g) * D + dim] = own[idx];
+          else dv[((size_t)b * p.nkv + g) * D + dim] = own[idx];
+        }
+      }
+    }
+    stamp(kTlGather);
+
+    // ---- Attention of the owned rows over their whole sequence ------------
+    for (int r = 0; r < RPC; ++r) {
+      const float* qr = own + r * NC;
+      attend_row<T, D, G>(p, qr, qr + G * D, qr + (G + 1) * D, s_pos[r0 + r], 0, 1, true, ring,
+                          full, empty, it, rsrecv, rec,
+                          (p.timeline != nullptr && r == 0) ? p.timeline + blockIdx.x * kTimelineSlots
+                                                           : nullptr);
+      // o = O / L into the owned slice of the gather buffer
+      for (int idx = tid; idx < GD; idx += kConsumers) {
+        const int h = idx / D, dim = idx % D;
+        const float L = rec[h * (D + 4) + D + 1];
+        ogath[(r0 + r) * GD + idx] = (L > 0.f) ? rec[h * (D + 4) + dim] / L : 0.f;
+      }
+      named_sync(kBarConsumers, kConsumers);
+    }
+    stamp(kTlAttn);
+
+    // ---- ClusterGather of o [CF §3.1.2]: every block gets all BT rows -----
+    cluster_gather<kConsumers, kBarConsumers>(ogath, SEo, &bars[BarIdx::ga], rank, N, tid,
+                                              p.errflag);
+    stamp(kTlMax);
+    if (p.dbg != nullptr && rank == 0) {
+      float* dob = p.dbg + (size_t)p.B * (p.nq + 2 * p.nkv) * D;
+      for (int idx = tid; idx < BT * GD; idx += kConsumers) {
+        const int rr = idx / GD, rem = idx % GD;
+        const int b = b0 + rr;
+        if (b >= p.B || s_pos[rr] < 0) continue;
+        dob[((size_t)b * p.nq + g * G) * D + rem] = ogath[idx];
+      }
+    }
+    // o as hi + lo 16-bit pairs for the O-projection A operand (in `red`,
+    // which the reduce-scatter no longer needs)
+    const int opitch = (GD + 8) * 2;
+    uint8_t* ohi = reinterpret_cast<uint8_t*>(red);
+    uint8_t* olo = ohi + BT * opitch;
+    for (int i2 = tid; i2 < BT * GD / 2; i2 += kConsumers) {
+      const int row = (2 * i2) / GD, k = (2 * i2) % GD;
+      uint32_t hi, lo;
+      MK::split2(ogath[row * GD + k], ogath[row * GD + k + 1], hi, lo);
+      *reinterpret_cast<uint32_t*>(ohi + row * opitch + k * 2) = hi;
+      *reinterpret_cast<uint32_t*>(olo + row * opitch + k * 2) = lo;
+    }
+    named_sync(kBarConsumers, kConsumers);
+    stamp(kTlSum);
+
+    // ---- Phase 3: [BT x GD] x [GD x Co] per column box on the tensor cores,
+    // fp32 atomics into the accumulator [CF §3.2] ----------------------------
+    {
+      const int ntiles = p.Co / 8;
+      const int gq = lane >> 2, tq = lane & 3;
+      for (int cb = 0; cb < ncb; ++cb) {
+        float acc[MT][4][4];  // up to 4 n-tiles per warp per box (Co <= 256)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
+        for (int rt = 0; rt < nrt; ++rt, ++it) {
+          const int s = it % p.stages;
+          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+          if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
+          uint8_t* st = ring + (size_t)s * p.stage_bytes;
+          for (int ks = 0; ks < p.Ro / 16; ++ks) {
+            const int kglob = rt * p.Ro + ks * 16;
+            uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              ldmatrix_a(ah[mt], ohi + mt * 16 * opitch + kglob * 2, opitch, lane);
+              ldmatrix_a(al[mt], olo + mt * 16 * opitch + kglob * 2, opitch, lane);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int nt = warp + j * kConsumerWarps;
+              if (nt < ntiles) {
+                const int n = nt * 8;
+                uint32_t b0r, b1r;
+                ldmatrix_b_sw128(b0r, b1r, st + (n / 64) * obox_bytes, ks * 16, n % 64, lane);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                  MK::mma(acc[mt][j], ah[mt], b0r, b1r);
+                  MK::mma(acc[mt][j], al[mt], b0r, b1r);
+                }
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int nt = warp + j * kConsumerWarps;
+          if (nt >= ntiles) continue;
+          const int col = k0 + cb * p.Co + nt * 8 + 2 * tq;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const int ra = mt * 16 + gq, rb = ra + 8;
+            if (b0 + ra < p.B && s_pos[ra] >= 0)
+              atomicAdd(reinterpret_cast<float2*>(p.acc + (size_t)(b0 + ra) * p.H + col),
+                        make_float2(acc[mt][j][0], acc[mt][j][1]));
+            if (b0 + rb < p.B && s_pos[rb] >= 0)
+              atomicAdd(reinterpret_cast<float2*>(p.acc + (size_t)(b0 + rb) * p.H + col),
+                        make_float2(acc[mt][j][2], acc[mt][j][3]));
+          }
+        }
+      }
+    }
+    stamp(kTlOproj);
+
+    // ---- Residual + finalize by the last block of each (tile, band) ------
+    __threadfence();
+    named_sync(kBarConsumers, kConsumers);
+    if (tid == 0) {
+      const int ticket = atomicAdd(&p.counters[bt * N + rank], 1);
+      const int last = (ticket == p.nkv - 1);
+      if (last) __threadfence();
+      s_flag[0] = last;
+    }
+    named_sync(kBarConsumers, kConsumers);
+    stamp(kTlTicket);
+    if (s_flag[0]) {
+      T* out = reinterpret_cast<T*>(p.out);
+      float* dproj = p.dbg ? p.dbg + (size_t)p.B * (2 * p.nq + 2 * p.nkv) * D : nullptr;
+      const int C4 = Hc / 4;
+      for (int i4 = tid; i4 < BT * C4; i4 += kConsumers) {
+        const int bb = i4 / C4, c4 = i4 % C4;
+        const int b = b0 + bb;
+        if (b >= p.B) continue;
+        const size_t off = (size_t)b * p.H + k0 + c4 * 4;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
+        __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
+        float xf[4];
+        load_cvt<T, 4>(hidden + off, xf);
+        const float r4[4] = {xf[0] + v.x, xf[1] + v.y, xf[2] + v.z, xf[3] + v.w};
+        store4<T>(out + off, r4);
+        if (dproj) {
+          dproj[off + 0] = v.x;
+          dproj[off + 1] = v.y;
+          dproj[off + 2] = v.z;
+          dproj[off + 3] = v.w;
+        }
+      }
+      if (tid == 0) p.counters[bt * N + rank] = 0;
+    }
+  }
+  stamp(kTlFinal);
+  __syncwarp();
+  cluster_sync_all();
+  stamp(kTlEnd);
+}
+
+}  // namespace cf

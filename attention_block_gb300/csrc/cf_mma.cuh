@@ -1,0 +1,86 @@
+// cf_mma.cuh -- warp-level tensor-core helpers for the batched projections:
+// mma.sync m16n8k16 (fp16 or bf16 inputs, fp32 accumulate) and ldmatrix
+// fragment loads from shared memory.
+//
+// Fragment conventions (one warp, lane = 0..31, gq = lane / 4, tq = lane % 4):
+//   A (16x16, row-major)  4 regs: (gq, 2tq..+1), (gq+8, ..), (gq, 2tq+8..), (gq+8, ..)
+//   B (16x8, k-major)     2 regs: (k = 2tq..+1, n = gq), (k = 2tq+8..+9, n = gq)
+//   C (16x8, fp32)        4 regs: (gq, 2tq), (gq, 2tq+1), (gq+8, 2tq), (gq+8, 2tq+1)
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+template <typename T>
+struct MmaKind;  // PTX type names of the 16-bit input types
+template <>
+struct MmaKind<__half> {
+  static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  // hi = nearest 16-bit value of v, lo = nearest 16-bit value of (v - hi),
+  // packed two per word (element e0 in the low half).
+  static __device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(v0, v1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  }
+};
+template <>
+struct MmaKind<__nv_bfloat16> {
+  static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  static __device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  }
+};
+
+// A fragment of a 16x16 block of a row-major 16-bit matrix at `base` (row
+// pitch `pitch` bytes, a multiple of 16 that is not a multiple of 128, so the
+// eight rows of each 8x8 sub-matrix fall in distinct banks).
+__device__ __forceinline__ void ldmatrix_a(uint32_t (&a)[4], const void* base, int pitch,
+                                           int lane) {
+  const int r = lane & 15, kh = lane >> 4;  // lanes 16..31 address the k+8 half
+  const uint32_t addr = smem_u32(base) + r * pitch + kh * 16;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr));
+}
+
+// B fragment (16 k-rows x 8 n-columns) from a TMA box written with the
+// 128-byte swizzle: the box holds rows of 64 16-bit elements (128 bytes);
+// the 16-byte chunk j of row k sits at chunk position j ^ (k & 7).  `box`
+// must be 1024-byte aligned; k0 is a multiple of 16, n0 a multiple of 8.
+__device__ __forceinline__ void ldmatrix_b_sw128(uint32_t& b0, uint32_t& b1, const void* box,
+                                                 int k0, int n0, int lane) {
+  const int k = k0 + (lane & 15);
+  const int chunk = (n0 >> 3) ^ (k & 7);
+  const uint32_t addr = smem_u32(box) + k * 128 + chunk * 16;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(b0), "=r"(b1)
+               : "r"(addr));
+}
+
+}  // namespace cf

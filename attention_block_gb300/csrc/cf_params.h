@@ -77,6 +77,7 @@ struct KParams {  // 128-byte aligned through its CUtensorMap members
   CUtensorMap tm_wo;     // 2D {H, nq*D},         box {Co, Ro}
   CUtensorMap tm_k;      // 4D {D, nkv, S, B},    box {D, 1, Rt, 1}
   CUtensorMap tm_v;      // 4D {D, nkv, S, B},    box {D, 1, Rt, 1}
+  CUtensorMap tm_x;      // 2D {H, B},            box {Rw, BT} (batched kernel only)
   const void* hidden;    // [B, H]
   const void* ln_w;      // [H]
   void* k_cache;         // [B, S, nkv, D]

@@ -291,6 +291,8 @@ def main(argv=None):
                     default=int(os.environ.get("CF_PREFETCH_AHEAD", 0)))
     ap.add_argument("--prefetch-late", type=int, default=int(os.environ.get("CF_PREFETCH_LATE", 0)))
     ap.add_argument("--max-stages", type=int, default=int(os.environ.get("CF_MAX_STAGES", 0)))
+    ap.add_argument("--rows-per-block", type=int,
+                    default=int(os.environ.get("CF_ROWS_PER_BLOCK", 0)))
     ap.add_argument("--pdl", type=int, default=int(os.environ.get("CF_PDL", 0)),
                     help="programmatic dependent launch: 0 default (on), -1 off")
     ap.add_argument("--timeline", action="store_true",
@@ -343,7 +345,7 @@ def main(argv=None):
         dtype=w.dtype, cluster_size=args.cluster_size, batch_tile=args.batch_tile,
         stage_bytes=args.stage_bytes, ctas_per_sm=args.ctas_per_sm,
         prefetch_ahead=args.prefetch_ahead, prefetch_late=args.prefetch_late, pdl=args.pdl,
-        max_stages=args.max_stages)
+        max_stages=args.max_stages, rows_per_block=args.rows_per_block)
     info = blk.launch_info()
     outs = [[torch.empty_like(L["hidden"]) for L in rep] for rep in reps]
 

@@ -80,6 +80,8 @@ typedef struct cf_config {
                              -1 = off                                         */
   int32_t max_stages;     /* 0 = as many ring stages as fit, else at most this
                              many (>= 2)                                      */
+  int32_t rows_per_block; /* batched mode (batch_tile >= 16, fp16/bf16): batch
+                             rows each block of a cluster owns; 0 = default  */
 } cf_config;
 
 typedef struct cf_handle cf_handle; /* opaque */
@@ -91,6 +93,8 @@ typedef struct cf_launch_info {
   int32_t wo_rows_per_tile, wo_cols_per_tile;   /* Ro, Co                   */
   int32_t stages, stage_bytes, smem_bytes;      /* per CTA                  */
   int32_t threads, max_active_clusters, sm_count;
+  int32_t mode;            /* 0: sequence-split kernel, 1: batched row-split kernel */
+  int32_t rows_per_block;  /* mode 1 */
 } cf_launch_info;
 
 /* Validate cfg, pick the kernel instance and launch shape, and allocate the

@@ -115,3 +115,25 @@ def check_cache_untouched_except_slot(before: torch.Tensor, after: torch.Tensor,
         if 0 <= p < before.shape[1]:
             mask[b, p] = False
     assert torch.equal(before[mask], after[mask]), "cache bytes outside the new slot changed"
+
+
+def full_check(w, seed=0, rows=None, debug=True, t=None, **tune):
+    t = t if t is not None else synth.make_layer(w, seed, device="cuda")
+    out, kc, vc, dbg, st = run_gpu(w, t, debug=debug, **tune)
+    assert st == binding.CF_OK, binding.strerror(st)
+    rows = list(range(w.batch)) if rows is None else list(rows)
+    ref = run_oracle(w, t, rows)
+    pos = t["positions"].tolist()
+    check(out[rows].double().cpu().numpy(), round_to(ref["out"], w.dtype), "out")
+    check_cache_untouched_except_slot(t["k_cache"], kc, pos)
+    check_cache_untouched_except_slot(t["v_cache"], vc, pos)
+    ks = torch.stack([kc[b, pos[b]].reshape(-1) for b in rows]).double().cpu().numpy()
+    vs = torch.stack([vc[b, pos[b]].reshape(-1) for b in rows]).double().cpu().numpy()
+    check(ks, round_to(ref["kslot"], w.dtype), "k slot")
+    check(vs, round_to(ref["vslot"], w.dtype), "v slot")
+    if debug:
+        d = split_dbg(dbg, w, w.batch)
+        # fp32 on-chip intermediates against the unrounded oracle
+        for name in ("q", "k", "v", "o", "proj"):
+            check(d[name][rows], ref[name], name)
+    return out, ref

@@ -12,8 +12,7 @@ import pytest
 import torch
 
 from attention_block_gb300 import binding, synth
-from parity_util import (check, check_cache_untouched_except_slot, make_block, round_to, run_gpu,
-                         run_oracle, split_dbg)
+from parity_util import (check, full_check, make_block, round_to, run_gpu, run_oracle)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,28 +22,6 @@ def _need_cuda():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     binding.lib()
-
-
-def full_check(w, seed=0, rows=None, debug=True, t=None, **tune):
-    t = t if t is not None else synth.make_layer(w, seed, device="cuda")
-    out, kc, vc, dbg, st = run_gpu(w, t, debug=debug, **tune)
-    assert st == binding.CF_OK, binding.strerror(st)
-    rows = list(range(w.batch)) if rows is None else list(rows)
-    ref = run_oracle(w, t, rows)
-    pos = t["positions"].tolist()
-    check(out[rows].double().cpu().numpy(), round_to(ref["out"], w.dtype), "out")
-    check_cache_untouched_except_slot(t["k_cache"], kc, pos)
-    check_cache_untouched_except_slot(t["v_cache"], vc, pos)
-    ks = torch.stack([kc[b, pos[b]].reshape(-1) for b in rows]).double().cpu().numpy()
-    vs = torch.stack([vc[b, pos[b]].reshape(-1) for b in rows]).double().cpu().numpy()
-    check(ks, round_to(ref["kslot"], w.dtype), "k slot")
-    check(vs, round_to(ref["vslot"], w.dtype), "v slot")
-    if debug:
-        d = split_dbg(dbg, w, w.batch)
-        # fp32 on-chip intermediates against the unrounded oracle
-        for name in ("q", "k", "v", "o", "proj"):
-            check(d[name][rows], ref[name], name)
-    return out, ref
 
 
 # ----------------------------------------------------- benchmark workloads --
