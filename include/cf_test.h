@@ -54,6 +54,18 @@ int cf_bench_tma_stream(int hidden, int n_q_heads, int n_kv_heads, int head_dim,
                         int cluster_size, int rows_per_tile, int stages, int ctas_per_sm,
                         const void* w, int* errflag, void* stream);
 
+/* Bare TMA streaming rate of the batched kernel's K/V access pattern: one
+ * launch of n_kv_heads * batch / rows_per_block blocks; block i streams, for
+ * KV head i % n_kv_heads and each of its rows_per_block batch rows, positions
+ * [0, len) of the fp16 caches k_cache, v_cache [batch, s_max, n_kv_heads,
+ * head_dim] in tiles of pos_per_tile positions (one K and one V box per
+ * stage) through `stages` stages, shared memory padded so that ctas_per_sm
+ * blocks fit per SM.  No compute.  Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
+int cf_bench_kv_stream(int batch, int s_max, int n_kv_heads, int head_dim, int elem_bytes,
+                       int len, int rows_per_block, int pos_per_tile, int stages,
+                       int ctas_per_sm, const void* k_cache, const void* v_cache, int* errflag,
+                       void* stream);
+
 /* Phase timeline of later cf_decode_attn_block calls of handle h (a tuning
  * aid): when `stamps` is a zeroed device buffer of grid_blocks * 32 unsigned
  * 64-bit values, every block writes %globaltimer (ns) at its phase
