@@ -107,7 +107,7 @@ struct Plan {
 
 // Shared-memory plan of the batched row-split kernel (one block per SM):
 // N = BT / RPC blocks per cluster, K band Hc = H / N.  Returns false when the
-// shape does not fit (the caller reports CF_ERR_UNSUPPORTED).
+// shape does not fit (the caller then tries another instance).
 bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cudaDeviceProp& prop,
                     Plan& pl) {
   const int es = esize(c.dtype), D = c.head_dim, H = c.hidden;
@@ -115,7 +115,7 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   const int N = BT / RPC;
   if (N < 1 || N > kMaxCluster || (N & (N - 1)) != 0 || H % (64 * N) != 0) return false;
   const int Hc = H / N;
-  const int nrounds = __builtin_ctz((unsigned)N);
+  const int MR = std::max(16, BT);
   pl.mode = 1;
   pl.RPC = RPC;
   pl.N = N;
@@ -127,14 +127,19 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   int rw = 16;
   while (rw * 2 <= 256 && Hc % (rw * 2) == 0 && (rw * 2) * (NC + BT) * es <= stage_req) rw *= 2;
   pl.Rw = rw;
-  pl.Rt = std::min(256, pow2_floor(std::max(16, stage_req / (2 * D * es))));
+  // K/V tile: Rt positions of K and of V (32 <= Rt <= 256, a power of two:
+  // the attention hands out 32-position chunks)
+  pl.Rt = std::min(256, pow2_floor(std::max(32, stage_req / (2 * D * es))));
   int ro = 16;
   while (ro * 2 <= 256 && GD % (ro * 2) == 0 && (ro * 2) * pl.Co * es <= stage_req) ro *= 2;
   pl.Ro = ro;
-  const int item = std::max((NC + BT) * pl.Rw * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
+  const int item =
+      std::max((NC + BT) * pl.Rw * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
   pl.stage_bytes = round_up(item, 1024);
 
-  const int SE = RPC * NC;
+  const int SE = RPC * NC + (RPC + 3) / 4 * 4;  // reduce-scatter slice (floats)
+  const int OP = 4 * GD + 16;                   // O-projection A row (bytes)
+  const int apitch = (pl.Rw + 8) * 2;           // staged x*g row (bytes)
   int off = 0;
   SmemLayout& L = pl.L;
   auto take = [&](int bytes) {
@@ -143,14 +148,17 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
     return o;
   };
   L.bars = take(BarIdx::count * 8);
-  L.red = take(BT * NC * 4);                                       // partials / O-proj A
-  L.scratch = take(std::max((N - 1) * SE, kConsumerWarps * G * (D + 4)) * 4);
-  L.qkv = take(BT * GD * 4);                                       // gathered o
-  L.sm = take(G * (D + 4) * 4);                                    // attention record
-  L.xn = take(4 * BT * (pl.Rw + 8) * 2);                           // A staging (2 x hi/lo)
-  L.scale = take(Hc * 4);                                          // ln_weight band
+  L.red = take(N * SE * 4);
+  // one region, three lifetimes: x*g staging (projection), warp states
+  // (attention), the O-projection A operand (after attention)
+  L.scratch =
+      take(std::max(4 * MR * apitch, std::max(kConsumerWarps * G * (D + 4) * 4, MR * OP)));
+  L.xn = take((D / 16) * 32 * 16);  // Q fragments of the attention
+  L.qkv = take(RPC * GD * 4);       // own rows' o
+  L.sm = take(G * (D + 4) * 4);     // attention record
+  L.scale = take(Hc * 4);           // ln_weight band
   L.rope = take(RPC * (D / 2) * 2 * 4);
-  L.misc = take((BT + 4 + RPC + kConsumerWarps * RPC) * 4);
+  L.misc = take((BT + 4 + RPC) * 4);
   const int extras = round_up(off, 1024);
   int budget = std::min((int)prop.sharedMemPerBlockOptin,
                         (int)prop.sharedMemPerMultiprocessor - (int)prop.reservedSharedMemPerBlock);
@@ -161,7 +169,7 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   pl.stages = stages;
   const int ring = stages * pl.stage_bytes;
   L.ring = 0;
-  for (int* f : {&L.bars, &L.red, &L.scratch, &L.qkv, &L.sm, &L.xn, &L.scale, &L.rope, &L.misc})
+  for (int* f : {&L.bars, &L.red, &L.scratch, &L.xn, &L.qkv, &L.sm, &L.scale, &L.rope, &L.misc})
     *f += ring;
   L.total = ring + extras + 1024;
   return true;
@@ -304,31 +312,93 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// The batched row-split instance for c with its plan, or nullptr when c takes
-// the sequence-split kernel: fp32 storage, batch tiles under 16 rows, or no
-// instance built (or fitting shared memory) for the shape.
+// Raise the function's dynamic shared-memory limit to `bytes` (never lower
+// it: the attribute is per function, shared by every handle) and allow
+// clusters above 8 blocks when needed.
+int prepare_function(const void* fn, int bytes, int N) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  cudaFuncAttributes cur;
+  if (cudaFuncGetAttributes(&cur, fn) != cudaSuccess) return CF_ERR_CUDA;
+  if (cur.maxDynamicSharedSizeBytes < bytes &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return CF_ERR_CUDA;
+  if (N > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                   cudaSuccess)
+    return CF_ERR_CLUSTER;
+  return CF_OK;
+}
+
+// Clusters of N blocks with `smem` bytes each that can be resident at once
+// (0 when none, or on error).
+int resident_clusters(const void* fn, int N, int smem) {
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = N;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3(N, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &lc) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Whether c takes the batched row-split kernel: 16-bit storage and either a
+// batch of at least 16 rows (by default) or an explicit rows_per_block or
+// batch tile of 16 or more.
+bool wants_rows(const cf_config& c) {
+  if (c.dtype == CF_F32) return false;
+  if (c.rows_per_block > 0 || c.batch_tile >= 16) return true;
+  return c.batch_tile == 0 && c.max_batch >= 16;
+}
+
+// The batched row-split instance for c with its plan, or nullptr.  Among the
+// instances whose plan fits, prefer those whose whole grid is resident at
+// once (one wave) and, among them, the one with the most blocks (more SMs
+// streaming), then the larger batch tile (fewer weight reads); if no grid
+// fits in one wave, the fewest waves, then the larger batch tile.
 const KernelEntry* pick_rows_entry(const cf_config& c, int stage_req, const cudaDeviceProp& prop,
                                    Plan& pl) {
-  if (c.dtype == CF_F32) return nullptr;
-  if (c.batch_tile > 0 && c.batch_tile < 16) return nullptr;
-  if (c.batch_tile == 0 && c.max_batch < 16) return nullptr;
+  if (!wants_rows(c)) return nullptr;
   const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
   const KernelEntry* e = nullptr;
   const int n = registry_rows(&e);
   const KernelEntry* best = nullptr;
+  long long best_waves = 0, best_blocks = 0;
   for (int i = 0; i < n; ++i) {
     const KernelEntry& k = e[i];
     if (k.dtype != c.dtype || k.D != D || k.G != G) continue;
     if (c.batch_tile > 0 && k.BT != c.batch_tile) continue;
     if (c.rows_per_block > 0 && k.RPC != c.rows_per_block) continue;
-    if (c.batch_tile == 0 && k.BT > std::max(16, c.max_batch)) continue;
+    if (c.batch_tile == 0 && k.BT > std::max(4, c.max_batch)) continue;
     Plan trial;
     if (!make_plan_rows(c, k.BT, k.RPC, stage_req, prop, trial)) continue;
-    // largest batch tile (weights read once per tile), then fewest rows per
-    // block (more blocks streaming)
-    if (best == nullptr || k.BT > best->BT || (k.BT == best->BT && k.RPC < best->RPC)) {
+    if (prepare_function(k.fn, trial.L.total, trial.N) != CF_OK) continue;
+    const int resident = resident_clusters(k.fn, trial.N, trial.L.total);
+    if (resident <= 0) continue;
+    const long long clusters = (long long)c.n_kv_heads * ((c.max_batch + k.BT - 1) / k.BT);
+    const long long waves = (clusters + resident - 1) / resident;
+    const long long blocks = std::min(clusters, (long long)resident) * trial.N;
+    bool better = best == nullptr;
+    if (!better) {
+      const bool one = waves == 1, best_one = best_waves == 1;
+      if (one != best_one) better = one;
+      else if (one) better = blocks > best_blocks || (blocks == best_blocks && k.BT > best->BT);
+      else better = waves < best_waves || (waves == best_waves && k.BT > best->BT);
+    }
+    if (better) {
       best = &k;
       pl = trial;
+      best_waves = waves;
+      best_blocks = blocks;
     }
   }
   return best;
@@ -347,7 +417,9 @@ int plan_handle(const cf_config& c, cf_handle& h) {
   Plan pl;
   const KernelEntry* ke = pick_rows_entry(c, stage_req, prop, pl);
   if (ke == nullptr) {
-    if (c.batch_tile >= 16) return CF_ERR_UNSUPPORTED;
+    // an explicit batched request with no fitting instance is an error; a
+    // default choice falls back to the sequence-split kernel
+    if (c.batch_tile >= 16 || c.rows_per_block > 0) return CF_ERR_UNSUPPORTED;
     // Batch tile: requested, else the largest compiled one <= max_batch.
     int BT = c.batch_tile;
     if (BT == 0) {
@@ -382,39 +454,12 @@ int plan_handle(const cf_config& c, cf_handle& h) {
         !(cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)))
       return CF_ERR_UNSUPPORTED;
   }
-  const int N = pl.N, BT = pl.BT;
-  const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
-  // The attribute is per function: only ever raise it, so a later handle with
-  // a smaller plan cannot break an earlier handle's launches.
+  const int N = pl.N;
   {
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    cudaFuncAttributes cur;
-    if (cudaFuncGetAttributes(&cur, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
-    if (cur.maxDynamicSharedSizeBytes < pl.L.total &&
-        cudaFuncSetAttribute(ke->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.L.total) !=
-            cudaSuccess)
-      return CF_ERR_CUDA;
+    const int rc = prepare_function(ke->fn, pl.L.total, N);
+    if (rc != CF_OK) return rc;
   }
-  if (N > 8 && cudaFuncSetAttribute(ke->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                   cudaSuccess)
-    return CF_ERR_CLUSTER;
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = N;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  lc.gridDim = dim3(N * clusters, 1, 1);
-  lc.blockDim = dim3(kThreads, 1, 1);
-  lc.dynamicSmemBytes = pl.L.total;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  int nclusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&nclusters, ke->fn, &lc) != cudaSuccess) {
-    cudaGetLastError();
-    return CF_ERR_CLUSTER;
-  }
+  const int nclusters = resident_clusters(ke->fn, N, pl.L.total);
   if (nclusters <= 0) return CF_ERR_CLUSTER;
   h.cfg = c;
   h.device = dev;
@@ -553,8 +598,8 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
     const void* base = which == 0 ? k_cache : v_cache;
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)nkv, (uint64_t)S, (uint64_t)batch};
     const uint64_t str[3] = {(uint64_t)D * es, (uint64_t)nkv * D * es, (uint64_t)S * nkv * D * es};
-    const uint32_t box[4] = {(uint32_t)D, 1u, (uint32_t)pl.Rt, 1u};
-    if (!get_map(which == 0 ? h->m_k : h->m_v, base, batch, 4, dims, str, box, false,
+    const uint32_t box[4] = {(uint32_t)(rows ? 64 : D), 1u, (uint32_t)pl.Rt, 1u};
+    if (!get_map(which == 0 ? h->m_k : h->m_v, base, batch, 4, dims, str, box, rows,
                  which == 0 ? kp.tm_k : kp.tm_v))
       return CF_ERR_CUDA;
   }

@@ -144,4 +144,61 @@ __device__ void cluster_gather(float* data, int se, uint64_t* gbar, int rank, in
   named_sync(kBar, NT);
 }
 
+// ---------------------------------------------------------- pull forms --
+// In the pull forms a block reads its peers' shared memory directly
+// (ld.shared::cluster) once they have signalled that the data is complete,
+// so no receive buffers are needed.  Each exchange uses one mbarrier per block,
+// initialized with count N-1 and completed (parity 0) by the peers'
+// release-arrivals.
+
+// Tell every other block of the cluster that this block's data for an
+// exchange is complete: a cluster-scope fence, then one release-arrival on
+// the same-offset mbarrier `bar` of each peer.  Called by one thread after
+// the producing threads have synchronized with it.
+__device__ __forceinline__ void cluster_signal_peers(uint64_t* bar, int rank, int N) {
+  fence_acq_rel_cluster();
+  const uint32_t b = smem_u32(bar);
+  for (int q = 1; q < N; ++q) mbar_remote_arrive(mapa(b, (uint32_t)((rank + q) % N)));
+}
+
+// ClusterReduce, reduce-scatter form by pulling [CF §3.1.1]: data holds N
+// slices of n floats (n % 4 == 0) in every block; afterwards slice `rank` of
+// this block holds the sum of slice `rank` over all blocks.  Slices other than
+// `rank` are only read (by their owners), so they stay valid.
+template <int NT>
+__device__ void cluster_pull_reduce_slice(float* data, int n, uint64_t* bar, int rank, int N,
+                                          int tid, int* err) {
+  mbar_wait_cluster(bar, 0, err);
+  float4* own = reinterpret_cast<float4*>(data + (size_t)rank * n);
+  const uint32_t base = smem_u32(own);
+  for (int i = tid; i < n / 4; i += NT) {
+    float4 v = own[i];
+    for (int q = 1; q < N; ++q) {
+      const float4 w = ld_dsmem_f4(mapa(base, (uint32_t)((rank + q) % N)) + 16u * i);
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    own[i] = v;
+  }
+}
+
+// ClusterGather by pulling [CF §3.1.2]: block q's slice is `nbytes` bytes
+// (a multiple of 16) at buf + q * stride in every block; afterwards every
+// block holds all N slices.
+template <int NT>
+__device__ void cluster_pull_gather(uint8_t* buf, int nbytes, int stride, uint64_t* bar, int rank,
+                                    int N, int tid, int* err) {
+  mbar_wait_cluster(bar, 0, err);
+  const int n16 = nbytes / 16;
+  for (int q = 1; q < N; ++q) {
+    const int peer = (rank + q) % N;
+    uint8_t* dst = buf + (size_t)peer * stride;
+    const uint32_t src = mapa(smem_u32(dst), (uint32_t)peer);
+    for (int i = tid; i < n16; i += NT)
+      *reinterpret_cast<uint4*>(dst + 16 * i) = ld_dsmem_u4(src + 16u * i);
+  }
+}
+
 }  // namespace cf

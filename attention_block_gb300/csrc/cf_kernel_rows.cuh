@@ -1,5 +1,5 @@
 // cf_kernel_rows.cuh -- the fused decode attention block for batched decode
-// (16 to 64 rows per cluster) on sm_103a.
+// (4 to 64 rows per cluster) on sm_103a.
 //
 // Pages cited by title and section:
 //   [CF]  "ClusterFusion框架深度解析：LLM推理优化的集群级通信革命" (devpress.csdn.net)
@@ -9,30 +9,38 @@
 // Same computation as cf_kernel.cuh ([CF §3.2] fused_qkv_attention_out,
 // [LNA §一]); the mapping changes with the batch.  One thread-block cluster
 // serves one KV head g and a tile of BT batch rows, so every weight byte of
-// the head group is read once per tile; its N = BT / RPC blocks
-//   * split the hidden (reduction) dimension of the QKV projection, now a
-//     real [BT x H] x [H x (G+2)d] contraction done on the tensor cores
-//     (mma.sync m16n8k16, fp32 accumulation; the fp32 activations enter as a
-//     pair of 16-bit values hi + lo, so the product keeps ~fp32 accuracy);
+// the head group is read once per tile (tiles of one head run together and
+// share the weights through L2); its N = BT / RPC blocks
+//   * split the hidden (reduction) dimension of the QKV projection, a
+//     [BT x H] x [H x (G+2)d] contraction on the tensor cores (mma.sync
+//     m16n8k16, fp32 accumulation; the fp32 activations enter as a pair of
+//     16-bit values hi + lo, so the product keeps ~fp32 accuracy; tiles of
+//     fewer than 16 rows are padded with zero rows);
 //   * combine the partial products with ClusterReduce in reduce-scatter form
 //     over BATCH ROWS [CF §3.1.1]: block c ends up owning rows
-//     [c*RPC, (c+1)*RPC) of the tile, applies the RMSNorm scale, RoPE and
-//     the KV append to them, and runs their attention over the whole
-//     sequence (no cross-block softmax merge is needed);
+//     [c*RPC, (c+1)*RPC) of the tile, fully summed, together with their
+//     sums of squares (each block adds x^2 over its hidden band while it
+//     stages x, so RMSNorm [LNA §三 stage 1] needs no separate pass over x);
+//     it applies the norm scale, RoPE and the KV append to its rows and runs
+//     their attention over the whole sequence on the tensor cores
+//     (cf_attention_tc.cuh), so no cross-block softmax merge is needed;
 //   * exchange the attention outputs with ClusterGather [CF §3.1.2] so that
 //     every block holds o for all BT rows, then split the output projection
 //     by columns (tensor cores again) and merge heads with fp32 atomics
 //     [CF §3.2 原子写合并]; the last block per (tile, column band) adds the
 //     residual and writes `out`.
-// Weight tiles arrive through TMA with the 128-byte swizzle so that the
-// ldmatrix fragment loads are free of bank conflicts; the batch rows of x
-// arrive with each weight tile.
+// Both cluster exchanges PULL: a block signals its peers (remote mbarrier
+// arrivals with cluster-scope release) when its data is complete and the
+// peers read it with ld.shared::cluster, so no receive buffers take shared
+// memory away from the TMA ring.  Weight and K/V tiles arrive through TMA
+// with the 128-byte swizzle, so the ldmatrix fragment loads are free of bank
+// conflicts; the batch rows of x arrive with each weight tile.
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "cf_attention.cuh"
+#include "cf_attention_tc.cuh"
 #include "cf_cluster.cuh"
 #include "cf_common.cuh"
 #include "cf_mma.cuh"
@@ -41,14 +49,28 @@
 
 namespace cf {
 
+// Floats of one reduce-scatter slice: RPC rows of NC projection partials,
+// then the RPC rows' sums of squares (padded to 4).
+__host__ __device__ constexpr int rows_slice_floats(int RPC, int NC) {
+  return RPC * NC + (RPC + 3) / 4 * 4;
+}
+// Bytes per row of the O-projection A operand: o as 16-bit hi (G*d values),
+// then lo, then 16 bytes of padding (an odd multiple of 16 bytes, so the
+// ldmatrix rows fall in distinct banks).
+__host__ __device__ constexpr int rows_aop_pitch(int GD) { return 4 * GD + 16; }
+
 template <typename T, int D, int G, int BT, int RPC>
 __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_constant__ KParams p) {
   constexpr int NSEG = G + 2;        // q heads of the group, k, v
   constexpr int NC = NSEG * D;       // projection columns of the group
-  constexpr int MT = BT / 16;        // MMA row tiles
+  constexpr int MR = BT < 16 ? 16 : BT;  // MMA rows (zero-padded)
+  constexpr int MT = MR / 16;        // MMA row tiles
   constexpr int NTW = NC / 8 / kConsumerWarps;  // projection n-tiles per warp
   constexpr int GD = G * D;          // O-projection reduction size
-  static_assert(BT % 16 == 0 && BT % RPC == 0, "batch tile");
+  constexpr int SE = rows_slice_floats(RPC, NC);
+  constexpr int OP = rows_aop_pitch(GD);
+  constexpr int NRW = (BT + kConsumerWarps - 1) / kConsumerWarps;  // rows per warp (sumsq)
+  static_assert(BT % RPC == 0 && MR % 16 == 0, "batch tile");
   static_assert(NC % (8 * kConsumerWarps) == 0, "projection columns per warp");
   static_assert(D % 64 == 0, "head_dim in 64-column swizzle boxes");
   using MK = MmaKind<T>;
@@ -66,26 +88,26 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   const int b0 = bt * BT;
   const int Hc = p.H / N;  // K band rows == O-proj column band
   const int k0 = rank * Hc;
-  const int nrounds = __ffs(N) - 1;
-  const int SE = RPC * NC;  // reduce-scatter slice (RPC rows)
-  const int SEo = RPC * GD; // gather slice of o
   const int r0 = rank * RPC;  // first owned row of the tile
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.L.bars);
   uint64_t* full = bars + BarIdx::full;
   uint64_t* empty = bars + BarIdx::empty;
+  uint64_t* rs_bar = bars + BarIdx::rs;  // peers' partial sums complete
+  uint64_t* ga_bar = bars + BarIdx::ga;  // peers' attention outputs complete
   uint8_t* ring = sm + p.L.ring;
-  float* red = reinterpret_cast<float*>(sm + p.L.red);          // [BT][NC] partials
-  float* rsrecv = reinterpret_cast<float*>(sm + p.L.scratch);   // RS receive, then warp states
-  float* ogath = reinterpret_cast<float*>(sm + p.L.qkv);        // [BT][GD] o of every row
-  float* rec = reinterpret_cast<float*>(sm + p.L.sm);           // [G][D+4] attention record
-  uint8_t* abuf = sm + p.L.xn;                                  // A operand staging
-  float* gband = reinterpret_cast<float*>(sm + p.L.scale);      // ln_weight band [Hc]
-  float* rope = reinterpret_cast<float*>(sm + p.L.rope);        // [RPC][D/2][2]
-  int* s_pos = reinterpret_cast<int*>(sm + p.L.misc);           // [BT]
+  float* red = reinterpret_cast<float*>(sm + p.L.red);       // [N][SE] partials
+  uint8_t* un = sm + p.L.scratch;                            // abuf | warp states | A of O-proj
+  float* wst = reinterpret_cast<float*>(un);
+  uint8_t* aop = un;                                         // [MR][OP] bytes
+  float* ofin = reinterpret_cast<float*>(sm + p.L.qkv);      // [RPC][GD] own rows' o
+  float* rec = reinterpret_cast<float*>(sm + p.L.sm);        // [G][D+4] attention record
+  uint4* qfr = reinterpret_cast<uint4*>(sm + p.L.xn);        // [D/16][32] Q fragments
+  float* gband = reinterpret_cast<float*>(sm + p.L.scale);   // ln_weight band [Hc]
+  float* rope = reinterpret_cast<float*>(sm + p.L.rope);     // [RPC][D/2][2]
+  int* s_pos = reinterpret_cast<int*>(sm + p.L.misc);        // [BT]
   int* s_flag = s_pos + BT;
-  float* s_rinv = reinterpret_cast<float*>(s_flag + 4);          // [RPC]
-  float* wred = s_rinv + RPC;                                    // [8][RPC]
+  float* s_rinv = reinterpret_cast<float*>(s_flag + 4);       // [RPC]
 
   // ---------------------------------------------------------------- setup --
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -94,15 +116,11 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    for (int r = 0; r < nrounds; ++r) {
-      mbar_init(&bars[BarIdx::rs + r], 1);
-      mbar_init(&bars[BarIdx::ga + r], 1);
+    if (N > 1) {
+      mbar_init(rs_bar, N - 1);
+      mbar_init(ga_bar, N - 1);
     }
     fence_mbar_init_cluster();
-    for (int r = 0; r < nrounds; ++r) {
-      mbar_arrive_expect_tx(&bars[BarIdx::rs + r], reduce_scatter_round_bytes(N, r, SE));
-      mbar_arrive_expect_tx(&bars[BarIdx::ga + r], gather_round_bytes(r, SEo));
-    }
   }
   if (warp == kConsumerWarps && lane == 0) {
     prefetch_tensormap(&p.tm_wqkv);
@@ -138,14 +156,17 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   const int nrt = GD / p.Ro;
   const int wboxes = NC / 64;                        // 64-column boxes per W_qkv tile
   const uint32_t wbox_bytes = (uint32_t)(p.Rw * 128);
-  const uint32_t x_bytes = (uint32_t)(BT * p.Rw * 2);
+  const uint32_t x_bytes = (uint32_t)(BT * p.Rw * (int)sizeof(T));
   const int obox = p.Co / 64;                        // 64-column boxes per W_o tile
   const uint32_t obox_bytes = (uint32_t)(p.Ro * 128);
 
   if (warp == kConsumerWarps) {
     // ============================================== TMA producer warp ====
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      // Weights: evict-first when this tile is the only reader, otherwise
+      // kept at normal priority for the head's other batch tiles.
+      const uint64_t pol_w = p.nbt > 1 ? policy_evict_normal() : policy_evict_first();
+      const uint64_t pol_kv = policy_evict_first();
       int it = 0;
       auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
         const int s = it % p.stages;
@@ -165,21 +186,28 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           const int sg = col / D, cin = col % D;
           const int gx = (sg < G) ? ((g * G + sg) * D + cin)
                                   : ((sg == G ? p.nq + g : p.nq + p.nkv + g) * D + cin);
-          tma_load_2d(dst + bx * wbox_bytes, &p.tm_wqkv, gx, y, bar, pol);
+          tma_load_2d(dst + bx * wbox_bytes, &p.tm_wqkv, gx, y, bar, pol_w);
         }
-        tma_load_2d(dst + wboxes * wbox_bytes, &p.tm_x, y, b0, bar, pol);
+        tma_load_2d(dst + wboxes * wbox_bytes, &p.tm_x, y, b0, bar, pol_w);
       }
       if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdW] = globaltimer_ns();
-      // Phase 2: K/V tiles of the owned rows, whole sequence each.
-      const uint32_t kv_bytes = (uint32_t)(p.Rt * D * sizeof(T));
+      // Phase 2: K/V tiles of the owned rows, whole sequence each, as
+      // 64-column swizzled boxes: K [D/64][Rt][64] then V.
+      const uint32_t kv_box = (uint32_t)(p.Rt * 128);
+      constexpr int NB = D / 64;
       for (int r = 0; r < RPC; ++r) {
         int t0, t1;
         kv_tile_range(s_pos[r0 + r], p.Rt, 0, 1, t0, t1);
         for (int t = t0; t < t1; ++t, ++it) {
           uint64_t* bar;
-          uint8_t* dst = slot(2 * kv_bytes, bar);
-          tma_load_4d(dst, &p.tm_k, 0, g, t * p.Rt, b0 + r0 + r, bar, pol);
-          tma_load_4d(dst + kv_bytes, &p.tm_v, 0, g, t * p.Rt, b0 + r0 + r, bar, pol);
+          uint8_t* dst = slot(2 * NB * kv_box, bar);
+#pragma unroll
+          for (int bx = 0; bx < NB; ++bx) {
+            tma_load_4d(dst + bx * kv_box, &p.tm_k, bx * 64, g, t * p.Rt, b0 + r0 + r, bar,
+                        pol_kv);
+            tma_load_4d(dst + (NB + bx) * kv_box, &p.tm_v, bx * 64, g, t * p.Rt, b0 + r0 + r,
+                        bar, pol_kv);
+          }
         }
       }
       if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdKV] = globaltimer_ns();
@@ -190,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           uint8_t* dst = slot(obox * obox_bytes, bar);
           for (int bx = 0; bx < obox; ++bx)
             tma_load_2d(dst + bx * obox_bytes, &p.tm_wo, k0 + cb * p.Co + bx * 64,
-                        g * GD + rt * p.Ro, bar, pol);
+                        g * GD + rt * p.Ro, bar, pol_w);
         }
       if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdAll] = globaltimer_ns();
     }
@@ -200,40 +228,33 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     const T* __restrict__ hidden = reinterpret_cast<const T*>(p.hidden);
     const T* __restrict__ lnw = reinterpret_cast<const T*>(p.ln_w);
     int it = 0;
+    const int apitch = (p.Rw + 8) * 2;  // bytes per staged A row (odd multiple of 16)
+    const int abytes = MR * apitch;
 
-    // ---- Phase 0: ln_weight band, sums of squares of the owned rows, the
-    // owned rows' RoPE factors [LNA §三 stage 1] --------------------------
+    // ---- Phase 0: ln_weight band, the owned rows' RoPE factors, zero
+    // padding rows of the A staging buffers --------------------------------
     for (int i = tid; i < Hc; i += kConsumers) gband[i] = Elem<T>::to_f(lnw[k0 + i]);
-    {
-      constexpr int EV = 16 / (int)sizeof(T);
-      for (int r = 0; r < RPC; ++r) {
-        float ss = 0.f;
-        const int b = b0 + r0 + r;
-        if (b < p.B) {
-          const T* x = hidden + (size_t)b * p.H;
-          for (int i = tid * EV; i < p.H; i += kConsumers * EV) {
-            float f[EV];
-            load_cvt<T, EV>(x + i, f);
-#pragma unroll
-            for (int e = 0; e < EV; ++e) ss = fmaf(f[e], f[e], ss);
-          }
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) wred[warp * RPC + r] = ss;
-      }
-      for (int idx = tid; idx < RPC * (D / 2); idx += kConsumers) {
-        const int r = idx / (D / 2), j = idx % (D / 2);
-        const int pos = s_pos[r0 + r];
-        float c = 1.f, sn = 0.f;
-        if (pos >= 0) rope_cos_sin(pos, p.turn_hi[j], p.turn_lo[j], c, sn);
-        rope[2 * idx] = c;
-        rope[2 * idx + 1] = sn;
+    for (int idx = tid; idx < RPC * (D / 2); idx += kConsumers) {
+      const int r = idx / (D / 2), j = idx % (D / 2);
+      const int pos = s_pos[r0 + r];
+      float c = 1.f, sn = 0.f;
+      if (pos >= 0) rope_cos_sin(pos, p.turn_hi[j], p.turn_lo[j], c, sn);
+      rope[2 * idx] = c;
+      rope[2 * idx + 1] = sn;
+    }
+    if (BT < MR) {
+      const int per = (MR - BT) * apitch / 16;
+      for (int i = tid; i < 4 * per; i += kConsumers) {
+        const int buf = i / per, rem = i % per;
+        *reinterpret_cast<uint4*>(un + buf * abytes + BT * apitch + rem * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
       }
     }
     named_sync(kBarConsumers, kConsumers);
     stamp(kTlNorm);
 
-    // ---- Phase 1: [BT x Hc] x [Hc x NC] on the tensor cores ---------------
+    // ---- Phase 1: [BT x Hc] x [Hc x NC] on the tensor cores, with the
+    // rows' sums of squares over the band [LNA §三 stage 1] -----------------
     {
       float acc[MT][NTW][4];
 #pragma unroll
@@ -242,25 +263,33 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
-      const int apitch = (p.Rw + 8) * 2;  // bytes per A row (odd multiple of 16)
-      const int abytes = BT * apitch;
+      float ss[NRW];
+#pragma unroll
+      for (int i = 0; i < NRW; ++i) ss[i] = 0.f;
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const int s = it % p.stages;
         mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
         uint8_t* st = ring + (size_t)s * p.stage_bytes;
         const T* xt = reinterpret_cast<const T*>(st + wboxes * wbox_bytes);  // [BT][Rw]
-        // x * g of this K slice as hi + lo 16-bit pairs (double-buffered)
-        uint8_t* ahi = abuf + (size_t)(kt & 1) * 2 * abytes;
+        // x * g of this K slice as hi + lo 16-bit pairs (double-buffered);
+        // warp w stages rows w, w+8, ...
+        uint8_t* ahi = un + (size_t)(kt & 1) * 2 * abytes;
         uint8_t* alo = ahi + abytes;
-        for (int i2 = tid; i2 < BT * p.Rw / 2; i2 += kConsumers) {
-          const int row = (2 * i2) / p.Rw, k = (2 * i2) % p.Rw;
-          float f[2];
-          load_cvt<T, 2>(xt + row * p.Rw + k, f);
-          const float v0 = f[0] * gband[kt * p.Rw + k], v1 = f[1] * gband[kt * p.Rw + k + 1];
-          uint32_t hi, lo;
-          MK::split2(v0, v1, hi, lo);
-          *reinterpret_cast<uint32_t*>(ahi + row * apitch + k * 2) = hi;
-          *reinterpret_cast<uint32_t*>(alo + row * apitch + k * 2) = lo;
+#pragma unroll
+        for (int i = 0; i < NRW; ++i) {
+          const int row = warp + i * kConsumerWarps;
+          if (row < BT) {
+            for (int k = 2 * lane; k < p.Rw; k += 64) {
+              float f[2];
+              load_cvt<T, 2>(xt + row * p.Rw + k, f);
+              ss[i] = fmaf(f[0], f[0], fmaf(f[1], f[1], ss[i]));
+              const float v0 = f[0] * gband[kt * p.Rw + k], v1 = f[1] * gband[kt * p.Rw + k + 1];
+              uint32_t hi, lo;
+              MK::split2(v0, v1, hi, lo);
+              *reinterpret_cast<uint32_t*>(ahi + row * apitch + k * 2) = hi;
+              *reinterpret_cast<uint32_t*>(alo + row * apitch + k * 2) = lo;
+            }
+          }
         }
         named_sync(kBarConsumers, kConsumers);
         for (int ks = 0; ks < p.Rw / 16; ++ks) {
@@ -286,36 +315,48 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       stamp(kTlProjLoop);
-      // partial sums -> red [BT][NC] (row-major, so the owned rows of block c
-      // form the contiguous slice c of the reduce-scatter)
+      // Partial sums -> red, slice-major: row r goes to slice r / RPC, so the
+      // rows block c owns form its contiguous slice c.
       const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int j = 0; j < NTW; ++j) {
           const int n = (warp * NTW + j) * 8 + 2 * tq;
-          const int row = mt * 16 + gq;
-          *reinterpret_cast<float2*>(red + row * NC + n) = make_float2(acc[mt][j][0], acc[mt][j][1]);
-          *reinterpret_cast<float2*>(red + (row + 8) * NC + n) =
-              make_float2(acc[mt][j][2], acc[mt][j][3]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = mt * 16 + gq + 8 * h;
+            if (row < BT)
+              *reinterpret_cast<float2*>(red + (row / RPC) * SE + (row % RPC) * NC + n) =
+                  make_float2(acc[mt][j][2 * h], acc[mt][j][2 * h + 1]);
+          }
         }
-      if (tid < RPC) {
-        float tot = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) tot += wred[w * RPC + tid];
-        s_rinv[tid] = (b0 + r0 + tid < p.B) ? 1.0f / sqrtf(tot / (float)p.H + p.eps) : 0.f;
+#pragma unroll
+      for (int i = 0; i < NRW; ++i) {
+        const int row = warp + i * kConsumerWarps;
+        const float v = warp_sum(ss[i]);
+        if (row < BT && lane == 0) red[(row / RPC) * SE + RPC * NC + row % RPC] = v;
       }
       named_sync(kBarConsumers, kConsumers);
     }
     stamp(kTlProj);
 
-    // ---- ClusterReduce (reduce-scatter over rows): block `rank` owns rows
-    // [rank*RPC, (rank+1)*RPC) of the tile, fully summed ----------------------
-    cluster_reduce_scatter<kConsumers, kBarConsumers>(red, SE, rsrecv, &bars[BarIdx::rs], rank, N,
-                                                      tid, p.errflag);
+    // ---- ClusterReduce (reduce-scatter over rows, pulled): block `rank`
+    // owns rows [rank*RPC, (rank+1)*RPC) of the tile, fully summed ---------
+    if (N > 1) {
+      if (tid == 0) cluster_signal_peers(rs_bar, rank, N);
+      cluster_pull_reduce_slice<kConsumers>(red, SE, rs_bar, rank, N, tid, p.errflag);
+      named_sync(kBarConsumers, kConsumers);
+    }
+    float* own = red + rank * SE;  // [RPC][NSEG][D], then [RPC] sums of squares
+    if (tid < RPC) {
+      s_rinv[tid] = (b0 + r0 + tid < p.B) ? 1.0f / sqrtf(own[RPC * NC + tid] / (float)p.H + p.eps)
+                                          : 0.f;
+    }
+    named_sync(kBarConsumers, kConsumers);
     stamp(kTlReduceScatter);
 
     // ---- RMSNorm scale, RoPE, KV append of the owned rows [LNA §三] -------
-    float* own = red + rank * SE;  // [RPC][NSEG][D]
     {
       T* kc = reinterpret_cast<T*>(p.k_cache);
       T* vc = reinterpret_cast<T*>(p.v_cache);
@@ -361,46 +402,52 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     // ---- Attention of the owned rows over their whole sequence ------------
     for (int r = 0; r < RPC; ++r) {
       const float* qr = own + r * NC;
-      attend_row<T, D, G>(p, qr, qr + G * D, qr + (G + 1) * D, s_pos[r0 + r], 0, 1, true, ring,
-                          full, empty, it, rsrecv, rec,
-                          (p.timeline != nullptr && r == 0) ? p.timeline + blockIdx.x * kTimelineSlots
-                                                           : nullptr);
-      // o = O / L into the owned slice of the gather buffer
+      attend_row_tc<T, D, G>(p, qr, qr + G * D, qr + (G + 1) * D, s_pos[r0 + r], true, ring, full,
+                             empty, it, wst, qfr, rec,
+                             (p.timeline != nullptr && r == 0)
+                                 ? p.timeline + blockIdx.x * kTimelineSlots
+                                 : nullptr);
       for (int idx = tid; idx < GD; idx += kConsumers) {
         const int h = idx / D, dim = idx % D;
         const float L = rec[h * (D + 4) + D + 1];
-        ogath[(r0 + r) * GD + idx] = (L > 0.f) ? rec[h * (D + 4) + dim] / L : 0.f;
+        ofin[r * GD + idx] = (L > 0.f) ? rec[h * (D + 4) + dim] / L : 0.f;
       }
       named_sync(kBarConsumers, kConsumers);
     }
     stamp(kTlAttn);
-
-    // ---- ClusterGather of o [CF §3.1.2]: every block gets all BT rows -----
-    cluster_gather<kConsumers, kBarConsumers>(ogath, SEo, &bars[BarIdx::ga], rank, N, tid,
-                                              p.errflag);
-    stamp(kTlMax);
-    if (p.dbg != nullptr && rank == 0) {
+    if (p.dbg != nullptr) {
       float* dob = p.dbg + (size_t)p.B * (p.nq + 2 * p.nkv) * D;
-      for (int idx = tid; idx < BT * GD; idx += kConsumers) {
-        const int rr = idx / GD, rem = idx % GD;
-        const int b = b0 + rr;
-        if (b >= p.B || s_pos[rr] < 0) continue;
-        dob[((size_t)b * p.nq + g * G) * D + rem] = ogath[idx];
+      for (int idx = tid; idx < RPC * GD; idx += kConsumers) {
+        const int r = idx / GD, rem = idx % GD;
+        const int b = b0 + r0 + r;
+        if (b >= p.B || s_pos[r0 + r] < 0) continue;
+        dob[((size_t)b * p.nq + g * G) * D + rem] = ofin[idx];
       }
     }
-    // o as hi + lo 16-bit pairs for the O-projection A operand (in `red`,
-    // which the reduce-scatter no longer needs)
-    const int opitch = (GD + 8) * 2;
-    uint8_t* ohi = reinterpret_cast<uint8_t*>(red);
-    uint8_t* olo = ohi + BT * opitch;
-    for (int i2 = tid; i2 < BT * GD / 2; i2 += kConsumers) {
-      const int row = (2 * i2) / GD, k = (2 * i2) % GD;
+    // Own rows of the O-projection A operand (o as hi + lo 16-bit values) and
+    // the zero padding rows; the warp states that shared this memory are no
+    // longer needed.
+    for (int i2 = tid; i2 < RPC * GD / 2; i2 += kConsumers) {
+      const int r = (2 * i2) / GD, k = (2 * i2) % GD;
       uint32_t hi, lo;
-      MK::split2(ogath[row * GD + k], ogath[row * GD + k + 1], hi, lo);
-      *reinterpret_cast<uint32_t*>(ohi + row * opitch + k * 2) = hi;
-      *reinterpret_cast<uint32_t*>(olo + row * opitch + k * 2) = lo;
+      MK::split2(ofin[r * GD + k], ofin[r * GD + k + 1], hi, lo);
+      uint8_t* row = aop + (r0 + r) * OP;
+      *reinterpret_cast<uint32_t*>(row + k * 2) = hi;
+      *reinterpret_cast<uint32_t*>(row + 2 * GD + k * 2) = lo;
     }
+    if (BT < MR)
+      for (int i = tid; i < (MR - BT) * OP / 16; i += kConsumers)
+        *reinterpret_cast<uint4*>(aop + BT * OP + i * 16) = make_uint4(0u, 0u, 0u, 0u);
     named_sync(kBarConsumers, kConsumers);
+    stamp(kTlMax);
+
+    // ---- ClusterGather of o [CF §3.1.2], pulled: every block gets all BT
+    // rows of the A operand ---------------------------------------------------
+    if (N > 1) {
+      if (tid == 0) cluster_signal_peers(ga_bar, rank, N);
+      cluster_pull_gather<kConsumers>(aop, RPC * OP, RPC * OP, ga_bar, rank, N, tid, p.errflag);
+      named_sync(kBarConsumers, kConsumers);
+    }
     stamp(kTlSum);
 
     // ---- Phase 3: [BT x GD] x [GD x Co] per column box on the tensor cores,
@@ -426,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
             uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              ldmatrix_a(ah[mt], ohi + mt * 16 * opitch + kglob * 2, opitch, lane);
-              ldmatrix_a(al[mt], olo + mt * 16 * opitch + kglob * 2, opitch, lane);
+              ldmatrix_a(ah[mt], aop + mt * 16 * OP + kglob * 2, OP, lane);
+              ldmatrix_a(al[mt], aop + mt * 16 * OP + 2 * GD + kglob * 2, OP, lane);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -453,15 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           if (nt >= ntiles) continue;
           const int col = k0 + cb * p.Co + nt * 8 + 2 * tq;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int ra = mt * 16 + gq, rb = ra + 8;
-            if (b0 + ra < p.B && s_pos[ra] >= 0)
-              atomicAdd(reinterpret_cast<float2*>(p.acc + (size_t)(b0 + ra) * p.H + col),
-                        make_float2(acc[mt][j][0], acc[mt][j][1]));
-            if (b0 + rb < p.B && s_pos[rb] >= 0)
-              atomicAdd(reinterpret_cast<float2*>(p.acc + (size_t)(b0 + rb) * p.H + col),
-                        make_float2(acc[mt][j][2], acc[mt][j][3]));
-          }
+          for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = mt * 16 + gq + 8 * h;
+              if (row < BT && b0 + row < p.B && s_pos[row] >= 0)
+                atomicAdd(reinterpret_cast<float2*>(p.acc + (size_t)(b0 + row) * p.H + col),
+                          make_float2(acc[mt][j][2 * h], acc[mt][j][2 * h + 1]));
+            }
         }
       }
     }
@@ -481,23 +527,38 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     if (s_flag[0]) {
       T* out = reinterpret_cast<T*>(p.out);
       float* dproj = p.dbg ? p.dbg + (size_t)p.B * (2 * p.nq + 2 * p.nkv) * D : nullptr;
-      const int C4 = Hc / 4;
-      for (int i4 = tid; i4 < BT * C4; i4 += kConsumers) {
-        const int bb = i4 / C4, c4 = i4 % C4;
-        const int b = b0 + bb;
-        if (b >= p.B) continue;
-        const size_t off = (size_t)b * p.H + k0 + c4 * 4;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
-        __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
-        float xf[4];
-        load_cvt<T, 4>(hidden + off, xf);
-        const float r4[4] = {xf[0] + v.x, xf[1] + v.y, xf[2] + v.z, xf[3] + v.w};
-        store4<T>(out + off, r4);
-        if (dproj) {
-          dproj[off + 0] = v.x;
-          dproj[off + 1] = v.y;
-          dproj[off + 2] = v.z;
-          dproj[off + 3] = v.w;
+      // Four rows' worth of loads in flight per thread before any store.
+      constexpr int UNR = 4;
+      const int C4 = Hc / 4, total = BT * C4;
+      for (int base = tid; base < total; base += kConsumers * UNR) {
+        float4 v[UNR];
+        float xf[UNR][4];
+        size_t off[UNR];
+        bool ok[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int i4 = base + u * kConsumers;
+          const int bb = i4 / C4, c4 = i4 % C4;
+          ok[u] = i4 < total && b0 + bb < p.B;
+          off[u] = (size_t)(b0 + bb) * p.H + k0 + c4 * 4;
+          if (ok[u]) {
+            v[u] = __ldcg(reinterpret_cast<const float4*>(p.acc + off[u]));
+            load_cvt<T, 4>(hidden + off[u], xf[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          if (!ok[u]) continue;
+          __stcg(reinterpret_cast<float4*>(p.acc + off[u]), make_float4(0.f, 0.f, 0.f, 0.f));
+          const float r4[4] = {xf[u][0] + v[u].x, xf[u][1] + v[u].y, xf[u][2] + v[u].z,
+                               xf[u][3] + v[u].w};
+          store4<T>(out + off[u], r4);
+          if (dproj) {
+            dproj[off[u] + 0] = v[u].x;
+            dproj[off[u] + 1] = v[u].y;
+            dproj[off[u] + 2] = v[u].z;
+            dproj[off[u] + 3] = v[u].w;
+          }
         }
       }
       if (tid == 0) p.counters[bt * N + rank] = 0;
@@ -505,6 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   }
   stamp(kTlFinal);
   __syncwarp();
+  // Peers may still read this block's shared memory (reduce-scatter slices,
+  // the A operand rows) until they pass this barrier.
   cluster_sync_all();
   stamp(kTlEnd);
 }

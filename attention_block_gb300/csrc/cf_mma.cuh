@@ -83,4 +83,36 @@ __device__ __forceinline__ void ldmatrix_b_sw128(uint32_t& b0, uint32_t& b1, con
                : "r"(addr));
 }
 
+// Four 8x8 16-bit matrices; lane l supplies the row address of matrix l / 8,
+// row l % 8.  Register i holds matrix i in the mma fragment layout (thread t:
+// row t / 4, elements 2 (t % 4) and 2 (t % 4) + 1); with .trans, matrix i is
+// transposed first.
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Transpose of an 8x8 16-bit matrix held in the mma fragment layout (thread
+// t: row t / 4, elements 2 (t % 4), 2 (t % 4) + 1): returns the fragment of
+// the transposed matrix in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// Byte offset of row r, 16-byte chunk c of a TMA box written with the
+// 128-byte swizzle (rows of 128 bytes, box base 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
 }  // namespace cf

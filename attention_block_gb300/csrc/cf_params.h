@@ -47,7 +47,12 @@ enum TimelineSlot {
   kTimelineSlots = 32
 };
 
-// Byte offsets of the shared-memory regions (from a 1024-aligned base).
+// Byte offsets of the shared-memory regions (from a 1024-aligned base).  The
+// comments give the sequence-split kernel's use; the batched kernel
+// (cf_kernel_rows.cuh) reuses the fields for its own regions: red = partial
+// sums [N][slice], scratch = x*g staging / warp states / O-projection A
+// operand, xn = attention Q fragments, qkv = its rows' o, sm = attention
+// record, scale = ln_weight band.
 struct SmemLayout {
   int ring;      // stages * stage_bytes       TMA ring
   int bars;      // mbarriers (see BarIdx)

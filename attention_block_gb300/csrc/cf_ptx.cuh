@@ -183,6 +183,12 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -209,6 +215,39 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t r
           raddr),
       "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
       : "memory");
+}
+
+// Arrive on the mbarrier at cluster shared address `rbar` (usually another
+// CTA's) with release semantics at cluster scope: this thread's earlier
+// memory operations, and those it has observed, are visible to a thread
+// that then completes an acquire wait on that barrier.
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
+// 16-byte loads from (possibly another CTA's) shared memory at a cluster
+// shared address.
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_dsmem_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 }  // namespace cf

@@ -1,5 +1,5 @@
-"""GPU parity of the batched row-split kernel (16 to 64 batch rows per
-cluster, tensor-core projections) against the float64 oracle.
+"""GPU parity of the batched row-split kernel (4 to 64 batch rows per
+cluster, tensor-core projections and attention) against the float64 oracle.
 
 Every compiled (dtype, head_dim, group, batch tile, rows per block) instance
 runs on a scaled shape with a ragged last batch tile and positions that hit
@@ -46,11 +46,13 @@ def _custom(dtype, H, nq, nkv, d, B, S):
 INSTANCES = [
     ("f16", 64, 1, 64, 16),
     ("f16", 64, 1, 32, 8),
-    ("f16", 64, 1, 16, 2),
-    ("f16", 128, 1, 16, 1),
-    ("f16", 128, 4, 16, 2),
-    ("bf16", 128, 4, 16, 1),
-    ("bf16", 128, 4, 16, 2),
+    ("f16", 64, 1, 16, 4),
+    ("f16", 128, 1, 16, 4),
+    ("f16", 128, 4, 16, 4),
+    ("f16", 128, 4, 4, 1),
+    ("bf16", 128, 4, 4, 1),
+    ("bf16", 128, 4, 8, 2),
+    ("bf16", 128, 4, 16, 4),
     ("bf16", 64, 1, 16, 4),
 ]
 
@@ -75,7 +77,7 @@ def test_every_instance_scaled_shape(inst):
 
 
 def test_default_picks_batched_kernel_for_batched_workloads():
-    for name, bt in ((synth.SMALL_HEAD_B64, 64), (synth.LLAMA3_GQA, 16)):
+    for name, bt in ((synth.SMALL_HEAD_B64, 64), (synth.LLAMA3_GQA, 4)):
         w = synth.WORKLOADS[name]
         info = make_block(w).launch_info()
         assert info["mode"] == 1 and info["batch_tile"] == bt, (name, info)
@@ -84,7 +86,7 @@ def test_default_picks_batched_kernel_for_batched_workloads():
         assert make_block(synth.WORKLOADS[name]).launch_info()["mode"] == 0
 
 
-@pytest.mark.parametrize("bt,rpc", [(64, 16), (32, 8), (16, 2)])
+@pytest.mark.parametrize("bt,rpc", [(64, 16), (32, 8), (16, 4)])
 def test_small_head_dim_batch64_every_batched_instance(bt, rpc):
     w = synth.WORKLOADS[synth.SMALL_HEAD_B64]
     t = synth.make_layer(w, 0, device="cuda")
@@ -93,9 +95,9 @@ def test_small_head_dim_batch64_every_batched_instance(bt, rpc):
     full_check(w, rows=rows, t=t, batch_tile=bt, rows_per_block=rpc)
 
 
-@pytest.mark.parametrize("rpc", [1, 2])
-def test_llama3_gqa_layer_full_batched(rpc):
-    full_check(synth.WORKLOADS[synth.LLAMA3_GQA], batch_tile=16, rows_per_block=rpc)
+@pytest.mark.parametrize("bt,rpc", [(4, 1), (8, 2), (16, 4)])
+def test_llama3_gqa_layer_full_batched(bt, rpc):
+    full_check(synth.WORKLOADS[synth.LLAMA3_GQA], batch_tile=bt, rows_per_block=rpc)
 
 
 def test_batched_workloads_on_sequence_split_kernel():
@@ -126,7 +128,7 @@ def test_batched_out_of_range_positions_flag_and_skip_rows():
                      batch=B, s_max=S, dtype="f16",
                      positions="list:" + ",".join(str(p) for p in pos))
     t = synth.make_layer(w, 2, device="cuda")
-    blk = make_block(w, batch_tile=16, rows_per_block=2)
+    blk = make_block(w, batch_tile=16, rows_per_block=4)
     assert blk.launch_info()["mode"] == 1
     out, kc, vc, _, st = run_gpu(w, t, block=blk)
     assert st == binding.CF_ERR_DEVICE_POS_RANGE
