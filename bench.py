@@ -36,7 +36,9 @@ METRIC = "decode attention-block µs/step and achieved HBM GB/s (fraction of GB3
 DEFAULT_WORKLOAD = "llama2_7b_layer_b1_p1024_f16"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_L2_BYTES = 129 * 1024 * 1024
-KERNEL_NAME = "cf_decode_kernel"
+# The fused kernel's name by launch mode (cf_launch_info.mode): 0 the
+# sequence-split kernel, 1 the batched row-split kernel.
+KERNEL_NAMES = {0: "cf_decode_kernel", 1: "cf_rows_kernel"}
 
 
 # ------------------------------------------------------------ host helpers --
@@ -539,7 +541,7 @@ def main(argv=None):
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": recorded_traffic(w.name),
-                "kernel": KERNEL_NAME,
+                "kernel": KERNEL_NAMES.get(info.get("mode", 0), "cf_decode_kernel"),
                 "launch_us_avg": round(launch_s_timed * 1e6, 3),
                 "launch_timing": "timed region (graph replays) / launches",
                 "isolated_launch_us_avg": round(launch_ms_avg * 1e3, 3),
