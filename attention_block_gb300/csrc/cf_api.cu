@@ -115,7 +115,6 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   const int N = BT / RPC;
   if (N < 1 || N > kMaxCluster || (N & (N - 1)) != 0 || H % (64 * N) != 0) return false;
   const int Hc = H / N;
-  const int MR = std::max(16, BT);
   pl.mode = 1;
   pl.RPC = RPC;
   pl.N = N;
@@ -149,30 +148,43 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   };
   L.bars = take(BarIdx::count * 8);
   L.red = take(N * SE * 4);
-  // one region, three lifetimes: x*g staging (projection), warp states
-  // (attention), the O-projection A operand (after attention)
-  L.scratch =
-      take(std::max(4 * MR * apitch, std::max(kConsumerWarps * G * (D + 4) * 4, MR * OP)));
+  // one region, three lifetimes: x*g staging of the BT rows (projection),
+  // warp states (attention merge), the O-projection A operand of the BT
+  // rows (after attention); rows BT..15 of a 16-row MMA tile read a zero chunk
+  const int slots = G > 1 ? 4 : 8;  // warp-state slots of the attention merge
+  L.scratch = take(std::max(4 * BT * apitch, std::max(slots * G * (D + 4) * 4, BT * OP)));
   L.xn = take((D / 16) * 32 * 16);  // Q fragments of the attention
   L.qkv = take(RPC * GD * 4);       // own rows' o
   L.sm = take(G * (D + 4) * 4);     // attention record
-  L.scale = take(Hc * 4);           // ln_weight band
+  L.scale = 0;                      // unused (ln_weight is read from L2)
   L.rope = take(RPC * (D / 2) * 2 * 4);
-  L.misc = take((BT + 4 + RPC) * 4);
+  L.misc = take((4 + BT + 4 + RPC) * 4);  // zero chunk, positions, flags, norm scales
   const int extras = round_up(off, 1024);
   int budget = std::min((int)prop.sharedMemPerBlockOptin,
                         (int)prop.sharedMemPerMultiprocessor - (int)prop.reservedSharedMemPerBlock);
   budget -= 1024;
   int stages = std::min((budget - extras) / pl.stage_bytes, kMaxStages);
   if (c.max_stages > 0) stages = std::min(stages, c.max_stages);
-  if (stages < 2) return false;
+  if (stages < 2) {
+    // a default stage size larger than 32 KB that leaves fewer than two
+    // stages: retry with 32 KB
+    if (c.stage_bytes == 0 && stage_req > 32768)
+      return make_plan_rows(c, BT, RPC, 32768, prop, pl);
+    return false;
+  }
   pl.stages = stages;
   const int ring = stages * pl.stage_bytes;
   L.ring = 0;
-  for (int* f : {&L.bars, &L.red, &L.scratch, &L.xn, &L.qkv, &L.sm, &L.scale, &L.rope, &L.misc})
+  for (int* f : {&L.bars, &L.red, &L.scratch, &L.xn, &L.qkv, &L.sm, &L.rope, &L.misc})
     *f += ring;
   L.total = ring + extras + 1024;
   return true;
+}
+
+// Completion counters for `batch_cap` rows: one per (batch tile, column
+// band).
+size_t counter_slots(const Plan& pl, int batch_cap) {
+  return (size_t)((batch_cap + pl.BT - 1) / pl.BT) * pl.N;
 }
 
 // Shared-memory plan for one (config, N, BT, stage size, CTAs/SM).  Returns
@@ -517,9 +529,8 @@ int cf_create(const cf_config* cfg, cf_handle** out) {
     delete h;
     return rc;
   }
-  const int BT = h->plan.BT, N = h->plan.N;
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
-  const size_t cnt_bytes = (size_t)((c.max_batch + BT - 1) / BT) * N * sizeof(int);
+  const size_t cnt_bytes = counter_slots(h->plan, c.max_batch) * sizeof(int);
   const size_t total = acc_bytes + cnt_bytes + 256;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     delete h;
@@ -763,7 +774,7 @@ std::mutex g_noalloc_mu;
 int noalloc_prepare(const cf_config& c, unsigned char* scratch, cf_handle& h) {
   const int rc = plan_handle(c, h);
   if (rc != CF_OK) return rc;
-  if ((size_t)((c.max_batch + h.plan.BT - 1) / h.plan.BT) * h.plan.N > kNoAllocCounters)
+  if (counter_slots(h.plan, c.max_batch) > kNoAllocCounters)
     return CF_ERR_INVALID_ARG;
   h.ws = nullptr;  // nothing to free: the workspace is the static scratch
   h.acc = reinterpret_cast<float*>(scratch);
@@ -818,8 +829,7 @@ extern "C" int cf_decode_attn_block_noalloc(const cf_config* cfg, int32_t batch,
   // the regions this call uses are cleared first, on the same stream.
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t acc_bytes = (size_t)batch * cfg->hidden * sizeof(float);
-  const size_t cnt_bytes =
-      (size_t)((batch + s.h.plan.BT - 1) / s.h.plan.BT) * s.h.plan.N * sizeof(int);
+  const size_t cnt_bytes = counter_slots(s.h.plan, batch) * sizeof(int);
   if (cudaMemsetAsync(s.h.acc, 0, acc_bytes, st) != cudaSuccess ||
       cudaMemsetAsync(s.h.counters, 0, cnt_bytes, st) != cudaSuccess ||
       cudaMemsetAsync(s.h.errflag, 0, sizeof(int), st) != cudaSuccess) {

@@ -21,8 +21,8 @@
 // that take alternate tiles, so several tiles are in work at once (every warp
 // still waits for and releases every tile in order).  Each warp
 // keeps its own running (m, l, o); the warps are merged through shared memory
-// at the end into `rec` = [G][D+4]: unnormalized o, then m at D and l at D+1
-// (log2 units).
+// (for G > 1 in two halves of 4 warps) at the end into `rec` = [G][D+4]: unnormalized o,
+// then m at D and l at D+1 (log2 units).
 #pragma once
 
 #include "cf_common.cuh"
@@ -32,10 +32,14 @@
 
 namespace cf {
 
+// Warp-state slots of the final merge (the `wst` scratch holds
+// attn_tc_slots(G) * G * (D + 4) floats).
+__host__ __device__ constexpr int attn_tc_slots(int G) { return G > 1 ? 4 : 8; }
+
 // q_in: [G][D] fp32 post-RoPE queries; kn, vn: the new token's key and value
 // [D] fp32 (folded in by warp 0 when `fold_new`); pos: the new token's
 // position (cached keys 0..pos-1 come from the ring), < 0 for an invalid row;
-// wst: [8][G][D+4] floats of scratch; qf: [D/16][32] uint4 of scratch for
+// wst: [attn_tc_slots(G)][G][D+4] floats of scratch; qf: [D/16][32] uint4 of scratch for
 // the Q fragments (shared by the 8 warps); `it` is the consumer's ring
 // counter.  Called by the 256 consumer threads together; Rt is a power of two
 // >= 32.
@@ -260,41 +264,70 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
     l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
     l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
   }
+  // Merge the 8 warps' states into the row's (o, m, l) record through
+  // attn_tc_slots<G>() warp slots of shared memory: for G > 1 in two halves
+  // (warps 0-3, then 4-7), for one head (small states) in one pass.
+  constexpr int HS = attn_tc_slots(G);                            // slots
+  constexpr int NH = kConsumerWarps / HS;                         // passes
+  constexpr int PER = (G * D + kConsumers - 1) / kConsumers;      // elements per thread
+  float PM[PER], PO[PER], PL[PER];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    if (h0 + j >= G) continue;
-    float* stw = wst + (warp * G + h0 + j) * (D + 4);
+  for (int half = 0; half < NH; ++half) {
+    if (warp / HS == half) {
 #pragma unroll
-    for (int md = 0; md < MD; ++md) {
-      stw[md * 16 + gq] = o[md][j];
-      stw[md * 16 + gq + 8] = o[md][2 + j];
-    }
-    if (gq == 0) {
-      stw[D] = m[j];
-      stw[D + 1] = l[j];
-    }
-  }
-  named_sync(kBarConsumers, kConsumers);
-  stamp(kTlAttnWarps);
-  // Merge the 8 warps into the row's (o, m, l) record.
-  for (int idx = tid; idx < G * D; idx += kConsumers) {
-    const int h = idx / D, dim = idx % D;
-    float M = -INFINITY;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wst[(w * G + h) * (D + 4) + D]);
-    float O = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* sw = wst + (w * G + h) * (D + 4);
-        const float f = exp2f(sw[D] - M);
-        O = fmaf(f, sw[dim], O);
-        L = fmaf(f, sw[D + 1], L);
+      for (int j = 0; j < 2; ++j) {
+        if (h0 + j >= G) continue;
+        float* stw = wst + ((warp % HS) * G + h0 + j) * (D + 4);
+#pragma unroll
+        for (int md = 0; md < MD; ++md) {
+          stw[md * 16 + gq] = o[md][j];
+          stw[md * 16 + gq + 8] = o[md][2 + j];
+        }
+        if (gq == 0) {
+          stw[D] = m[j];
+          stw[D + 1] = l[j];
+        }
       }
     }
+    named_sync(kBarConsumers, kConsumers);
+    if (half == 0) stamp(kTlAttnWarps);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int idx = tid + u * kConsumers;
+      if (idx >= G * D) continue;
+      const int h = idx / D, dim = idx % D;
+      float M = half ? PM[u] : -INFINITY;
+      for (int w = 0; w < HS; ++w) M = fmaxf(M, wst[(w * G + h) * (D + 4) + D]);
+      float O = 0.f, L = 0.f;
+      if (M != -INFINITY) {
+        if (half && PM[u] != -INFINITY) {
+          const float f = exp2f(PM[u] - M);
+          O = PO[u] * f;
+          L = PL[u] * f;
+        }
+        for (int w = 0; w < HS; ++w) {
+          const float* sw = wst + (w * G + h) * (D + 4);
+          const float f = exp2f(sw[D] - M);
+          O = fmaf(f, sw[dim], O);
+          L = fmaf(f, sw[D + 1], L);
+        }
+      }
+      PM[u] = M;
+      PO[u] = O;
+      PL[u] = L;
+    }
+    named_sync(kBarConsumers, kConsumers);
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int idx = tid + u * kConsumers;
+    if (idx >= G * D) continue;
+    const int h = idx / D, dim = idx % D;
     float* dst = rec + h * (D + 4);
-    dst[dim] = O;
+    dst[dim] = PO[u];
     if (dim == 0) {
-      dst[D] = M;
-      dst[D + 1] = L;
+      dst[D] = PM[u];
+      dst[D + 1] = PL[u];
     }
   }
   named_sync(kBarConsumers, kConsumers);

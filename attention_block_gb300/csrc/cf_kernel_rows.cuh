@@ -14,8 +14,8 @@
 //   * split the hidden (reduction) dimension of the QKV projection, a
 //     [BT x H] x [H x (G+2)d] contraction on the tensor cores (mma.sync
 //     m16n8k16, fp32 accumulation; the fp32 activations enter as a pair of
-//     16-bit values hi + lo, so the product keeps ~fp32 accuracy; tiles of
-//     fewer than 16 rows are padded with zero rows);
+//     16-bit values hi + lo, so the product keeps ~fp32 accuracy; in tiles of
+//     fewer than 16 rows the missing rows read a 16-byte zero chunk);
 //   * combine the partial products with ClusterReduce in reduce-scatter form
 //     over BATCH ROWS [CF §3.1.1]: block c ends up owning rows
 //     [c*RPC, (c+1)*RPC) of the tile, fully summed, together with their
@@ -63,7 +63,7 @@ template <typename T, int D, int G, int BT, int RPC>
 __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_constant__ KParams p) {
   constexpr int NSEG = G + 2;        // q heads of the group, k, v
   constexpr int NC = NSEG * D;       // projection columns of the group
-  constexpr int MR = BT < 16 ? 16 : BT;  // MMA rows (zero-padded)
+  constexpr int MR = BT < 16 ? 16 : BT;  // MMA rows (rows >= BT read a zero chunk)
   constexpr int MT = MR / 16;        // MMA row tiles
   constexpr int NTW = NC / 8 / kConsumerWarps;  // projection n-tiles per warp
   constexpr int GD = G * D;          // O-projection reduction size
@@ -99,13 +99,13 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   float* red = reinterpret_cast<float*>(sm + p.L.red);       // [N][SE] partials
   uint8_t* un = sm + p.L.scratch;                            // abuf | warp states | A of O-proj
   float* wst = reinterpret_cast<float*>(un);
-  uint8_t* aop = un;                                         // [MR][OP] bytes
+  uint8_t* aop = un;                                         // [BT][OP] bytes
   float* ofin = reinterpret_cast<float*>(sm + p.L.qkv);      // [RPC][GD] own rows' o
   float* rec = reinterpret_cast<float*>(sm + p.L.sm);        // [G][D+4] attention record
   uint4* qfr = reinterpret_cast<uint4*>(sm + p.L.xn);        // [D/16][32] Q fragments
-  float* gband = reinterpret_cast<float*>(sm + p.L.scale);   // ln_weight band [Hc]
   float* rope = reinterpret_cast<float*>(sm + p.L.rope);     // [RPC][D/2][2]
-  int* s_pos = reinterpret_cast<int*>(sm + p.L.misc);        // [BT]
+  const uint32_t* zero16 = reinterpret_cast<const uint32_t*>(sm + p.L.misc);  // 16 zero bytes
+  int* s_pos = reinterpret_cast<int*>(sm + p.L.misc + 16);   // [BT]
   int* s_flag = s_pos + BT;
   float* s_rinv = reinterpret_cast<float*>(s_flag + 4);       // [RPC]
 
@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     }
     fence_mbar_init_cluster();
   }
+  if (tid < 4) reinterpret_cast<uint32_t*>(sm + p.L.misc)[tid] = 0u;
   if (warp == kConsumerWarps && lane == 0) {
     prefetch_tensormap(&p.tm_wqkv);
     prefetch_tensormap(&p.tm_x);
@@ -229,11 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     const T* __restrict__ lnw = reinterpret_cast<const T*>(p.ln_w);
     int it = 0;
     const int apitch = (p.Rw + 8) * 2;  // bytes per staged A row (odd multiple of 16)
-    const int abytes = MR * apitch;
+    const int abytes = BT * apitch;
 
-    // ---- Phase 0: ln_weight band, the owned rows' RoPE factors, zero
-    // padding rows of the A staging buffers --------------------------------
-    for (int i = tid; i < Hc; i += kConsumers) gband[i] = Elem<T>::to_f(lnw[k0 + i]);
+    // ---- Phase 0: the owned rows' RoPE factors ------------------------------
     for (int idx = tid; idx < RPC * (D / 2); idx += kConsumers) {
       const int r = idx / (D / 2), j = idx % (D / 2);
       const int pos = s_pos[r0 + r];
@@ -241,14 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       if (pos >= 0) rope_cos_sin(pos, p.turn_hi[j], p.turn_lo[j], c, sn);
       rope[2 * idx] = c;
       rope[2 * idx + 1] = sn;
-    }
-    if (BT < MR) {
-      const int per = (MR - BT) * apitch / 16;
-      for (int i = tid; i < 4 * per; i += kConsumers) {
-        const int buf = i / per, rem = i % per;
-        *reinterpret_cast<uint4*>(un + buf * abytes + BT * apitch + rem * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
     }
     named_sync(kBarConsumers, kConsumers);
     stamp(kTlNorm);
@@ -283,7 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
               float f[2];
               load_cvt<T, 2>(xt + row * p.Rw + k, f);
               ss[i] = fmaf(f[0], f[0], fmaf(f[1], f[1], ss[i]));
-              const float v0 = f[0] * gband[kt * p.Rw + k], v1 = f[1] * gband[kt * p.Rw + k + 1];
+              float gw[2];
+              load_cvt<T, 2>(lnw + k0 + kt * p.Rw + k, gw);
+              const float v0 = f[0] * gw[0], v1 = f[1] * gw[1];
               uint32_t hi, lo;
               MK::split2(v0, v1, hi, lo);
               *reinterpret_cast<uint32_t*>(ahi + row * apitch + k * 2) = hi;
@@ -296,8 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            ldmatrix_a(ah[mt], ahi + mt * 16 * apitch + ks * 32, apitch, lane);
-            ldmatrix_a(al[mt], alo + mt * 16 * apitch + ks * 32, apitch, lane);
+            ldmatrix_a_rows(ah[mt], ahi + mt * 16 * apitch + ks * 32, apitch, BT - mt * 16, zero16,
+                            lane);
+            ldmatrix_a_rows(al[mt], alo + mt * 16 * apitch + ks * 32, apitch, BT - mt * 16, zero16,
+                            lane);
           }
 #pragma unroll
           for (int j = 0; j < NTW; ++j) {
@@ -424,9 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         dob[((size_t)b * p.nq + g * G) * D + rem] = ofin[idx];
       }
     }
-    // Own rows of the O-projection A operand (o as hi + lo 16-bit values) and
-    // the zero padding rows; the warp states that shared this memory are no
-    // longer needed.
+    // Own rows of the O-projection A operand (o as hi + lo 16-bit values); the
+    // warp states that shared this memory are no longer needed.
     for (int i2 = tid; i2 < RPC * GD / 2; i2 += kConsumers) {
       const int r = (2 * i2) / GD, k = (2 * i2) % GD;
       uint32_t hi, lo;
@@ -435,9 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       *reinterpret_cast<uint32_t*>(row + k * 2) = hi;
       *reinterpret_cast<uint32_t*>(row + 2 * GD + k * 2) = lo;
     }
-    if (BT < MR)
-      for (int i = tid; i < (MR - BT) * OP / 16; i += kConsumers)
-        *reinterpret_cast<uint4*>(aop + BT * OP + i * 16) = make_uint4(0u, 0u, 0u, 0u);
     named_sync(kBarConsumers, kConsumers);
     stamp(kTlMax);
 
@@ -473,8 +464,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
             uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              ldmatrix_a(ah[mt], aop + mt * 16 * OP + kglob * 2, OP, lane);
-              ldmatrix_a(al[mt], aop + mt * 16 * OP + 2 * GD + kglob * 2, OP, lane);
+              ldmatrix_a_rows(ah[mt], aop + mt * 16 * OP + kglob * 2, OP, BT - mt * 16, zero16,
+                              lane);
+              ldmatrix_a_rows(al[mt], aop + mt * 16 * OP + 2 * GD + kglob * 2, OP, BT - mt * 16,
+                              zero16, lane);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {

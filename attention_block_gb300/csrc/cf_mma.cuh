@@ -69,6 +69,18 @@ __device__ __forceinline__ void ldmatrix_a(uint32_t (&a)[4], const void* base, i
                : "r"(addr));
 }
 
+// ldmatrix_a for a matrix with only `nrows` stored rows: the lanes of rows
+// >= nrows read the 16-byte zero chunk at `zero16` instead (the zero padding
+// rows of a 16-row tile need no storage).
+__device__ __forceinline__ void ldmatrix_a_rows(uint32_t (&a)[4], const void* base, int pitch,
+                                                int nrows, const void* zero16, int lane) {
+  const int r = lane & 15, kh = lane >> 4;
+  const uint32_t addr = r < nrows ? smem_u32(base) + r * pitch + kh * 16 : smem_u32(zero16);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr));
+}
+
 // B fragment (16 k-rows x 8 n-columns) from a TMA box written with the
 // 128-byte swizzle: the box holds rows of 64 16-bit elements (128 bytes);
 // the 16-byte chunk j of row k sits at chunk position j ^ (k & 7).  `box`
