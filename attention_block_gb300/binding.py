@@ -56,6 +56,7 @@ _vp = ctypes.c_void_p
 SIGNATURES = {
     "cf_create": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.POINTER(_vp)]),
     "cf_decode_attn_block": (ctypes.c_int, [_vp, ctypes.c_int32] + [_vp] * 9),
+    "cf_decode_attn_block_unfused": (ctypes.c_int, [_vp, ctypes.c_int32] + [_vp] * 9),
     "cf_get_status": (ctypes.c_int, [_vp]),
     "cf_set_debug": (ctypes.c_int, [_vp, _vp]),
     "cf_get_launch_info": (ctypes.c_int, [_vp, ctypes.POINTER(CfLaunchInfo)]),
@@ -166,6 +167,15 @@ def cf_decode_attn_block(handle, batch, hidden_states, ln_weight, w_qkv, w_o, k_
                                       _ptr(positions), _ptr(out), _stream(stream))
 
 
+def cf_decode_attn_block_unfused(handle, batch, hidden_states, ln_weight, w_qkv, w_o, k_cache,
+                                 v_cache, positions, out, stream=None) -> int:
+    """The same step as three kernels with HBM intermediates (fusion baseline)."""
+    return lib().cf_decode_attn_block_unfused(handle, int(batch), _ptr(hidden_states),
+                                              _ptr(ln_weight), _ptr(w_qkv), _ptr(w_o),
+                                              _ptr(k_cache), _ptr(v_cache), _ptr(positions),
+                                              _ptr(out), _stream(stream))
+
+
 def cf_decode_attn_block_noalloc(cfg: CfConfig, batch, hidden_states, ln_weight, w_qkv, w_o,
                                  k_cache, v_cache, positions, out, stream=None) -> int:
     """Allocation-free decode step (no handle; scratch in a static device array)."""
@@ -241,6 +251,15 @@ class DecodeAttnBlock:
                                   k_cache, v_cache, positions, out, stream)
         if rc != CF_OK:
             raise CfError(rc, "cf_decode_attn_block")
+        return out
+
+    def unfused(self, batch, hidden_states, ln_weight, w_qkv, w_o, k_cache, v_cache, positions,
+                out, stream=None):
+        """The same step through the three-kernel path (the fusion baseline)."""
+        rc = cf_decode_attn_block_unfused(self.handle, batch, hidden_states, ln_weight, w_qkv, w_o,
+                                          k_cache, v_cache, positions, out, stream)
+        if rc != CF_OK:
+            raise CfError(rc, "cf_decode_attn_block_unfused")
         return out
 
     def launch_info(self) -> dict:

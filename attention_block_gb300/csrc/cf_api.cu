@@ -17,6 +17,7 @@
 #include "cf_params.h"
 #include "cf_registry.h"
 #include "cf_test.h"
+#include "cf_unfused.h"
 
 using namespace cf;
 
@@ -274,6 +275,12 @@ struct cf_handle {
   bool pdl = true;
   float turn_hi[64], turn_lo[64];  // RoPE turn rates as float pairs (see KParams)
   MapCache m_wqkv, m_wo, m_k, m_v, m_x;
+  // three-kernel (unfused) path: HBM intermediates and counters
+  void* uf_ws = nullptr;
+  float *uf_y = nullptr, *uf_part = nullptr, *uf_o32 = nullptr;
+  int *uf_cnt_attn = nullptr, *uf_cnt_out = nullptr;
+  float* uf_rinv = nullptr;
+  int uf_NS = 1, uf_KS = 1, uf_KS1 = 1;
 };
 
 namespace {
@@ -544,6 +551,44 @@ int cf_create(const cf_config* cfg, cf_handle** out) {
   h->acc = static_cast<float*>(h->ws);
   h->counters = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes);
   h->errflag = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes + cnt_bytes);
+  // Workspace of the three-kernel path (cf_decode_attn_block_unfused).
+  {
+    const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads, H = c.hidden;
+    const int Cq = (c.n_q_heads + 2 * c.n_kv_heads) * D;
+    const int sms = h->sm_count;
+    // about four blocks per SM in each of the three kernels
+    int NS = (4 * sms + c.max_batch * c.n_kv_heads - 1) / (c.max_batch * c.n_kv_heads);
+    NS = std::max(1, std::min(32, NS));
+    const int nbt = c.max_batch == 1 ? 1 : (c.max_batch + 7) / 8;
+    auto splits = [&](int bands, int K) {
+      int ks = 1;
+      while (ks < 16 && bands * nbt * ks * 2 <= 4 * sms && K % (ks * 2 * 64) == 0) ks *= 2;
+      return ks;
+    };
+    h->uf_NS = NS;
+    h->uf_KS1 = splits(Cq % 128 == 0 ? Cq / 128 : Cq / 64, H);
+    h->uf_KS = splits(H % 128 == 0 ? H / 128 : H / 64, c.n_q_heads * D);
+    const size_t y_b = (size_t)c.max_batch * Cq * 4;
+    const size_t part_b = (size_t)c.max_batch * c.n_kv_heads * NS * G * (D + 4) * 4;
+    const size_t o_b = (size_t)c.max_batch * c.n_q_heads * D * 4;
+    const size_t ca_b = (size_t)c.max_batch * c.n_kv_heads * 4;
+    const size_t co_b = (size_t)c.max_batch * (H / 64) * 4;
+    const size_t ri_b = ((size_t)c.max_batch * 4 + 255) / 256 * 256;
+    const size_t tot = y_b + part_b + o_b + ca_b + co_b + ri_b + 256;
+    if (cudaMalloc(&h->uf_ws, tot) != cudaSuccess || cudaMemset(h->uf_ws, 0, tot) != cudaSuccess) {
+      if (h->uf_ws) cudaFree(h->uf_ws);
+      cudaFree(h->ws);
+      delete h;
+      return CF_ERR_CUDA;
+    }
+    char* w = static_cast<char*>(h->uf_ws);
+    h->uf_y = reinterpret_cast<float*>(w);
+    h->uf_part = reinterpret_cast<float*>(w + y_b);
+    h->uf_o32 = reinterpret_cast<float*>(w + y_b + part_b);
+    h->uf_cnt_attn = reinterpret_cast<int*>(w + y_b + part_b + o_b);
+    h->uf_cnt_out = reinterpret_cast<int*>(w + y_b + part_b + o_b + ca_b);
+    h->uf_rinv = reinterpret_cast<float*>(w + y_b + part_b + o_b + ca_b + co_b);
+  }
   *out = h;
   return CF_OK;
 }
@@ -728,8 +773,67 @@ int cf_get_launch_info(const cf_handle* h, cf_launch_info* info) {
   return CF_OK;
 }
 
+int cf_decode_attn_block_unfused(cf_handle* h, int32_t batch, const void* hidden_states,
+                                 const void* ln_weight, const void* w_qkv, const void* w_o,
+                                 void* k_cache, void* v_cache, const int32_t* positions, void* out,
+                                 void* stream) {
+  if (h == nullptr || h->uf_ws == nullptr) return CF_ERR_INVALID_ARG;
+  const cf_config& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return CF_ERR_INVALID_ARG;
+  if (batch == 0) return CF_OK;
+  const void* ptrs[] = {hidden_states, ln_weight, w_qkv, w_o, k_cache, v_cache, positions, out};
+  for (const void* p : ptrs)
+    if (p == nullptr || ((uintptr_t)p & 15u) != 0) return CF_ERR_INVALID_ARG;
+  const int es = esize(c.dtype), D = c.head_dim, H = c.hidden;
+  const int nq = c.n_q_heads, nkv = c.n_kv_heads, S = c.s_max;
+  const size_t out_bytes = (size_t)batch * H * es;
+  const size_t cache_bytes = (size_t)batch * S * nkv * D * es;
+  if (overlaps(out, out_bytes, hidden_states, (size_t)batch * H * es) ||
+      overlaps(out, out_bytes, ln_weight, (size_t)H * es) ||
+      overlaps(out, out_bytes, w_qkv, (size_t)H * (nq + 2 * nkv) * D * es) ||
+      overlaps(out, out_bytes, w_o, (size_t)nq * D * H * es) ||
+      overlaps(out, out_bytes, k_cache, cache_bytes) ||
+      overlaps(out, out_bytes, v_cache, cache_bytes) ||
+      overlaps(out, out_bytes, positions, (size_t)batch * 4))
+    return CF_ERR_ALIAS;
+  UfParams p;
+  p.hidden = hidden_states;
+  p.ln_w = ln_weight;
+  p.w_qkv = w_qkv;
+  p.w_o = w_o;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.positions = positions;
+  p.out = out;
+  p.y = h->uf_y;
+  p.part = h->uf_part;
+  p.o32 = h->uf_o32;
+  p.rinv = h->uf_rinv;
+  p.acc = h->acc;
+  p.cnt_attn = h->uf_cnt_attn;
+  p.cnt_out = h->uf_cnt_out;
+  p.errflag = h->errflag;
+  p.B = batch;
+  p.H = H;
+  p.nq = nq;
+  p.nkv = nkv;
+  p.D = D;
+  p.S = S;
+  p.NS = h->uf_NS;
+  p.KS = h->uf_KS;
+  p.KS1 = h->uf_KS1;
+  p.eps = c.rms_eps;
+  p.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  for (int i = 0; i < 64; ++i) {
+    p.turn_hi[i] = h->turn_hi[i];
+    p.turn_lo[i] = h->turn_lo[i];
+  }
+  return unfused_launch(p, c.dtype, nq / nkv, static_cast<cudaStream_t>(stream));
+}
+
 void cf_destroy(cf_handle* h) {
   if (h == nullptr) return;
+  if (h->uf_ws) cudaFree(h->uf_ws);
   if (h->ws) cudaFree(h->ws);
   delete h;
 }

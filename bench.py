@@ -300,6 +300,9 @@ def main(argv=None):
     ap.add_argument("--timeline", action="store_true",
                     help="add per-phase block timings (globaltimer) of a few launches")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time the three-kernel path with HBM intermediates (the fusion "
+                         "baseline) instead of the fused kernel")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args(argv)
@@ -349,6 +352,8 @@ def main(argv=None):
         prefetch_ahead=args.prefetch_ahead, prefetch_late=args.prefetch_late, pdl=args.pdl,
         max_stages=args.max_stages, rows_per_block=args.rows_per_block)
     info = blk.launch_info()
+    step_fn = blk.unfused if args.unfused else blk
+    kernels_per_layer = 3 if args.unfused else 1
     outs = [[torch.empty_like(L["hidden"]) for L in rep] for rep in reps]
 
     stream = torch.cuda.Stream(device=dev)
@@ -356,8 +361,8 @@ def main(argv=None):
     def run_step(r):
         x = reps[r][0]["hidden"]
         for l, L in enumerate(reps[r]):
-            blk(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"], L["v_cache"],
-                L["positions"], outs[r][l], stream)
+            step_fn(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"],
+                    L["v_cache"], L["positions"], outs[r][l], stream)
             x = outs[r][l]
 
     with torch.cuda.stream(stream):
@@ -379,8 +384,8 @@ def main(argv=None):
             x = reps[r][0]["hidden"]
             for l, L in enumerate(reps[r]):
                 evs[k][0].record(stream)
-                blk(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"],
-                    L["v_cache"], L["positions"], outs[r][l], stream)
+                step_fn(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"],
+                        L["v_cache"], L["positions"], outs[r][l], stream)
                 evs[k][1].record(stream)
                 x = outs[r][l]
                 k += 1
@@ -460,8 +465,8 @@ def main(argv=None):
         p_dev[r].copy_(p_in[r], non_blocking=True)
         x = x_dev[r]
         for l, L in enumerate(reps[r]):
-            blk(B, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"], L["v_cache"],
-                p_dev[r], outs[r][l], stream)
+            step_fn(B, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"], L["v_cache"],
+                    p_dev[r], outs[r][l], stream)
             x = outs[r][l]
         h_out.copy_(outs[r][-1], non_blocking=True)
 
@@ -534,6 +539,7 @@ def main(argv=None):
                               f"{l2 / 1e6:.0f} MB"),
                 "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
                 "launch": info,
+                "path": "unfused (3 kernels, HBM intermediates)" if args.unfused else "fused",
             },
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
@@ -541,7 +547,9 @@ def main(argv=None):
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "traffic": recorded_traffic(w.name),
-                "kernel": KERNEL_NAMES.get(info.get("mode", 0), "cf_decode_kernel"),
+                "kernel": ("unfused path: uf_proj_kernel, uf_attn_kernel, uf_proj_kernel"
+                           if args.unfused else
+                           KERNEL_NAMES.get(info.get("mode", 0), "cf_decode_kernel")),
                 "launch_us_avg": round(launch_s_timed * 1e6, 3),
                 "launch_timing": "timed region (graph replays) / launches",
                 "isolated_launch_us_avg": round(launch_ms_avg * 1e3, 3),
@@ -553,7 +561,7 @@ def main(argv=None):
                     "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
-            "gpu_launches": args.steps * w.layers,
+            "gpu_launches": args.steps * w.layers * kernels_per_layer,
             **({"timeline_us": timeline} if timeline else {}),
             "clocks": clk.result(),
             "cpu_baseline": cpu,

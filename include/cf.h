@@ -99,7 +99,8 @@ typedef struct cf_launch_info {
 
 /* Validate cfg, pick the kernel instance and launch shape, and allocate the
  * handle's device workspace (fp32 output accumulator [max_batch, H],
- * completion counters, error flag) on the current device.  On failure
+ * completion counters, error flag, and the intermediates of the three-kernel
+ * path below) on the current device.  On failure
  * nothing stays allocated and *out is NULL.
  * Errors: INVALID_ARG (NULL, non-positive sizes, nq % nkv != 0, odd d, H not
  * a multiple of 64, cluster_size not in {0,1,2,4,8,16} or > d/4),
@@ -132,6 +133,19 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
                          const void* ln_weight, const void* w_qkv,
                          const void* w_o, void* k_cache, void* v_cache,
                          const int32_t* positions, void* out, void* stream);
+
+/* The same decode step as three separate kernels with fp32 intermediates in
+ * HBM -- the unfused layout [CF §1.1] compares the fused kernel with: (1)
+ * (x ∘ g) · W_qkv; (2) RMSNorm scale, RoPE, KV append and split-KV attention;
+ * (3) the output projection and residual.  It exists to measure the fusion
+ * gain.  Same arguments, results (within the parity tolerance) and errors
+ * as cf_decode_attn_block, on the same handle (whose workspace cf_create
+ * sizes for it too); head_dim 64 or 128, query heads per KV head 1 or 4.
+ * Asynchronous, no allocation. */
+int cf_decode_attn_block_unfused(cf_handle* h, int32_t batch, const void* hidden_states,
+                                 const void* ln_weight, const void* w_qkv, const void* w_o,
+                                 void* k_cache, void* v_cache, const int32_t* positions,
+                                 void* out, void* stream);
 
 /* Read and clear the device-side error flag.  Call after the work has
  * finished (synchronize the stream first).  Returns CF_OK,

@@ -64,7 +64,8 @@ def make_block(w: synth.Workload, **tune) -> binding.DecodeAttnBlock:
         dtype=w.dtype, **tune)
 
 
-def run_gpu(w: synth.Workload, t: dict, block=None, debug: bool = False, **tune):
+def run_gpu(w: synth.Workload, t: dict, block=None, debug: bool = False, unfused: bool = False,
+            **tune):
     """One fused decode step on the GPU; returns (out, k_cache, v_cache, dbg).
 
     ``t`` holds the layer's device tensors (they are cloned, not modified).
@@ -77,7 +78,8 @@ def run_gpu(w: synth.Workload, t: dict, block=None, debug: bool = False, **tune)
         dbg = torch.full((dbg_size(w, w.batch),), float("nan"), dtype=torch.float32,
                          device=t["hidden"].device)
         blk.set_debug(dbg)
-    blk(w.batch, t["hidden"], t["ln_weight"], t["w_qkv"], t["w_o"], kc, vc, t["positions"], out)
+    step = blk.unfused if unfused else blk
+    step(w.batch, t["hidden"], t["ln_weight"], t["w_qkv"], t["w_o"], kc, vc, t["positions"], out)
     torch.cuda.synchronize()
     st = binding.cf_get_status(blk.handle)
     if debug:
