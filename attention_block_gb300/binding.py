@@ -72,6 +72,8 @@ SIGNATURES = {
     "cf_set_timeline": (ctypes.c_int, [_vp, _vp]),
     "cf_bench_tma_stream": (ctypes.c_int, [ctypes.c_int] * 8 + [_vp, _vp, _vp]),
     "cf_bench_kv_stream": (ctypes.c_int, [ctypes.c_int] * 10 + [_vp] * 4),
+    "cf_bench_box_stream": (ctypes.c_int, [_vp] + [ctypes.c_int] * 10 + [_vp, _vp]),
+    "cf_bench_contig_stream": (ctypes.c_int, [_vp, ctypes.c_longlong, ctypes.c_longlong] + [ctypes.c_int] * 5 + [_vp, _vp]),
     "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
                                      + [_vp] * 9),
 }

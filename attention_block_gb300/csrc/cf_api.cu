@@ -123,9 +123,12 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   pl.G = G;
   pl.ctas_per_sm = 1;
   pl.Co = (Hc % 256 == 0) ? 256 : ((Hc % 128 == 0) ? 128 : 64);
-  // W_qkv tile: Rw rows of the NC group columns plus the [BT x Rw] slice of x
+  // W_qkv stage: Rw rows of CB 64-column boxes of the group's NC columns;
+  // the first stage of each slice of Rw rows also holds the [BT x Rw] slice
+  // of x
+  const int CB = rows_wqkv_boxes(NC);
   int rw = 16;
-  while (rw * 2 <= 256 && Hc % (rw * 2) == 0 && (rw * 2) * (NC + BT) * es <= stage_req) rw *= 2;
+  while (rw * 2 <= 256 && Hc % (rw * 2) == 0 && (rw * 2) * CB * 64 * es <= stage_req) rw *= 2;
   pl.Rw = rw;
   // K/V tile: Rt positions of K and of V (32 <= Rt <= 256, a power of two:
   // the attention hands out 32-position chunks)
@@ -134,7 +137,7 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   while (ro * 2 <= 256 && GD % (ro * 2) == 0 && (ro * 2) * pl.Co * es <= stage_req) ro *= 2;
   pl.Ro = ro;
   const int item =
-      std::max((NC + BT) * pl.Rw * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
+      std::max((CB * 64 + BT) * pl.Rw * es, std::max(2 * pl.Rt * D * es, pl.Ro * pl.Co * es));
   pl.stage_bytes = round_up(item, 1024);
 
   const int SE = RPC * NC + (RPC + 3) / 4 * 4;  // reduce-scatter slice (floats)

@@ -124,6 +124,118 @@ __global__ void __launch_bounds__(64) kv_stream_kernel(const __grid_constant__ K
   }
 }
 
+
+// Generic weight-band streaming skeleton: block i streams rows
+// [r_i, r_i + band_rows) x columns [c_i, c_i + band_cols) of a row-major
+// 16-bit [rows, cols] matrix as tiles of `bps` boxes {box_cols, box_rows} side
+// by side (one stage per tile), no compute.
+struct BoxStreamParams {
+  CUtensorMap tm;
+  int rows, cols, box_cols, box_rows, bps, band_rows, band_cols, stages, stage_bytes;
+  int col_major;  // tiles walk the band's rows first (columns outer)
+  int* errflag;
+};
+
+__global__ void __launch_bounds__(64) box_stream_kernel(const __grid_constant__ BoxStreamParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)p.stages * p.stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb_c = p.cols / p.band_cols;
+  const int c_i = (blockIdx.x % nb_c) * p.band_cols;
+  const int r_i = ((blockIdx.x / nb_c) * p.band_rows) % p.rows;
+  const int tc = p.bps * p.box_cols;  // columns per tile
+  const int n_r = p.band_rows / p.box_rows, n_c = p.band_cols / tc, total = n_r * n_c;
+  const uint32_t box_bytes = (uint32_t)(p.box_cols * p.box_rows * 2);
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      for (int it = 0; it < total; ++it) {
+        const int s = it % p.stages;
+        if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+        mbar_arrive_expect_tx(&full[s], p.bps * box_bytes);
+        uint8_t* dst = sm + (size_t)s * p.stage_bytes;
+        const int ti = p.col_major ? (it % n_r) : (it / n_c);
+        const int tj = p.col_major ? (it / n_r) : (it % n_c);
+        const int rr = r_i + ti * p.box_rows, cc = c_i + tj * tc;
+        for (int j = 0; j < p.bps; ++j)
+          tma_load_2d(dst + j * box_bytes, &p.tm, cc + j * p.box_cols, rr, &full[s], pol);
+      }
+    }
+    __syncwarp();
+  } else {
+    for (int it = 0; it < total; ++it) {
+      const int s = it % p.stages;
+      mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+}
+
+
+// Contiguous streaming skeleton: block i streams bytes [r_i, r_i + region) of
+// w, r_i = (i mod nregions) * region, in stages of stage_bytes made of
+// `pieces` equal bulk copies.  No compute.
+struct ContigStreamParams {
+  const uint8_t* w;
+  long long region;
+  int nregions, stage_bytes, pieces, stages;
+  int* errflag;
+};
+
+__global__ void __launch_bounds__(64) contig_stream_kernel(const __grid_constant__ ContigStreamParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)p.stages * p.stage_bytes);
+  uint64_t* empty = full + kMaxStages;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint8_t* src = p.w + (long long)(blockIdx.x % p.nregions) * p.region;
+  const int total = (int)(p.region / p.stage_bytes);
+  const uint32_t piece = (uint32_t)(p.stage_bytes / p.pieces);
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      for (int it = 0; it < total; ++it) {
+        const int s = it % p.stages;
+        if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)p.stage_bytes);
+        uint8_t* dst = sm + (size_t)s * p.stage_bytes;
+        for (int j = 0; j < p.pieces; ++j)
+          bulk_load_1d(dst + j * piece, src + (long long)it * p.stage_bytes + j * piece, piece,
+                       &full[s], pol);
+      }
+    }
+    __syncwarp();
+  } else {
+    for (int it = 0; it < total; ++it) {
+      const int s = it % p.stages;
+      mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+}
+
 }  // namespace
 
 extern "C" int cf_bench_tma_stream(int hidden, int n_q_heads, int n_kv_heads, int head_dim,
@@ -244,6 +356,104 @@ extern "C" int cf_bench_kv_stream(int batch, int s_max, int n_kv_heads, int head
     return CF_ERR_CUDA;
   const int grid = n_kv_heads * (batch / rows_per_block);
   kv_stream_kernel<<<grid, 64, per_block, static_cast<cudaStream_t>(stream)>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+  return CF_OK;
+}
+
+extern "C" int cf_bench_box_stream(const void* w, int rows, int cols, int box_cols, int box_rows,
+                                   int flags, int bps, int band_rows, int band_cols,
+                                   int stages, int blocks, int* errflag, void* stream) {
+  if (w == nullptr || errflag == nullptr || ((uintptr_t)w & 15u)) return CF_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || box_cols <= 0 || box_cols > 256 || box_rows <= 0 ||
+      box_rows > 256 || (box_cols * 2) % 16 != 0 || bps <= 0 || blocks <= 0)
+    return CF_ERR_INVALID_ARG;
+  const bool swizzle128 = flags & 1;
+  const int promo = (flags >> 1) & 3;  // 0: 256 B, 1: 128 B, 2: none, 3: 64 B
+  const bool shared_sm = (flags >> 3) & 1;
+  if (swizzle128 && box_cols * 2 > 128) return CF_ERR_INVALID_ARG;
+  if (band_rows % box_rows || band_cols % (bps * box_cols) || cols % band_cols ||
+      rows % band_rows || stages < 1 || stages > kMaxStages)
+    return CF_ERR_INVALID_ARG;
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (enc == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return CF_ERR_CUDA;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  BoxStreamParams p;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t str[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(&p.tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(w), dims, str, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+          promo == 0   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+          : promo == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+          : promo == 2 ? CU_TENSOR_MAP_L2_PROMOTION_NONE
+                       : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CF_ERR_CUDA;
+  p.rows = rows;
+  p.cols = cols;
+  p.box_cols = box_cols;
+  p.box_rows = box_rows;
+  p.bps = bps;
+  p.band_rows = band_rows;
+  p.band_cols = band_cols;
+  p.stages = stages;
+  p.col_major = (flags >> 4) & 1;
+  p.stage_bytes = (bps * box_cols * box_rows * 2 + 1023) / 1024 * 1024;
+  p.errflag = errflag;
+  cudaDeviceProp prop;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+    return CF_ERR_CUDA;
+  const int need = stages * p.stage_bytes + 2 * kMaxStages * 8 + 1024;
+  const int per_block = (int)prop.sharedMemPerBlockOptin;
+  if (need > per_block) return CF_ERR_INVALID_ARG;
+  const int smem = shared_sm ? need : per_block;
+  if (cudaFuncSetAttribute(box_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           per_block) != cudaSuccess)
+    return CF_ERR_CUDA;
+  box_stream_kernel<<<blocks, 64, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
+  return CF_OK;
+}
+
+extern "C" int cf_bench_contig_stream(const void* w, long long total_bytes, long long region_bytes,
+                                      int stage_bytes, int pieces, int stages, int blocks,
+                                      int shared_sm, int* errflag, void* stream) {
+  if (w == nullptr || errflag == nullptr || ((uintptr_t)w & 15u)) return CF_ERR_INVALID_ARG;
+  if (blocks <= 0 || stages < 1 || stages > kMaxStages || pieces < 1 || stage_bytes <= 0 ||
+      stage_bytes % (16 * pieces) != 0 || region_bytes <= 0 || region_bytes % stage_bytes != 0 ||
+      region_bytes > total_bytes)
+    return CF_ERR_INVALID_ARG;
+  ContigStreamParams p;
+  p.w = static_cast<const uint8_t*>(w);
+  p.region = region_bytes;
+  const long long nr = total_bytes / region_bytes;
+  p.nregions = (int)(nr < blocks ? nr : blocks);
+  p.stage_bytes = stage_bytes;
+  p.pieces = pieces;
+  p.stages = stages;
+  p.errflag = errflag;
+  cudaDeviceProp prop;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+    return CF_ERR_CUDA;
+  const int need = stages * ((stage_bytes + 1023) / 1024 * 1024) + 2 * kMaxStages * 8 + 1024;
+  const int per_block = (int)prop.sharedMemPerBlockOptin;
+  if (need > per_block || stage_bytes % 1024 != 0) return CF_ERR_INVALID_ARG;
+  if (cudaFuncSetAttribute(contig_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           per_block) != cudaSuccess)
+    return CF_ERR_CUDA;
+  contig_stream_kernel<<<blocks, 64, shared_sm ? need : per_block,
+                         static_cast<cudaStream_t>(stream)>>>(p);
   if (cudaGetLastError() != cudaSuccess) return CF_ERR_CUDA;
   return CF_OK;
 }

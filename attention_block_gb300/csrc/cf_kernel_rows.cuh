@@ -66,6 +66,15 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   constexpr int MR = BT < 16 ? 16 : BT;  // MMA rows (rows >= BT read a zero chunk)
   constexpr int MT = MR / 16;        // MMA row tiles
   constexpr int NTW = NC / 8 / kConsumerWarps;  // projection n-tiles per warp
+  constexpr int CB = rows_wqkv_boxes(NC);        // 64-column boxes per W_qkv stage
+  constexpr int NCG = NC / 64 / CB;              // W_qkv stages per K slice
+  // Tiles of at most four rows run both projections transposed (out^T =
+  // W^T x^T): 16 weight columns form the mma's M side and the N side holds
+  // the rows' hi and lo halves (4 + 4 columns), so one mma does the work of
+  // eight of the row-major form (M = 16 rows, 12 of them zero, and hi and lo
+  // in separate mmas).
+  constexpr bool TP = BT <= 4 && CB % 2 == 0;
+  constexpr int MPW = CB / 2;                    // m-tiles per warp per W_qkv stage (TP)
   constexpr int GD = G * D;          // O-projection reduction size
   constexpr int SE = rows_slice_floats(RPC, NC);
   constexpr int OP = rows_aop_pitch(GD);
@@ -73,6 +82,8 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   static_assert(BT % RPC == 0 && MR % 16 == 0, "batch tile");
   static_assert(NC % (8 * kConsumerWarps) == 0, "projection columns per warp");
   static_assert(D % 64 == 0, "head_dim in 64-column swizzle boxes");
+  static_assert(NCG * CB * 64 == NC && CB * 8 % kConsumerWarps == 0 && NTW == NCG * CB,
+                "W_qkv column groups");
   using MK = MmaKind<T>;
 
   extern __shared__ uint8_t smem_raw[];
@@ -155,7 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   const int nkt = Hc / p.Rw;
   const int ncb = Hc / p.Co;
   const int nrt = GD / p.Ro;
-  const int wboxes = NC / 64;                        // 64-column boxes per W_qkv tile
   const uint32_t wbox_bytes = (uint32_t)(p.Rw * 128);
   const uint32_t x_bytes = (uint32_t)(BT * p.Rw * (int)sizeof(T));
   const int obox = p.Co / 64;                        // 64-column boxes per W_o tile
@@ -176,20 +186,24 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         mbar_arrive_expect_tx(bar, bytes);
         return ring + (size_t)s * p.stage_bytes;
       };
-      // Phase 1: W_qkv tiles (G+2 head slices, 64-column swizzled boxes) of the
-      // K band, each followed by the matching [BT x Rw] slice of x.
-      for (int kt = 0; kt < nkt; ++kt, ++it) {
-        uint64_t* bar;
-        uint8_t* dst = slot(wboxes * wbox_bytes + x_bytes, bar);
+      // Phase 1: W_qkv tiles of the K band.  Each slice of Rw rows comes as
+      // NCG stages of CB 64-column swizzled boxes (the G+2 head slices' NC
+      // columns in order); the first stage of a slice also carries the
+      // matching [BT x Rw] slice of x.
+      for (int kt = 0; kt < nkt; ++kt) {
         const int y = k0 + kt * p.Rw;
-        for (int bx = 0; bx < wboxes; ++bx) {
-          const int col = bx * 64;  // column inside the group's NC columns
-          const int sg = col / D, cin = col % D;
-          const int gx = (sg < G) ? ((g * G + sg) * D + cin)
-                                  : ((sg == G ? p.nq + g : p.nq + p.nkv + g) * D + cin);
-          tma_load_2d(dst + bx * wbox_bytes, &p.tm_wqkv, gx, y, bar, pol_w);
+        for (int cg = 0; cg < NCG; ++cg, ++it) {
+          uint64_t* bar;
+          uint8_t* dst = slot(CB * wbox_bytes + (cg == 0 ? x_bytes : 0u), bar);
+          for (int bx = 0; bx < CB; ++bx) {
+            const int col = (cg * CB + bx) * 64;  // column inside the group's NC columns
+            const int sg = col / D, cin = col % D;
+            const int gx = (sg < G) ? ((g * G + sg) * D + cin)
+                                    : ((sg == G ? p.nq + g : p.nq + p.nkv + g) * D + cin);
+            tma_load_2d(dst + bx * wbox_bytes, &p.tm_wqkv, gx, y, bar, pol_w);
+          }
+          if (cg == 0) tma_load_2d(dst + CB * wbox_bytes, &p.tm_x, y, b0, bar, pol_w);
         }
-        tma_load_2d(dst + wboxes * wbox_bytes, &p.tm_x, y, b0, bar, pol_w);
       }
       if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdW] = globaltimer_ns();
       // Phase 2: K/V tiles of the owned rows, whole sequence each, as
@@ -254,78 +268,126 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         for (int j = 0; j < NTW; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
+      float acct[TP ? NCG * MPW : 1][4];  // transposed form: [m-tile][c-fragment]
+#pragma unroll
+      for (int j = 0; j < (TP ? NCG * MPW : 1); ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acct[j][e] = 0.f;
       float ss[NRW];
 #pragma unroll
       for (int i = 0; i < NRW; ++i) ss[i] = 0.f;
-      for (int kt = 0; kt < nkt; ++kt, ++it) {
-        const int s = it % p.stages;
-        mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
-        uint8_t* st = ring + (size_t)s * p.stage_bytes;
-        const T* xt = reinterpret_cast<const T*>(st + wboxes * wbox_bytes);  // [BT][Rw]
-        // x * g of this K slice as hi + lo 16-bit pairs (double-buffered);
-        // warp w stages rows w, w+8, ...
+      for (int kt = 0; kt < nkt; ++kt) {
+        // x * g of this K slice as hi + lo 16-bit pairs (double-buffered)
         uint8_t* ahi = un + (size_t)(kt & 1) * 2 * abytes;
         uint8_t* alo = ahi + abytes;
 #pragma unroll
-        for (int i = 0; i < NRW; ++i) {
-          const int row = warp + i * kConsumerWarps;
-          if (row < BT) {
-            for (int k = 2 * lane; k < p.Rw; k += 64) {
-              float f[2];
-              load_cvt<T, 2>(xt + row * p.Rw + k, f);
-              ss[i] = fmaf(f[0], f[0], fmaf(f[1], f[1], ss[i]));
-              float gw[2];
-              load_cvt<T, 2>(lnw + k0 + kt * p.Rw + k, gw);
-              const float v0 = f[0] * gw[0], v1 = f[1] * gw[1];
-              uint32_t hi, lo;
-              MK::split2(v0, v1, hi, lo);
-              *reinterpret_cast<uint32_t*>(ahi + row * apitch + k * 2) = hi;
-              *reinterpret_cast<uint32_t*>(alo + row * apitch + k * 2) = lo;
+        for (int cg = 0; cg < NCG; ++cg, ++it) {
+          const int s = it % p.stages;
+          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+          uint8_t* st = ring + (size_t)s * p.stage_bytes;
+          if (cg == 0) {
+            // stage the slice's x * g; warp w stages rows w, w+8, ...
+            const T* xt = reinterpret_cast<const T*>(st + CB * wbox_bytes);  // [BT][Rw]
+#pragma unroll
+            for (int i = 0; i < NRW; ++i) {
+              const int row = warp + i * kConsumerWarps;
+              if (row < BT) {
+                for (int k = 2 * lane; k < p.Rw; k += 64) {
+                  float f[2];
+                  load_cvt<T, 2>(xt + row * p.Rw + k, f);
+                  ss[i] = fmaf(f[0], f[0], fmaf(f[1], f[1], ss[i]));
+                  float gw[2];
+                  load_cvt<T, 2>(lnw + k0 + kt * p.Rw + k, gw);
+                  const float v0 = f[0] * gw[0], v1 = f[1] * gw[1];
+                  uint32_t hi, lo;
+                  MK::split2(v0, v1, hi, lo);
+                  *reinterpret_cast<uint32_t*>(ahi + row * apitch + k * 2) = hi;
+                  *reinterpret_cast<uint32_t*>(alo + row * apitch + k * 2) = lo;
+                }
+              }
+            }
+            named_sync(kBarConsumers, kConsumers);
+          }
+          if constexpr (TP) {
+            for (int ks = 0; ks < p.Rw / 16; ++ks) {
+              uint32_t b0x, b1x;
+              ldmatrix_b_hilo_rows(b0x, b1x, ahi, alo, apitch, BT, zero16, ks * 16, lane);
+#pragma unroll
+              for (int jj = 0; jj < MPW; ++jj) {
+                const int m0 = (warp * MPW + jj) * 16;  // column inside the stage's CB*64
+                uint32_t a[4];
+                ldmatrix_at_sw128(a, st + (m0 / 64) * wbox_bytes, ks * 16, m0 % 64, lane);
+                MK::mma(acct[cg * MPW + jj], a, b0x, b1x);
+              }
+            }
+          } else {
+            for (int ks = 0; ks < p.Rw / 16; ++ks) {
+              uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                ldmatrix_a_rows(ah[mt], ahi + mt * 16 * apitch + ks * 32, apitch, BT - mt * 16,
+                                zero16, lane);
+                ldmatrix_a_rows(al[mt], alo + mt * 16 * apitch + ks * 32, apitch, BT - mt * 16,
+                                zero16, lane);
+              }
+#pragma unroll
+              for (int jj = 0; jj < CB; ++jj) {
+                const int n = (warp * CB + jj) * 8;  // column inside the stage's CB*64
+                uint32_t b0r, b1r;
+                ldmatrix_b_sw128(b0r, b1r, st + (n / 64) * wbox_bytes, ks * 16, n % 64, lane);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                  MK::mma(acc[mt][cg * CB + jj], ah[mt], b0r, b1r);
+                  MK::mma(acc[mt][cg * CB + jj], al[mt], b0r, b1r);
+                }
+              }
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
         }
-        named_sync(kBarConsumers, kConsumers);
-        for (int ks = 0; ks < p.Rw / 16; ++ks) {
-          uint32_t ah[MT][4], al[MT][4];
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            ldmatrix_a_rows(ah[mt], ahi + mt * 16 * apitch + ks * 32, apitch, BT - mt * 16, zero16,
-                            lane);
-            ldmatrix_a_rows(al[mt], alo + mt * 16 * apitch + ks * 32, apitch, BT - mt * 16, zero16,
-                            lane);
-          }
-#pragma unroll
-          for (int j = 0; j < NTW; ++j) {
-            const int n = (warp * NTW + j) * 8;  // column in [0, NC)
-            uint32_t b0r, b1r;
-            ldmatrix_b_sw128(b0r, b1r, st + (n / 64) * wbox_bytes, ks * 16, n % 64, lane);
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              MK::mma(acc[mt][j], ah[mt], b0r, b1r);
-              MK::mma(acc[mt][j], al[mt], b0r, b1r);
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
       }
       stamp(kTlProjLoop);
       // Partial sums -> red, slice-major: row r goes to slice r / RPC, so the
       // rows block c owns form its contiguous slice c.
       const int gq = lane >> 2, tq = lane & 3;
+      if constexpr (TP) {
+        // acct j holds columns (gq, gq + 8) of m-tile warp*MPW + j%MPW of
+        // column group j/MPW; its c-fragment columns 2tq, 2tq+1 are rows
+        // 2tq, 2tq+1 (hi) for tq < 2 and the lo halves of rows 2tq-4, 2tq-3
+        // for tq >= 2: lane tq adds the lo part from lane tq + 2.
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+        for (int j = 0; j < NCG * MPW; ++j) {
+          float v[4];
 #pragma unroll
-        for (int j = 0; j < NTW; ++j) {
-          const int n = (warp * NTW + j) * 8 + 2 * tq;
+          for (int e = 0; e < 4; ++e) v[e] = acct[j][e] + __shfl_xor_sync(0xffffffffu, acct[j][e], 2);
+          const int col = (j / MPW) * CB * 64 + (warp * MPW + j % MPW) * 16 + gq;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int row = mt * 16 + gq + 8 * h;
-            if (row < BT)
-              *reinterpret_cast<float2*>(red + (row / RPC) * SE + (row % RPC) * NC + n) =
-                  make_float2(acc[mt][j][2 * h], acc[mt][j][2 * h + 1]);
+            const int row = 2 * tq + h;
+            if (tq < 2 && row < BT) {
+              float* dst = red + (row / RPC) * SE + (row % RPC) * NC + col;
+              dst[0] = v[h];
+              dst[8] = v[2 + h];
+            }
           }
         }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int j = 0; j < NTW; ++j) {
+            // acc j covers n-tile warp*CB + j%CB of column group j/CB
+            const int n = (j / CB) * CB * 64 + (warp * CB + j % CB) * 8 + 2 * tq;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = mt * 16 + gq + 8 * h;
+              if (row < BT)
+                *reinterpret_cast<float2*>(red + (row / RPC) * SE + (row % RPC) * NC + n) =
+                    make_float2(acc[mt][j][2 * h], acc[mt][j][2 * h + 1]);
+            }
+          }
+      }
 #pragma unroll
       for (int i = 0; i < NRW; ++i) {
         const int row = warp + i * kConsumerWarps;
@@ -443,7 +505,66 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
 
     // ---- Phase 3: [BT x GD] x [GD x Co] per column box on the tensor cores,
     // fp32 atomics into the accumulator [CF §3.2] ----------------------------
-    {
+    if constexpr (BT <= 4) {
+      // Transposed (out^T = W_o^T o^T, see the projection): per column band,
+      // warp w takes m-tiles w, w + 8 (16 columns each) of the Co columns.
+      const int mtiles = p.Co / 16;
+      const int gq = lane >> 2, tq = lane & 3;
+      const bool even = (gq & 1) == 0;
+      for (int cb = 0; cb < ncb; ++cb) {
+        float acc[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+        for (int rt = 0; rt < nrt; ++rt, ++it) {
+          const int s = it % p.stages;
+          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+          if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
+          uint8_t* st = ring + (size_t)s * p.stage_bytes;
+          for (int ks = 0; ks < p.Ro / 16; ++ks) {
+            const int kglob = rt * p.Ro + ks * 16;
+            uint32_t b0x, b1x;
+            ldmatrix_b_hilo_rows(b0x, b1x, aop, aop + 2 * GD, OP, BT, zero16, kglob, lane);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int mt = warp + j * kConsumerWarps;
+              if (mt < mtiles) {
+                const int m0 = mt * 16;
+                uint32_t a[4];
+                ldmatrix_at_sw128(a, st + (m0 / 64) * obox_bytes, ks * 16, m0 % 64, lane);
+                MK::mma(acc[j], a, b0x, b1x);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        // c-fragment: columns (gq, gq + 8) x rows (2tq, 2tq + 1), lo halves in
+        // lanes tq + 2.  After adding them, even-gq lanes take row 2tq of
+        // columns (gq, gq + 1) and (gq + 8, gq + 9) and odd-gq lanes row
+        // 2tq + 1 of (gq - 1, gq) and (gq + 7, gq + 8), so each atomic adds two
+        // adjacent columns.
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int mt = warp + j * kConsumerWarps;
+          if (mt >= mtiles) continue;  // warp-uniform
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = acc[j][e] + __shfl_xor_sync(0xffffffffu, acc[j][e], 2);
+          const float x = __shfl_xor_sync(0xffffffffu, even ? v[1] : v[0], 4);
+          const float y = __shfl_xor_sync(0xffffffffu, even ? v[3] : v[2], 4);
+          const int row = 2 * tq + (even ? 0 : 1);
+          const int col = k0 + cb * p.Co + mt * 16 + (even ? gq : gq - 1);
+          if (tq < 2 && row < BT && b0 + row < p.B && s_pos[row] >= 0) {
+            float* dst = p.acc + (size_t)(b0 + row) * p.H + col;
+            atomicAdd(reinterpret_cast<float2*>(dst), even ? make_float2(v[0], x) : make_float2(x, v[1]));
+            atomicAdd(reinterpret_cast<float2*>(dst + 8),
+                      even ? make_float2(v[2], y) : make_float2(y, v[3]));
+          }
+        }
+      }
+    } else {
       const int ntiles = p.Co / 8;
       const int gq = lane >> 2, tq = lane & 3;
       for (int cb = 0; cb < ncb; ++cb) {

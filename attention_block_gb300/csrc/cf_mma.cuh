@@ -95,6 +95,40 @@ __device__ __forceinline__ void ldmatrix_b_sw128(uint32_t& b0, uint32_t& b1, con
                : "r"(addr));
 }
 
+// A fragment (16 m-rows x 16 k-columns) of the TRANSPOSE of a TMA box written
+// with the 128-byte swizzle: A[m][k] = box[k0 + k][m0 + m], i.e. the 8x8
+// blocks (k0..7, m0..7), (k0..7, m8..15), (k8..15, m0..7), (k8..15, m8..15)
+// of the box, each transposed.  m0 is a multiple of 16 below 64, k0 of 16.
+__device__ __forceinline__ void ldmatrix_at_sw128(uint32_t (&a)[4], const void* box, int k0,
+                                                  int m0, int lane) {
+  const int i = lane >> 3;  // sub-matrix this lane addresses
+  const int k = k0 + ((i >> 1) << 3) + (lane & 7);
+  const int chunk = ((m0 >> 3) + (i & 1)) ^ (k & 7);
+  const uint32_t addr = smem_u32(box) + k * 128 + chunk * 16;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr));
+}
+
+// B fragment (16 k-rows x 8 n-columns) whose columns are the rows of two
+// row-major 16-bit matrices: B[k][n] = hi[n][k0 + k] for n < 4 and
+// lo[n - 4][k0 + k] for n >= 4 (row pitch `pitch` bytes, a multiple of 16);
+// rows >= nrows (<= 4) of either read the 16-byte zero chunk at `zero16`.
+// With hi + lo the two halves of a split fp32 operand, one mma gives both
+// partial products of four rows in separate accumulator columns.
+__device__ __forceinline__ void ldmatrix_b_hilo_rows(uint32_t& b0, uint32_t& b1, const void* hi,
+                                                     const void* lo, int pitch, int nrows,
+                                                     const void* zero16, int k0, int lane) {
+  const int n = lane & 7, kh = (lane >> 3) & 1;  // lanes 0..15 address the two matrices
+  const int r = n & 3;
+  const void* rowp = n < 4 ? hi : lo;
+  const uint32_t addr =
+      r < nrows ? smem_u32(rowp) + r * pitch + (k0 + kh * 8) * 2 : smem_u32(zero16);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(b0), "=r"(b1)
+               : "r"(addr));
+}
+
 // Four 8x8 16-bit matrices; lane l supplies the row address of matrix l / 8,
 // row l % 8.  Register i holds matrix i in the mma fragment layout (thread t:
 // row t / 4, elements 2 (t % 4) and 2 (t % 4) + 1); with .trans, matrix i is

@@ -18,6 +18,15 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxRounds = 4;                     // log2(kMaxCluster)
 constexpr int kMaxStages = 32;
 
+// Batched kernel: 64-column boxes per W_qkv stage.  The head group's NC
+// projection columns come in NC/64/CB stages per slice of Rw hidden rows.  A
+// few tall boxes per stage stream faster than many short ones (the TMA cost
+// grows with the number of boxes and stages, not only with the bytes), so a
+// stage holds four boxes where NC/64 allows.
+__host__ __device__ constexpr int rows_wqkv_boxes(int NC) {
+  return (NC / 64) % 4 == 0 ? 4 : ((NC / 64) % 3 == 0 ? 3 : NC / 64);
+}
+
 // Phase stamps of the optional timeline (one row of kTimelineSlots per block).
 enum TimelineSlot {
   kTlStart = 0,       // after the start-up cluster barrier

@@ -130,6 +130,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ------------------------------------------------------------ TMA loads --
+// Contiguous bulk copy global -> this CTA's shared memory of `bytes` bytes
+// (both addresses 16-byte aligned, bytes a multiple of 16), completing on
+// `bar` with complete_tx of `bytes`.
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Tiled tensor copies global -> this CTA's shared memory, completing on `bar`
 // with complete_tx of the box's byte count.  The innermost coordinate x is
 // always a multiple of 16 bytes (host-checked layouts).

@@ -66,6 +66,30 @@ int cf_bench_kv_stream(int batch, int s_max, int n_kv_heads, int head_dim, int e
                        int ctas_per_sm, const void* k_cache, const void* v_cache, int* errflag,
                        void* stream);
 
+/* Bare TMA streaming rate of weight-band tile shapes: `blocks` blocks, block i
+ * streaming band_rows x band_cols of the row-major fp16 [rows, cols] matrix w
+ * (band i mod cols/band_cols, row block i / (cols/band_cols) mod
+ * rows/band_rows) as tiles of `bps` boxes {box_cols, box_rows} side by side,
+ * through `stages` stages.  No compute.  flags: bit 0 the 128-byte swizzle;
+ * bits 1-2 the L2 promotion (0: 256 B, 1: 128 B, 2: none, 3: 64 B); bit 3
+ * launch with only the shared memory the ring needs (several blocks per SM),
+ * else with the full opt-in amount (one block per SM); bit 4 walk the band's
+ * tiles down its rows first (column groups outer).  Errors:
+ * CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
+int cf_bench_box_stream(const void* w, int rows, int cols, int box_cols, int box_rows,
+                        int flags, int bps, int band_rows, int band_cols, int stages,
+                        int blocks, int* errflag, void* stream);
+
+/* Bare streaming rate of contiguous per-block regions: `blocks` blocks, block
+ * i streaming bytes [(i mod n) * region_bytes, +region_bytes) of w (n =
+ * min(blocks, total_bytes / region_bytes)) in stages of stage_bytes (a
+ * multiple of 1024), each filled by `pieces` equal bulk copies, through
+ * `stages` stages; shared_sm != 0 launches with only the shared memory the
+ * ring needs.  No compute.  Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
+int cf_bench_contig_stream(const void* w, long long total_bytes, long long region_bytes,
+                           int stage_bytes, int pieces, int stages, int blocks, int shared_sm,
+                           int* errflag, void* stream);
+
 /* Phase timeline of later cf_decode_attn_block calls of handle h (a tuning
  * aid): when `stamps` is a zeroed device buffer of grid_blocks * 32 unsigned
  * 64-bit values, every block writes %globaltimer (ns) at its phase
