@@ -31,7 +31,8 @@ class CfConfig(ctypes.Structure):
         ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)] + [
         (n, ctypes.c_int32) for n in (
             "dtype", "cluster_size", "batch_tile", "stage_bytes", "ctas_per_sm",
-            "prefetch_ahead", "prefetch_late", "pdl", "max_stages", "rows_per_block")]
+            "prefetch_ahead", "prefetch_late", "pdl", "max_stages", "rows_per_block",
+            "kv_prefetch")]
 
 
 class CfLaunchInfo(ctypes.Structure):
@@ -137,14 +138,14 @@ def strerror(code: int) -> str:
 def make_config(hidden, n_q_heads, n_kv_heads, head_dim, max_batch, s_max, rope_theta=1e4,
                 rms_eps=1e-6, dtype=CF_F16, cluster_size=0, batch_tile=0, stage_bytes=0,
                 ctas_per_sm=0, prefetch_ahead=0, prefetch_late=0, pdl=0,
-                max_stages=0, rows_per_block=0) -> CfConfig:
+                max_stages=0, rows_per_block=0, kv_prefetch=0) -> CfConfig:
     if isinstance(dtype, str):
         dtype = {"f32": CF_F32, "f16": CF_F16, "bf16": CF_BF16}[dtype]
     return CfConfig(int(hidden), int(n_q_heads), int(n_kv_heads), int(head_dim),
                     int(max_batch), int(s_max), float(rope_theta), float(rms_eps), int(dtype),
                     int(cluster_size), int(batch_tile), int(stage_bytes), int(ctas_per_sm),
                     int(prefetch_ahead), int(prefetch_late), int(pdl), int(max_stages),
-                    int(rows_per_block))
+                    int(rows_per_block), int(kv_prefetch))
 
 
 def cf_create(cfg: CfConfig) -> int:

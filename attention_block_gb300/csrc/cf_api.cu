@@ -274,7 +274,7 @@ struct cf_handle {
   int* errflag = nullptr;
   float* dbg = nullptr;
   unsigned long long* timeline = nullptr;
-  int prefetch_ahead = 0, prefetch_late = 0;
+  int prefetch_ahead = 0, prefetch_late = 0, kv_prefetch = 0;
   bool pdl = true;
   float turn_hi[64], turn_lo[64];  // RoPE turn rates as float pairs (see KParams)
   MapCache m_wqkv, m_wo, m_k, m_v, m_x;
@@ -306,6 +306,7 @@ int validate_config(const cf_config* c) {
   if (c->ctas_per_sm < 0 || c->ctas_per_sm > 2) return CF_ERR_INVALID_ARG;
   if (c->prefetch_ahead < -1 || c->prefetch_ahead > 64) return CF_ERR_INVALID_ARG;
   if (c->prefetch_late < -1 || c->prefetch_late > 3) return CF_ERR_INVALID_ARG;
+  if (c->kv_prefetch < -1 || c->kv_prefetch > 64) return CF_ERR_INVALID_ARG;
   if (c->pdl < -1 || c->pdl > 1) return CF_ERR_INVALID_ARG;
   if (c->max_stages < 0 || c->max_stages == 1 || c->max_stages > kMaxStages)
     return CF_ERR_INVALID_ARG;
@@ -496,6 +497,7 @@ int plan_handle(const cf_config& c, cf_handle& h) {
   // with the W_qkv stream), so they are off unless asked for.
   h.prefetch_ahead = std::max(0, c.prefetch_ahead);
   h.prefetch_late = std::max(0, c.prefetch_late);
+  h.kv_prefetch = c.kv_prefetch < 0 ? 0 : (c.kv_prefetch > 0 ? c.kv_prefetch : kDefaultKvPrefetch);
   h.pdl = c.pdl != -1;
   for (int i = 0; i < 64; ++i) {
     // turns per position: theta^(-2i/d) / (2 pi), split into hi + lo floats
@@ -686,6 +688,7 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
   kp.timeline = h->timeline;
   kp.prefetch_ahead = h->prefetch_ahead;
   kp.prefetch_late = h->prefetch_late;
+  kp.kv_prefetch = h->kv_prefetch;
   kp.B = batch;
   kp.H = H;
   kp.nq = nq;

@@ -11,8 +11,9 @@
 // transposing form); the probabilities P leave the S^T accumulators as packed
 // 16-bit pairs and become the B operand of the second product through
 // movmatrix.trans.  Q (fp32) and P (fp32, in [0, 1]) enter as 16-bit hi + lo
-// pairs, so both products keep about fp32 accuracy; K and V are exact in their
-// storage type.
+// pairs for bf16 storage, so both products keep about fp32 accuracy, and as
+// single fp16 values for fp16 storage (MmaKind::kAttnHiLo); K and V are exact
+// in their storage type.
 //
 // K/V tiles arrive as boxes of 64 columns (128 bytes) written with the
 // 128-byte swizzle: stage = K [D/64][Rt][64] then V [D/64][Rt][64].  A warp
@@ -151,7 +152,7 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
           ldsm_x4(a[0], a[1], a[2], a[3],
                   kbase + (ch >> 3) * box_bytes + sw128(cb + mt * 16 + lrow, ch & 7));
           MK::mma(sa[mt], a, f.x, f.y);
-          MK::mma(sb[mt], a, f.z, f.w);
+          if constexpr (MK::kAttnHiLo) MK::mma(sb[mt], a, f.z, f.w);
         }
       }
       // ---- online softmax per head column (positions are spread over gq)
@@ -210,8 +211,10 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
         MK::split2(pr[mt][2], pr[mt][3], h23, l23);
         bh[mt][0] = movmatrix_trans(h01);
         bh[mt][1] = movmatrix_trans(h23);
-        bl[mt][0] = movmatrix_trans(l01);
-        bl[mt][1] = movmatrix_trans(l23);
+        if constexpr (MK::kAttnHiLo) {
+          bl[mt][0] = movmatrix_trans(l01);
+          bl[mt][1] = movmatrix_trans(l23);
+        }
       }
       // ---- O^T += V^T P^T: k = 32 positions in two steps
 #pragma unroll
@@ -223,7 +226,7 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
           ldsm_x4_trans(a[0], a[2], a[1], a[3],
                         vbase + (ch >> 3) * box_bytes + sw128(cb + mt * 16 + lrow, ch & 7));
           MK::mma(o[md], a, bh[mt][0], bh[mt][1]);
-          MK::mma(o[md], a, bl[mt][0], bl[mt][1]);
+          if constexpr (MK::kAttnHiLo) MK::mma(o[md], a, bl[mt][0], bl[mt][1]);
         }
       }
     }

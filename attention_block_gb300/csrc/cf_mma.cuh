@@ -20,6 +20,12 @@ template <typename T>
 struct MmaKind;  // PTX type names of the 16-bit input types
 template <>
 struct MmaKind<__half> {
+  // The attention's fp32 operands (scaled query, probabilities) enter as one
+  // fp16 value each (11 significant bits; the products still accumulate in
+  // fp32): the attention output then carries a mean relative error of about
+  // the fp16 unit roundoff (2.6e-4 measured on the 64-row, 2048-hidden MHA
+  // layer, against a 1e-3 bound) and the block output about 1e-5.
+  static constexpr bool kAttnHiLo = false;
   static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                              uint32_t b1) {
     asm volatile(
@@ -40,6 +46,9 @@ struct MmaKind<__half> {
 };
 template <>
 struct MmaKind<__nv_bfloat16> {
+  // bf16 keeps 8 significant bits: the attention operands enter as hi + lo
+  // pairs (about fp32 accuracy).
+  static constexpr bool kAttnHiLo = true;
   static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                              uint32_t b1) {
     asm volatile(

@@ -82,6 +82,10 @@ typedef struct cf_config {
                              many (>= 2)                                      */
   int32_t rows_per_block; /* batched mode (batch_tile >= 16, fp16/bf16): batch
                              rows each block of a cluster owns; 0 = default  */
+  int32_t kv_prefetch;    /* batched mode: K/V tiles of each owned row that are
+                             prefetched into L2 while the QKV projection
+                             streams (spread over the sequence); 0 = default,
+                             -1 = none, else at most that many (<= 64)       */
 } cf_config;
 
 typedef struct cf_handle cf_handle; /* opaque */
