@@ -152,11 +152,12 @@ __device__ void cluster_gather(float* data, int se, uint64_t* gbar, int rank, in
 // release-arrivals.
 
 // Tell every other block of the cluster that this block's data for an
-// exchange is complete: a cluster-scope fence, then one release-arrival on
-// the same-offset mbarrier `bar` of each peer.  Called by one thread after
-// the producing threads have synchronized with it.
+// exchange is complete: one release-arrival (cluster scope) on the
+// same-offset mbarrier `bar` of each peer.  Called by one thread after the
+// producing threads have synchronized with it through a CTA barrier; the
+// release is cumulative, so it also orders their shared-memory writes
+// before the peers' acquiring waits (no separate fence is needed).
 __device__ __forceinline__ void cluster_signal_peers(uint64_t* bar, int rank, int N) {
-  fence_acq_rel_cluster();
   const uint32_t b = smem_u32(bar);
   for (int q = 1; q < N; ++q) mbar_remote_arrive(mapa(b, (uint32_t)((rank + q) % N)));
 }

@@ -238,10 +238,6 @@ __device__ __forceinline__ void mbar_remote_arrive(uint32_t rbar) {
                : "memory");
 }
 
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
 // 16-byte loads from (possibly another CTA's) shared memory at a cluster
 // shared address.
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
