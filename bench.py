@@ -72,13 +72,20 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Sources of the fused decode kernels and their launch planning (not the
+# measurement probes, the test primitives or the unfused baseline).
+FUSED_KERNEL_SOURCES = ("cf_api.cu", "cf_attention.cuh", "cf_attention_tc.cuh", "cf_cluster.cuh",
+                        "cf_common.cuh", "cf_inst_bf16.cu", "cf_inst_f16.cu", "cf_inst_f32.cu",
+                        "cf_inst_rows.cu", "cf_kernel.cuh", "cf_kernel_rows.cuh", "cf_mma.cuh",
+                        "cf_params.h", "cf_ptx.cuh", "cf_registry.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_block_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode() + fh.read())
+    for name in FUSED_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
