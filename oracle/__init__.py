@@ -74,6 +74,10 @@ def _load():
                                            _dp, _dp, _dp, ctypes.c_int, _dp, _dp,
                                            _dp, _dp, _dp, _dp, _dp]
             lib.orc_decode_row.restype = ctypes.c_int
+            lib.orc_silu.argtypes = [ctypes.c_double]
+            lib.orc_silu.restype = ctypes.c_double
+            lib.orc_ffn_row.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double] + [_dp] * 9
+            lib.orc_ffn_row.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -166,4 +170,30 @@ def decode(cfg: dict, X, g, wqkv, wo, KC, VC, positions, rows=None):
     rows = range(X.shape[0]) if rows is None else rows
     outs = [decode_row(cfg, X[b], g, wqkv, wo, KC[b], VC[b], int(positions[b]))
             for b in rows]
+    return {k: np.stack([o[k] for o in outs]) for k in outs[0]}
+
+
+def silu(z: float) -> float:
+    return float(_load().orc_silu(float(z)))
+
+
+def ffn_row(h, g2, wg, wu, wd, eps: float):
+    """Second RMSNorm + SwiGLU FFN + residual for one row h [H]; wg, wu, wd
+    are [I, H].  Returns a dict with out, n, a, proj (float64)."""
+    h, g2, wg, wu, wd = _f64(h), _f64(g2), _f64(wg), _f64(wu), _f64(wd)
+    H = h.shape[0]
+    I = wg.shape[0]
+    assert wg.shape == (I, H) and wu.shape == (I, H) and wd.shape == (I, H)
+    res = {"out": np.empty(H), "n": np.empty(H), "a": np.empty(I), "proj": np.empty(H)}
+    rc = _load().orc_ffn_row(H, I, float(eps), _p(h), _p(g2), _p(wg), _p(wu), _p(wd),
+                             _p(res["out"]), _p(res["n"]), _p(res["a"]), _p(res["proj"]))
+    if rc != 0:
+        raise ValueError("oracle rejected the FFN shape")
+    return res
+
+
+def ffn(Hs, g2, wg, wu, wd, eps: float, rows=None):
+    """Batch form of ffn_row over the rows of Hs [B, H] (or the selected rows)."""
+    rows = range(Hs.shape[0]) if rows is None else rows
+    outs = [ffn_row(Hs[b], g2, wg, wu, wd, eps) for b in rows]
     return {k: np.stack([o[k] for o in outs]) for k in outs[0]}

@@ -201,3 +201,40 @@ int orc_decode_row(const orc_config* c, const double* x, const double* g,
   free(proj);
   return 0;
 }
+
+double orc_silu(double z) { return z / (1.0 + exp(-z)); }
+
+int orc_ffn_row(int H, int I, double eps, const double* h, const double* g2,
+                const double* wg, const double* wu, const double* wd,
+                double* out, double* dbg_n, double* dbg_a, double* dbg_proj) {
+  if (H <= 0 || I <= 0) return -1;
+  double* n = (double*)malloc(sizeof(double) * (size_t)H);
+  double* a = (double*)malloc(sizeof(double) * (size_t)I);
+  double* proj = (double*)malloc(sizeof(double) * (size_t)H);
+  /* 1. Second RMSNorm [LNA §一], the same form as the first. */
+  orc_rmsnorm(H, h, g2, eps, n);
+  /* 2. Gate and up projections, SiLU on the gate, elementwise product. */
+  for (int i = 0; i < I; ++i) {
+    const double* grow = wg + (size_t)i * (size_t)H;
+    const double* urow = wu + (size_t)i * (size_t)H;
+    double gs = 0.0, us = 0.0;
+    for (int k = 0; k < H; ++k) {
+      gs += grow[k] * n[k];
+      us += urow[k] * n[k];
+    }
+    a[i] = orc_silu(gs) * us;
+  }
+  /* 3. Down projection (a . Wd) and residual [LNA §一]. */
+  orc_matvec(I, H, a, wd, proj);
+  for (int j = 0; j < H; ++j) out[j] = h[j] + proj[j];
+  if (dbg_n)
+    for (int k = 0; k < H; ++k) dbg_n[k] = n[k];
+  if (dbg_a)
+    for (int i = 0; i < I; ++i) dbg_a[i] = a[i];
+  if (dbg_proj)
+    for (int j = 0; j < H; ++j) dbg_proj[j] = proj[j];
+  free(n);
+  free(a);
+  free(proj);
+  return 0;
+}

@@ -25,6 +25,8 @@
  *                                   d contiguous columns (x . W form)
  *   wo          [nq*d, H]           (attn . W_o form)
  *   kc, vc      [S, nkv, d]         one batch row of the KV cache
+ *   wg, wu, wd  [I, H]              FFN weights, one row per intermediate
+ *                                   unit (see orc_ffn_row)
  */
 #ifndef CF_ORACLE_H
 #define CF_ORACLE_H
@@ -95,6 +97,23 @@ int orc_decode_row(const orc_config* c, const double* x, const double* g,
                    double* vc, int pos, double* out, double* dbg_n,
                    double* dbg_q, double* dbg_k, double* dbg_v,
                    double* dbg_o, double* dbg_proj);
+
+/* SiLU, the gate activation of the LLaMA FFN: silu(z) = z / (1 + exp(-z)). */
+double orc_silu(double z);
+
+/* The rest of the decoder block for one batch row: the second RMS Norm, the
+ * FFN and its residual, in the block order of [LNA §一] ("第二个 RMS Norm、
+ * FFN", LLaMA architecture).  The pages name the FFN but not its inner form;
+ * the LLaMA FFN is the gated (SwiGLU) one, read here as
+ *   n   = RMSNorm(h; g2)                       (as orc_rmsnorm)
+ *   a_i = silu( sum_k Wg[i,k] n_k ) * ( sum_k Wu[i,k] n_k ),   i < I
+ *   out_j = h_j + sum_i a_i Wd[i,j],                           j < H
+ * with Wg, Wu, Wd all [I, H] row-major (row i holds intermediate unit i's
+ * weights).  dbg_n [H], dbg_a [I] and dbg_proj [H] (the FFN output before the
+ * residual) may each be NULL.  Returns 0, or -1 for a bad shape.           */
+int orc_ffn_row(int H, int I, double eps, const double* h, const double* g2,
+                const double* wg, const double* wu, const double* wd,
+                double* out, double* dbg_n, double* dbg_a, double* dbg_proj);
 
 #ifdef __cplusplus
 }

@@ -31,6 +31,16 @@ MUTATIONS = {
     "no_rope_on_q": ("for (int h = 0; h < nq; ++h) orc_rope(", "for (int h = 0; h < 0; ++h) orc_rope("),
     "no_rope_on_k": ("for (int j = 0; j < nkv; ++j) orc_rope(", "for (int j = 0; j < 0; ++j) orc_rope("),
     "split_without_rescale": ("double r = exp(mc[c] - m);", "double r = 1.0;"),
+    "ffn_silu_on_up": ("a[i] = orc_silu(gs) * us;", "a[i] = gs * orc_silu(us);"),
+    "ffn_silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "ffn_drop_residual": ("out[j] = h[j] + proj[j];", "out[j] = proj[j];"),
+    "ffn_up_from_gate_rows": ("us += urow[k] * n[k];", "us += grow[k] * n[k];"),
+    "ffn_norm_weight_dropped": ("orc_rmsnorm(H, h, g2, eps, n);", "orc_rmsnorm(H, h, h, eps, n);"),
+    "ffn_gate_row_read_as_column": ("gs += grow[k] * n[k];",
+                                    "gs += wg[(size_t)k * (size_t)I + (size_t)i % (size_t)I] * n[k];"),
+    "ffn_down_transposed": ("orc_matvec(I, H, a, wd, proj);",
+                            "for (int j = 0; j < H; ++j) {\n    proj[j] = 0.0;\n    "
+                            "for (int i = 0; i < I; ++i) proj[j] += a[i] * wd[(size_t)j * (size_t)I + i];\n  }"),
     "transposed_weight": (
         "const double* row = W + (size_t)i * (size_t)N;\n    for (int j = 0; j < N; ++j) y[j] += xi * row[j];",
         "for (int j = 0; j < N; ++j) y[j] += xi * W[(size_t)j * (size_t)K + i];"),

@@ -332,3 +332,109 @@ def test_oracle_regression_fixture():
     stored = {row[0]: np.array([float(v) for v in row[1:]]) for row in rows}
     np.testing.assert_allclose(r["out"][0], stored["out"], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(r["o"][0], stored["o"], rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------- second RMSNorm + SwiGLU FFN --
+# [LNA §一] puts "第二个 RMS Norm、FFN" after the residual of the attention block
+# of the LLaMA architecture; the FFN is read as LLaMA's gated form
+# out = h + (silu(n Wg^T) * (n Wu^T)) Wd, with Wg, Wu, Wd [I, H].
+def test_silu_closed_forms():
+    # silu(z) = z * sigmoid(z): silu(0) = 0, silu(z) - silu(-z) = z exactly in
+    # real arithmetic (sigmoid(z) + sigmoid(-z) = 1), silu(1) = 1/(1 + 1/e),
+    # silu(z) -> z for large z, slope 1/2 at 0.
+    assert oracle.silu(0.0) == 0.0
+    for z in (0.3, -1.7, 4.0, 11.0):
+        assert abs(oracle.silu(z) - oracle.silu(-z) - z) < 1e-14 * max(1.0, abs(z))
+    assert abs(oracle.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12
+    assert abs(oracle.silu(1e-6) / 1e-6 - 0.5) < 1e-6
+
+
+def _ffn_inputs(H, I, seed=0):
+    r = np.random.default_rng(seed)
+    return (r.normal(size=H), 1.0 + 0.1 * r.normal(size=H), 0.2 * r.normal(size=(I, H)),
+            0.2 * r.normal(size=(I, H)), 0.2 * r.normal(size=(I, H)))
+
+
+def test_ffn_hand_example_gate_and_up_roles():
+    # h = 1, g2 = 1, eps = 0 gives n = 1.  Unit i's gate row sums to 1 and its
+    # up row to 2, so a_i = silu(1) * 2 = 1.4621171572600098; swapping the two
+    # matrices gives silu(2) * 1 = 1.7615941559557649 instead (the activation
+    # belongs to the gate).  Wd = [[0,1,2,3],[4,5,6,7]] then sums the units.
+    H = 4
+    wg = np.array([[1.0, 0, 0, 0], [0, 0.5, 0.5, 0]])
+    wu = np.array([[2.0, 0, 0, 0], [0, 0, 1.0, 1.0]])
+    wd = np.arange(8.0).reshape(2, 4)
+    r = oracle.ffn_row(np.ones(H), np.ones(H), wg, wu, wd, 0.0)
+    a = 1.4621171572600098
+    np.testing.assert_allclose(r["a"], [a, a], rtol=1e-15)
+    np.testing.assert_allclose(r["out"], 1.0 + a * np.array([4.0, 6.0, 8.0, 10.0]), rtol=1e-15)
+    r2 = oracle.ffn_row(np.ones(H), np.ones(H), wu, wg, wd, 0.0)
+    np.testing.assert_allclose(r2["a"], [1.7615941559557649] * 2, rtol=1e-15)
+
+
+def test_ffn_zero_matrices_give_the_residual_exactly():
+    h, g2, wg, wu, wd = _ffn_inputs(16, 24)
+    for k in range(3):
+        mats = [wg, wu, wd]
+        mats[k] = np.zeros_like(mats[k])
+        r = oracle.ffn_row(h, g2, *mats, 1e-6)
+        assert np.array_equal(r["out"], h), k
+
+
+def test_ffn_second_norm_is_the_block_rmsnorm():
+    # The FFN input is RMSNorm(h; g2) with eps inside the sqrt: compare with the
+    # constant-vector closed form through a one-unit FFN whose gate and up rows
+    # pick coordinate 3 (n_3 = g2_3 * c / sqrt(c^2 + eps)).
+    H, c, eps = 8, 2.5, 0.5
+    g2 = np.linspace(0.5, 1.5, H)
+    e3 = np.zeros((1, H))
+    e3[0, 3] = 1.0
+    r = oracle.ffn_row(np.full(H, c), g2, e3, e3, np.ones((1, H)), eps)
+    n3 = g2[3] * c / math.sqrt(c * c + eps)
+    assert abs(r["a"][0] - (n3 / (1.0 + math.exp(-n3))) * n3) < 1e-14
+
+
+def test_ffn_invariant_under_permuting_the_intermediate_units():
+    # Reordering the units (the same rows of Wg, Wu and Wd) cannot change the
+    # output; a mixed-up row index between the three matrices would.
+    h, g2, wg, wu, wd = _ffn_inputs(12, 20, seed=3)
+    perm = np.random.default_rng(5).permutation(20)
+    r0 = oracle.ffn_row(h, g2, wg, wu, wd, 1e-6)
+    r1 = oracle.ffn_row(h, g2, wg[perm], wu[perm], wd[perm], 1e-6)
+    np.testing.assert_allclose(r1["out"], r0["out"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r1["a"], r0["a"][perm], rtol=1e-12, atol=1e-15)
+
+
+def test_ffn_is_linear_in_down_and_up_and_separable_over_units():
+    # out - h is linear in Wd and in Wu, and a sum over the units: splitting the
+    # I units into two halves adds the two halves' contributions.
+    h, g2, wg, wu, wd = _ffn_inputs(10, 16, seed=7)
+    base = oracle.ffn_row(h, g2, wg, wu, wd, 1e-6)["out"] - h
+    np.testing.assert_allclose(oracle.ffn_row(h, g2, wg, wu, 3.0 * wd, 1e-6)["out"] - h,
+                               3.0 * base, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(oracle.ffn_row(h, g2, wg, -2.0 * wu, wd, 1e-6)["out"] - h,
+                               -2.0 * base, rtol=1e-12, atol=1e-13)
+    lo = oracle.ffn_row(h, g2, wg[:7], wu[:7], wd[:7], 1e-6)["out"] - h
+    hi = oracle.ffn_row(h, g2, wg[7:], wu[7:], wd[7:], 1e-6)["out"] - h
+    np.testing.assert_allclose(lo + hi, base, rtol=1e-12, atol=1e-13)
+
+
+def test_ffn_single_unit_one_hot_weights_transpose_check():
+    # Unit 0 reads coordinate 1 of n through both gate and up and writes only
+    # output coordinate 4 with weight 2: a transposed Wd (read as [H, I]) or a
+    # gate row read as a column moves or drops the contribution.
+    H, I = 6, 3
+    h = np.linspace(-1.0, 1.5, H)
+    g2 = np.ones(H)
+    wg = np.zeros((I, H))
+    wu = np.zeros((I, H))
+    wd = np.zeros((I, H))
+    wg[0, 1] = 1.0
+    wu[0, 1] = 1.0
+    wd[0, 4] = 2.0
+    r = oracle.ffn_row(h, g2, wg, wu, wd, 0.0)
+    n1 = h[1] / math.sqrt(np.mean(h * h))
+    expect = h.copy()
+    expect[4] += 2.0 * (n1 / (1.0 + math.exp(-n1))) * n1
+    np.testing.assert_allclose(r["out"], expect, rtol=1e-14, atol=1e-15)
