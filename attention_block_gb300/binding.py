@@ -35,6 +35,12 @@ class CfConfig(ctypes.Structure):
             "kv_prefetch")]
 
 
+class CfFfnConfig(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("max_batch", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+                ("dtype", ctypes.c_int32), ("stage_bytes", ctypes.c_int32)]
+
+
 class CfLaunchInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cluster_size", "batch_tile", "group", "rows_per_wtile", "pos_per_ktile",
@@ -74,6 +80,11 @@ SIGNATURES = {
     "cf_bench_tma_stream": (ctypes.c_int, [ctypes.c_int] * 8 + [_vp, _vp, _vp]),
     "cf_bench_kv_stream": (ctypes.c_int, [ctypes.c_int] * 10 + [_vp] * 4),
     "cf_bench_box_stream": (ctypes.c_int, [_vp] + [ctypes.c_int] * 10 + [_vp, _vp]),
+    "cf_ffn_create": (ctypes.c_int, [ctypes.POINTER(CfFfnConfig), ctypes.POINTER(_vp)]),
+    "cf_ffn_forward": (ctypes.c_int, [_vp, ctypes.c_int32] + [_vp] * 7),
+    "cf_ffn_get_status": (ctypes.c_int, [_vp]),
+    "cf_ffn_launch_info": (ctypes.c_int, [_vp] + [ctypes.POINTER(ctypes.c_int32)] * 3),
+    "cf_ffn_destroy": (None, [_vp]),
     "cf_bench_contig_stream": (ctypes.c_int, [_vp, ctypes.c_longlong, ctypes.c_longlong] + [ctypes.c_int] * 5 + [_vp, _vp]),
     "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
                                      + [_vp] * 9),
@@ -281,6 +292,66 @@ class DecodeAttnBlock:
     def close(self) -> None:
         if getattr(self, "handle", None):
             cf_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------- FFN --
+def cf_ffn_create(cfg: CfFfnConfig) -> int:
+    h = _vp()
+    rc = lib().cf_ffn_create(ctypes.byref(cfg), ctypes.byref(h))
+    if rc != CF_OK:
+        raise CfError(rc, "cf_ffn_create")
+    return h.value
+
+
+def cf_ffn_forward(handle, batch, hidden, ln_weight, w_gate, w_up, w_down, out,
+                   stream=None) -> int:
+    return lib().cf_ffn_forward(handle, int(batch), _ptr(hidden), _ptr(ln_weight), _ptr(w_gate),
+                                _ptr(w_up), _ptr(w_down), _ptr(out), _stream(stream))
+
+
+class FfnBlock:
+    """Owns one cf_ffn_handle; calling it enqueues the second RMSNorm, the
+    gated FFN and the residual for ``batch`` rows.  Raises CfError on any
+    non-zero return code."""
+
+    def __init__(self, hidden, intermediate, max_batch, rms_eps=1e-6, dtype=CF_F16,
+                 stage_bytes=0):
+        if isinstance(dtype, str):
+            dtype = {"f32": CF_F32, "f16": CF_F16, "bf16": CF_BF16}[dtype]
+        self.cfg = CfFfnConfig(int(hidden), int(intermediate), int(max_batch), float(rms_eps),
+                               int(dtype), int(stage_bytes))
+        self.handle = cf_ffn_create(self.cfg)
+
+    def __call__(self, batch, hidden, ln_weight, w_gate, w_up, w_down, out, stream=None):
+        rc = cf_ffn_forward(self.handle, batch, hidden, ln_weight, w_gate, w_up, w_down, out,
+                            stream)
+        if rc != CF_OK:
+            raise CfError(rc, "cf_ffn_forward")
+        return out
+
+    def launch_info(self) -> dict:
+        b, r, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        rc = lib().cf_ffn_launch_info(self.handle, ctypes.byref(b), ctypes.byref(r),
+                                      ctypes.byref(s))
+        if rc != CF_OK:
+            raise CfError(rc, "cf_ffn_launch_info")
+        return {"blocks": b.value, "rows_per_stage": r.value, "stages": s.value}
+
+    def status(self) -> int:
+        import torch
+        torch.cuda.synchronize()
+        return lib().cf_ffn_get_status(self.handle)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            lib().cf_ffn_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -1,0 +1,488 @@
+// cf_ffn.cu -- second RMSNorm + gated FFN + residual for decode batches, as
+// one kernel on sm_103a, and its C ABI (include/cf_ffn.h).
+//
+// Page cited by title and section:
+//   [LNA] "大模型推理中的算子融合优化：LayerNorm + Attention 的 CUDA Kernel
+//         手写与验证" (asdsk.com), §一 (the LLaMA block ends with a second
+//         RMS Norm and the FFN) and §三 stage 1 (RMSNorm with warp-shuffle
+//         reductions).
+//
+// The whole step is weight streaming: 3·I·H weights per call against a few
+// KB of activations.  The mapping is chosen so that every byte crosses HBM
+// once and in long contiguous runs:
+//   * one block per SM; block k owns intermediate units [k·I/G, (k+1)·I/G)
+//     (balanced to one unit), whose gate, up and down rows are contiguous
+//     in the [I, H] weight layout, so each shared-memory stage is ONE bulk
+//     copy of R whole rows (cp.async.bulk, mbarrier completion);
+//   * a producer warp streams first the gate and up rows of all the block's
+//     units (R units per stage, gate and up alternating), then their down
+//     rows; it needs nothing from the previous kernel, so with programmatic
+//     dependent launch the stream starts while that kernel drains (the
+//     consumers wait for it before reading `hidden`);
+//   * the normalized rows n live in the consumers' registers in fp32 (each
+//     thread owns 4-element chunks q = tid + 256 j of the hidden dimension);
+//     for a gate or up stage every warp reduces its threads' dot-product
+//     partials by shuffles and stores one sum per (unit, row) in its own
+//     shared-memory slot, so no block barrier stalls the stream; after the
+//     last up stage one barrier, a = silu(gate) * up for all the block's
+//     units, and another barrier; the down rows are then accumulated into
+//     per-thread partial outputs over the owned chunks (measured: a barrier
+//     per group of R units left the stream waiting on the 3-stage ring and
+//     cost ~40 % of the step);
+//   * the blocks' partial outputs meet in an fp32 accumulator through float4
+//     atomics; the last block (ticket) adds the residual, writes `out` and
+//     clears the accumulator for the next call.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "cf.h"
+#include "cf_common.cuh"
+#include "cf_ffn.h"
+#include "cf_params.h"
+#include "cf_ptx.cuh"
+
+namespace cf {
+namespace {
+
+constexpr int kFfnMaxH = 4096;                          // hidden size the registers hold
+constexpr int kFfnKC = kFfnMaxH / (4 * kConsumers);     // 4-element chunks per thread
+constexpr int kFfnMaxR = 16;                            // weight rows per stage
+constexpr int kFfnMaxUnits = 128;                       // intermediate units per block
+constexpr int kFfnMaxStages = 8;
+
+struct FfnParams {
+  const void* h;
+  const void* g2;
+  const void* wg;
+  const void* wu;
+  const void* wd;
+  void* out;
+  float* acc;    // [max_batch, H], zero between calls
+  int* counter;  // zero between calls
+  int* errflag;
+  int B, H, I, R, stages, stage_bytes;
+  float eps;
+};
+
+// Shared memory after the ring: mbarriers, then float scratch.
+__host__ __device__ constexpr int ffn_scratch_floats(int bmax) {
+  return kConsumerWarps * 2 * kFfnMaxUnits * bmax  // per-warp gate / up sums
+         + kFfnMaxUnits * bmax                     // activations
+         + kConsumerWarps * bmax + 4;              // sums of squares, flag
+}
+
+template <typename T, int BMAX>
+__global__ void __launch_bounds__(kThreads, 1) cf_ffn_kernel(const __grid_constant__ FfnParams p) {
+  constexpr int UB = kFfnMaxUnits * BMAX;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                           ~uintptr_t(127));
+  uint8_t* ring = sm;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)p.stages * p.stage_bytes);
+  uint64_t* empty = full + kFfnMaxStages;
+  float* wsum = reinterpret_cast<float*>(empty + kFfnMaxStages);  // [8][2][units][BMAX]
+  float* av = wsum + kConsumerWarps * 2 * UB;                      // [units][BMAX]
+  float* ssq = av + UB;                                            // [8][BMAX]
+  int* flag = reinterpret_cast<int*>(ssq + kConsumerWarps * BMAX);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int i0 = (int)((long long)blockIdx.x * p.I / G);
+  const int i1 = (int)((long long)(blockIdx.x + 1) * p.I / G);
+  const int nchunk = (i1 - i0 + p.R - 1) / p.R;
+  const size_t row_bytes = (size_t)p.H * sizeof(T);
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init_cluster();
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == kConsumerWarps) {
+    // ============================================== weight stream ====
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const uint8_t* mats[3] = {static_cast<const uint8_t*>(p.wg),
+                                static_cast<const uint8_t*>(p.wu),
+                                static_cast<const uint8_t*>(p.wd)};
+      int it = 0;
+      // gate and up rows of every group, then the down rows
+      for (int pass = 0; pass < 2; ++pass)
+        for (int c = 0; c < nchunk; ++c) {
+          const int r0 = i0 + c * p.R;
+          const uint32_t bytes = (uint32_t)(min(p.R, i1 - r0) * row_bytes);
+          for (int m = pass * 2; m < (pass ? 3 : 2); ++m, ++it) {
+            const int s = it % p.stages;
+            if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_load_1d(ring + (size_t)s * p.stage_bytes, mats[m] + (size_t)r0 * row_bytes,
+                         bytes, &full[s], pol);
+          }
+        }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ================================================== consumer warps ====
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // `hidden` comes from the previous kernel
+  const T* __restrict__ hid = static_cast<const T*>(p.h);
+  const T* __restrict__ g2 = static_cast<const T*>(p.g2);
+  const int HC = p.H / 4;
+
+  // ---- Second RMSNorm [LNA §一, §三 stage 1]: this thread's chunks of every
+  // row, the sums of squares reduced by warp shuffles and across warps --------
+  float n[kFfnKC][BMAX][4];
+  float ss[BMAX];
+#pragma unroll
+  for (int b = 0; b < BMAX; ++b) ss[b] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kFfnKC; ++j) {
+    const int q = tid + j * kConsumers;
+#pragma unroll
+    for (int b = 0; b < BMAX; ++b) {
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (q < HC && b < p.B) load_cvt<T, 4>(hid + (size_t)b * p.H + 4 * q, x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        n[j][b][e] = x[e];
+        ss[b] = fmaf(x[e], x[e], ss[b]);
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < BMAX; ++b) {
+    const float v = warp_sum(ss[b]);
+    if (lane == 0) ssq[warp * BMAX + b] = v;
+  }
+  named_sync(kBarConsumers, kConsumers);
+#pragma unroll
+  for (int b = 0; b < BMAX; ++b) {
+    float t = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) t += ssq[w * BMAX + b];
+    ss[b] = b < p.B ? 1.0f / sqrtf(t / (float)p.H + p.eps) : 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < kFfnKC; ++j) {
+    const int q = tid + j * kConsumers;
+    float g[4] = {0.f, 0.f, 0.f, 0.f};
+    if (q < HC) load_cvt<T, 4>(g2 + 4 * q, g);
+#pragma unroll
+    for (int b = 0; b < BMAX; ++b)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) n[j][b][e] = n[j][b][e] * ss[b] * g[e];
+  }
+
+  // ---- Phase A: gate and up dot products of every unit; each warp keeps
+  // its own shuffle-reduced sums (no block barrier while the stream runs) --
+  const int nunits = i1 - i0;
+  int it = 0;
+  for (int c = 0; c < nchunk; ++c) {
+    const int rc = min(p.R, nunits - c * p.R);
+#pragma unroll
+    for (int m = 0; m < 2; ++m, ++it) {
+      const int s = it % p.stages;
+      mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+      const uint8_t* st = ring + (size_t)s * p.stage_bytes;
+      float part[kFfnMaxR][BMAX];
+#pragma unroll
+      for (int r = 0; r < kFfnMaxR; ++r) {
+#pragma unroll
+        for (int b = 0; b < BMAX; ++b) part[r][b] = 0.f;
+        if (r < rc) {
+          const T* row = reinterpret_cast<const T*>(st + (size_t)r * row_bytes);
+#pragma unroll
+          for (int j = 0; j < kFfnKC; ++j) {
+            const int q = tid + j * kConsumers;
+            if (q < HC) {
+              float w[4];
+              load_cvt<T, 4>(row + 4 * q, w);
+#pragma unroll
+              for (int b = 0; b < BMAX; ++b)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) part[r][b] = fmaf(w[e], n[j][b][e], part[r][b]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      float* dst = wsum + (warp * 2 + m) * UB + c * p.R * BMAX;
+#pragma unroll
+      for (int r = 0; r < kFfnMaxR; ++r) {
+        if (r < rc) {
+#pragma unroll
+          for (int b = 0; b < BMAX; ++b) {
+            const float v = warp_sum(part[r][b]);
+            if (lane == 0) dst[r * BMAX + b] = v;
+          }
+        }
+      }
+    }
+  }
+  named_sync(kBarConsumers, kConsumers);
+  for (int idx = tid; idx < nunits * BMAX; idx += kConsumers) {
+    float gs = 0.f, us = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      gs += wsum[(w * 2) * UB + idx];
+      us += wsum[(w * 2 + 1) * UB + idx];
+    }
+    av[idx] = gs / (1.0f + expf(-gs)) * us;  // silu(gate) * up
+  }
+  named_sync(kBarConsumers, kConsumers);
+
+  // ---- Phase B: down rows, o += a_u * Wd[u, owned chunks] -----------------
+  float o[kFfnKC][BMAX][4];
+#pragma unroll
+  for (int j = 0; j < kFfnKC; ++j)
+#pragma unroll
+    for (int b = 0; b < BMAX; ++b)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[j][b][e] = 0.f;
+  for (int c = 0; c < nchunk; ++c, ++it) {
+    const int rc = min(p.R, nunits - c * p.R);
+    const int s = it % p.stages;
+    mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+    const uint8_t* st = ring + (size_t)s * p.stage_bytes;
+    for (int r = 0; r < rc; ++r) {
+      const T* row = reinterpret_cast<const T*>(st + (size_t)r * row_bytes);
+      float a[BMAX];
+#pragma unroll
+      for (int b = 0; b < BMAX; ++b) a[b] = av[(c * p.R + r) * BMAX + b];
+#pragma unroll
+      for (int j = 0; j < kFfnKC; ++j) {
+        const int q = tid + j * kConsumers;
+        if (q < HC) {
+          float w[4];
+          load_cvt<T, 4>(row + 4 * q, w);
+#pragma unroll
+          for (int b = 0; b < BMAX; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[j][b][e] = fmaf(a[b], w[e], o[j][b][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ---- Merge the blocks' partial outputs, then residual by the last block --
+#pragma unroll
+  for (int j = 0; j < kFfnKC; ++j) {
+    const int q = tid + j * kConsumers;
+    if (q < HC) {
+#pragma unroll
+      for (int b = 0; b < BMAX; ++b)
+        if (b < p.B)
+          atomicAdd(reinterpret_cast<float4*>(p.acc + (size_t)b * p.H + 4 * q),
+                    make_float4(o[j][b][0], o[j][b][1], o[j][b][2], o[j][b][3]));
+    }
+  }
+  __threadfence();
+  named_sync(kBarConsumers, kConsumers);
+  if (tid == 0) {
+    const int last = (atomicAdd(p.counter, 1) == G - 1);
+    if (last) __threadfence();
+    flag[0] = last;
+  }
+  named_sync(kBarConsumers, kConsumers);
+  if (flag[0]) {
+    T* out = static_cast<T*>(p.out);
+    for (int idx = tid; idx < p.B * HC; idx += kConsumers) {
+      const int b = idx / HC, q = idx % HC;
+      const size_t off = (size_t)b * p.H + 4 * q;
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
+      float x[4];
+      load_cvt<T, 4>(hid + off, x);
+      const float r4[4] = {x[0] + v.x, x[1] + v.y, x[2] + v.z, x[3] + v.w};
+      store4<T>(out + off, r4);
+      __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+    if (tid == 0) *p.counter = 0;
+  }
+}
+
+using FfnFn = void (*)(FfnParams);
+
+FfnFn ffn_entry(int dtype, int bmax) {
+  if (dtype == CF_F32) return bmax == 1 ? cf_ffn_kernel<float, 1> : cf_ffn_kernel<float, 2>;
+  if (dtype == CF_F16) return bmax == 1 ? cf_ffn_kernel<__half, 1> : cf_ffn_kernel<__half, 2>;
+  return bmax == 1 ? cf_ffn_kernel<__nv_bfloat16, 1> : cf_ffn_kernel<__nv_bfloat16, 2>;
+}
+
+int dtype_bytes(int dtype) { return dtype == CF_F32 ? 4 : 2; }
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+}  // namespace cf
+
+using namespace cf;
+
+struct cf_ffn_handle {
+  cf_ffn_config cfg;
+  FfnFn fn = nullptr;
+  int blocks = 0, R = 0, stages = 0, stage_bytes = 0, smem = 0, bmax = 1;
+  void* ws = nullptr;  // acc | counter | errflag
+  float* acc = nullptr;
+  int* counter = nullptr;
+  int* errflag = nullptr;
+};
+
+extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
+  if (out == nullptr) return CF_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg == nullptr) return CF_ERR_INVALID_ARG;
+  const cf_ffn_config c = *cfg;
+  if (c.hidden <= 0 || c.hidden % 8 != 0 || c.intermediate <= 0 || c.max_batch <= 0 ||
+      c.dtype < CF_F32 || c.dtype > CF_BF16 || !(c.rms_eps >= 0.f) || c.stage_bytes < 0)
+    return CF_ERR_INVALID_ARG;
+  if (c.hidden > kFfnMaxH || c.max_batch > 2) return CF_ERR_UNSUPPORTED;
+  const int row_bytes = c.hidden * dtype_bytes(c.dtype);
+  if (c.stage_bytes != 0 && c.stage_bytes < row_bytes) return CF_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+    return CF_ERR_CUDA;
+  cf_ffn_handle* h = new (std::nothrow) cf_ffn_handle();
+  if (h == nullptr) return CF_ERR_CUDA;
+  h->cfg = c;
+  h->bmax = c.max_batch <= 1 ? 1 : 2;
+  h->fn = ffn_entry(c.dtype, h->bmax);
+  const int extras = 2 * kFfnMaxStages * 8 + ffn_scratch_floats(h->bmax) * 4 + 128;
+  const int budget = (int)prop.sharedMemPerBlockOptin;
+  // Default: the largest stage of whole rows that still leaves two stages
+  // (measured on the Llama-2-7B FFN: 2 x 96 KB streams at 0.74 of the copy
+  // bandwidth, 3 x 64 KB at 0.68, 6 x 32 KB at 0.52 -- the cost per stage
+  // outweighs the depth of the ring).
+  const int req = c.stage_bytes ? c.stage_bytes : (budget - extras) / 2 / 128 * 128;
+  h->R = std::min(kFfnMaxR, req / row_bytes);
+  if (h->R < 1) {
+    delete h;
+    return CF_ERR_UNSUPPORTED;
+  }
+  h->stage_bytes = (h->R * row_bytes + 127) / 128 * 128;
+  h->stages = std::min(kFfnMaxStages, (budget - extras) / h->stage_bytes);
+  if (h->stages < 2) {
+    delete h;
+    return CF_ERR_UNSUPPORTED;
+  }
+  h->smem = h->stages * h->stage_bytes + extras;
+  h->blocks = std::min(prop.multiProcessorCount, c.intermediate);
+  if ((c.intermediate + h->blocks - 1) / h->blocks > kFfnMaxUnits) {
+    delete h;
+    return CF_ERR_UNSUPPORTED;
+  }
+  if (cudaFuncSetAttribute(h->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return CF_ERR_CUDA;
+  }
+  const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
+  if (cudaMalloc(&h->ws, acc_bytes + 256) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return CF_ERR_CUDA;
+  }
+  if (cudaMemset(h->ws, 0, acc_bytes + 256) != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return CF_ERR_CUDA;
+  }
+  h->acc = static_cast<float*>(h->ws);
+  h->counter = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes);
+  h->errflag = h->counter + 32;
+  *out = h;
+  return CF_OK;
+}
+
+extern "C" int cf_ffn_forward(cf_ffn_handle* h, int32_t batch, const void* hidden,
+                              const void* ln_weight, const void* w_gate, const void* w_up,
+                              const void* w_down, void* out, void* stream) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  const cf_ffn_config& c = h->cfg;
+  if (batch < 0 || batch > c.max_batch) return CF_ERR_INVALID_ARG;
+  if (batch == 0) return CF_OK;
+  const void* ptrs[] = {hidden, ln_weight, w_gate, w_up, w_down, out};
+  for (const void* q : ptrs)
+    if (q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) != 0) return CF_ERR_INVALID_ARG;
+  const size_t es = dtype_bytes(c.dtype);
+  const size_t act = (size_t)batch * c.hidden * es, mat = (size_t)c.intermediate * c.hidden * es;
+  if (ranges_overlap(out, act, hidden, act) ||
+      ranges_overlap(out, act, ln_weight, (size_t)c.hidden * es) ||
+      ranges_overlap(out, act, w_gate, mat) || ranges_overlap(out, act, w_up, mat) ||
+      ranges_overlap(out, act, w_down, mat))
+    return CF_ERR_ALIAS;
+  FfnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.h = hidden;
+  p.g2 = ln_weight;
+  p.wg = w_gate;
+  p.wu = w_up;
+  p.wd = w_down;
+  p.out = out;
+  p.acc = h->acc;
+  p.counter = h->counter;
+  p.errflag = h->errflag;
+  p.B = batch;
+  p.H = c.hidden;
+  p.I = c.intermediate;
+  p.R = h->R;
+  p.stages = h->stages;
+  p.stage_bytes = h->stage_bytes;
+  p.eps = c.rms_eps;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = dim3(h->blocks, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = h->smem;
+  lc.stream = static_cast<cudaStream_t>(stream);
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  void* args[] = {&p};
+  if (cudaLaunchKernelExC(&lc, reinterpret_cast<const void*>(h->fn), args) != cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
+  return CF_OK;
+}
+
+extern "C" int cf_ffn_get_status(cf_ffn_handle* h) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  int flag = 0;
+  if (cudaMemcpy(&flag, h->errflag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CF_ERR_CUDA;
+  if (flag != 0 && cudaMemset(h->errflag, 0, sizeof(int)) != cudaSuccess) return CF_ERR_CUDA;
+  return (flag & kDevErrTimeout) ? CF_ERR_DEVICE_TIMEOUT : CF_OK;
+}
+
+extern "C" int cf_ffn_launch_info(const cf_ffn_handle* h, int32_t* blocks, int32_t* rows_per_stage,
+                                  int32_t* stages) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  if (blocks) *blocks = h->blocks;
+  if (rows_per_stage) *rows_per_stage = h->R;
+  if (stages) *stages = h->stages;
+  return CF_OK;
+}
+
+extern "C" void cf_ffn_destroy(cf_ffn_handle* h) {
+  if (h == nullptr) return;
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+}

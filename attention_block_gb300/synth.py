@@ -8,6 +8,12 @@ W_qkv, W_o, k_cache, v_cache, positions.
 Value laws (the same for every workload): hidden ~ N(0,1), ln_weight ~
 1 + N(0, 0.1), W_qkv and W_o ~ N(0, 0.02), KV cache ~ N(0,1) everywhere
 (including the slot the new token will overwrite, so an append is visible).
+
+The FFN that follows the attention block (second RMSNorm, gated FFN,
+residual) draws, in this order, hidden ~ N(0,1) (unless the attention
+block's output is passed in), its norm weight ~ 1 + N(0, 0.1) and W_gate,
+W_up, W_down ~ N(0, 0.02), each [I, H]: the same laws as the attention
+block's, since no workload states others.
 """
 from __future__ import annotations
 
@@ -114,6 +120,60 @@ def make_layer(w: Workload, seed: int = 0, device="cpu") -> dict:
     out["k_cache"] = randn(B, S, nkv, d)
     out["v_cache"] = randn(B, S, nkv, d)
     out["positions"] = _positions(w, gen, device)
+    return out
+
+
+@dataclasses.dataclass(frozen=True)
+class FfnWorkload:
+    name: str
+    hidden: int
+    intermediate: int
+    batch: int
+    dtype: str
+    rms_eps: float
+
+
+# FFN shapes of the two model families the attention workloads stand in for
+# (Llama-2-7B: I = 11008; Llama-3-8B: I = 14336), plus a small fp32 case.
+FFN_WORKLOADS = {w.name: w for w in [
+    FfnWorkload("llama2_7b_ffn_i11008_b1_f16", 4096, 11008, 1, "f16", 1e-6),
+    FfnWorkload("llama3_8b_ffn_i14336_b2_bf16", 4096, 14336, 2, "bf16", 1e-6),
+    FfnWorkload("tiny_ffn_h256_i688_b1_f32", 256, 688, 1, "f32", 1e-6),
+]}
+LLAMA2_FFN = "llama2_7b_ffn_i11008_b1_f16"
+LLAMA3_FFN = "llama3_8b_ffn_i14336_b2_bf16"
+TINY_FFN = "tiny_ffn_h256_i688_b1_f32"
+
+
+def custom_ffn(name: str = "custom_ffn", **kw) -> FfnWorkload:
+    base = dict(hidden=256, intermediate=688, batch=1, dtype="f32", rms_eps=1e-6)
+    base.update(kw)
+    return FfnWorkload(name=name, **base)
+
+
+def make_ffn(w: FfnWorkload, seed: int = 0, device="cpu", hidden=None) -> dict:
+    """Draw one FFN's tensors (storage dtype) on ``device``; ``hidden`` [B, H]
+    (e.g. the attention block's output) replaces the drawn input rows."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    dt = DTYPES[w.dtype]
+    B, H, I = w.batch, w.hidden, w.intermediate
+
+    def randn(*shape, std=1.0, mean=0.0):
+        t = torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        if mean != 0.0:
+            t.add_(mean)
+        return t.to(dt)
+
+    out = {"hidden": randn(B, H)}
+    if hidden is not None:
+        out["hidden"] = hidden.to(device=device, dtype=dt).contiguous()
+    out["ln_weight"] = randn(H, std=0.1, mean=1.0)
+    out["w_gate"] = randn(I, H, std=0.02)
+    out["w_up"] = randn(I, H, std=0.02)
+    out["w_down"] = randn(I, H, std=0.02)
     return out
 
 

@@ -55,6 +55,27 @@ def algorithmic_bytes(w, positions) -> int:
     return weights + kv_read + kv_write + io
 
 
+def ffn_bytes(wf) -> int:
+    """Bytes the FFN after the attention block must move: W_gate, W_up, W_down,
+    its norm weight, the rows read and written."""
+    es = 4 if wf.dtype == "f32" else 2
+    return 3 * wf.intermediate * wf.hidden * es + wf.hidden * es + 2 * wf.batch * wf.hidden * es
+
+
+def ffn_flops(wf) -> int:
+    return 6 * wf.batch * wf.intermediate * wf.hidden
+
+
+def tensor_bytes(d) -> int:
+    """Bytes of the tensors in a (possibly nested) dict of tensors."""
+    return sum(tensor_bytes(v) if isinstance(v, dict) else v.numel() * v.element_size()
+               for v in d.values())
+
+
+def to_cpu(d):
+    return {k: (to_cpu(v) if isinstance(v, dict) else v.cpu()) for k, v in d.items()}
+
+
 def flops_per_step(w, positions) -> int:
     d, nq, H, B = w.head_dim, w.n_q_heads, w.hidden, w.batch
     proj = 2 * B * H * w.qkv_cols + 2 * B * nq * d * H
@@ -256,14 +277,18 @@ def phase_timeline(blk, binding, w, reps, outs, stream, dev, info, R, launches=4
 
 
 # ---------------------------------------------------------------- oracle --
-def time_oracle(w, layer_cpu, budget_s: float, max_steps: int | None = None):
+def time_oracle(w, layer_cpu, budget_s: float, max_steps: int | None = None, wf=None):
     """Run the float64 oracle over batch rows of one step until budget_s is
-    spent (at least one row).  Returns (seconds per full step, rows done)."""
+    spent (at least one row); with an FFN workload ``wf`` each row also runs
+    the FFN on the attention block's output (layer_cpu["ffn"] holds its
+    tensors).  Returns (seconds per full step, rows done)."""
     import numpy as np
     import oracle
     from attention_block_gb300 import synth
 
     f = {k: synth.to_f64(layer_cpu[k]) for k in ("hidden", "ln_weight", "w_qkv", "w_o")}
+    ff = ({k: synth.to_f64(layer_cpu["ffn"][k]) for k in ("ln_weight", "w_gate", "w_up", "w_down")}
+          if wf is not None else None)
     pos = layer_cpu["positions"].numpy()
     cfg = w.oracle_cfg()
     rows_done, t_rows = 0, 0.0
@@ -273,8 +298,11 @@ def time_oracle(w, layer_cpu, budget_s: float, max_steps: int | None = None):
         kc = np.ascontiguousarray(synth.to_f64(layer_cpu["k_cache"][b]))
         vc = np.ascontiguousarray(synth.to_f64(layer_cpu["v_cache"][b]))
         s = time.perf_counter()
-        oracle.decode_row(cfg, f["hidden"][b], f["ln_weight"], f["w_qkv"], f["w_o"], kc, vc,
-                          int(pos[b]))
+        r = oracle.decode_row(cfg, f["hidden"][b], f["ln_weight"], f["w_qkv"], f["w_o"], kc, vc,
+                              int(pos[b]))
+        if ff is not None:
+            oracle.ffn_row(r["out"], ff["ln_weight"], ff["w_gate"], ff["w_up"], ff["w_down"],
+                           wf.rms_eps)
         t_rows += time.perf_counter() - s
         rows_done += 1
         b = (b + 1) % w.batch
@@ -300,6 +328,10 @@ def main(argv=None):
                     default=int(os.environ.get("CF_PREFETCH_AHEAD", 0)))
     ap.add_argument("--prefetch-late", type=int, default=int(os.environ.get("CF_PREFETCH_LATE", 0)))
     ap.add_argument("--max-stages", type=int, default=int(os.environ.get("CF_MAX_STAGES", 0)))
+    ap.add_argument("--ffn", type=int, default=0,
+                    help="intermediate size of the gated FFN that follows the attention block "
+                         "in every layer (a whole decoder layer per step); 0 = the attention "
+                         "block alone")
     ap.add_argument("--kv-prefetch", type=int, default=int(os.environ.get("CF_KV_PREFETCH", 0)),
                     help="batched kernel: K/V tiles per owned row prefetched into L2 during "
                          "the QKV projection (0 default, -1 none)")
@@ -352,8 +384,19 @@ def main(argv=None):
         n_rep = max(1, -(-4 * l2 // algorithmic_bytes(w, pos0)))
         reps = [[layer0]] + [[synth.make_layer(w, seed=r, device=dev)] for r in range(1, n_rep)]
     R = len(reps)
-    footprint = sum(sum(t.numel() * t.element_size() for t in L.values())
-                    for rep in reps for L in rep)
+    # The whole decoder layer: every layer's attention block is followed by
+    # the second RMSNorm + gated FFN + residual, with its own weights.
+    wf, ffn_blk = None, None
+    if args.ffn > 0:
+        wf = synth.custom_ffn(name=f"ffn_i{args.ffn}", hidden=w.hidden, intermediate=args.ffn,
+                              batch=w.batch, dtype=w.dtype, rms_eps=w.rms_eps)
+        ffn_blk = binding.FfnBlock(w.hidden, args.ffn, w.batch, w.rms_eps, w.dtype)
+        for ri, rep in enumerate(reps):
+            for li, L in enumerate(rep):
+                L["ffn"] = synth.make_ffn(wf, seed=1000 * (ri + 1) + li, device=dev)
+                L["h_mid"] = torch.empty_like(L["hidden"])
+        step_bytes += ffn_bytes(wf) * w.layers
+    footprint = sum(tensor_bytes(L) for rep in reps for L in rep)
     blk = binding.DecodeAttnBlock(
         hidden=w.hidden, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim,
         max_batch=w.batch, s_max=w.s_max, rope_theta=w.rope_theta, rms_eps=w.rms_eps,
@@ -369,11 +412,26 @@ def main(argv=None):
 
     stream = torch.cuda.Stream(device=dev)
 
+    def layer_step(x, L, pos, out, ev=None):
+        """One layer: the attention block (then the FFN) on `stream`; ev, if
+        given, holds events recorded before, between and after."""
+        if ev:
+            ev[0].record(stream)
+        mid = out if ffn_blk is None else L["h_mid"]
+        step_fn(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"], L["v_cache"],
+                pos, mid, stream)
+        if ev:
+            ev[1].record(stream)
+        if ffn_blk is not None:
+            F = L["ffn"]
+            ffn_blk(w.batch, mid, F["ln_weight"], F["w_gate"], F["w_up"], F["w_down"], out, stream)
+            if ev:
+                ev[2].record(stream)
+
     def run_step(r):
         x = reps[r][0]["hidden"]
         for l, L in enumerate(reps[r]):
-            step_fn(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"],
-                    L["v_cache"], L["positions"], outs[r][l], stream)
+            layer_step(x, L, L["positions"], outs[r][l])
             x = outs[r][l]
 
     with torch.cuda.stream(stream):
@@ -386,7 +444,7 @@ def main(argv=None):
 
     # ---- per-launch kernel durations (eager, CUDA events on the launch stream)
     n_lat = min(args.steps, 4 * R if w.layers == 1 else 4)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
            for _ in range(n_lat * w.layers)]
     with torch.cuda.stream(stream):
         k = 0
@@ -394,18 +452,16 @@ def main(argv=None):
             r = i % R
             x = reps[r][0]["hidden"]
             for l, L in enumerate(reps[r]):
-                evs[k][0].record(stream)
-                step_fn(w.batch, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"],
-                        L["v_cache"], L["positions"], outs[r][l], stream)
-                evs[k][1].record(stream)
+                layer_step(x, L, L["positions"], outs[r][l], evs[k])
                 x = outs[r][l]
                 k += 1
     stream.synchronize()
-    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    launch_ms = [e[0].elapsed_time(e[1]) for e in evs]
     launch_ms_avg = sum(launch_ms) / len(launch_ms)
+    ffn_ms = [e[1].elapsed_time(e[2]) for e in evs] if ffn_blk is not None else []
 
     timeline = None
-    if args.timeline:
+    if args.timeline and ffn_blk is None:
         timeline = phase_timeline(blk, binding, w, reps, outs, stream, dev, info, R)
 
     # ---- the timed region: graph-captured steps.  One graph holds all R
@@ -457,6 +513,32 @@ def main(argv=None):
     if st != binding.CF_OK:
         raise RuntimeError(f"device status after timed steps: {binding.strerror(st)}")
 
+    # ---- the FFN kernel on its own (its roofline line): graph replays of the
+    # FFN launches of every replica and layer, on the attention outputs
+    ffn_launch_s = None
+    if ffn_blk is not None:
+        if ffn_blk.status() != binding.CF_OK:
+            raise RuntimeError("FFN device status after timed steps")
+        g_ffn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ffn, stream=stream):
+            for r in range(R):
+                for l, L in enumerate(reps[r]):
+                    F = L["ffn"]
+                    ffn_blk(w.batch, L["h_mid"], F["ln_weight"], F["w_gate"], F["w_up"],
+                            F["w_down"], outs[r][l], stream)
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup // R)):
+                g_ffn.replay()
+        n_ffn = max(1, args.steps // R)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            f0.record(stream)
+            for _ in range(n_ffn):
+                g_ffn.replay()
+            f1.record(stream)
+        stream.synchronize()
+        ffn_launch_s = f0.elapsed_time(f1) / 1e3 / (n_ffn * R * w.layers)
+
     # ---- end to end through the public API with host buffers
     B, H = w.batch, w.hidden
     h_in = [torch.empty_like(reps[r][0]["hidden"], device="cpu").pin_memory() for r in range(R)]
@@ -476,8 +558,7 @@ def main(argv=None):
         p_dev[r].copy_(p_in[r], non_blocking=True)
         x = x_dev[r]
         for l, L in enumerate(reps[r]):
-            step_fn(B, x, L["ln_weight"], L["w_qkv"], L["w_o"], L["k_cache"], L["v_cache"],
-                    p_dev[r], outs[r][l], stream)
+            layer_step(x, L, p_dev[r], outs[r][l])
             x = outs[r][l]
         h_out.copy_(outs[r][-1], non_blocking=True)
 
@@ -512,16 +593,42 @@ def main(argv=None):
         # kernel per layer, launched back to back on one stream, timed with
         # CUDA events on that stream.
         launch_s_timed = elapsed_s / (args.steps * w.layers)
+        kernel_name = ("unfused path: uf_proj_kernel, uf_attn_kernel, uf_proj_kernel"
+                       if args.unfused else
+                       KERNEL_NAMES.get(info.get("mode", 0), "cf_decode_kernel"))
+        traffic = recorded_traffic(w.name)
+        layer_kernels = None
+        if wf is not None:
+            # Two kernels per layer: the attention block's share of the layer
+            # time is the layer time less the FFN's (timed alone above); the
+            # roofline line is the kernel that takes longer.
+            attn_s = max(launch_s_timed - ffn_launch_s, 1e-9)
+            layer_kernels = {
+                kernel_name: {"us": round(attn_s * 1e6, 3), "bytes": per_launch_bytes,
+                              "GBs": round(per_launch_bytes / attn_s / 1e9, 1)},
+                "cf_ffn_kernel": {"us": round(ffn_launch_s * 1e6, 3), "bytes": ffn_bytes(wf),
+                                  "GBs": round(ffn_bytes(wf) / ffn_launch_s / 1e9, 1),
+                                  "timing": "FFN-only graph replays / launches"},
+            }
+            if ffn_launch_s >= attn_s:
+                kernel_name, per_launch_bytes, traffic = "cf_ffn_kernel", ffn_bytes(wf), None
+                launch_s_timed = ffn_launch_s
+                launch_ms = ffn_ms
+                launch_ms_avg = sum(ffn_ms) / len(ffn_ms)
+            else:
+                launch_s_timed = attn_s
         achieved = per_launch_bytes / launch_s_timed / 1e9
         us_step = elapsed_s / args.steps * 1e6
         cpu = None
         if world == 1:
-            lay_cpu = {k: v.cpu() for k, v in reps[0][0].items()}
-            t_cpu, rows = time_oracle(w, lay_cpu, args.cpu_budget)
+            lay_cpu = to_cpu(reps[0][0])
+            t_cpu, rows = time_oracle(w, lay_cpu, args.cpu_budget, wf=wf)
             cpu = {"value": step_bytes / t_cpu / 1e9, "unit": "GB/s", "cores": 1,
                    "kind": "oracle", "us_per_step": t_cpu * 1e6,
                    "sample": (f"{rows} batch row(s) of layer 0 of this workload through the "
-                              f"float64 single-threaded C oracle; per-step time = per-row time "
+                              f"float64 single-threaded C oracle"
+                              f"{' (attention block, then the FFN)' if wf else ''}; "
+                              f"per-step time = per-row time "
                               f"x {w.batch} rows x {w.layers} layer(s)"),
                    "host_cpus": os.cpu_count()}
         line = {
@@ -539,30 +646,35 @@ def main(argv=None):
             "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": w.name, "hidden": w.hidden, "q_heads": w.n_q_heads,
+                "workload": w.name + (f"+ffn_i{args.ffn}" if wf else ""),
+                "hidden": w.hidden, "q_heads": w.n_q_heads,
                 "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "batch": w.batch,
                 "positions": w.positions, "layers_per_step": w.layers,
                 "storage_dtype": w.dtype, "accumulate": "f32",
                 "algorithmic_bytes_per_step": step_bytes,
-                "flops_per_step": flops_per_step(w, pos0) * w.layers,
+                "flops_per_step": (flops_per_step(w, pos0) + (ffn_flops(wf) if wf else 0))
+                * w.layers,
+                **({"ffn_intermediate": args.ffn, "ffn_launch": ffn_blk.launch_info()}
+                   if wf else {}),
                 "l2_defeat": (f"inputs larger than L2: {R} independently seeded replica(s) "
                               f"rotated, {footprint / 1e9:.2f} GB resident vs L2 "
                               f"{l2 / 1e6:.0f} MB"),
                 "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
                 "launch": info,
-                "path": "unfused (3 kernels, HBM intermediates)" if args.unfused else "fused",
+                "path": ("unfused (3 kernels, HBM intermediates)" if args.unfused else "fused")
+                + (" attention block, then the FFN kernel" if wf else ""),
             },
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "traffic": recorded_traffic(w.name),
-                "kernel": ("unfused path: uf_proj_kernel, uf_attn_kernel, uf_proj_kernel"
-                           if args.unfused else
-                           KERNEL_NAMES.get(info.get("mode", 0), "cf_decode_kernel")),
+                "traffic": traffic,
+                "kernel": kernel_name,
                 "launch_us_avg": round(launch_s_timed * 1e6, 3),
-                "launch_timing": "timed region (graph replays) / launches",
+                "launch_timing": ("timed region (graph replays) / launches" if wf is None else
+                                  "dominant kernel of the layer, see layer_kernels"),
+                **({"layer_kernels": layer_kernels} if layer_kernels else {}),
                 "isolated_launch_us_avg": round(launch_ms_avg * 1e3, 3),
                 "isolated_launch_us_min": round(min(launch_ms) * 1e3, 3),
                 "bytes_per_launch": per_launch_bytes,
@@ -572,7 +684,7 @@ def main(argv=None):
                     "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
-            "gpu_launches": args.steps * w.layers * kernels_per_layer,
+            "gpu_launches": args.steps * w.layers * (kernels_per_layer + (1 if wf else 0)),
             **({"timeline_us": timeline} if timeline else {}),
             "clocks": clk.result(),
             "cpu_baseline": cpu,
@@ -595,12 +707,18 @@ def run_reference(args, w, rank, world):
     layer = synth.make_layer(w, seed=0, device="cpu")
     pos = layer["positions"].tolist()
     step_bytes = algorithmic_bytes(w, pos) * w.layers
+    wf = None
+    if args.ffn > 0:
+        wf = synth.custom_ffn(name=f"ffn_i{args.ffn}", hidden=w.hidden, intermediate=args.ffn,
+                              batch=w.batch, dtype=w.dtype, rms_eps=w.rms_eps)
+        layer["ffn"] = synth.make_ffn(wf, seed=1000, device="cpu")
+        step_bytes += ffn_bytes(wf) * w.layers
     budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        time_oracle(w, layer, 0.0, max_steps=1)
+        time_oracle(w, layer, 0.0, max_steps=1, wf=wf)
     times, rows_total = [], 0
     for _ in range(args.steps):
-        t_step, rows = time_oracle(w, layer, budget)
+        t_step, rows = time_oracle(w, layer, budget, wf=wf)
         times.append(t_step)
         rows_total += rows
     t = sum(times) / len(times)
@@ -613,10 +731,12 @@ def run_reference(args, w, rank, world):
         "us_per_step": round(t * 1e6, 1), "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "hidden": w.hidden, "q_heads": w.n_q_heads,
+        "config": {"workload": w.name + (f"+ffn_i{args.ffn}" if wf else ""),
+                   "hidden": w.hidden, "q_heads": w.n_q_heads,
                    "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "batch": w.batch,
                    "positions": w.positions, "layers_per_step": w.layers,
-                   "storage_dtype": w.dtype, "algorithmic_bytes_per_step": step_bytes},
+                   "storage_dtype": w.dtype, "algorithmic_bytes_per_step": step_bytes,
+                   **({"ffn_intermediate": args.ffn} if wf else {})},
         "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample, "host_cpus": os.cpu_count()},
         "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
