@@ -22,13 +22,14 @@
 //   * the normalized rows n live in the consumers' registers in fp32 (each
 //     thread owns 4-element chunks q = tid + 256 j of the hidden dimension);
 //     for a gate or up stage every warp reduces its threads' dot-product
-//     partials by shuffles and stores one sum per (unit, row) in its own
-//     shared-memory slot, so no block barrier stalls the stream; after the
-//     last up stage one barrier, a = silu(gate) * up for all the block's
-//     units, and another barrier; the down rows are then accumulated into
-//     per-thread partial outputs over the owned chunks (measured: a barrier
-//     per group of R units left the stream waiting on the 3-stage ring and
-//     cost ~40 % of the step);
+//     partials with one transposed shuffle reduction (all R·B sums at once)
+//     and stores one sum per (unit, row) in its own shared-memory slot, so
+//     no block barrier stalls the stream; after the last up stage one
+//     barrier, a = silu(gate) * up for all the block's units, and another
+//     barrier; the down rows are then accumulated into per-thread partial
+//     outputs over the owned chunks.  Measured on the Llama-2-7B shape: a
+//     block barrier per group of R units cost 23 % of the step, one
+//     5-shuffle butterfly per (row, batch row) another 23 %;
 //   * the blocks' partial outputs meet in an fp32 accumulator through float4
 //     atomics; the last block (ticket) adds the residual, writes `out` and
 //     clears the accumulator for the next call.
@@ -75,6 +76,33 @@ __host__ __device__ constexpr int ffn_scratch_floats(int bmax) {
   return kConsumerWarps * 2 * kFfnMaxUnits * bmax  // per-warp gate / up sums
          + kFfnMaxUnits * bmax                     // activations
          + kConsumerWarps * bmax + 4;              // sums of squares, flag
+}
+
+// Sum of V values (V a power of two <= 32) over the 32 lanes of a warp as a
+// transposed reduction: each round every lane keeps half of its values and
+// adds the partner's copies of them, so after five rounds lane l holds the
+// full sum of value l / (32 / V) -- V - 1 + (5 - log2 V) shuffles with a
+// dependency depth of five, against 5 V for one butterfly per value.
+template <int V>
+__device__ __forceinline__ float warp_transposed_sum(float (&pv)[V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two <= 32");
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int o = 16 >> step;
+    const int c = V >> step;  // values held before this round
+    if (c >= 2) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < c / 2; ++i) {
+        const float send = upper ? pv[i] : pv[i + c / 2];
+        const float keep = upper ? pv[i + c / 2] : pv[i];
+        pv[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    } else {
+      pv[0] += __shfl_xor_sync(0xffffffffu, pv[0], o);
+    }
+  }
+  return pv[0];
 }
 
 template <typename T, int BMAX>
@@ -194,11 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1) cf_ffn_kernel(const __grid_consta
       const int s = it % p.stages;
       mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
       const uint8_t* st = ring + (size_t)s * p.stage_bytes;
-      float part[kFfnMaxR][BMAX];
+      constexpr int V = kFfnMaxR * BMAX;  // (row, batch row) partials per thread
+      float part[V];
 #pragma unroll
       for (int r = 0; r < kFfnMaxR; ++r) {
 #pragma unroll
-        for (int b = 0; b < BMAX; ++b) part[r][b] = 0.f;
+        for (int b = 0; b < BMAX; ++b) part[r * BMAX + b] = 0.f;
         if (r < rc) {
           const T* row = reinterpret_cast<const T*>(st + (size_t)r * row_bytes);
 #pragma unroll
@@ -210,24 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1) cf_ffn_kernel(const __grid_consta
 #pragma unroll
               for (int b = 0; b < BMAX; ++b)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) part[r][b] = fmaf(w[e], n[j][b][e], part[r][b]);
+                for (int e = 0; e < 4; ++e)
+                  part[r * BMAX + b] = fmaf(w[e], n[j][b][e], part[r * BMAX + b]);
             }
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      float* dst = wsum + (warp * 2 + m) * UB + c * p.R * BMAX;
-#pragma unroll
-      for (int r = 0; r < kFfnMaxR; ++r) {
-        if (r < rc) {
-#pragma unroll
-          for (int b = 0; b < BMAX; ++b) {
-            const float v = warp_sum(part[r][b]);
-            if (lane == 0) dst[r * BMAX + b] = v;
-          }
-        }
-      }
+      // lanes (v * 32/V .. ) end up with value v's warp sum; one of them stores it
+      const float v = warp_transposed_sum<V>(part, lane);
+      const int vi = lane / (32 / V);
+      if (lane % (32 / V) == 0 && vi < rc * BMAX)
+        wsum[(warp * 2 + m) * UB + c * p.R * BMAX + vi] = v;
     }
   }
   named_sync(kBarConsumers, kConsumers);
@@ -364,10 +388,11 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
   h->fn = ffn_entry(c.dtype, h->bmax);
   const int extras = 2 * kFfnMaxStages * 8 + ffn_scratch_floats(h->bmax) * 4 + 128;
   const int budget = (int)prop.sharedMemPerBlockOptin;
-  // Default: the largest stage of whole rows that still leaves two stages
-  // (measured on the Llama-2-7B FFN: 2 x 96 KB streams at 0.74 of the copy
-  // bandwidth, 3 x 64 KB at 0.68, 6 x 32 KB at 0.52 -- the cost per stage
-  // outweighs the depth of the ring).
+  // Default: the largest stage of whole rows that still leaves two stages.
+  // Measured (fraction of the copy bandwidth, Llama-2-7B FFN / Llama-3-8B FFN
+  // at B = 2): 2 x 104 KB 0.96 / 0.92, 3 x 64 KB 0.98 / 0.88, 4 x 48 KB
+  // 0.90 / 0.78, 6 x 32 KB 0.73 / 0.63 -- the cost per stage outweighs the
+  // depth of the ring.
   const int req = c.stage_bytes ? c.stage_bytes : (budget - extras) / 2 / 128 * 128;
   h->R = std::min(kFfnMaxR, req / row_bytes);
   if (h->R < 1) {
