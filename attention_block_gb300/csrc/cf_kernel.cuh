@@ -122,8 +122,29 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
   }
   __syncthreads();
   cluster_sync_all();  // peers' barriers are initialized before any DSMEM traffic
-  // Everything above touched only shared memory; from here on global memory
-  // may hold a preceding kernel's results (e.g. the previous layer's out).
+  // Prologue fill: the weights are read-only, so the first ring-full of
+  // W_qkv tiles is requested before waiting for the preceding kernel (with
+  // programmatic dependent launch this overlaps its tail).  These stages are
+  // fresh, so no empty-barrier wait is needed; the producer loop below
+  // continues after them.
+  const int nkt_all = (p.H / N) / p.Rw;
+  const int fill = min(p.stages, nkt_all);
+  const uint32_t seg_bytes = (uint32_t)(p.Rw * D * sizeof(T));
+  if (warp == kConsumerWarps && lane == 0) {
+    const uint64_t pol = policy_evict_first();
+    for (int kt = 0; kt < fill; ++kt) {
+      uint64_t* bar = &full[kt];
+      uint8_t* dst = ring + (size_t)kt * p.stage_bytes;
+      mbar_arrive_expect_tx(bar, NSEG * seg_bytes);
+      const int y = k0 + kt * p.Rw;
+      for (int j = 0; j < G; ++j)
+        tma_load_2d(dst + j * seg_bytes, &p.tm_wqkv, (g * G + j) * D, y, bar, pol);
+      tma_load_2d(dst + G * seg_bytes, &p.tm_wqkv, (p.nq + g) * D, y, bar, pol);
+      tma_load_2d(dst + (G + 1) * seg_bytes, &p.tm_wqkv, (p.nq + p.nkv + g) * D, y, bar, pol);
+    }
+  }
+  // From here on global memory may hold a preceding kernel's results (the
+  // previous layer's out, the K/V slot the previous step appended).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid < BT) {
     const int b = b0 + tid;
@@ -189,10 +210,15 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
         tma_prefetch_2d(&p.tm_wqkv, (p.nq + g) * D, y, pol);
         tma_prefetch_2d(&p.tm_wqkv, (p.nq + p.nkv + g) * D, y, pol);
       };
-      // Phase 1: W_qkv row tiles of this block's K band, G+2 head slices each.
-      const uint32_t seg_bytes = (uint32_t)(p.Rw * D * sizeof(T));
-      const int fill = min(p.stages, nkt);
+      // Phase 1: W_qkv row tiles of this block's K band, G+2 head slices each
+      // (the first `fill` were requested before the dependency wait).
       for (int kt = 0; kt < nkt; ++kt, ++it) {
+        if (kt < fill) {
+          if (kt == fill - 1 && p.prefetch_ahead > 0)
+            for (int k2 = fill; k2 < min(nkt, fill + p.prefetch_ahead); ++k2) prefetch_w(k2);
+          if (kt == fill - 1 && p.prefetch_late == 2) prefetch_late();
+          continue;
+        }
         uint64_t* bar;
         uint8_t* dst = slot(NSEG * seg_bytes, bar);
         const int y = k0 + kt * p.Rw;
