@@ -32,7 +32,7 @@ class CfConfig(ctypes.Structure):
         (n, ctypes.c_int32) for n in (
             "dtype", "cluster_size", "batch_tile", "stage_bytes", "ctas_per_sm",
             "prefetch_ahead", "prefetch_late", "pdl", "max_stages", "rows_per_block",
-            "kv_prefetch")]
+            "kv_prefetch", "adaptive")]
 
 
 class CfFfnConfig(ctypes.Structure):
@@ -67,6 +67,7 @@ SIGNATURES = {
     "cf_get_status": (ctypes.c_int, [_vp]),
     "cf_set_debug": (ctypes.c_int, [_vp, _vp]),
     "cf_get_launch_info": (ctypes.c_int, [_vp, ctypes.POINTER(CfLaunchInfo)]),
+    "cf_get_launch_info_batch": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.POINTER(CfLaunchInfo)]),
     "cf_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "cf_destroy": (None, [_vp]),
     "cf_test_cluster_allreduce": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -149,14 +150,14 @@ def strerror(code: int) -> str:
 def make_config(hidden, n_q_heads, n_kv_heads, head_dim, max_batch, s_max, rope_theta=1e4,
                 rms_eps=1e-6, dtype=CF_F16, cluster_size=0, batch_tile=0, stage_bytes=0,
                 ctas_per_sm=0, prefetch_ahead=0, prefetch_late=0, pdl=0,
-                max_stages=0, rows_per_block=0, kv_prefetch=0) -> CfConfig:
+                max_stages=0, rows_per_block=0, kv_prefetch=0, adaptive=0) -> CfConfig:
     if isinstance(dtype, str):
         dtype = {"f32": CF_F32, "f16": CF_F16, "bf16": CF_BF16}[dtype]
     return CfConfig(int(hidden), int(n_q_heads), int(n_kv_heads), int(head_dim),
                     int(max_batch), int(s_max), float(rope_theta), float(rms_eps), int(dtype),
                     int(cluster_size), int(batch_tile), int(stage_bytes), int(ctas_per_sm),
                     int(prefetch_ahead), int(prefetch_late), int(pdl), int(max_stages),
-                    int(rows_per_block), int(kv_prefetch))
+                    int(rows_per_block), int(kv_prefetch), int(adaptive))
 
 
 def cf_create(cfg: CfConfig) -> int:
@@ -206,9 +207,13 @@ def cf_set_debug(handle, dbg) -> int:
     return lib().cf_set_debug(handle, _ptr(dbg))
 
 
-def cf_get_launch_info(handle) -> dict:
+def cf_get_launch_info(handle, batch=None) -> dict:
+    """What the handle launches for max_batch rows, or for `batch` rows."""
     info = CfLaunchInfo()
-    rc = lib().cf_get_launch_info(handle, ctypes.byref(info))
+    if batch is None:
+        rc = lib().cf_get_launch_info(handle, ctypes.byref(info))
+    else:
+        rc = lib().cf_get_launch_info_batch(handle, int(batch), ctypes.byref(info))
     if rc != CF_OK:
         raise CfError(rc, "cf_get_launch_info")
     return {n: getattr(info, n) for n, _ in CfLaunchInfo._fields_}
@@ -276,8 +281,8 @@ class DecodeAttnBlock:
             raise CfError(rc, "cf_decode_attn_block_unfused")
         return out
 
-    def launch_info(self) -> dict:
-        return cf_get_launch_info(self.handle)
+    def launch_info(self, batch=None) -> dict:
+        return cf_get_launch_info(self.handle, batch)
 
     def set_debug(self, dbg) -> None:
         rc = cf_set_debug(self.handle, dbg)

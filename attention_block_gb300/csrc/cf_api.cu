@@ -262,12 +262,31 @@ bool make_plan(const cf_config& c, int N, int BT, int stage_req, int ctas_per_sm
 
 }  // namespace
 
-struct cf_handle {
-  cf_config cfg;
-  int device = 0, sm_count = 0;
+// One launch shape of a handle, used for batches of at most `cap` rows.
+struct PlanSlot {
+  int cap = 0;
   Plan plan;
   const void* fn = nullptr;
   int max_active_clusters = 0;
+  MapCache m_wqkv, m_wo, m_k, m_v, m_x;  // tensor maps have the plan's box shapes
+};
+constexpr int kMaxPlanSlots = 8;
+
+struct cf_handle {
+  cf_config cfg;
+  int device = 0, sm_count = 0;
+  // Launch shapes in ascending batch capacity; the last serves max_batch.
+  // A call uses the first slot whose capacity holds its batch (runtime choice
+  // of the kernel instance and cluster shape per batch).
+  PlanSlot slots[kMaxPlanSlots];
+  int nslots = 0;
+  PlanSlot& main() { return slots[nslots - 1]; }
+  const PlanSlot& main() const { return slots[nslots - 1]; }
+  const PlanSlot& slot_for(int batch) const {
+    for (int i = 0; i < nslots; ++i)
+      if (batch <= slots[i].cap) return slots[i];
+    return main();
+  }
   void* ws = nullptr;       // one allocation: acc | counters | errflag
   float* acc = nullptr;
   int* counters = nullptr;
@@ -277,7 +296,6 @@ struct cf_handle {
   int prefetch_ahead = 0, prefetch_late = 0, kv_prefetch = 0;
   bool pdl = true;
   float turn_hi[64], turn_lo[64];  // RoPE turn rates as float pairs (see KParams)
-  MapCache m_wqkv, m_wo, m_k, m_v, m_x;
   // three-kernel (unfused) path: HBM intermediates and counters
   void* uf_ws = nullptr;
   float *uf_y = nullptr, *uf_part = nullptr, *uf_o32 = nullptr;
@@ -307,6 +325,7 @@ int validate_config(const cf_config* c) {
   if (c->prefetch_ahead < -1 || c->prefetch_ahead > 64) return CF_ERR_INVALID_ARG;
   if (c->prefetch_late < -1 || c->prefetch_late > 3) return CF_ERR_INVALID_ARG;
   if (c->kv_prefetch < -1 || c->kv_prefetch > 64) return CF_ERR_INVALID_ARG;
+  if (c->adaptive < -1 || c->adaptive > 1) return CF_ERR_INVALID_ARG;
   if (c->pdl < -1 || c->pdl > 1) return CF_ERR_INVALID_ARG;
   if (c->max_stages < 0 || c->max_stages == 1 || c->max_stages > kMaxStages)
     return CF_ERR_INVALID_ARG;
@@ -490,9 +509,12 @@ int plan_handle(const cf_config& c, cf_handle& h) {
   h.cfg = c;
   h.device = dev;
   h.sm_count = prop.multiProcessorCount;
-  h.plan = pl;
-  h.fn = ke->fn;
-  h.max_active_clusters = nclusters;
+  h.nslots = 1;
+  h.slots[0] = PlanSlot();
+  h.slots[0].cap = c.max_batch;
+  h.slots[0].plan = pl;
+  h.slots[0].fn = ke->fn;
+  h.slots[0].max_active_clusters = nclusters;
   // Both L2 prefetches measured slower on the B = 1 Llama2 layer (they compete
   // with the W_qkv stream), so they are off unless asked for.
   h.prefetch_ahead = std::max(0, c.prefetch_ahead);
@@ -541,8 +563,46 @@ int cf_create(const cf_config* cfg, cf_handle** out) {
     delete h;
     return rc;
   }
+  // Runtime choice per batch: unless the launch shape was fixed by the
+  // caller, also plan for batch caps 1, 2, 4 and 8 below max_batch and keep
+  // each plan that differs from the next larger one.  Measured (one GB300):
+  // a handle for the 64-row, head_dim-64 MHA layer runs 1-, 2-, 4- and 8-row
+  // calls 2.2-2.8x faster on the sequence-split plans of those caps than on
+  // its 64-row tile; for GQA (several query heads per KV head) the batched
+  // 4-row-tile plan of the Llama-3 layer beat the sequence-split plans at
+  // 2-8 rows by 1.4-3.1x and tied at one row, so GQA handles keep one plan.
+  const bool fixed_shape = c.cluster_size || c.batch_tile || c.stage_bytes || c.ctas_per_sm ||
+                           c.rows_per_block || c.max_stages || c.adaptive == -1;
+  if (!fixed_shape && c.n_q_heads == c.n_kv_heads) {
+    PlanSlot top = h->slots[0];
+    PlanSlot found[kMaxPlanSlots];
+    int nfound = 0;
+    for (int cap = 1; cap < c.max_batch && cap <= 8 && nfound < kMaxPlanSlots - 1; cap *= 2) {
+      cf_config cc = c;
+      cc.max_batch = cap;
+      cf_handle tmp;
+      if (plan_handle(cc, tmp) != CF_OK) continue;
+      found[nfound++] = tmp.slots[0];
+    }
+    // keep a slot only if it differs from the next kept larger one
+    PlanSlot kept[kMaxPlanSlots];
+    int nk = 0;
+    kept[nk++] = top;
+    for (int i = nfound - 1; i >= 0; --i) {
+      const PlanSlot& up = kept[nk - 1];
+      const bool same = found[i].fn == up.fn && found[i].plan.N == up.plan.N &&
+                        found[i].plan.BT == up.plan.BT && found[i].plan.RPC == up.plan.RPC &&
+                        found[i].plan.L.total == up.plan.L.total;
+      if (!same) kept[nk++] = found[i];  // else the larger slot serves these batches
+    }
+    h->nslots = nk;
+    for (int i = 0; i < nk; ++i) h->slots[i] = kept[nk - 1 - i];
+  }
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
-  const size_t cnt_bytes = counter_slots(h->plan, c.max_batch) * sizeof(int);
+  size_t cnt_slots = 0;
+  for (int i = 0; i < h->nslots; ++i)
+    cnt_slots = std::max(cnt_slots, counter_slots(h->slots[i].plan, h->slots[i].cap));
+  const size_t cnt_bytes = cnt_slots * sizeof(int);
   const size_t total = acc_bytes + cnt_bytes + 256;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     delete h;
@@ -624,7 +684,8 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
       overlaps(out, out_bytes, positions, (size_t)batch * 4))
     return CF_ERR_ALIAS;
 
-  const Plan& pl = h->plan;
+  PlanSlot& ps = const_cast<PlanSlot&>(h->slot_for(batch));
+  const Plan& pl = ps.plan;
   KParams kp;
   std::memset(&kp, 0, sizeof(kp));
   // Tensor maps (encoded on the host, cached per pointer and extent).
@@ -650,20 +711,20 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
     const uint64_t dims[2] = {(uint64_t)C, (uint64_t)H};
     const uint64_t str[1] = {(uint64_t)C * es};
     const uint32_t box[2] = {(uint32_t)(rows ? 64 : D), (uint32_t)pl.Rw};
-    if (!get_map(h->m_wqkv, w_qkv, 0, 2, dims, str, box, rows, kp.tm_wqkv)) return CF_ERR_CUDA;
+    if (!get_map(ps.m_wqkv, w_qkv, 0, 2, dims, str, box, rows, kp.tm_wqkv)) return CF_ERR_CUDA;
   }
   {
     const uint64_t dims[2] = {(uint64_t)H, (uint64_t)nq * D};
     const uint64_t str[1] = {(uint64_t)H * es};
     const uint32_t box[2] = {(uint32_t)(rows ? 64 : pl.Co), (uint32_t)pl.Ro};
-    if (!get_map(h->m_wo, w_o, 0, 2, dims, str, box, rows, kp.tm_wo)) return CF_ERR_CUDA;
+    if (!get_map(ps.m_wo, w_o, 0, 2, dims, str, box, rows, kp.tm_wo)) return CF_ERR_CUDA;
   }
   for (int which = 0; which < 2; ++which) {
     const void* base = which == 0 ? k_cache : v_cache;
     const uint64_t dims[4] = {(uint64_t)D, (uint64_t)nkv, (uint64_t)S, (uint64_t)batch};
     const uint64_t str[3] = {(uint64_t)D * es, (uint64_t)nkv * D * es, (uint64_t)S * nkv * D * es};
     const uint32_t box[4] = {(uint32_t)(rows ? 64 : D), 1u, (uint32_t)pl.Rt, 1u};
-    if (!get_map(which == 0 ? h->m_k : h->m_v, base, batch, 4, dims, str, box, rows,
+    if (!get_map(which == 0 ? ps.m_k : ps.m_v, base, batch, 4, dims, str, box, rows,
                  which == 0 ? kp.tm_k : kp.tm_v))
       return CF_ERR_CUDA;
   }
@@ -671,7 +732,7 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
     const uint64_t dims[2] = {(uint64_t)H, (uint64_t)batch};
     const uint64_t str[1] = {(uint64_t)H * es};
     const uint32_t box[2] = {(uint32_t)pl.Rw, (uint32_t)pl.BT};
-    if (!get_map(h->m_x, hidden_states, batch, 2, dims, str, box, false, kp.tm_x))
+    if (!get_map(ps.m_x, hidden_states, batch, 2, dims, str, box, false, kp.tm_x))
       return CF_ERR_CUDA;
   }
 
@@ -728,7 +789,7 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
   lc.attrs = attr;
   lc.numAttrs = h->pdl ? 2 : 1;
   void* args[] = {&kp};
-  if (cudaLaunchKernelExC(&lc, h->fn, args) != cudaSuccess) {
+  if (cudaLaunchKernelExC(&lc, ps.fn, args) != cudaSuccess) {
     cudaGetLastError();
     return CF_ERR_CUDA;
   }
@@ -759,8 +820,15 @@ int cf_set_timeline(cf_handle* h, unsigned long long* stamps) {
 }
 
 int cf_get_launch_info(const cf_handle* h, cf_launch_info* info) {
-  if (h == nullptr || info == nullptr) return CF_ERR_INVALID_ARG;
-  const Plan& pl = h->plan;
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  return cf_get_launch_info_batch(h, h->cfg.max_batch, info);
+}
+
+int cf_get_launch_info_batch(const cf_handle* h, int32_t batch, cf_launch_info* info) {
+  if (h == nullptr || info == nullptr || batch < 1 || batch > h->cfg.max_batch)
+    return CF_ERR_INVALID_ARG;
+  const PlanSlot& ps = h->slot_for(batch);
+  const Plan& pl = ps.plan;
   info->cluster_size = pl.N;
   info->batch_tile = pl.BT;
   info->group = pl.G;
@@ -772,7 +840,7 @@ int cf_get_launch_info(const cf_handle* h, cf_launch_info* info) {
   info->stage_bytes = pl.stage_bytes;
   info->smem_bytes = pl.L.total;
   info->threads = kThreads;
-  info->max_active_clusters = h->max_active_clusters;
+  info->max_active_clusters = ps.max_active_clusters;
   info->sm_count = h->sm_count;
   info->mode = pl.mode;
   info->rows_per_block = pl.RPC;
@@ -884,7 +952,7 @@ std::mutex g_noalloc_mu;
 int noalloc_prepare(const cf_config& c, unsigned char* scratch, cf_handle& h) {
   const int rc = plan_handle(c, h);
   if (rc != CF_OK) return rc;
-  if (counter_slots(h.plan, c.max_batch) > kNoAllocCounters)
+  if (counter_slots(h.main().plan, c.max_batch) > kNoAllocCounters)
     return CF_ERR_INVALID_ARG;
   h.ws = nullptr;  // nothing to free: the workspace is the static scratch
   h.acc = reinterpret_cast<float*>(scratch);
@@ -892,7 +960,8 @@ int noalloc_prepare(const cf_config& c, unsigned char* scratch, cf_handle& h) {
   h.errflag = reinterpret_cast<int*>(scratch + kNoAllocAccFloats * 4 + kNoAllocCounters * 4);
   h.dbg = nullptr;
   h.timeline = nullptr;
-  for (MapCache* mc : {&h.m_wqkv, &h.m_wo, &h.m_k, &h.m_v, &h.m_x}) {
+  PlanSlot& ps = h.main();
+  for (MapCache* mc : {&ps.m_wqkv, &ps.m_wo, &ps.m_k, &ps.m_v, &ps.m_x}) {
     for (int i = 0; i < MapCache::kSlots; ++i) mc->ptr[i] = nullptr;
     mc->next = 0;
   }
@@ -939,7 +1008,7 @@ extern "C" int cf_decode_attn_block_noalloc(const cf_config* cfg, int32_t batch,
   // the regions this call uses are cleared first, on the same stream.
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t acc_bytes = (size_t)batch * cfg->hidden * sizeof(float);
-  const size_t cnt_bytes = counter_slots(s.h.plan, batch) * sizeof(int);
+  const size_t cnt_bytes = counter_slots(s.h.main().plan, batch) * sizeof(int);
   if (cudaMemsetAsync(s.h.acc, 0, acc_bytes, st) != cudaSuccess ||
       cudaMemsetAsync(s.h.counters, 0, cnt_bytes, st) != cudaSuccess ||
       cudaMemsetAsync(s.h.errflag, 0, sizeof(int), st) != cudaSuccess) {

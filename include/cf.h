@@ -86,6 +86,12 @@ typedef struct cf_config {
                              prefetched into L2 while the QKV projection
                              streams (spread over the sequence); 0 = default,
                              -1 = none, else at most that many (<= 64)       */
+  int32_t adaptive;       /* 0 or 1 = default: for MHA (nq == nkv), besides the
+                             max_batch plan, plan for batch caps 1, 2, 4 and 8
+                             and give each call the smallest one that holds
+                             its batch (kept only where the instance or shape
+                             differs; off whenever a launch-shape field above
+                             is set); -1 = one plan                           */
 } cf_config;
 
 typedef struct cf_handle cf_handle; /* opaque */
@@ -164,6 +170,11 @@ int cf_get_status(cf_handle* h);
 int cf_set_debug(cf_handle* h, float* dbg);
 
 int cf_get_launch_info(const cf_handle* h, cf_launch_info* info);
+
+/* What a call with `batch` rows (1 <= batch <= max_batch) launches: the plan
+ * of the smallest batch cap that holds it (see cf_config.adaptive).  Errors:
+ * CF_ERR_INVALID_ARG. */
+int cf_get_launch_info_batch(const cf_handle* h, int32_t batch, cf_launch_info* info);
 
 /* Static message for a CF_* code. */
 const char* cf_strerror(int code);

@@ -199,3 +199,28 @@ def test_batched_graph_replay_matches_eager():
         check(out_g.double().cpu().numpy(), out_e.double().cpu().numpy(), "graph vs eager",
               mean_rel=1e-4)
     assert binding.cf_get_status(blk.handle) == binding.CF_OK
+
+
+def test_runtime_choice_per_batch_matches_oracle_and_changes_kernel():
+    """A handle sized for 64 rows plans for batch caps 1, 2, 4, ... as well and
+    gives each call the smallest plan that holds its batch: a one-row call runs
+    the sequence-split kernel, a 64-row call the batched one; every call
+    matches the oracle on its rows.  adaptive = -1 keeps the single plan."""
+    w = synth.WORKLOADS[synth.SMALL_HEAD_B64]
+    t = synth.make_layer(w, 7, device="cuda")
+    blk = make_block(w)
+    assert blk.launch_info(1)["mode"] == 0
+    assert blk.launch_info(64)["mode"] == 1 and blk.launch_info(64)["batch_tile"] == 64
+    assert blk.launch_info() == blk.launch_info(64)
+    fixed = make_block(w, adaptive=-1)
+    assert fixed.launch_info(1) == fixed.launch_info(64)
+    for b in (1, 5, 16, 64):
+        out = torch.full_like(t["hidden"], float("nan"))
+        kc, vc = t["k_cache"].clone(), t["v_cache"].clone()
+        blk(b, t["hidden"], t["ln_weight"], t["w_qkv"], t["w_o"], kc, vc, t["positions"], out)
+        assert blk.status() == binding.CF_OK
+        rows = sorted({0, b // 2, b - 1})
+        ref = run_oracle(w, t, rows=rows)
+        check(out[rows].double().cpu().numpy(), round_to(ref["out"], w.dtype), f"batch {b}")
+        if b < w.batch:
+            assert torch.isnan(out[b:]).all()
