@@ -1,0 +1,112 @@
+// cf_tc05.cuh -- fifth-generation tensor-core (tcgen05) helpers for sm_103a:
+// tensor-memory (TMEM) allocation, the shared-memory matrix descriptor of a
+// K-major operand written with the 128-byte swizzle, the instruction
+// descriptor of kind::f16, the MMA itself, its commit to an mbarrier, and
+// TMEM loads.  Inline PTX only.
+//
+// Conventions used throughout:
+//   * one CTA (cta_group::1); the MMA is issued by a single thread;
+//   * A is M x K and B is N x K, both K-major in shared memory, in slabs of
+//     64 16-bit elements (128 bytes) per row, rows of a slab consecutive and
+//     8-row groups 1024 bytes apart; inside a row the 16-byte chunk j of row r
+//     sits at chunk j ^ (r & 7) (the 128-byte swizzle), slab bases 1024-byte
+//     aligned;
+//   * the fp32 accumulator D (M = 128) occupies TMEM lanes 0..127 (row m in
+//     lane m) and N consecutive columns from the allocation's base column.
+#pragma once
+
+#include <stdint.h>
+
+#include "cf_ptx.cuh"
+
+namespace cf {
+
+// Allocate `ncols` TMEM columns (a power of two, 32..512) for this CTA; the
+// whole warp executes it and the TMEM address lands in the shared word `dst`.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+// Free the allocation (the warp that allocated, after every use).
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Order tcgen05 operations across a thread barrier.
+__device__ __forceinline__ void tc05_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc05_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte
+// swizzle: start address (16-byte units, bits 0-13), leading byte offset
+// (bits 16-29; not used by this layout, 16 bytes), stride byte offset between
+// 8-row groups (bits 32-45), descriptor version 1 (bits 46-47), base offset 0,
+// layout 2 = 128-byte swizzle (bits 61-63).  A k offset inside the 128-byte
+// rows is added to the start address (32 bytes per 16-element k step).
+__device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
+// 4-5 = 1), A and B both fp16 (0) or both bf16 (1) (bits 7-9, 10-12), both
+// K-major (bits 15, 16 = 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_kind_f16(bool bf16, int M, int N) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[adesc] . B[bdesc]^T for one K step of 16 elements; issued by
+// one thread.  accumulate = false overwrites D.
+__device__ __forceinline__ void tc05_mma_f16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive (once) on `bar` when every MMA this thread issued so far completes.
+__device__ __forceinline__ void tc05_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 8 consecutive fp32 columns of the 32 TMEM lanes of this warp's quarter
+// (warp w % 4 reads lanes 32 (w % 4) .. +31; taddr carries the lane base in
+// bits 16-31 and the column in bits 0-15); waits for the load.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r0, r1, r2, r3, r4, r5, r6, r7;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  v[0] = __uint_as_float(r0);
+  v[1] = __uint_as_float(r1);
+  v[2] = __uint_as_float(r2);
+  v[3] = __uint_as_float(r3);
+  v[4] = __uint_as_float(r4);
+  v[5] = __uint_as_float(r5);
+  v[6] = __uint_as_float(r6);
+  v[7] = __uint_as_float(r7);
+}
+
+}  // namespace cf
