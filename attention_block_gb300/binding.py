@@ -75,7 +75,7 @@ SIGNATURES = {
     "cf_test_cluster_reduce_scatter": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _vp, _vp,
                                                       _vp, _vp]),
     "cf_test_cluster_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp]),
-    "cf_test_tc05_gemm": (ctypes.c_int, [ctypes.c_int] * 3 + [_vp] * 5),
+    "cf_test_tc05_gemm": (ctypes.c_int, [ctypes.c_int] * 4 + [_vp] * 5),
     "cf_bench_cluster_collective": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    _vp, _vp, _vp, _vp, _vp]),
     "cf_set_timeline": (ctypes.c_int, [_vp, _vp]),
@@ -247,9 +247,9 @@ def cf_test_cluster_gather(cluster_size, n, inp, out, errflag, stream=None) -> i
                                         _ptr(errflag), _stream(stream))
 
 
-def cf_test_tc05_gemm(dtype, n, k, a, b, d, errflag, stream=None) -> int:
-    return lib().cf_test_tc05_gemm(int(dtype), int(n), int(k), _ptr(a), _ptr(b), _ptr(d),
-                                   _ptr(errflag), _stream(stream))
+def cf_test_tc05_gemm(dtype, n, k, a, b, d, errflag, stream=None, a_mn=False) -> int:
+    return lib().cf_test_tc05_gemm(int(dtype), int(bool(a_mn)), int(n), int(k), _ptr(a), _ptr(b),
+                                   _ptr(d), _ptr(errflag), _stream(stream))
 
 
 def cf_bench_cluster_collective(kind, cluster_size, n, inp, out, errflag, cycles,

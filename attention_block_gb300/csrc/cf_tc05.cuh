@@ -6,10 +6,12 @@
 //
 // Conventions used throughout:
 //   * one CTA (cta_group::1); the MMA is issued by a single thread;
-//   * A is M x K and B is N x K, both K-major in shared memory, in slabs of
-//     64 16-bit elements (128 bytes) per row, rows of a slab consecutive and
-//     8-row groups 1024 bytes apart; inside a row the 16-byte chunk j of row r
-//     sits at chunk j ^ (r & 7) (the 128-byte swizzle), slab bases 1024-byte
+//   * A is M x K and B is N x K.  A K-major operand lies in slabs of 64
+//     16-bit elements (128 bytes) per row, rows of a slab consecutive and
+//     8-row groups 1024 bytes apart; an M-major A lies in 64-column boxes of
+//     K rows of 128 bytes (the layout a 2D TMA load with the 128-byte swizzle
+//     writes).  Inside a 128-byte row r the 16-byte chunk j sits at chunk
+//     j ^ (r & 7) (the 128-byte swizzle); slab and box bases are 1024-byte
 //     aligned;
 //   * the fp32 accumulator D (M = 128) occupies TMEM lanes 0..127 (row m in
 //     lane m) and N consecutive columns from the allocation's base column.
@@ -61,12 +63,31 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr, uint32_t s
   return d;
 }
 
+// Shared-memory matrix descriptor of an M- (or N-) major operand with the
+// 128-byte swizzle: rows of 64 consecutive M elements (128 bytes) along K,
+// one K row every 128 bytes, 8-row K groups `sbo_bytes` apart (1024 when the
+// rows are consecutive) and successive 64-element M blocks `lbo_bytes` apart
+// (the distance between two 64-column TMA boxes).  A K step of 16 rows
+// advances the start address by 16 * 128 bytes.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                       uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
-// 4-5 = 1), A and B both fp16 (0) or both bf16 (1) (bits 7-9, 10-12), both
-// K-major (bits 15, 16 = 0), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t idesc_kind_f16(bool bf16, int M, int N) {
+// 4-5 = 1), A and B both fp16 (0) or both bf16 (1) (bits 7-9, 10-12), A
+// M-major (bit 15 = 1) or K-major (0), B K-major (bit 16 = 0), N >> 3 (bits
+// 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_kind_f16(bool bf16, int M, int N,
+                                                      bool a_mn = false) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+         ((a_mn ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[adesc] . B[bdesc]^T for one K step of 16 elements; issued by

@@ -101,12 +101,14 @@ struct cf_handle;
 int cf_set_timeline(struct cf_handle* h, unsigned long long* stamps);
 
 /* One fifth-generation tensor-core product by one block:
- * d[128, n] = a[128, k] . b[n, k]^T with fp32 accumulation, a and b row-major
- * fp16 (dtype CF_F16) or bf16 (CF_BF16) device arrays (16-byte aligned), d a
- * row-major fp32 device array.  n a multiple of 16 in [16, 256], k a multiple
- * of 64 with the staged operands inside the block's shared memory.  Errors:
- * CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
-int cf_test_tc05_gemm(int dtype, int n, int k, const void* a, const void* b, float* d,
+ * d[128, n] = A . b[n, k]^T with fp32 accumulation, where A = a as a [128, k]
+ * row-major array (a_mn = 0, K-major operand) or A = a^T with a a [k, 128]
+ * row-major array (a_mn = 1, M-major operand staged as two 64-column boxes).
+ * a and b are fp16 (dtype CF_F16) or bf16 (CF_BF16) device arrays (16-byte
+ * aligned), d a row-major fp32 device array.  n a multiple of 16 in
+ * [16, 256], k a multiple of 64 with the staged operands inside the block's
+ * shared memory.  Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
+int cf_test_tc05_gemm(int dtype, int a_mn, int n, int k, const void* a, const void* b, float* d,
                       int* errflag, void* stream);
 
 #ifdef __cplusplus

@@ -25,11 +25,11 @@ def _need_cuda():
 DT = {"f16": (binding.CF_F16, torch.float16), "bf16": (binding.CF_BF16, torch.bfloat16)}
 
 
-def _run(dt, n, k, a, b):
+def _run(dt, n, k, a, b, a_mn=False):
     code, _ = DT[dt]
     d = torch.full((128, n), float("nan"), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    assert binding.cf_test_tc05_gemm(code, n, k, a, b, d, err) == binding.CF_OK
+    assert binding.cf_test_tc05_gemm(code, n, k, a, b, d, err, a_mn=a_mn) == binding.CF_OK
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     return d
@@ -44,6 +44,20 @@ def test_integer_product_is_exact(dt, n, k):
     b = torch.randint(-8, 9, (n, k), generator=g).to(tt)
     d = _run(dt, n, k, a.cuda(), b.cuda())
     ref = (a.double() @ b.double().T).float()
+    assert torch.equal(d.cpu(), ref)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("n,k", [(32, 64), (64, 128), (128, 64), (256, 192)])
+def test_m_major_a_integer_product_is_exact(dt, n, k):
+    """A read as the transpose of a [k, 128] weight tile held in two swizzled
+    64-column boxes (the transposed projections' operand)."""
+    _, tt = DT[dt]
+    g = torch.Generator().manual_seed(n * 13 + k)
+    w = torch.randint(-8, 9, (k, 128), generator=g).to(tt)
+    b = torch.randint(-8, 9, (n, k), generator=g).to(tt)
+    d = _run(dt, n, k, w.cuda(), b.cuda(), a_mn=True)
+    ref = (w.double().T @ b.double().T).float()
     assert torch.equal(d.cpu(), ref)
 
 
