@@ -123,6 +123,9 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   pl.G = G;
   pl.ctas_per_sm = 1;
   pl.Co = (Hc % 256 == 0) ? 256 : ((Hc % 128 == 0) ? 128 : 64);
+  // tiles of 16+ rows run the O projection on tcgen05 in 128-column tiles
+  const bool tc5 = BT >= 16;
+  if (tc5 && pl.Co < 128) return false;
   // W_qkv stage: Rw rows of CB 64-column boxes of the group's NC columns;
   // the first stage of each slice of Rw rows also holds the [BT x Rw] slice
   // of x
@@ -156,7 +159,14 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   // warp states (attention merge), the O-projection A operand of the BT
   // rows (after attention); rows BT..15 of a 16-row MMA tile read a zero chunk
   const int slots = G > 1 ? 4 : 8;  // warp-state slots of the attention merge
-  L.scratch = take(std::max(4 * BT * apitch, std::max(slots * G * (D + 4) * 4, BT * OP)));
+  int scratch = std::max(4 * BT * apitch, std::max(slots * G * (D + 4) * 4, BT * OP));
+  if (tc5) {
+    // tcgen05 operands in 128-byte-swizzled slabs (1024-byte aligned): two
+    // x buffers of ceil(Rw/64) slabs of 2*BT rows, later o in G*D/64 slabs
+    scratch = std::max(scratch, std::max(2 * ((pl.Rw + 63) / 64) * 256 * BT, (GD / 64) * 256 * BT));
+    off = round_up(off, 1024);
+  }
+  L.scratch = take(scratch);
   L.xn = take((D / 16) * 32 * 16);  // Q fragments of the attention
   L.qkv = take(RPC * GD * 4);       // own rows' o
   L.sm = take(G * (D + 4) * 4);     // attention record

@@ -12,10 +12,11 @@
 // the head group is read once per tile (tiles of one head run together and
 // share the weights through L2); its N = BT / RPC blocks
 //   * split the hidden (reduction) dimension of the QKV projection, a
-//     [BT x H] x [H x (G+2)d] contraction on the tensor cores (mma.sync
-//     m16n8k16, fp32 accumulation; the fp32 activations enter as a pair of
-//     16-bit values hi + lo, so the product keeps ~fp32 accuracy; in tiles of
-//     fewer than 16 rows the missing rows read a 16-byte zero chunk);
+//     [BT x H] x [H x (G+2)d] contraction on the tensor cores with fp32
+//     accumulation; the fp32 activations enter as a pair of 16-bit values
+//     hi + lo, so the product keeps ~fp32 accuracy.  Tiles of 16 or more rows
+//     use the fifth-generation tensor cores (tcgen05, accumulators in tensor
+//     memory), smaller tiles mma.sync m16n8k16;
 //   * combine the partial products with ClusterReduce in reduce-scatter form
 //     over BATCH ROWS [CF §3.1.1]: block c ends up owning rows
 //     [c*RPC, (c+1)*RPC) of the tile, fully summed, together with their
@@ -46,6 +47,7 @@
 #include "cf_mma.cuh"
 #include "cf_params.h"
 #include "cf_ptx.cuh"
+#include "cf_tc05.cuh"
 
 namespace cf {
 
@@ -79,6 +81,20 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   constexpr int SE = rows_slice_floats(RPC, NC);
   constexpr int OP = rows_aop_pitch(GD);
   constexpr int NRW = (BT + kConsumerWarps - 1) / kConsumerWarps;  // rows per warp (sumsq)
+  // Tiles of 16 or more rows run both projections transposed on tcgen05:
+  // M = 128 weight (or output) columns, read straight from the swizzled TMA
+  // boxes as an M-major operand; N = 2*BT, the tile's rows as hi halves then
+  // lo halves (a K-major operand the consumers stage); K = 16 per MMA.  One
+  // thread issues the MMAs and commits them to the ring's empty barriers; the
+  // fp32 accumulators live in tensor memory (lane = column, column = row
+  // half) and each consumer warp reads one lane quarter, adding hi and lo.
+  constexpr bool TC5 = BT >= 16;
+  constexpr int N5 = 2 * BT;                     // MMA N
+  constexpr int NT5 = (CB + 1) / 2;              // 128-column tiles per W_qkv stage
+  constexpr int TCOLS = tmem_cols_for(NCG * NT5 * N5 > 4 * N5 ? NCG * NT5 * N5 : 4 * N5);
+  static_assert(!TC5 || (CB >= 2 && NCG * NT5 * N5 <= 512 && 4 * N5 <= 512 && GD % 64 == 0 &&
+                         BT % 16 == 0),
+                "tensor-memory plan");
   static_assert(BT % RPC == 0 && MR % 16 == 0, "batch tile");
   static_assert(NC % (8 * kConsumerWarps) == 0, "projection columns per warp");
   static_assert(D % 64 == 0, "head_dim in 64-column swizzle boxes");
@@ -119,6 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   int* s_pos = reinterpret_cast<int*>(sm + p.L.misc + 16);   // [BT]
   int* s_flag = s_pos + BT;
   float* s_rinv = reinterpret_cast<float*>(s_flag + 4);       // [RPC]
+  // tcgen05 completions: [0], [1] x buffers free again, [2], [3] O-projection
+  // accumulator buffers ready
+  uint64_t* tc_bar = bars + BarIdx::sm;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_flag + 1);  // tensor-memory base
 
   // ---------------------------------------------------------------- setup --
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -131,9 +151,18 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       mbar_init(rs_bar, N - 1);
       mbar_init(ga_bar, N - 1);
     }
+    if constexpr (TC5)
+      for (int i = 0; i < 4; ++i) mbar_init(&tc_bar[i], 1);
     fence_mbar_init_cluster();
   }
   if (tid < 4) reinterpret_cast<uint32_t*>(sm + p.L.misc)[tid] = 0u;
+  if constexpr (TC5) {
+    if (warp == 0) {
+      tmem_alloc(s_tmem, TCOLS);
+      tmem_relinquish();
+    }
+    tc05_fence_before();
+  }
   if (warp == kConsumerWarps && lane == 0) {
     prefetch_tensormap(&p.tm_wqkv);
     prefetch_tensormap(&p.tm_x);
@@ -142,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     prefetch_tensormap(&p.tm_wo);
   }
   __syncthreads();
+  if constexpr (TC5) tc05_fence_after();
   cluster_sync_all();
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = tid; i < BT; i += kThreads) {
@@ -286,7 +316,115 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
 
     // ---- Phase 1: [BT x Hc] x [Hc x NC] on the tensor cores, with the
     // rows' sums of squares over the band [LNA §三 stage 1] -----------------
-    {
+    const uint32_t tmem = TC5 ? *s_tmem : 0u;
+    if constexpr (TC5) {
+      // x * g of each K slice as the B operand: ceil(Rw/64) K-major swizzled
+      // slabs of N5 rows (hi rows 0..BT-1, lo rows BT..2BT-1), double-buffered
+      const int xslab = N5 * 128;
+      const uint32_t xbuf = (uint32_t)(((p.Rw + 63) / 64) * xslab);
+      const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, true);
+      float ss[NRW];
+#pragma unroll
+      for (int i = 0; i < NRW; ++i) ss[i] = 0.f;
+      for (int kt = 0; kt < nkt; ++kt) {
+        uint8_t* xs = un + (size_t)(kt & 1) * xbuf;
+        for (int cg = 0; cg < NCG; ++cg, ++it) {
+          const int s = it % p.stages;
+          uint8_t* st = ring + (size_t)s * p.stage_bytes;
+          if (cg == 0) {
+            mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+            // the MMAs of slice kt - 2 read this buffer
+            if (kt >= 2) mbar_wait(&tc_bar[kt & 1], ((kt - 2) >> 1) & 1, p.errflag);
+            const T* xt = reinterpret_cast<const T*>(st + CB * wbox_bytes);  // [BT][Rw]
+#pragma unroll
+            for (int i = 0; i < NRW; ++i) {
+              const int row = warp + i * kConsumerWarps;
+              if (row < BT) {
+                for (int k = 2 * lane; k < p.Rw; k += 64) {
+                  float f[2];
+                  load_cvt<T, 2>(xt + row * p.Rw + k, f);
+                  ss[i] = fmaf(f[0], f[0], fmaf(f[1], f[1], ss[i]));
+                  float gw[2];
+                  load_cvt<T, 2>(lnw + k0 + kt * p.Rw + k, gw);
+                  uint32_t hi, lo;
+                  MK::split2(f[0] * gw[0], f[1] * gw[1], hi, lo);
+                  uint8_t* sl = xs + (k >> 6) * xslab;
+                  const int j = (k & 63) >> 3, e2 = (k & 7) * 2, rl = BT + row;
+                  *reinterpret_cast<uint32_t*>(sl + row * 128 + ((j ^ (row & 7)) << 4) + e2) = hi;
+                  *reinterpret_cast<uint32_t*>(sl + rl * 128 + ((j ^ (rl & 7)) << 4) + e2) = lo;
+                }
+              }
+            }
+            fence_proxy_async_smem();
+            named_sync(kBarConsumers, kConsumers);
+          }
+          if (tid == 0) {
+            if (cg != 0) mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+            tc05_fence_after();
+#pragma unroll
+            for (int t = 0; t < NT5; ++t) {
+              // 128 columns from box c0 / 64 (the last tile of a 3-box stage
+              // overlaps the previous one; its duplicate half is not stored)
+              const int c0 = (128 * t < CB * 64 - 128) ? 128 * t : CB * 64 - 128;
+              const uint32_t a0 = smem_u32(st + (c0 / 64) * wbox_bytes);
+              const uint32_t d = tmem + (uint32_t)((cg * NT5 + t) * N5);
+              for (int ks = 0; ks < p.Rw / 16; ++ks) {
+                const uint64_t ad = smem_desc_mn_sw128(a0 + (uint32_t)ks * 2048u, wbox_bytes, 1024);
+                const uint64_t bd =
+                    smem_desc_k_sw128(smem_u32(xs + (ks >> 2) * xslab) + (uint32_t)(ks & 3) * 32u,
+                                      1024);
+                tc05_mma_f16(d, ad, bd, idesc, kt > 0 || ks > 0);
+              }
+            }
+            // the other warps' shares of the stage release, then the MMAs'
+            mbar_arrive_cnt(&empty[s], kConsumerWarps - 1);
+            tc05_commit(&empty[s]);
+            if (cg == NCG - 1) tc05_commit(&tc_bar[kt & 1]);
+          }
+          __syncwarp();
+        }
+      }
+      // the last slice's commit covers every earlier MMA
+      mbar_wait(&tc_bar[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, p.errflag);
+      tc05_fence_after();
+      stamp(kTlProjLoop);
+      // Partial sums -> red, slice-major (row r to slice r / RPC).  Warp w
+      // reads lane quarter w % 4 (32 columns) for rows [h*BT/2, (h+1)*BT/2),
+      // h = w / 4: lanes store consecutive columns of one row.
+      const int qd = warp & 3, hrow = (warp >> 2) * (BT / 2);
+#pragma unroll
+      for (int cg = 0; cg < NCG; ++cg)
+#pragma unroll
+        for (int t = 0; t < NT5; ++t) {
+          const int c0 = (128 * t < CB * 64 - 128) ? 128 * t : CB * 64 - 128;
+          const int cin = c0 + 32 * qd + lane;
+          const bool keep = cin >= 128 * t;
+          const int n = cg * CB * 64 + cin;
+          const uint32_t d =
+              tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)((cg * NT5 + t) * N5 + hrow);
+#pragma unroll
+          for (int r8 = 0; r8 < BT / 2; r8 += 8) {
+            float vh[8], vl[8];
+            tmem_ld_32x32b_x8(d + (uint32_t)r8, vh);
+            tmem_ld_32x32b_x8(d + (uint32_t)(BT + r8), vl);
+            if (keep) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int row = hrow + r8 + i;
+                red[(row / RPC) * SE + (row % RPC) * NC + n] = vh[i] + vl[i];
+              }
+            }
+          }
+        }
+      tc05_fence_before();
+#pragma unroll
+      for (int i = 0; i < NRW; ++i) {
+        const int row = warp + i * kConsumerWarps;
+        const float v = warp_sum(ss[i]);
+        if (row < BT && lane == 0) red[(row / RPC) * SE + RPC * NC + row % RPC] = v;
+      }
+      named_sync(kBarConsumers, kConsumers);
+    } else {
       float acc[MT][NTW][4];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -507,16 +645,25 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         dob[((size_t)b * p.nq + g * G) * D + rem] = ofin[idx];
       }
     }
-    // Own rows of the O-projection A operand (o as hi + lo 16-bit values); the
-    // warp states that shared this memory are no longer needed.
+    // Own rows of the O-projection operand (o as hi + lo 16-bit values); the
+    // warp states that shared this memory are no longer needed.  For tcgen05
+    // it is K-major swizzled: GD/64 slabs of N5 rows (hi rows, then lo rows).
     for (int i2 = tid; i2 < RPC * GD / 2; i2 += kConsumers) {
       const int r = (2 * i2) / GD, k = (2 * i2) % GD;
       uint32_t hi, lo;
       MK::split2(ofin[r * GD + k], ofin[r * GD + k + 1], hi, lo);
-      uint8_t* row = aop + (r0 + r) * OP;
-      *reinterpret_cast<uint32_t*>(row + k * 2) = hi;
-      *reinterpret_cast<uint32_t*>(row + 2 * GD + k * 2) = lo;
+      if constexpr (TC5) {
+        uint8_t* sl = aop + (k >> 6) * (N5 * 128);
+        const int j = (k & 63) >> 3, e2 = (k & 7) * 2, rh = r0 + r, rl = BT + r0 + r;
+        *reinterpret_cast<uint32_t*>(sl + rh * 128 + ((j ^ (rh & 7)) << 4) + e2) = hi;
+        *reinterpret_cast<uint32_t*>(sl + rl * 128 + ((j ^ (rl & 7)) << 4) + e2) = lo;
+      } else {
+        uint8_t* row = aop + (r0 + r) * OP;
+        *reinterpret_cast<uint32_t*>(row + k * 2) = hi;
+        *reinterpret_cast<uint32_t*>(row + 2 * GD + k * 2) = lo;
+      }
     }
+    if constexpr (TC5) fence_proxy_async_smem();
     named_sync(kBarConsumers, kConsumers);
     stamp(kTlMax);
 
@@ -524,14 +671,90 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     // rows of the A operand ---------------------------------------------------
     if (N > 1) {
       if (tid == 0) cluster_signal_peers(ga_bar, rank, N);
-      cluster_pull_gather<kConsumers>(aop, RPC * OP, RPC * OP, ga_bar, rank, N, tid, p.errflag);
+      if constexpr (TC5) {
+        // block q's rows: RPC rows of 128 bytes in the hi and the lo half of
+        // every slab
+        for (int sl = 0; sl < GD / 64; ++sl)
+          for (int h = 0; h < 2; ++h)
+            cluster_pull_gather<kConsumers>(aop + sl * (N5 * 128) + h * (BT * 128), RPC * 128,
+                                            RPC * 128, ga_bar, rank, N, tid, p.errflag);
+        fence_proxy_async_smem();
+      } else {
+        cluster_pull_gather<kConsumers>(aop, RPC * OP, RPC * OP, ga_bar, rank, N, tid, p.errflag);
+      }
       named_sync(kBarConsumers, kConsumers);
     }
     stamp(kTlSum);
 
     // ---- Phase 3: [BT x GD] x [GD x Co] per column box on the tensor cores,
     // fp32 atomics into the accumulator [CF §3.2] ----------------------------
-    if constexpr (BT <= 4) {
+    if constexpr (TC5) {
+      // Transposed on tcgen05: per column band, Co/128 tiles of 128 output
+      // columns (M) x N5 (the rows' hi and lo halves), K = the band's GD rows
+      // of W_o in Ro-row stages.  Bands alternate between two accumulator
+      // buffers, so the MMAs of band cb run while the warps drain band cb - 1.
+      const int ntl = p.Co / 128;
+      const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, true);
+      const int it0 = it;
+      const int qd = warp & 3, hrow = (warp >> 2) * (BT / 2);
+      for (int cb = 0; cb <= ncb; ++cb) {
+        if (cb < ncb && tid == 0) {
+          tc05_fence_after();
+          const uint32_t dbuf = tmem + (uint32_t)((cb & 1) * 2 * N5);
+          for (int rt = 0; rt < nrt; ++rt) {
+            const int i = it0 + cb * nrt + rt, s = i % p.stages;
+            mbar_wait(&full[s], (i / p.stages) & 1, p.errflag);
+            if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
+            uint8_t* st = ring + (size_t)s * p.stage_bytes;
+            for (int tt = 0; tt < ntl; ++tt) {
+              const uint32_t a0 = smem_u32(st + 2 * tt * obox_bytes);
+              for (int ks = 0; ks < p.Ro / 16; ++ks) {
+                const int kg = rt * p.Ro + ks * 16;
+                const uint64_t ad = smem_desc_mn_sw128(a0 + (uint32_t)ks * 2048u, obox_bytes, 1024);
+                const uint64_t bd = smem_desc_k_sw128(
+                    smem_u32(aop + (kg >> 6) * (N5 * 128)) + (uint32_t)((kg & 63) >> 4) * 32u, 1024);
+                tc05_mma_f16(dbuf + (uint32_t)(tt * N5), ad, bd, idesc, rt > 0 || ks > 0);
+              }
+            }
+            mbar_arrive_cnt(&empty[s], kConsumerWarps - 1);
+            tc05_commit(&empty[s]);
+          }
+          tc05_commit(&tc_bar[2 + (cb & 1)]);
+        }
+        __syncwarp();
+        if (cb >= 1) {
+          const int pc = cb - 1;
+          mbar_wait(&tc_bar[2 + (pc & 1)], (pc >> 1) & 1, p.errflag);
+          tc05_fence_after();
+          for (int tt = 0; tt < ntl; ++tt) {
+            const int col = k0 + pc * p.Co + 128 * tt + 32 * qd + lane;
+            const uint32_t d = tmem + ((uint32_t)(32 * qd) << 16) +
+                               (uint32_t)((pc & 1) * 2 * N5 + tt * N5 + hrow);
+#pragma unroll
+            for (int r8 = 0; r8 < BT / 2; r8 += 8) {
+              float vh[8], vl[8];
+              tmem_ld_32x32b_x8(d + (uint32_t)r8, vh);
+              tmem_ld_32x32b_x8(d + (uint32_t)(BT + r8), vl);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int row = hrow + r8 + i;
+                if (b0 + row < p.B && s_pos[row] >= 0)
+                  atomicAdd(p.acc + (size_t)(b0 + row) * p.H + col, vh[i] + vl[i]);
+              }
+            }
+          }
+          tc05_fence_before();
+        }
+        named_sync(kBarConsumers, kConsumers);
+      }
+      it = it0 + ncb * nrt;
+      // Every MMA has completed (the last band's commit was waited for); make
+      // sure of it even after an expired wait before the memory is freed.
+      if (tid == 0) {
+        tc05_commit(&tc_bar[0]);
+        tc05_drain(&tc_bar[0], (uint32_t)(((nkt + 1) / 2) & 1), 1u << 22);
+      }
+    } else if constexpr (BT <= 4) {
       // Transposed (out^T = W_o^T o^T, see the projection): per column band,
       // warp w takes m-tiles w, w + 8 (16 columns each) of the Co columns.
       const int mtiles = p.Co / 16;
@@ -656,6 +879,12 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     // ---- Residual + finalize by the last block of each (tile, band) ------
     __threadfence();
     named_sync(kBarConsumers, kConsumers);
+    if constexpr (TC5) {
+      if (warp == 0) {
+        tc05_fence_after();
+        tmem_dealloc(tmem, TCOLS);
+      }
+    }
     if (tid == 0) {
       const int ticket = atomicAdd(&p.counters[bt * N + rank], 1);
       const int last = (ticket == p.nkv - 1);

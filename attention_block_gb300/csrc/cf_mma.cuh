@@ -26,6 +26,7 @@ struct MmaKind<__half> {
   // the fp16 unit roundoff (2.6e-4 measured on the 64-row, 2048-hidden MHA
   // layer, against a 1e-3 bound) and the block output about 1e-5.
   static constexpr bool kAttnHiLo = false;
+  static constexpr bool kBf16 = false;
   static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                              uint32_t b1) {
     asm volatile(
@@ -49,6 +50,7 @@ struct MmaKind<__nv_bfloat16> {
   // bf16 keeps 8 significant bits: the attention operands enter as hi + lo
   // pairs (about fp32 accuracy).
   static constexpr bool kAttnHiLo = true;
+  static constexpr bool kBf16 = true;
   static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                              uint32_t b1) {
     asm volatile(

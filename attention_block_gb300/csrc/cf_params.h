@@ -87,6 +87,8 @@ struct BarIdx {
   static constexpr int rs = 2 * kMaxStages;            // [kMaxRounds] reduce-scatter
   static constexpr int ga = rs + kMaxRounds;           // [kMaxRounds] gather
   static constexpr int sm = ga + kMaxRounds;           // [kMaxRounds] softmax-merge all-reduce
+                                                       // (the batched kernel: tensor-core
+                                                       // completions)
   static constexpr int count = sm + kMaxRounds;
 };
 

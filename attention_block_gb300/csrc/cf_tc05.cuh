@@ -130,4 +130,20 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, float (&v)[8])
   v[7] = __uint_as_float(r7);
 }
 
+// TMEM columns to allocate for `need` columns: a power of two, at least 32.
+__host__ __device__ constexpr int tmem_cols_for(int need) {
+  return need <= 32 ? 32 : (need <= 64 ? 64 : (need <= 128 ? 128 : (need <= 256 ? 256 : 512)));
+}
+
+// Wait for the phase of `bar` with the given parity, at most ~`limit` polls,
+// without the early exit on a recorded error that the ring waits take: used
+// before freeing TMEM, to let MMAs still in flight finish.  Returns whether
+// the phase completed.
+__device__ __forceinline__ bool tc05_drain(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait_cta(a, parity)) return true;
+  return false;
+}
+
 }  // namespace cf
