@@ -165,40 +165,68 @@ __device__ __forceinline__ void cluster_signal_peers(uint64_t* bar, int rank, in
 // ClusterReduce, reduce-scatter form by pulling [CF §3.1.1]: data holds N
 // slices of n floats (n % 4 == 0) in every block; afterwards slice `rank` of
 // this block holds the sum of slice `rank` over all blocks.  Slices other than
-// `rank` are only read (by their owners), so they stay valid.
+// `rank` are only read (by their owners), so they stay valid.  Each thread
+// keeps four remote loads in flight per peer before it adds them.
 template <int NT>
 __device__ void cluster_pull_reduce_slice(float* data, int n, uint64_t* bar, int rank, int N,
                                           int tid, int* err) {
+  constexpr int U = 4;
   mbar_wait_cluster(bar, 0, err);
   float4* own = reinterpret_cast<float4*>(data + (size_t)rank * n);
   const uint32_t base = smem_u32(own);
-  for (int i = tid; i < n / 4; i += NT) {
-    float4 v = own[i];
+  const int n4 = n / 4;
+  for (int i0 = tid; i0 < n4; i0 += NT * U) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * NT < n4) v[u] = own[i0 + u * NT];
     for (int q = 1; q < N; ++q) {
-      const float4 w = ld_dsmem_f4(mapa(base, (uint32_t)((rank + q) % N)) + 16u * i);
-      v.x += w.x;
-      v.y += w.y;
-      v.z += w.z;
-      v.w += w.w;
+      const uint32_t rb = mapa(base, (uint32_t)((rank + q) % N));
+      float4 w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (i0 + u * NT < n4) w[u] = ld_dsmem_f4(rb + 16u * (uint32_t)(i0 + u * NT));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        v[u].x += w[u].x;
+        v[u].y += w[u].y;
+        v[u].z += w[u].z;
+        v[u].w += w[u].w;
+      }
     }
-    own[i] = v;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * NT < n4) own[i0 + u * NT] = v[u];
   }
 }
 
-// ClusterGather by pulling [CF §3.1.2]: block q's slice is `nbytes` bytes
-// (a multiple of 16) at buf + q * stride in every block; afterwards every
-// block holds all N slices.
+// ClusterGather by pulling [CF §3.1.2]: block q's slice is `npieces` pieces
+// of `nbytes` bytes (a multiple of 16) at buf + k * piece_stride + q * stride
+// (k < npieces) in every block; afterwards every block holds all N slices.
+// Each thread keeps four remote loads in flight before it stores them.
 template <int NT>
-__device__ void cluster_pull_gather(uint8_t* buf, int nbytes, int stride, uint64_t* bar, int rank,
-                                    int N, int tid, int* err) {
+__device__ void cluster_pull_gather(uint8_t* buf, int nbytes, int stride, int npieces,
+                                    int piece_stride, uint64_t* bar, int rank, int N, int tid,
+                                    int* err) {
+  constexpr int U = 4;
   mbar_wait_cluster(bar, 0, err);
-  const int n16 = nbytes / 16;
-  for (int q = 1; q < N; ++q) {
-    const int peer = (rank + q) % N;
-    uint8_t* dst = buf + (size_t)peer * stride;
-    const uint32_t src = mapa(smem_u32(dst), (uint32_t)peer);
-    for (int i = tid; i < n16; i += NT)
-      *reinterpret_cast<uint4*>(dst + 16 * i) = ld_dsmem_u4(src + 16u * i);
+  const int n16 = nbytes / 16, per_peer = npieces * n16, total = (N - 1) * per_peer;
+  for (int i0 = tid; i0 < total; i0 += NT * U) {
+    uint4 w[U];
+    uint8_t* dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = i0 + u * NT;
+      if (idx < total) {
+        const int peer = (rank + 1 + idx / per_peer) % N;
+        const int rem = idx % per_peer;
+        dst[u] = buf + (size_t)(rem / n16) * piece_stride + (size_t)peer * stride + 16 * (rem % n16);
+        w[u] = ld_dsmem_u4(mapa(smem_u32(dst[u]), (uint32_t)peer));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * NT < total) *reinterpret_cast<uint4*>(dst[u]) = w[u];
   }
 }
 

@@ -673,14 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       if (tid == 0) cluster_signal_peers(ga_bar, rank, N);
       if constexpr (TC5) {
         // block q's rows: RPC rows of 128 bytes in the hi and the lo half of
-        // every slab
-        for (int sl = 0; sl < GD / 64; ++sl)
-          for (int h = 0; h < 2; ++h)
-            cluster_pull_gather<kConsumers>(aop + sl * (N5 * 128) + h * (BT * 128), RPC * 128,
-                                            RPC * 128, ga_bar, rank, N, tid, p.errflag);
+        // every slab, i.e. 2 * GD / 64 pieces BT * 128 bytes apart
+        cluster_pull_gather<kConsumers>(aop, RPC * 128, RPC * 128, 2 * (GD / 64), BT * 128, ga_bar,
+                                        rank, N, tid, p.errflag);
         fence_proxy_async_smem();
       } else {
-        cluster_pull_gather<kConsumers>(aop, RPC * OP, RPC * OP, ga_bar, rank, N, tid, p.errflag);
+        cluster_pull_gather<kConsumers>(aop, RPC * OP, RPC * OP, 1, 0, ga_bar, rank, N, tid,
+                                        p.errflag);
       }
       named_sync(kBarConsumers, kConsumers);
     }
@@ -726,6 +725,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           const int pc = cb - 1;
           mbar_wait(&tc_bar[2 + (pc & 1)], (pc >> 1) & 1, p.errflag);
           tc05_fence_after();
+          // lane = output column: each atomic instruction of the warp adds
+          // 32 consecutive floats of one row (float4 atomics after a lane
+          // transpose measured slower: the L2 cost follows the bytes)
           for (int tt = 0; tt < ntl; ++tt) {
             const int col = k0 + pc * p.Co + 128 * tt + 32 * qd + lane;
             const uint32_t d = tmem + ((uint32_t)(32 * qd) << 16) +
@@ -896,8 +898,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     if (s_flag[0]) {
       T* out = reinterpret_cast<T*>(p.out);
       float* dproj = p.dbg ? p.dbg + (size_t)p.B * (2 * p.nq + 2 * p.nkv) * D : nullptr;
-      // Four rows' worth of loads in flight per thread before any store.
-      constexpr int UNR = 4;
+      // UNR rows' worth of loads in flight per thread before any store (one
+      // block finalizes the whole band, so its memory parallelism sets the
+      // launch's tail).
+      constexpr int UNR = BT >= 32 ? 8 : 4;
       const int C4 = Hc / 4, total = BT * C4;
       for (int base = tid; base < total; base += kConsumers * UNR) {
         float4 v[UNR];
