@@ -887,22 +887,34 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         tmem_dealloc(tmem, TCOLS);
       }
     }
+    // The last F blocks to arrive for a (tile, band) split its rows; all but
+    // the very last wait (bounded) until every KV head has arrived.  The host
+    // asks for F > 1 only when the whole grid is resident at once.  The same
+    // counter then counts finished shares; the last share resets it.
+    const int F = p.fin_split > 1 ? p.fin_split : 1;
+    int* ctr = &p.counters[bt * N + rank];
     if (tid == 0) {
-      const int ticket = atomicAdd(&p.counters[bt * N + rank], 1);
-      const int last = (ticket == p.nkv - 1);
-      if (last) __threadfence();
-      s_flag[0] = last;
+      const int ticket = atomicAdd(ctr, 1);
+      int share = -1;
+      if (ticket >= p.nkv - F) {
+        share = ticket - (p.nkv - F);
+        if (ticket != p.nkv - 1) wait_count_at_least(ctr, p.nkv, p.errflag);
+        __threadfence();
+      }
+      s_flag[0] = share;
     }
     named_sync(kBarConsumers, kConsumers);
     stamp(kTlTicket);
-    if (s_flag[0]) {
+    if (s_flag[0] >= 0) {
+      const int share = s_flag[0];
+      const int rbeg = share * BT / F, rend = (share + 1) * BT / F;
       T* out = reinterpret_cast<T*>(p.out);
       float* dproj = p.dbg ? p.dbg + (size_t)p.B * (2 * p.nq + 2 * p.nkv) * D : nullptr;
       // UNR rows' worth of loads in flight per thread before any store (one
       // block finalizes the whole band, so its memory parallelism sets the
       // launch's tail).
       constexpr int UNR = BT >= 32 ? 8 : 4;
-      const int C4 = Hc / 4, total = BT * C4;
+      const int C4 = Hc / 4, total = (rend - rbeg) * C4;
       for (int base = tid; base < total; base += kConsumers * UNR) {
         float4 v[UNR];
         float xf[UNR][4];
@@ -911,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
           const int i4 = base + u * kConsumers;
-          const int bb = i4 / C4, c4 = i4 % C4;
+          const int bb = rbeg + i4 / C4, c4 = i4 % C4;
           ok[u] = i4 < total && b0 + bb < p.B;
           off[u] = (size_t)(b0 + bb) * p.H + k0 + c4 * 4;
           if (ok[u]) {
@@ -934,7 +946,13 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           }
         }
       }
-      if (tid == 0) p.counters[bt * N + rank] = 0;
+      if (F == 1) {
+        if (tid == 0) *ctr = 0;
+      } else {
+        __threadfence();
+        named_sync(kBarConsumers, kConsumers);
+        if (tid == 0 && atomicAdd(ctr, 1) == p.nkv + F - 1) *ctr = 0;
+      }
     }
   }
   stamp(kTlFinal);

@@ -114,6 +114,8 @@ struct KParams {  // 128-byte aligned through its CUtensorMap members
                          // 1 after the last W_qkv tile is issued, 2 at the start
   int kv_prefetch;       // batched kernel: K/V tiles per owned row prefetched into
                          // L2 during the QKV projection (0 = none)
+  int fin_split;         // batched kernel: blocks sharing the finalize of a
+                         // (tile, band) (<= 1: the last block alone)
   int B, H, nq, nkv, S;
   int N;                 // cluster size
   int nbt;               // batch tiles

@@ -130,6 +130,24 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   return mbar_wait_slow<true>(a, parity, errflag);
 }
 
+// Bounded wait until the global counter reaches `target` (blocks of the same,
+// fully resident grid are the only writers).  On expiry it records
+// kDevErrTimeout and returns false.
+static __device__ __noinline__ bool wait_count_at_least(const int* ctr, int target, int* errflag) {
+  const long long t0 = clock64();
+  for (uint32_t spins = 1;; ++spins) {
+    if (*reinterpret_cast<const volatile int*>(ctr) >= target) return true;
+    if ((spins & 255u) == 0) {
+      if (*reinterpret_cast<volatile int*>(errflag) & kDevErrTimeout) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        atomicOr(errflag, kDevErrTimeout);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+}
+
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
