@@ -87,6 +87,7 @@ SIGNATURES = {
     "cf_ffn_get_status": (ctypes.c_int, [_vp]),
     "cf_ffn_launch_info": (ctypes.c_int, [_vp] + [ctypes.POINTER(ctypes.c_int32)] * 3),
     "cf_ffn_destroy": (None, [_vp]),
+    "cf_ffn_kernels": (ctypes.c_int, [_vp, ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 2),
     "cf_bench_contig_stream": (ctypes.c_int, [_vp, ctypes.c_longlong, ctypes.c_longlong] + [ctypes.c_int] * 5 + [_vp, _vp]),
     "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
                                      + [_vp] * 9),
@@ -354,6 +355,15 @@ class FfnBlock:
         if rc != CF_OK:
             raise CfError(rc, "cf_ffn_launch_info")
         return {"blocks": b.value, "rows_per_stage": r.value, "stages": s.value}
+
+    def kernels(self, batch) -> dict:
+        """Kernels (1: the one- and two-row kernel, 2: the tensor-core pair)
+        and grids a call of ``batch`` rows launches."""
+        b1, b2 = ctypes.c_int32(), ctypes.c_int32()
+        n = lib().cf_ffn_kernels(self.handle, int(batch), ctypes.byref(b1), ctypes.byref(b2))
+        if n < 0:
+            raise CfError(n, "cf_ffn_kernels")
+        return {"kernels": n, "blocks1": b1.value, "blocks2": b2.value}
 
     def status(self) -> int:
         import torch

@@ -45,8 +45,10 @@
 #include "cf.h"
 #include "cf_common.cuh"
 #include "cf_ffn.h"
+#include "cf_ffn_tc.cuh"
 #include "cf_params.h"
 #include "cf_ptx.cuh"
+#include "cf_tmap.h"
 
 namespace cf {
 namespace {
@@ -337,6 +339,41 @@ __global__ void __launch_bounds__(kThreads, 1) cf_ffn_kernel(const __grid_consta
 }
 
 using FfnFn = void (*)(FfnParams);
+using FfnTcFn = void (*)(FfnTcParams);
+
+// Tensor-core pair for batches of 3..64 rows: batch tile BP = 16, 32 or 64.
+void ffn_tc_entries(int dtype, int bp, FfnTcFn& gu, FfnTcFn& down) {
+  if (dtype == CF_F16) {
+    gu = bp == 16 ? cf_ffn_gu_kernel<__half, 16>
+                  : (bp == 32 ? cf_ffn_gu_kernel<__half, 32> : cf_ffn_gu_kernel<__half, 64>);
+    down = bp == 16 ? cf_ffn_down_kernel<__half, 16>
+                    : (bp == 32 ? cf_ffn_down_kernel<__half, 32> : cf_ffn_down_kernel<__half, 64>);
+  } else {
+    gu = bp == 16 ? cf_ffn_gu_kernel<__nv_bfloat16, 16>
+                  : (bp == 32 ? cf_ffn_gu_kernel<__nv_bfloat16, 32>
+                              : cf_ffn_gu_kernel<__nv_bfloat16, 64>);
+    down = bp == 16 ? cf_ffn_down_kernel<__nv_bfloat16, 16>
+                    : (bp == 32 ? cf_ffn_down_kernel<__nv_bfloat16, 32>
+                                : cf_ffn_down_kernel<__nv_bfloat16, 64>);
+  }
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, never lowering it
+// (the attribute belongs to the function, shared by every handle).
+bool raise_smem(const void* fn, int bytes) {
+  cudaFuncAttributes cur;
+  if (cudaFuncGetAttributes(&cur, fn) != cudaSuccess) return false;
+  return cur.maxDynamicSharedSizeBytes >= bytes ||
+         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+             cudaSuccess;
+}
+
+// One cached tensor map per operand, keyed by (pointer, outer extent).
+struct TmapSlot {
+  const void* ptr = nullptr;
+  int outer = 0;
+  CUtensorMap map;
+};
 
 FfnFn ffn_entry(int dtype, int bmax) {
   if (dtype == CF_F32) return bmax == 1 ? cf_ffn_kernel<float, 1> : cf_ffn_kernel<float, 2>;
@@ -360,11 +397,85 @@ struct cf_ffn_handle {
   cf_ffn_config cfg;
   FfnFn fn = nullptr;
   int blocks = 0, R = 0, stages = 0, stage_bytes = 0, smem = 0, bmax = 1;
-  void* ws = nullptr;  // acc | counter | errflag
+  void* ws = nullptr;  // acc | counters | errflag | a_hi | a_lo
   float* acc = nullptr;
   int* counter = nullptr;
   int* errflag = nullptr;
+  // tensor-core pair (max_batch >= 3): kernel 1 gate/up, kernel 2 down
+  bool tc = false;
+  int BP = 0, Ip = 0;
+  FfnTcFn fn_gu = nullptr, fn_down = nullptr;
+  int blocks1 = 0, UB = 0, nsl1 = 0, stages1 = 0, stage1_bytes = 0, smem1 = 0;
+  int blocks2 = 0, S = 0, nsl2 = 0, stages2 = 0, stage2_bytes = 0, smem2 = 0;
+  void* a_hi = nullptr;
+  void* a_lo = nullptr;
+  TmapSlot m_wg, m_wu, m_wd, m_h;
+  CUtensorMap m_ahi, m_alo;
 };
+
+namespace {
+
+// Plan of the tensor-core pair on a device with `sms` SMs and `budget` bytes
+// of shared memory per block.  False when the shape does not fit.
+bool plan_ffn_tc(cf_ffn_handle* h, int sms, int budget) {
+  const cf_ffn_config& c = h->cfg;
+  const int H = c.hidden, I = c.intermediate;
+  h->BP = c.max_batch <= 16 ? 16 : (c.max_batch <= 32 ? 32 : 64);
+  const int BP = h->BP, N5 = 2 * BP;
+  h->Ip = (I + 7) / 8 * 8;
+  // kernel 1: one block per SM, each at most UB (multiple of 8) units
+  h->blocks1 = std::min(sms, I);
+  const int umax = (I + h->blocks1 - 1) / h->blocks1;
+  h->UB = (umax + 7) / 8 * 8;
+  if (h->UB > 128) return false;
+  const int slab1 = (2 * h->UB + BP) * 128;
+  int extras1 = 2 * N5 * 128 + (2 * kFfnTcMaxStages + 2) * 8 + (kConsumerWarps * BP + BP) * 4 + 16;
+  // the M = 128 operand reads of a slab's boxes run up to 16 KB past the
+  // box start: keep that much shared memory after the ring
+  extras1 = std::max(extras1, 16384 - (h->UB + BP) * 128);
+  extras1 = (extras1 + 1023) / 1024 * 1024;
+  h->nsl1 = std::max(1, std::min(H / 64, 65536 / slab1));
+  for (;; --h->nsl1) {
+    h->stage1_bytes = h->nsl1 * slab1;
+    h->stages1 = std::min(kFfnTcMaxStages, (budget - extras1) / h->stage1_bytes);
+    if (h->stages1 >= 2 || h->nsl1 == 1) break;
+  }
+  if (h->stages1 < 2) return false;
+  h->smem1 = h->stages1 * h->stage1_bytes + extras1 + 1024;
+  // kernel 2: H / 128 column tiles x S splits of the 64-unit slabs
+  const int tiles = H / 128, slabs = (I + 63) / 64;
+  h->S = std::max(1, std::min(slabs, sms / tiles));
+  h->blocks2 = tiles * h->S;
+  const int slab2 = (128 + N5) * 128;
+  const int extras2 = 1024;
+  h->nsl2 = std::max(1, std::min((slabs + h->S - 1) / h->S, 65536 / slab2));
+  h->stage2_bytes = h->nsl2 * slab2;
+  h->stages2 = std::min(kFfnTcMaxStages, (budget - extras2) / h->stage2_bytes);
+  if (h->stages2 < 2) return false;
+  h->smem2 = h->stages2 * h->stage2_bytes + extras2 + 1024;
+  ffn_tc_entries(c.dtype, BP, h->fn_gu, h->fn_down);
+  if (!raise_smem(reinterpret_cast<const void*>(h->fn_gu), h->smem1) ||
+      !raise_smem(reinterpret_cast<const void*>(h->fn_down), h->smem2)) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+const CUtensorMap* cached_map(TmapSlot& slot, int dtype, const void* ptr, uint64_t inner,
+                              uint64_t outer, uint32_t box_outer) {
+  if (slot.ptr != ptr || slot.outer != (int)outer) {
+    if (!encode_tmap_2d(&slot.map, dtype, ptr, inner, outer, inner * 2, 64, box_outer, true)) {
+      slot.ptr = nullptr;
+      return nullptr;
+    }
+    slot.ptr = ptr;
+    slot.outer = (int)outer;
+  }
+  return &slot.map;
+}
+
+}  // namespace
 
 extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
   if (out == nullptr) return CF_ERR_INVALID_ARG;
@@ -374,7 +485,10 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
   if (c.hidden <= 0 || c.hidden % 8 != 0 || c.intermediate <= 0 || c.max_batch <= 0 ||
       c.dtype < CF_F32 || c.dtype > CF_BF16 || !(c.rms_eps >= 0.f) || c.stage_bytes < 0)
     return CF_ERR_INVALID_ARG;
-  if (c.hidden > kFfnMaxH || c.max_batch > 2) return CF_ERR_UNSUPPORTED;
+  // batches of 3+ rows: the tensor-core pair (16-bit storage, H a multiple
+  // of 128, at most 64 rows)
+  if (c.hidden > kFfnMaxH || c.max_batch > 64) return CF_ERR_UNSUPPORTED;
+  if (c.max_batch > 2 && (c.dtype == CF_F32 || c.hidden % 128 != 0)) return CF_ERR_UNSUPPORTED;
   const int row_bytes = c.hidden * dtype_bytes(c.dtype);
   if (c.stage_bytes != 0 && c.stage_bytes < row_bytes) return CF_ERR_INVALID_ARG;
   int dev = 0;
@@ -411,29 +525,115 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
     delete h;
     return CF_ERR_UNSUPPORTED;
   }
-  if (cudaFuncSetAttribute(h->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem) !=
-      cudaSuccess) {
+  if (!raise_smem(reinterpret_cast<const void*>(h->fn), h->smem)) {
     cudaGetLastError();
     delete h;
     return CF_ERR_CUDA;
+  }
+  h->tc = c.max_batch > 2;
+  if (h->tc && !plan_ffn_tc(h, prop.multiProcessorCount,
+                            (int)prop.sharedMemPerBlockOptin - 1024)) {
+    delete h;
+    return CF_ERR_UNSUPPORTED;
   }
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
-  if (cudaMalloc(&h->ws, acc_bytes + 256) != cudaSuccess) {
+  const size_t a_bytes = h->tc ? (size_t)c.max_batch * h->Ip * 2 : 0;
+  const size_t total = acc_bytes + 256 + 2 * a_bytes;
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return CF_ERR_CUDA;
   }
-  if (cudaMemset(h->ws, 0, acc_bytes + 256) != cudaSuccess) {
+  if (cudaMemset(h->ws, 0, total) != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
     return CF_ERR_CUDA;
   }
   h->acc = static_cast<float*>(h->ws);
-  h->counter = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes);
+  h->counter = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes);  // [32]
   h->errflag = h->counter + 32;
+  if (h->tc) {
+    h->a_hi = static_cast<char*>(h->ws) + acc_bytes + 256;
+    h->a_lo = static_cast<char*>(h->a_hi) + a_bytes;
+    if (!encode_tmap_2d(&h->m_ahi, c.dtype, h->a_hi, c.intermediate, c.max_batch, h->Ip * 2, 64,
+                        h->BP, true) ||
+        !encode_tmap_2d(&h->m_alo, c.dtype, h->a_lo, c.intermediate, c.max_batch, h->Ip * 2, 64,
+                        h->BP, true)) {
+      cudaFree(h->ws);
+      delete h;
+      return CF_ERR_CUDA;
+    }
+  }
   *out = h;
   return CF_OK;
 }
+
+namespace {
+
+// Batches of 3+ rows: gate/up kernel, then the down kernel as its
+// programmatic dependent.
+int ffn_forward_tc(cf_ffn_handle* h, int batch, const void* hidden, const void* ln_weight,
+                   const void* w_gate, const void* w_up, const void* w_down, void* out,
+                   void* stream) {
+  const cf_ffn_config& c = h->cfg;
+  const uint64_t H = c.hidden, I = c.intermediate;
+  const CUtensorMap* mg = cached_map(h->m_wg, c.dtype, w_gate, H, I, h->UB);
+  const CUtensorMap* mu = cached_map(h->m_wu, c.dtype, w_up, H, I, h->UB);
+  const CUtensorMap* md = cached_map(h->m_wd, c.dtype, w_down, H, I, 64);
+  const CUtensorMap* mh = cached_map(h->m_h, c.dtype, hidden, H, (uint64_t)batch, h->BP);
+  if (!mg || !mu || !md || !mh) return CF_ERR_CUDA;
+  FfnTcParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.tm_wg = *mg;
+  p.tm_wu = *mu;
+  p.tm_h = *mh;
+  p.tm_wd = *md;
+  p.tm_ahi = h->m_ahi;
+  p.tm_alo = h->m_alo;
+  p.h = hidden;
+  p.g2 = ln_weight;
+  p.a_hi = h->a_hi;
+  p.a_lo = h->a_lo;
+  p.out = out;
+  p.acc = h->acc;
+  p.counters = h->counter;
+  p.errflag = h->errflag;
+  p.B = batch;
+  p.H = c.hidden;
+  p.I = c.intermediate;
+  p.Ip = h->Ip;
+  p.UB = h->UB;
+  p.nsl1 = h->nsl1;
+  p.stages1 = h->stages1;
+  p.stage1_bytes = h->stage1_bytes;
+  p.S = h->S;
+  p.nsl2 = h->nsl2;
+  p.stages2 = h->stages2;
+  p.stage2_bytes = h->stage2_bytes;
+  p.eps = c.rms_eps;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  void* args[] = {&p};
+  const FfnTcFn fns[2] = {h->fn_gu, h->fn_down};
+  const int grids[2] = {h->blocks1, h->blocks2}, smems[2] = {h->smem1, h->smem2};
+  for (int k = 0; k < 2; ++k) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grids[k], 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = smems[k];
+    lc.stream = static_cast<cudaStream_t>(stream);
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelExC(&lc, reinterpret_cast<const void*>(fns[k]), args) != cudaSuccess) {
+      cudaGetLastError();
+      return CF_ERR_CUDA;
+    }
+  }
+  return CF_OK;
+}
+
+}  // namespace
 
 extern "C" int cf_ffn_forward(cf_ffn_handle* h, int32_t batch, const void* hidden,
                               const void* ln_weight, const void* w_gate, const void* w_up,
@@ -452,6 +652,8 @@ extern "C" int cf_ffn_forward(cf_ffn_handle* h, int32_t batch, const void* hidde
       ranges_overlap(out, act, w_gate, mat) || ranges_overlap(out, act, w_up, mat) ||
       ranges_overlap(out, act, w_down, mat))
     return CF_ERR_ALIAS;
+  if (batch > 2) return ffn_forward_tc(h, batch, hidden, ln_weight, w_gate, w_up, w_down, out,
+                                       stream);
   FfnParams p;
   std::memset(&p, 0, sizeof(p));
   p.h = hidden;
@@ -504,6 +706,15 @@ extern "C" int cf_ffn_launch_info(const cf_ffn_handle* h, int32_t* blocks, int32
   if (rows_per_stage) *rows_per_stage = h->R;
   if (stages) *stages = h->stages;
   return CF_OK;
+}
+
+extern "C" int cf_ffn_kernels(const cf_ffn_handle* h, int32_t batch, int32_t* blocks1,
+                              int32_t* blocks2) {
+  if (h == nullptr || batch < 1 || batch > h->cfg.max_batch) return CF_ERR_INVALID_ARG;
+  const bool tc = batch > 2;
+  if (blocks1) *blocks1 = tc ? h->blocks1 : h->blocks;
+  if (blocks2) *blocks2 = tc ? h->blocks2 : 0;
+  return tc ? 2 : 1;
 }
 
 extern "C" void cf_ffn_destroy(cf_ffn_handle* h) {

@@ -1,0 +1,441 @@
+// cf_ffn_tc.cuh -- the gated FFN of the decoder block for decode batches of
+// 3 to 64 rows on the fifth-generation tensor cores (tcgen05, accumulators in
+// tensor memory), as two kernels launched back to back (the second as a
+// programmatic dependent of the first).
+//
+// Page cited by title and section:
+//   [LNA] "大模型推理中的算子融合优化：LayerNorm + Attention 的 CUDA Kernel
+//         手写与验证" (asdsk.com), §一 (the LLaMA block ends with a second
+//         RMS Norm and the FFN) and §三 stage 1 (RMSNorm).
+//
+// Per batch row b (the same computation as the one- and two-row kernel):
+//   n_b = h_b * g2 * rinv_b,   rinv_b = 1 / sqrt(mean(h_b^2) + eps)
+//   a_bi = silu(Wg[i,:] . n_b) * (Wu[i,:] . n_b)
+//   out_b = h_b + sum_i a_bi Wd[i,:]
+//
+// Kernel 1 (gate and up): one block per SM owns the intermediate units
+// [i0, i1) (at most UB <= 128 of them).  Both products run transposed:
+// M = 128 unit rows of W_gate / W_up (one TMA box of the block's rows, the
+// [I, H] layout read as a K-major operand; the rows past the block's units
+// are not used), N = 2 * BP (the rows' h * g2 as 16-bit hi halves, then lo
+// halves), K = the hidden dimension in 64-column slabs.  The norm scale rinv
+// is applied in the epilogue (each block sees every column of h, so it sums
+// h^2 while staging).  The epilogue writes a as 16-bit hi and lo arrays
+// [B, I], exactly the operand layout kernel 2 loads.
+//
+// Kernel 2 (down): (H / 128) column tiles x S splits of the units.  Each
+// block computes out^T[128 columns, rows] = Wd^T a^T over its units: M = 128
+// output columns (two swizzled 64-column TMA boxes of Wd, an M-major
+// operand), N = 2 * BP (a's hi and lo rows, loaded by TMA straight into a
+// K-major slab), K = units.  Partial sums meet in an fp32 accumulator by
+// atomics; the last split of a column tile adds the residual, writes `out`
+// and clears the accumulator.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "cf_common.cuh"
+#include "cf_mma.cuh"
+#include "cf_params.h"
+#include "cf_ptx.cuh"
+#include "cf_tc05.cuh"
+
+namespace cf {
+
+constexpr int kFfnTcMaxStages = 8;
+
+struct FfnTcParams {
+  CUtensorMap tm_wg;   // W_gate [I, H], box {64, UB}, 128-byte swizzle
+  CUtensorMap tm_wu;   // W_up   [I, H], box {64, UB}
+  CUtensorMap tm_h;    // hidden [B, H], box {64, BP}
+  CUtensorMap tm_wd;   // W_down [I, H], box {64, 64}
+  CUtensorMap tm_ahi;  // a hi   [B, I], box {64, BP}
+  CUtensorMap tm_alo;  // a lo   [B, I], box {64, BP}
+  const void* h;       // hidden [B, H] (residual)
+  const void* g2;      // ln_weight [H]
+  void* a_hi;          // [B, Ip] 16-bit
+  void* a_lo;          // [B, Ip] 16-bit
+  void* out;           // [B, H]
+  float* acc;          // [B, H] fp32, zero between calls
+  int* counters;       // [H / 128], zero between calls
+  int* errflag;
+  int B, H, I;
+  int Ip;              // row stride of a_hi / a_lo (I rounded up to 8)
+  int UB;              // kernel 1: unit rows per box (multiple of 8, <= 128)
+  int nsl1, stages1, stage1_bytes;  // kernel 1: 64-column slabs per stage, ring
+  int S;               // kernel 2: splits of the units
+  int nsl2, stages2, stage2_bytes;  // kernel 2: 64-unit slabs per stage, ring
+  float eps;
+};
+
+// 16-bit hi + lo split of one fp32 value (hi = round(v), lo = round(v - hi)).
+template <typename T>
+__device__ __forceinline__ void split1(float v, T& hi, T& lo) {
+  hi = Elem<T>::from_f(v);
+  lo = Elem<T>::from_f(v - Elem<T>::to_f(hi));
+}
+
+// ------------------------------------------------------------ kernel 1 ---
+template <typename T, int BP>
+__global__ void __launch_bounds__(kThreads, 1)
+    cf_ffn_gu_kernel(const __grid_constant__ FfnTcParams p) {
+  constexpr int N5 = 2 * BP;
+  constexpr int TCOLS = tmem_cols_for(2 * N5);  // gate and up accumulators
+  constexpr int NRW = BP / kConsumerWarps;      // rows per warp while staging
+  using MK = MmaKind<T>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const int slab1 = (2 * p.UB + BP) * 128;  // gate box | up box | h box
+  uint8_t* ring = sm;
+  uint8_t* nbuf = ring + (size_t)p.stages1 * p.stage1_bytes;  // [2][N5 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(nbuf + 2 * N5 * 128);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kFfnTcMaxStages;
+  uint64_t* nbar = bars + 2 * kFfnTcMaxStages;  // [2] n buffer free again
+  float* ssq = reinterpret_cast<float*>(bars + 2 * kFfnTcMaxStages + 2);  // [8][BP]
+  float* rinv = ssq + kConsumerWarps * BP;                                // [BP]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(rinv + BP);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int i0 = (int)((long long)blockIdx.x * p.I / G);
+  const int i1 = (int)((long long)(blockIdx.x + 1) * p.I / G);
+  const int nslab = p.H / 64;
+  const int nst = (nslab + p.nsl1 - 1) / p.nsl1;  // stages of the stream
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages1; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_init(&nbar[0], 1);
+    mbar_init(&nbar[1], 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, TCOLS);
+    tmem_relinquish();
+  }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == kConsumerWarps) {
+    // ================================================ TMA producer ====
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_wg);
+      prefetch_tensormap(&p.tm_wu);
+      prefetch_tensormap(&p.tm_h);
+      const uint64_t pol_w = policy_evict_first(), pol_h = policy_evict_normal();
+      auto stage_slabs = [&](int st) { return min(p.nsl1, nslab - st * p.nsl1); };
+      auto load_w = [&](int st) {
+        uint8_t* base = ring + (size_t)(st % p.stages1) * p.stage1_bytes;
+        for (int j = 0; j < stage_slabs(st); ++j) {
+          const int x = (st * p.nsl1 + j) * 64;
+          tma_load_2d(base + j * slab1, &p.tm_wg, x, i0, &full[st % p.stages1], pol_w);
+          tma_load_2d(base + j * slab1 + p.UB * 128, &p.tm_wu, x, i0, &full[st % p.stages1],
+                      pol_w);
+        }
+      };
+      auto load_h = [&](int st) {
+        uint8_t* base = ring + (size_t)(st % p.stages1) * p.stage1_bytes;
+        for (int j = 0; j < stage_slabs(st); ++j)
+          tma_load_2d(base + j * slab1 + 2 * p.UB * 128, &p.tm_h, (st * p.nsl1 + j) * 64, 0,
+                      &full[st % p.stages1], pol_h);
+      };
+      // The weights do not depend on the previous kernel: the first stages'
+      // weight boxes go out before the dependency wait, their h boxes after.
+      const int fill = min(p.stages1, nst);
+      for (int st = 0; st < fill; ++st) {
+        mbar_arrive_expect_tx(&full[st], (uint32_t)(stage_slabs(st) * slab1));
+        load_w(st);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      for (int st = 0; st < fill; ++st) load_h(st);
+      for (int st = fill; st < nst; ++st) {
+        const int s = st % p.stages1;
+        mbar_wait(&empty[s], ((st / p.stages1) + 1) & 1, p.errflag);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(stage_slabs(st) * slab1));
+        load_w(st);
+        load_h(st);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================ consumers ========
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // a is read by the previous call
+    const T* __restrict__ g2 = static_cast<const T*>(p.g2);
+    const uint32_t tmem = *s_tmem;
+    const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, false);
+    float ss[NRW];
+#pragma unroll
+    for (int i = 0; i < NRW; ++i) ss[i] = 0.f;
+    for (int j = 0; j < nslab; ++j) {
+      const int st = j / p.nsl1, within = j % p.nsl1, s = st % p.stages1;
+      uint8_t* sl = ring + (size_t)s * p.stage1_bytes + within * slab1;
+      if (within == 0) mbar_wait(&full[s], (st / p.stages1) & 1, p.errflag);
+      uint8_t* nb = nbuf + (j & 1) * (N5 * 128);
+      if (j >= 2) mbar_wait(&nbar[j & 1], ((j - 2) >> 1) & 1, p.errflag);
+      // h * g2 of the slab's 64 columns as hi rows 0..BP-1 and lo rows
+      // BP..2BP-1 of a K-major swizzled slab; warp w takes rows w, w + 8, ...
+      {
+        const uint8_t* hb = sl + 2 * p.UB * 128;  // [BP rows][128 B], swizzled by TMA
+        const int k = 2 * lane, jc = k >> 3, e2 = (k & 7) * 2;
+        float gw[2];
+        load_cvt<T, 2>(g2 + j * 64 + k, gw);
+#pragma unroll
+        for (int i = 0; i < NRW; ++i) {
+          const int row = warp + i * kConsumerWarps;
+          float f[2];
+          load_cvt<T, 2>(reinterpret_cast<const T*>(hb + row * 128 + ((jc ^ (row & 7)) << 4) + e2),
+                         f);
+          ss[i] = fmaf(f[0], f[0], fmaf(f[1], f[1], ss[i]));
+          uint32_t hi, lo;
+          MK::split2(f[0] * gw[0], f[1] * gw[1], hi, lo);
+          const int rl = BP + row;
+          *reinterpret_cast<uint32_t*>(nb + row * 128 + ((jc ^ (row & 7)) << 4) + e2) = hi;
+          *reinterpret_cast<uint32_t*>(nb + rl * 128 + ((jc ^ (rl & 7)) << 4) + e2) = lo;
+        }
+      }
+      fence_proxy_async_smem();
+      named_sync(kBarConsumers, kConsumers);
+      if (tid == 0) {
+        tc05_fence_after();
+        const uint32_t ag = smem_u32(sl), au = smem_u32(sl + p.UB * 128), bn = smem_u32(nb);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bd = smem_desc_k_sw128(bn + ks * 32u, 1024);
+          tc05_mma_f16(tmem, smem_desc_k_sw128(ag + ks * 32u, 1024), bd, idesc, j > 0 || ks > 0);
+          tc05_mma_f16(tmem + (uint32_t)N5, smem_desc_k_sw128(au + ks * 32u, 1024), bd, idesc,
+                       j > 0 || ks > 0);
+        }
+        tc05_commit(&nbar[j & 1]);
+        if (within == p.nsl1 - 1 || j == nslab - 1) {
+          mbar_arrive_cnt(&empty[s], kConsumerWarps - 1);
+          tc05_commit(&empty[s]);
+        }
+      }
+      __syncwarp();
+    }
+    // the last slab's commit covers every MMA
+    mbar_wait(&nbar[(nslab - 1) & 1], ((nslab - 1) >> 1) & 1, p.errflag);
+    tc05_fence_after();
+    // RMSNorm scale of every row [LNA §三 stage 1]
+#pragma unroll
+    for (int i = 0; i < NRW; ++i) {
+      const float v = warp_sum(ss[i]);
+      if (lane == 0) ssq[warp + i * kConsumerWarps] = v;
+    }
+    named_sync(kBarConsumers, kConsumers);
+    if (tid < BP) rinv[tid] = 1.0f / sqrtf(ssq[tid] / (float)p.H + p.eps);
+    named_sync(kBarConsumers, kConsumers);
+    // a = silu(gate) * up: warp w reads units 32 (w % 4) + lane (its TMEM
+    // lane quarter) for rows [h * BP/2, (h+1) * BP/2), h = w / 4
+    T* ahi = static_cast<T*>(p.a_hi);
+    T* alo = static_cast<T*>(p.a_lo);
+    const int qd = warp & 3, hrow = (warp >> 2) * (BP / 2);
+    const int unit = i0 + 32 * qd + lane;
+    const uint32_t dq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)hrow;
+#pragma unroll
+    for (int r8 = 0; r8 < BP / 2; r8 += 8) {
+      float gh[8], gl[8], uh[8], ul[8];
+      tmem_ld_32x32b_x8(dq + (uint32_t)r8, gh);
+      tmem_ld_32x32b_x8(dq + (uint32_t)(BP + r8), gl);
+      tmem_ld_32x32b_x8(dq + (uint32_t)(N5 + r8), uh);
+      tmem_ld_32x32b_x8(dq + (uint32_t)(N5 + BP + r8), ul);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int b = hrow + r8 + e;
+        if (b < p.B && unit < i1) {
+          const float z = (gh[e] + gl[e]) * rinv[b];
+          const float u = (uh[e] + ul[e]) * rinv[b];
+          const float a = z / (1.0f + expf(-z)) * u;
+          T hi, lo;
+          split1<T>(a, hi, lo);
+          ahi[(size_t)b * p.Ip + unit] = hi;
+          alo[(size_t)b * p.Ip + unit] = lo;
+        }
+      }
+    }
+  }
+  tc05_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc05_fence_after();
+    tmem_dealloc(*s_tmem, TCOLS);
+  }
+}
+
+// ------------------------------------------------------------ kernel 2 ---
+template <typename T, int BP>
+__global__ void __launch_bounds__(kThreads, 1)
+    cf_ffn_down_kernel(const __grid_constant__ FfnTcParams p) {
+  constexpr int N5 = 2 * BP;
+  constexpr int TCOLS = tmem_cols_for(N5);
+  using MK = MmaKind<T>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  // slab: Wd box of columns j0..j0+63 | Wd box j0+64.. | a hi box | a lo box
+  constexpr int kWBox = 64 * 128;
+  constexpr int kSlab = 2 * kWBox + N5 * 128;
+  uint8_t* ring = sm;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)p.stages2 * p.stage2_bytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kFfnTcMaxStages;
+  uint64_t* done = bars + 2 * kFfnTcMaxStages;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kFfnTcMaxStages + 1);
+  int* s_flag = reinterpret_cast<int*>(s_tmem + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int jt = blockIdx.x / p.S, split = blockIdx.x % p.S;
+  const int j0 = jt * 128;
+  const int nslab_all = (p.I + 63) / 64;
+  const int sl0 = (int)((long long)split * nslab_all / p.S);
+  const int sl1 = (int)((long long)(split + 1) * nslab_all / p.S);
+  const int nslab = sl1 - sl0;
+  const int nst = (nslab + p.nsl2 - 1) / p.nsl2;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages2; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, TCOLS);
+    tmem_relinquish();
+  }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == kConsumerWarps) {
+    // ================================================ TMA producer ====
+    if (lane == 0) {
+      prefetch_tensormap(&p.tm_wd);
+      prefetch_tensormap(&p.tm_ahi);
+      prefetch_tensormap(&p.tm_alo);
+      const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_normal();
+      auto stage_slabs = [&](int st) { return min(p.nsl2, nslab - st * p.nsl2); };
+      auto load_w = [&](int st) {
+        uint8_t* base = ring + (size_t)(st % p.stages2) * p.stage2_bytes;
+        for (int j = 0; j < stage_slabs(st); ++j) {
+          const int u = (sl0 + st * p.nsl2 + j) * 64;
+          tma_load_2d(base + j * kSlab, &p.tm_wd, j0, u, &full[st % p.stages2], pol_w);
+          tma_load_2d(base + j * kSlab + kWBox, &p.tm_wd, j0 + 64, u, &full[st % p.stages2],
+                      pol_w);
+        }
+      };
+      auto load_a = [&](int st) {
+        uint8_t* base = ring + (size_t)(st % p.stages2) * p.stage2_bytes;
+        for (int j = 0; j < stage_slabs(st); ++j) {
+          const int u = (sl0 + st * p.nsl2 + j) * 64;
+          tma_load_2d(base + j * kSlab + 2 * kWBox, &p.tm_ahi, u, 0, &full[st % p.stages2],
+                      pol_a);
+          tma_load_2d(base + j * kSlab + 2 * kWBox + BP * 128, &p.tm_alo, u, 0,
+                      &full[st % p.stages2], pol_a);
+        }
+      };
+      const int fill = min(p.stages2, nst);
+      for (int st = 0; st < fill; ++st) {
+        mbar_arrive_expect_tx(&full[st], (uint32_t)(stage_slabs(st) * kSlab));
+        load_w(st);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // a comes from kernel 1
+      for (int st = 0; st < fill; ++st) load_a(st);
+      for (int st = fill; st < nst; ++st) {
+        const int s = st % p.stages2;
+        mbar_wait(&empty[s], ((st / p.stages2) + 1) & 1, p.errflag);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(stage_slabs(st) * kSlab));
+        load_w(st);
+        load_a(st);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================ consumers ========
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint32_t tmem = *s_tmem;
+    const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, true);
+    if (tid == 0) {
+      for (int st = 0; st < nst; ++st) {
+        const int s = st % p.stages2;
+        mbar_wait(&full[s], (st / p.stages2) & 1, p.errflag);
+        tc05_fence_after();
+        const int ns = min(p.nsl2, nslab - st * p.nsl2);
+        uint8_t* base = ring + (size_t)s * p.stage2_bytes;
+        for (int j = 0; j < ns; ++j) {
+          const uint32_t aw = smem_u32(base + j * kSlab), ba = smem_u32(base + j * kSlab + 2 * kWBox);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc05_mma_f16(tmem, smem_desc_mn_sw128(aw + ks * 2048u, kWBox, 1024),
+                         smem_desc_k_sw128(ba + ks * 32u, 1024), idesc, st > 0 || j > 0 || ks > 0);
+        }
+        mbar_arrive_cnt(&empty[s], kConsumerWarps - 1);
+        tc05_commit(&empty[s]);
+      }
+      tc05_commit(done);
+    }
+    __syncwarp();
+    mbar_wait(done, 0, p.errflag);
+    tc05_fence_after();
+    // lane = output column j0 + 32 (w % 4) + lane; rows [h BP/2, (h+1) BP/2)
+    const int qd = warp & 3, hrow = (warp >> 2) * (BP / 2);
+    const int col = j0 + 32 * qd + lane;
+    const uint32_t dq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)hrow;
+    if (nslab > 0) {
+#pragma unroll
+      for (int r8 = 0; r8 < BP / 2; r8 += 8) {
+        float vh[8], vl[8];
+        tmem_ld_32x32b_x8(dq + (uint32_t)r8, vh);
+        tmem_ld_32x32b_x8(dq + (uint32_t)(BP + r8), vl);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int b = hrow + r8 + e;
+          if (b < p.B) atomicAdd(p.acc + (size_t)b * p.H + col, vh[e] + vl[e]);
+        }
+      }
+    }
+    tc05_fence_before();
+    __threadfence();
+    named_sync(kBarConsumers, kConsumers);
+    if (tid == 0) {
+      const int last = atomicAdd(&p.counters[jt], 1) == p.S - 1;
+      if (last) __threadfence();
+      s_flag[0] = last;
+    }
+    named_sync(kBarConsumers, kConsumers);
+    if (s_flag[0]) {
+      // residual of the column tile [LNA §一]
+      const T* hid = static_cast<const T*>(p.h);
+      T* out = static_cast<T*>(p.out);
+      for (int idx = tid; idx < p.B * 32; idx += kConsumers) {
+        const int b = idx / 32, c4 = idx % 32;
+        const size_t off = (size_t)b * p.H + j0 + 4 * c4;
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
+        float x[4];
+        load_cvt<T, 4>(hid + off, x);
+        const float r4[4] = {x[0] + v.x, x[1] + v.y, x[2] + v.z, x[3] + v.w};
+        store4<T>(out + off, r4);
+        __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
+      }
+      if (tid == 0) p.counters[jt] = 0;
+    }
+  }
+  tc05_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc05_fence_after();
+    tmem_dealloc(*s_tmem, TCOLS);
+  }
+}
+
+}  // namespace cf

@@ -139,10 +139,17 @@ FFN_WORKLOADS = {w.name: w for w in [
     FfnWorkload("llama2_7b_ffn_i11008_b1_f16", 4096, 11008, 1, "f16", 1e-6),
     FfnWorkload("llama3_8b_ffn_i14336_b2_bf16", 4096, 14336, 2, "bf16", 1e-6),
     FfnWorkload("tiny_ffn_h256_i688_b1_f32", 256, 688, 1, "f32", 1e-6),
+    # batched decode: the FFNs that follow the 64-row, 2048-hidden layer
+    # (intermediate 5632 = 8/3 * 2048 rounded up to a multiple of 256, the
+    # LLaMA sizing rule) and the 16-row Llama-3 GQA layer
+    FfnWorkload("h2048_ffn_i5632_b64_f16", 2048, 5632, 64, "f16", 1e-6),
+    FfnWorkload("llama3_8b_ffn_i14336_b16_bf16", 4096, 14336, 16, "bf16", 1e-6),
 ]}
 LLAMA2_FFN = "llama2_7b_ffn_i11008_b1_f16"
 LLAMA3_FFN = "llama3_8b_ffn_i14336_b2_bf16"
 TINY_FFN = "tiny_ffn_h256_i688_b1_f32"
+B64_FFN = "h2048_ffn_i5632_b64_f16"
+LLAMA3_FFN_B16 = "llama3_8b_ffn_i14336_b16_bf16"
 
 
 def custom_ffn(name: str = "custom_ffn", **kw) -> FfnWorkload:

@@ -408,6 +408,9 @@ def main(argv=None):
     info = blk.launch_info()
     step_fn = blk.unfused if args.unfused else blk
     kernels_per_layer = 3 if args.unfused else 1
+    # the FFN runs one kernel for 1-2 rows, a tensor-core pair for more
+    ffn_kernels = ffn_blk.kernels(w.batch)["kernels"] if ffn_blk is not None else 0
+    ffn_name = "cf_ffn_kernel" if ffn_kernels <= 1 else "cf_ffn_gu_kernel+cf_ffn_down_kernel"
     outs = [[torch.empty_like(L["hidden"]) for L in rep] for rep in reps]
 
     stream = torch.cuda.Stream(device=dev)
@@ -623,12 +626,12 @@ def main(argv=None):
             layer_kernels = {
                 kernel_name: {"us": round(attn_s * 1e6, 3), "bytes": per_launch_bytes,
                               "GBs": round(per_launch_bytes / attn_s / 1e9, 1)},
-                "cf_ffn_kernel": {"us": round(ffn_launch_s * 1e6, 3), "bytes": ffn_bytes(wf),
+                ffn_name: {"us": round(ffn_launch_s * 1e6, 3), "bytes": ffn_bytes(wf),
                                   "GBs": round(ffn_bytes(wf) / ffn_launch_s / 1e9, 1),
                                   "timing": "FFN-only graph replays / launches"},
             }
             if ffn_launch_s >= attn_s:
-                kernel_name, per_launch_bytes, traffic = "cf_ffn_kernel", ffn_bytes(wf), None
+                kernel_name, per_launch_bytes, traffic = ffn_name, ffn_bytes(wf), None
                 launch_s_timed = ffn_launch_s
                 launch_ms = ffn_ms
                 launch_ms_avg = sum(ffn_ms) / len(ffn_ms)
@@ -671,7 +674,8 @@ def main(argv=None):
                 "algorithmic_bytes_per_step": step_bytes,
                 "flops_per_step": (flops_per_step(w, pos0) + (ffn_flops(wf) if wf else 0))
                 * w.layers,
-                **({"ffn_intermediate": args.ffn, "ffn_launch": ffn_blk.launch_info()}
+                **({"ffn_intermediate": args.ffn,
+                    "ffn_launch": {**ffn_blk.launch_info(), **ffn_blk.kernels(w.batch)}}
                    if wf else {}),
                 "l2_defeat": (f"inputs larger than L2: {R} independently seeded replica(s) "
                               f"rotated, {footprint / 1e9:.2f} GB resident vs L2 "
@@ -701,7 +705,7 @@ def main(argv=None):
                     "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "cuda_graph": bool(e2e_graphs)},
-            "gpu_launches": args.steps * w.layers * (kernels_per_layer + (1 if wf else 0)),
+            "gpu_launches": args.steps * w.layers * (kernels_per_layer + ffn_kernels),
             **({"timeline_us": timeline} if timeline else {}),
             "clocks": clk.result(),
             "cpu_baseline": cpu,

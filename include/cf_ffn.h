@@ -11,7 +11,11 @@
  *           n   = h_b * g2 / sqrt(mean(h_b^2) + eps)
  *           a_i = silu(Wg[i,:] . n) * (Wu[i,:] . n),   silu(z) = z/(1+e^-z)
  *           out_b[j] = h_b[j] + sum_i a_i Wd[i, j]
- *         with all products accumulated in fp32.
+ *         with all products accumulated in fp32.  Batches of 1-2 rows run
+ *         one CUDA-core kernel; batches of 3-64 rows run a tensor-core pair
+ *         (tcgen05): gate/up, with a = silu(gate)*up kept as 16-bit hi + lo
+ *         values in the handle's workspace, then the down projection and the
+ *         residual (launched as a programmatic dependent of the first).
  *
  * Layouts (row-major, contiguous, device memory, every pointer 16-byte
  * aligned):
@@ -47,7 +51,9 @@ typedef struct cf_ffn_config {
   int32_t hidden;        /* H: multiple of 8, at most 4096                  */
   int32_t intermediate;  /* I >= 1, at most 128 units per SM (19456 on a
                             152-SM part)                                    */
-  int32_t max_batch;     /* upper bound on `batch`: 1 or 2                  */
+  int32_t max_batch;     /* upper bound on `batch`: 1..64; above 2 the
+                            storage dtype is 16-bit and hidden a multiple
+                            of 128                                          */
   float rms_eps;         /* eps of the second RMSNorm (inside the sqrt)     */
   int32_t dtype;         /* cf_dtype of every tensor                        */
   int32_t stage_bytes;   /* 0 = default, else bytes of weight rows per
@@ -58,8 +64,11 @@ typedef struct cf_ffn_handle cf_ffn_handle; /* opaque */
 
 /* Validate cfg, prepare the kernel and allocate the workspace on the current
  * device.  Errors: CF_ERR_INVALID_ARG (bad field), CF_ERR_UNSUPPORTED (H, I
- * or max_batch outside the compiled range), CF_ERR_CUDA.  Nothing is left
- * allocated on failure. */
+ * or max_batch outside the compiled range; max_batch above 2 with fp32
+ * storage or H not a multiple of 128), CF_ERR_CUDA.  Nothing is left
+ * allocated on failure.  The workspace holds the fp32 accumulator
+ * [max_batch, H] and, for max_batch above 2, a as 16-bit hi and lo arrays
+ * [max_batch, I rounded up to 8]. */
 int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out);
 
 /* out = hidden + FFN(RMSNorm(hidden; ln_weight)) for `batch` rows (0 <= batch
@@ -74,10 +83,15 @@ int cf_ffn_forward(cf_ffn_handle* h, int32_t batch, const void* hidden, const vo
  * stream); clears it.  CF_OK or CF_ERR_DEVICE_TIMEOUT. */
 int cf_ffn_get_status(cf_ffn_handle* h);
 
-/* Blocks per launch and rows per weight stage the handle uses (for tests and
- * the bench); any pointer may be NULL. */
+/* Blocks per launch and rows per weight stage the handle's one- and two-row
+ * kernel uses (for tests and the bench); any pointer may be NULL. */
 int cf_ffn_launch_info(const cf_ffn_handle* h, int32_t* blocks, int32_t* rows_per_stage,
                        int32_t* stages);
+
+/* Kernels a call of `batch` rows launches: returns 1 (the one- and two-row
+ * kernel, *blocks1 its grid, *blocks2 = 0) or 2 (the tensor-core pair, their
+ * grids), or CF_ERR_INVALID_ARG.  Either pointer may be NULL. */
+int cf_ffn_kernels(const cf_ffn_handle* h, int32_t batch, int32_t* blocks1, int32_t* blocks2);
 
 void cf_ffn_destroy(cf_ffn_handle* h); /* NULL-safe */
 

@@ -81,6 +81,84 @@ def test_scaled_shapes(shape):
     full_ffn_check(w, seed=3, stage_bytes=sb)
 
 
+# batched decode on the tensor-core pair: dtype, H, I, max_batch, batch
+TC_SHAPES = [
+    ("f16", 2048, 5632, 64, 64),    # the 64-row layer's FFN
+    ("bf16", 4096, 14336, 16, 16),  # the Llama-3 layer's FFN at 16 rows
+    ("f16", 1024, 777, 16, 3),      # 3 rows (smallest batch of the pair), ragged I
+    ("bf16", 512, 152, 32, 21),     # one unit per block, 21 of 32 rows
+    ("f16", 384, 4000, 64, 40),     # H of three column tiles, UB 32
+    ("bf16", 4096, 100, 16, 9),     # fewer units than SMs, more columns than units
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES,
+                         ids=lambda s: f"{s[0]}-H{s[1]}-I{s[2]}-M{s[3]}-B{s[4]}")
+def test_tensor_core_pair_scaled_shapes(shape):
+    dt, H, I, M, B = shape
+    w = synth.custom_ffn(name="ffn_tc", hidden=H, intermediate=I, batch=B, dtype=dt)
+    t = synth.make_ffn(w, 11, device="cuda")
+    blk = binding.FfnBlock(H, I, M, w.rms_eps, dt)
+    assert blk.kernels(B)["kernels"] == 2 and blk.kernels(2)["kernels"] == 1
+    out, st = run_ffn(w, t, blk)
+    assert st == binding.CF_OK
+    rows = sorted({0, B // 2, B - 1})
+    ref = oracle_ffn(w, t, rows)
+    got = out[rows].double().cpu().numpy()
+    want = round_to(ref["out"], w.dtype)
+    check(got, want, "out")
+    x = synth.to_f64(t["hidden"][rows])
+    check(got - x, want - x, "out - hidden")
+
+
+def test_tensor_core_pair_small_batches_and_repeats_on_one_handle():
+    """One handle of max_batch 64 serves 1, 2 (the CUDA-core kernel), 3, 17
+    and 64 rows (the pair), in any order, leaving its workspace clean."""
+    w64 = synth.FFN_WORKLOADS[synth.B64_FFN]
+    t = synth.make_ffn(w64, 12, device="cuda")
+    blk = make_ffn_block(w64)
+    firsts = {}
+    for B in (64, 3, 1, 17, 2, 64, 3):
+        out = torch.full_like(t["hidden"], float("nan"))
+        blk(B, t["hidden"], t["ln_weight"], t["w_gate"], t["w_up"], t["w_down"], out)
+        assert blk.status() == binding.CF_OK
+        assert torch.isnan(out[B:]).all()
+        if B in firsts:
+            check(out[:B].double().cpu().numpy(), firsts[B], f"repeat B={B}", mean_rel=1e-5)
+            continue
+        firsts[B] = out[:B].double().cpu().numpy()
+        rows = sorted({0, B - 1})
+        ref = oracle_ffn(w64, t, rows)
+        check(out[rows].double().cpu().numpy(), round_to(ref["out"], w64.dtype), f"out B={B}")
+
+
+def test_tensor_core_pair_zero_down_projection_returns_hidden_bit_exact():
+    w = synth.custom_ffn(name="ffn_tc0", hidden=1024, intermediate=3000, batch=32, dtype="bf16")
+    t = synth.make_ffn(w, 13, device="cuda")
+    t["w_down"].zero_()
+    out, st = run_ffn(w, t, make_ffn_block(w))
+    assert st == binding.CF_OK and torch.equal(out, t["hidden"])
+
+
+def test_tensor_core_pair_graph_replay():
+    w = synth.FFN_WORKLOADS[synth.LLAMA3_FFN_B16]
+    t = synth.make_ffn(w, 14, device="cuda")
+    blk = make_ffn_block(w)
+    first, st = run_ffn(w, t, blk)
+    assert st == binding.CF_OK
+    out = torch.empty_like(t["hidden"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        blk(w.batch, t["hidden"], t["ln_weight"], t["w_gate"], t["w_up"], t["w_down"], out, s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert blk.status() == binding.CF_OK
+    check(out.double().cpu().numpy(), first.double().cpu().numpy(), "graph", mean_rel=1e-5)
+
+
 def test_zero_down_projection_returns_hidden_bit_exact_and_batch_below_max():
     w = synth.custom_ffn(name="ffn0", hidden=2048, intermediate=3000, batch=2, dtype="bf16")
     t = synth.make_ffn(w, 1, device="cuda")
@@ -126,7 +204,8 @@ def test_argument_errors():
     assert binding.cf_ffn_forward(blk.handle, 2, *args, t["w_up"]) == binding.CF_ERR_ALIAS
     bad = [t["hidden"].data_ptr() + 2] + args[1:]
     assert binding.cf_ffn_forward(blk.handle, 2, *bad, out) == binding.CF_ERR_INVALID_ARG
-    for cfg in (dict(hidden=4100), dict(hidden=8192), dict(max_batch=3), dict(intermediate=0)):
+    for cfg in (dict(hidden=4100), dict(hidden=8192), dict(max_batch=65), dict(intermediate=0),
+                dict(max_batch=3, dtype=binding.CF_F32), dict(max_batch=3, hidden=320)):
         base = dict(hidden=256, intermediate=64, max_batch=1, rms_eps=1e-6, dtype=binding.CF_F16,
                     stage_bytes=0)
         base.update(cfg)
