@@ -409,8 +409,11 @@ struct cf_ffn_handle {
   int blocks2 = 0, S = 0, nsl2 = 0, stages2 = 0, stage2_bytes = 0, smem2 = 0;
   void* a_hi = nullptr;
   void* a_lo = nullptr;
-  TmapSlot m_wg, m_wu, m_wd, m_h;
-  CUtensorMap m_ahi, m_alo;
+  void* n = nullptr;      // [2 * BP, H] 16-bit: h * g2 as hi rows, then lo rows
+  float* ssq = nullptr;   // [BP] rows' sums of squares
+  int* grid = nullptr;    // kernel 1's grid barrier: [0] arrivals, [1] generation
+  TmapSlot m_wg, m_wu, m_wd;
+  CUtensorMap m_ahi, m_alo, m_n;
 };
 
 namespace {
@@ -428,11 +431,11 @@ bool plan_ffn_tc(cf_ffn_handle* h, int sms, int budget) {
   const int umax = (I + h->blocks1 - 1) / h->blocks1;
   h->UB = (umax + 7) / 8 * 8;
   if (h->UB > 128) return false;
-  const int slab1 = (2 * h->UB + BP) * 128;
-  int extras1 = 2 * N5 * 128 + (2 * kFfnTcMaxStages + 2) * 8 + (kConsumerWarps * BP + BP) * 4 + 16;
-  // the M = 128 operand reads of a slab's boxes run up to 16 KB past the
-  // box start: keep that much shared memory after the ring
-  extras1 = std::max(extras1, 16384 - (h->UB + BP) * 128);
+  const int slab1 = (2 * h->UB + N5) * 128;  // gate box | up box | n box
+  int extras1 = (2 * kFfnTcMaxStages + 1) * 8 + BP * 4 + 16;  // barriers, rinv, TMEM word
+  // the M = 128 operand reads of a slab's gate and up boxes run up to 16 KB
+  // past the box start: keep that much shared memory after the ring
+  extras1 = std::max(extras1, 16384 - (h->UB + N5) * 128);
   extras1 = (extras1 + 1023) / 1024 * 1024;
   h->nsl1 = std::max(1, std::min(H / 64, 65536 / slab1));
   for (;; --h->nsl1) {
@@ -536,9 +539,12 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
     delete h;
     return CF_ERR_UNSUPPORTED;
   }
+  // workspace: acc | 512-byte control block (counters [32], errflag, grid
+  // barrier [2], row sums [64] from byte 256) | a_hi | a_lo | n
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
   const size_t a_bytes = h->tc ? (size_t)c.max_batch * h->Ip * 2 : 0;
-  const size_t total = acc_bytes + 256 + 2 * a_bytes;
+  const size_t n_bytes = h->tc ? (size_t)2 * h->BP * c.hidden * 2 : 0;
+  const size_t total = acc_bytes + 512 + 2 * a_bytes + n_bytes;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -553,8 +559,17 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
   h->counter = reinterpret_cast<int*>(static_cast<char*>(h->ws) + acc_bytes);  // [32]
   h->errflag = h->counter + 32;
   if (h->tc) {
-    h->a_hi = static_cast<char*>(h->ws) + acc_bytes + 256;
+    h->grid = h->errflag + 1;
+    h->ssq = reinterpret_cast<float*>(static_cast<char*>(h->ws) + acc_bytes + 256);
+    h->a_hi = static_cast<char*>(h->ws) + acc_bytes + 512;
     h->a_lo = static_cast<char*>(h->a_hi) + a_bytes;
+    h->n = static_cast<char*>(h->a_lo) + a_bytes;
+    if (!encode_tmap_2d(&h->m_n, c.dtype, h->n, c.hidden, 2 * h->BP, (uint64_t)c.hidden * 2, 64,
+                        2 * h->BP, true)) {
+      cudaFree(h->ws);
+      delete h;
+      return CF_ERR_CUDA;
+    }
     if (!encode_tmap_2d(&h->m_ahi, c.dtype, h->a_hi, c.intermediate, c.max_batch, h->Ip * 2, 64,
                         h->BP, true) ||
         !encode_tmap_2d(&h->m_alo, c.dtype, h->a_lo, c.intermediate, c.max_batch, h->Ip * 2, 64,
@@ -580,13 +595,16 @@ int ffn_forward_tc(cf_ffn_handle* h, int batch, const void* hidden, const void* 
   const CUtensorMap* mg = cached_map(h->m_wg, c.dtype, w_gate, H, I, h->UB);
   const CUtensorMap* mu = cached_map(h->m_wu, c.dtype, w_up, H, I, h->UB);
   const CUtensorMap* md = cached_map(h->m_wd, c.dtype, w_down, H, I, 64);
-  const CUtensorMap* mh = cached_map(h->m_h, c.dtype, hidden, H, (uint64_t)batch, h->BP);
-  if (!mg || !mu || !md || !mh) return CF_ERR_CUDA;
+  if (!mg || !mu || !md) return CF_ERR_CUDA;
   FfnTcParams p;
   std::memset(&p, 0, sizeof(p));
   p.tm_wg = *mg;
   p.tm_wu = *mu;
-  p.tm_h = *mh;
+  p.tm_n = h->m_n;
+  p.n = h->n;
+  p.ssq = h->ssq;
+  p.grid_count = h->grid;
+  p.grid_gen = h->grid + 1;
   p.tm_wd = *md;
   p.tm_ahi = h->m_ahi;
   p.tm_alo = h->m_alo;

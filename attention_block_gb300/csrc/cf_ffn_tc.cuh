@@ -49,12 +49,16 @@ constexpr int kFfnTcMaxStages = 8;
 struct FfnTcParams {
   CUtensorMap tm_wg;   // W_gate [I, H], box {64, UB}, 128-byte swizzle
   CUtensorMap tm_wu;   // W_up   [I, H], box {64, UB}
-  CUtensorMap tm_h;    // hidden [B, H], box {64, BP}
+  CUtensorMap tm_n;    // n [2*BP, H] (h * g2 as hi rows, then lo rows), box {64, 2*BP}
   CUtensorMap tm_wd;   // W_down [I, H], box {64, 64}
   CUtensorMap tm_ahi;  // a hi   [B, I], box {64, BP}
   CUtensorMap tm_alo;  // a lo   [B, I], box {64, BP}
   const void* h;       // hidden [B, H] (residual)
   const void* g2;      // ln_weight [H]
+  void* n;             // [2*BP, H] 16-bit
+  float* ssq;          // [BP] rows' sums of squares, zero between calls
+  int* grid_count;     // arrivals at kernel 1's grid barrier, zero between calls
+  int* grid_gen;       // generations of that barrier (only ever increases)
   void* a_hi;          // [B, Ip] 16-bit
   void* a_lo;          // [B, Ip] 16-bit
   void* out;           // [B, H]
@@ -70,6 +74,30 @@ struct FfnTcParams {
   float eps;
 };
 
+// Bounded wait until the grid-barrier generation differs from `gen0` (every
+// block of this fully resident grid has arrived).  On expiry it records
+// kDevErrTimeout and returns false.
+static __device__ __noinline__ bool wait_generation(const int* gen, int gen0, int* errflag) {
+  const long long t0 = clock64();
+  for (uint32_t spins = 1;; ++spins) {
+    if (*reinterpret_cast<const volatile int*>(gen) != gen0) return true;
+    if ((spins & 255u) == 0) {
+      if (*reinterpret_cast<volatile int*>(errflag) & kDevErrTimeout) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        atomicOr(errflag, kDevErrTimeout);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
+// Orders global writes this thread has observed (by the generic proxy) before
+// its later bulk-tensor (async proxy) reads of them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // 16-bit hi + lo split of one fp32 value (hi = round(v), lo = round(v - hi)).
 template <typename T>
 __device__ __forceinline__ void split1(float v, T& hi, T& lo) {
@@ -83,20 +111,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     cf_ffn_gu_kernel(const __grid_constant__ FfnTcParams p) {
   constexpr int N5 = 2 * BP;
   constexpr int TCOLS = tmem_cols_for(2 * N5);  // gate and up accumulators
-  constexpr int NRW = BP / kConsumerWarps;      // rows per warp while staging
   using MK = MmaKind<T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const int slab1 = (2 * p.UB + BP) * 128;  // gate box | up box | h box
+  const int slab1 = (2 * p.UB + N5) * 128;  // gate box | up box | n box
   uint8_t* ring = sm;
-  uint8_t* nbuf = ring + (size_t)p.stages1 * p.stage1_bytes;  // [2][N5 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(nbuf + 2 * N5 * 128);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)p.stages1 * p.stage1_bytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kFfnTcMaxStages;
-  uint64_t* nbar = bars + 2 * kFfnTcMaxStages;  // [2] n buffer free again
-  float* ssq = reinterpret_cast<float*>(bars + 2 * kFfnTcMaxStages + 2);  // [8][BP]
-  float* rinv = ssq + kConsumerWarps * BP;                                // [BP]
+  uint64_t* done = bars + 2 * kFfnTcMaxStages;
+  float* rinv = reinterpret_cast<float*>(bars + 2 * kFfnTcMaxStages + 1);  // [BP]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(rinv + BP);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -105,14 +130,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i1 = (int)((long long)(blockIdx.x + 1) * p.I / G);
   const int nslab = p.H / 64;
   const int nst = (nslab + p.nsl1 - 1) / p.nsl1;  // stages of the stream
+  // generation of the grid barrier before this launch arrives (it only
+  // advances once every block of this launch has arrived)
+  const int gen0 = *reinterpret_cast<volatile int*>(p.grid_gen);
 
   if (tid == 0) {
     for (int s = 0; s < p.stages1; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    mbar_init(&nbar[0], 1);
-    mbar_init(&nbar[1], 1);
+    mbar_init(done, 1);
     fence_mbar_init_cluster();
   }
   if (warp == 0) {
@@ -129,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&p.tm_wg);
       prefetch_tensormap(&p.tm_wu);
-      prefetch_tensormap(&p.tm_h);
-      const uint64_t pol_w = policy_evict_first(), pol_h = policy_evict_normal();
+      prefetch_tensormap(&p.tm_n);
+      const uint64_t pol_w = policy_evict_first(), pol_n = policy_evict_normal();
       auto stage_slabs = [&](int st) { return min(p.nsl1, nslab - st * p.nsl1); };
       auto load_w = [&](int st) {
         uint8_t* base = ring + (size_t)(st % p.stages1) * p.stage1_bytes;
@@ -141,98 +168,124 @@ __global__ void __launch_bounds__(kThreads, 1)
                       pol_w);
         }
       };
-      auto load_h = [&](int st) {
+      auto load_n = [&](int st) {
         uint8_t* base = ring + (size_t)(st % p.stages1) * p.stage1_bytes;
         for (int j = 0; j < stage_slabs(st); ++j)
-          tma_load_2d(base + j * slab1 + 2 * p.UB * 128, &p.tm_h, (st * p.nsl1 + j) * 64, 0,
-                      &full[st % p.stages1], pol_h);
+          tma_load_2d(base + j * slab1 + 2 * p.UB * 128, &p.tm_n, (st * p.nsl1 + j) * 64, 0,
+                      &full[st % p.stages1], pol_n);
       };
-      // The weights do not depend on the previous kernel: the first stages'
-      // weight boxes go out before the dependency wait, their h boxes after.
+      // The weights need nothing from this launch or the previous kernel:
+      // the first stages' weight boxes go out at once, their n boxes after
+      // the grid barrier that publishes n.
       const int fill = min(p.stages1, nst);
       for (int st = 0; st < fill; ++st) {
         mbar_arrive_expect_tx(&full[st], (uint32_t)(stage_slabs(st) * slab1));
         load_w(st);
       }
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      for (int st = 0; st < fill; ++st) load_h(st);
+      wait_generation(p.grid_gen, gen0, p.errflag);
+      fence_proxy_async_global();  // n was written by other blocks' threads
+      for (int st = 0; st < fill; ++st) load_n(st);
       for (int st = fill; st < nst; ++st) {
         const int s = st % p.stages1;
         mbar_wait(&empty[s], ((st / p.stages1) + 1) & 1, p.errflag);
         mbar_arrive_expect_tx(&full[s], (uint32_t)(stage_slabs(st) * slab1));
         load_w(st);
-        load_h(st);
+        load_n(st);
       }
     }
     __syncwarp();
   } else {
     // ================================================ consumers ========
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // a is read by the previous call
-    const T* __restrict__ g2 = static_cast<const T*>(p.g2);
-    const uint32_t tmem = *s_tmem;
-    const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, false);
-    float ss[NRW];
+    // h comes from the previous kernel; n, a and the row sums are reused
+    // across calls, so nothing is written before this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // ---- Phase 0: this block's columns of n = h * g2 as 16-bit hi rows
+    // 0..BP-1 and lo rows BP..2BP-1 of n [2*BP, H], and the rows' sums of
+    // squares over them [LNA §三 stage 1] -------------------------------------
+    {
+      const T* __restrict__ hid = static_cast<const T*>(p.h);
+      const T* __restrict__ g2 = static_cast<const T*>(p.g2);
+      T* n = static_cast<T*>(p.n);
+      const int H8 = p.H / 8;
+      const int c0 = (int)((long long)blockIdx.x * H8 / G), c1 = (int)((long long)(blockIdx.x + 1) * H8 / G);
+      float ssl[BP / kConsumerWarps];
 #pragma unroll
-    for (int i = 0; i < NRW; ++i) ss[i] = 0.f;
-    for (int j = 0; j < nslab; ++j) {
-      const int st = j / p.nsl1, within = j % p.nsl1, s = st % p.stages1;
-      uint8_t* sl = ring + (size_t)s * p.stage1_bytes + within * slab1;
-      if (within == 0) mbar_wait(&full[s], (st / p.stages1) & 1, p.errflag);
-      uint8_t* nb = nbuf + (j & 1) * (N5 * 128);
-      if (j >= 2) mbar_wait(&nbar[j & 1], ((j - 2) >> 1) & 1, p.errflag);
-      // h * g2 of the slab's 64 columns as hi rows 0..BP-1 and lo rows
-      // BP..2BP-1 of a K-major swizzled slab; warp w takes rows w, w + 8, ...
-      {
-        const uint8_t* hb = sl + 2 * p.UB * 128;  // [BP rows][128 B], swizzled by TMA
-        const int k = 2 * lane, jc = k >> 3, e2 = (k & 7) * 2;
-        float gw[2];
-        load_cvt<T, 2>(g2 + j * 64 + k, gw);
+      for (int i = 0; i < BP / kConsumerWarps; ++i) ssl[i] = 0.f;
+      // warp w: rows w, w + 8, ...; lanes over 8-element column groups
+      for (int c = c0 + lane; c < c1; c += 32) {
+        float g[8];
+        load_cvt<T, 8>(g2 + 8 * c, g);
 #pragma unroll
-        for (int i = 0; i < NRW; ++i) {
-          const int row = warp + i * kConsumerWarps;
-          float f[2];
-          load_cvt<T, 2>(reinterpret_cast<const T*>(hb + row * 128 + ((jc ^ (row & 7)) << 4) + e2),
-                         f);
-          ss[i] = fmaf(f[0], f[0], fmaf(f[1], f[1], ss[i]));
-          uint32_t hi, lo;
-          MK::split2(f[0] * gw[0], f[1] * gw[1], hi, lo);
-          const int rl = BP + row;
-          *reinterpret_cast<uint32_t*>(nb + row * 128 + ((jc ^ (row & 7)) << 4) + e2) = hi;
-          *reinterpret_cast<uint32_t*>(nb + rl * 128 + ((jc ^ (rl & 7)) << 4) + e2) = lo;
+        for (int i = 0; i < BP / kConsumerWarps; ++i) {
+          const int b = warp + i * kConsumerWarps;
+          float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (b < p.B) load_cvt<T, 8>(hid + (size_t)b * p.H + 8 * c, x);
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ssl[i] = fmaf(x[2 * e], x[2 * e], fmaf(x[2 * e + 1], x[2 * e + 1], ssl[i]));
+            MK::split2(x[2 * e] * g[2 * e], x[2 * e + 1] * g[2 * e + 1], hi[e], lo[e]);
+          }
+          *reinterpret_cast<uint4*>(n + (size_t)b * p.H + 8 * c) =
+              make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(n + (size_t)(BP + b) * p.H + 8 * c) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
-      fence_proxy_async_smem();
+#pragma unroll
+      for (int i = 0; i < BP / kConsumerWarps; ++i) {
+        const float v = warp_sum(ssl[i]);
+        const int b = warp + i * kConsumerWarps;
+        if (lane == 0 && b < p.B && v != 0.f) atomicAdd(p.ssq + b, v);
+      }
+      // grid barrier: every block's n columns and row sums are published
+      __threadfence();
       named_sync(kBarConsumers, kConsumers);
       if (tid == 0) {
-        tc05_fence_after();
-        const uint32_t ag = smem_u32(sl), au = smem_u32(sl + p.UB * 128), bn = smem_u32(nb);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = smem_desc_k_sw128(bn + ks * 32u, 1024);
-          tc05_mma_f16(tmem, smem_desc_k_sw128(ag + ks * 32u, 1024), bd, idesc, j > 0 || ks > 0);
-          tc05_mma_f16(tmem + (uint32_t)N5, smem_desc_k_sw128(au + ks * 32u, 1024), bd, idesc,
-                       j > 0 || ks > 0);
+        if (atomicAdd(p.grid_count, 1) == G - 1) {
+          *reinterpret_cast<volatile int*>(p.grid_count) = 0;
+          __threadfence();
+          atomicAdd(p.grid_gen, 1);
+        } else {
+          wait_generation(p.grid_gen, gen0, p.errflag);
         }
-        tc05_commit(&nbar[j & 1]);
-        if (within == p.nsl1 - 1 || j == nslab - 1) {
-          mbar_arrive_cnt(&empty[s], kConsumerWarps - 1);
-          tc05_commit(&empty[s]);
-        }
+        __threadfence();
       }
-      __syncwarp();
+      named_sync(kBarConsumers, kConsumers);
     }
-    // the last slab's commit covers every MMA
-    mbar_wait(&nbar[(nslab - 1) & 1], ((nslab - 1) >> 1) & 1, p.errflag);
-    tc05_fence_after();
-    // RMSNorm scale of every row [LNA §三 stage 1]
+    if (tid < BP)
+      rinv[tid] = tid < p.B ? 1.0f / sqrtf(__ldcg(p.ssq + tid) / (float)p.H + p.eps) : 0.f;
+    // ---- gate and up: one thread issues each stage's MMAs as it lands ----
+    const uint32_t tmem = *s_tmem;
+    const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, false);
+    if (tid == 0) {
+      for (int st = 0; st < nst; ++st) {
+        const int s = st % p.stages1;
+        mbar_wait(&full[s], (st / p.stages1) & 1, p.errflag);
+        tc05_fence_after();
+        const int ns = min(p.nsl1, nslab - st * p.nsl1);
+        uint8_t* base = ring + (size_t)s * p.stage1_bytes;
+        for (int j = 0; j < ns; ++j) {
+          const uint32_t ag = smem_u32(base + j * slab1), au = ag + (uint32_t)p.UB * 128u;
+          const uint32_t bn = ag + 2u * (uint32_t)p.UB * 128u;
 #pragma unroll
-    for (int i = 0; i < NRW; ++i) {
-      const float v = warp_sum(ss[i]);
-      if (lane == 0) ssq[warp + i * kConsumerWarps] = v;
+          for (int ks = 0; ks < 4; ++ks) {
+            const bool acc = st > 0 || j > 0 || ks > 0;
+            const uint64_t bd = smem_desc_k_sw128(bn + ks * 32u, 1024);
+            tc05_mma_f16(tmem, smem_desc_k_sw128(ag + ks * 32u, 1024), bd, idesc, acc);
+            tc05_mma_f16(tmem + (uint32_t)N5, smem_desc_k_sw128(au + ks * 32u, 1024), bd, idesc,
+                         acc);
+          }
+        }
+        mbar_arrive_cnt(&empty[s], kConsumerWarps - 1);
+        tc05_commit(&empty[s]);
+      }
+      tc05_commit(done);
     }
-    named_sync(kBarConsumers, kConsumers);
-    if (tid < BP) rinv[tid] = 1.0f / sqrtf(ssq[tid] / (float)p.H + p.eps);
-    named_sync(kBarConsumers, kConsumers);
+    __syncwarp();
+    named_sync(kBarConsumers, kConsumers);  // rinv
+    mbar_wait(done, 0, p.errflag);
+    tc05_fence_after();
     // a = silu(gate) * up: warp w reads units 32 (w % 4) + lane (its TMEM
     // lane quarter) for rows [h * BP/2, (h+1) * BP/2), h = w / 4
     T* ahi = static_cast<T*>(p.a_hi);
@@ -363,6 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================ consumers ========
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // kernel 1 of this call is complete: clear its row sums for the next call
+    if (blockIdx.x == 0 && tid < BP) p.ssq[tid] = 0.f;
     const uint32_t tmem = *s_tmem;
     const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, true);
     if (tid == 0) {
