@@ -17,7 +17,6 @@
 #include "cf_params.h"
 #include "cf_registry.h"
 #include "cf_test.h"
-#include "cf_tmap.h"
 #include "cf_unfused.h"
 
 using namespace cf;
@@ -359,20 +358,6 @@ bool encode(CUtensorMap* m, int dtype, int rank, const void* base, const uint64_
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
-
-}  // namespace
-
-bool cf::encode_tmap_2d(CUtensorMap* m, int dtype, const void* base, uint64_t inner,
-                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                        uint32_t box_outer, bool swizzle128) {
-  if (!get_encode()) return false;
-  const uint64_t dims[2] = {inner, outer};
-  const uint64_t str[1] = {row_bytes};
-  const uint32_t box[2] = {box_inner, box_outer};
-  return encode(m, dtype, 2, base, dims, str, box, swizzle128);
-}
-
-namespace {
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;

@@ -1,5 +1,5 @@
-// cf_tmap.h -- internal: 2D TMA tensor-map encoding shared by the host files
-// of the library (implemented in cf_api.cu).
+// cf_tmap.h -- internal: 2D TMA tensor-map encoding for the FFN's host code
+// (implemented in cf_tmap.cu).
 #pragma once
 
 #include <cuda.h>
