@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const T* __restrict__ g2 = static_cast<const T*>(p.g2);
       T* n = static_cast<T*>(p.n);
       const int H8 = p.H / 8;
-      const int c0 = (int)((long long)blockIdx.x * H8 / G), c1 = (int)((long long)(blockIdx.x + 1) * H8 / G);
+      const int c0 = (int)((long long)blockIdx.x * H8 / G);
+      const int c1 = (int)((long long)(blockIdx.x + 1) * H8 / G);
       float ssl[BP / kConsumerWarps];
 #pragma unroll
       for (int i = 0; i < BP / kConsumerWarps; ++i) ssl[i] = 0.f;
@@ -428,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ns = min(p.nsl2, nslab - st * p.nsl2);
         uint8_t* base = ring + (size_t)s * p.stage2_bytes;
         for (int j = 0; j < ns; ++j) {
-          const uint32_t aw = smem_u32(base + j * kSlab), ba = smem_u32(base + j * kSlab + 2 * kWBox);
+          const uint32_t aw = smem_u32(base + j * kSlab);
+          const uint32_t ba = smem_u32(base + j * kSlab + 2 * kWBox);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             tc05_mma_f16(tmem, smem_desc_mn_sw128(aw + ks * 2048u, kWBox, 1024),
