@@ -346,6 +346,9 @@ def main(argv=None):
                     help="time the three-kernel path with HBM intermediates (the fusion "
                          "baseline) instead of the fused kernel")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=0.0,
+                    help="--impl reference: seconds of oracle work per step (0 = the run's "
+                         "~150 s spread over its steps)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -734,7 +737,8 @@ def run_reference(args, w, rank, world):
                               batch=w.batch, dtype=w.dtype, rms_eps=w.rms_eps)
         layer["ffn"] = synth.make_ffn(wf, seed=1000, device="cpu")
         step_bytes += ffn_bytes(wf) * w.layers
-    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    budget = (args.ref_budget if args.ref_budget > 0
+              else max(1.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(w, layer, 0.0, max_steps=1, wf=wf)
     times, rows_total = [], 0

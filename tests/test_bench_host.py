@@ -69,3 +69,27 @@ def test_two_rank_gather_and_aggregate_over_gloo():
     for rank, rows, agg in res:
         assert rows == [[1e9, 1.0, 5.0], [2e9, 2.0, 5.0]]
         assert agg["seconds"] == 2.0 and agg["gbs"] == pytest.approx(1.5)
+
+
+def test_reference_arm_prints_the_contract_line_on_the_host():
+    """`bench.py --impl reference` (the float64 oracle on the host cores) needs
+    no GPU: one short run on the tiny workload prints one JSON line with the
+    contract's keys and a positive value."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_h256_mha4x64_b1_p128_f32", "--steps", "2",
+                        "--warmup", "3", "--ref-budget", "0.2"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "tiny_h256_mha4x64_b1_p128_f32"
