@@ -88,6 +88,7 @@ SIGNATURES = {
     "cf_ffn_launch_info": (ctypes.c_int, [_vp] + [ctypes.POINTER(ctypes.c_int32)] * 3),
     "cf_ffn_destroy": (None, [_vp]),
     "cf_ffn_kernels": (ctypes.c_int, [_vp, ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 2),
+    "cf_ffn_set_timeline": (ctypes.c_int, [_vp, _vp]),
     "cf_bench_contig_stream": (ctypes.c_int, [_vp, ctypes.c_longlong, ctypes.c_longlong] + [ctypes.c_int] * 5 + [_vp, _vp]),
     "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
                                      + [_vp] * 9),

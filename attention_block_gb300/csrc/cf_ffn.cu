@@ -410,9 +410,10 @@ struct cf_ffn_handle {
   void* a_hi = nullptr;
   void* a_lo = nullptr;
   void* n = nullptr;      // [2 * BP, H] 16-bit: h * g2 as hi rows, then lo rows
-  float* ssq = nullptr;   // [BP] rows' sums of squares
+  float* ssq = nullptr;   // [8][BP] rows' sums of squares (copies)
   int* grid = nullptr;    // kernel 1's grid barrier: [0] arrivals, [1] generation
   TmapSlot m_wg, m_wu, m_wd;
+  unsigned long long* timeline = nullptr;  // optional stamps of kernel 1
   CUtensorMap m_ahi, m_alo, m_n;
 };
 
@@ -540,11 +541,12 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
     return CF_ERR_UNSUPPORTED;
   }
   // workspace: acc | 512-byte control block (counters [32], errflag, grid
-  // barrier [2], row sums [64] from byte 256) | a_hi | a_lo | n
+  // barrier [2]) | row sums [8][64] | a_hi | a_lo | n
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
   const size_t a_bytes = h->tc ? (size_t)c.max_batch * h->Ip * 2 : 0;
   const size_t n_bytes = h->tc ? (size_t)2 * h->BP * c.hidden * 2 : 0;
-  const size_t total = acc_bytes + 512 + 2 * a_bytes + n_bytes;
+  const size_t ssq_bytes = (size_t)kFfnSsqCopies * 64 * sizeof(float);
+  const size_t total = acc_bytes + 512 + ssq_bytes + 2 * a_bytes + n_bytes;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -560,8 +562,8 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
   h->errflag = h->counter + 32;
   if (h->tc) {
     h->grid = h->errflag + 1;
-    h->ssq = reinterpret_cast<float*>(static_cast<char*>(h->ws) + acc_bytes + 256);
-    h->a_hi = static_cast<char*>(h->ws) + acc_bytes + 512;
+    h->ssq = reinterpret_cast<float*>(static_cast<char*>(h->ws) + acc_bytes + 512);
+    h->a_hi = static_cast<char*>(h->ws) + acc_bytes + 512 + ssq_bytes;
     h->a_lo = static_cast<char*>(h->a_hi) + a_bytes;
     h->n = static_cast<char*>(h->a_lo) + a_bytes;
     if (!encode_tmap_2d(&h->m_n, c.dtype, h->n, c.hidden, 2 * h->BP, (uint64_t)c.hidden * 2, 64,
@@ -629,6 +631,7 @@ int ffn_forward_tc(cf_ffn_handle* h, int batch, const void* hidden, const void* 
   p.stages2 = h->stages2;
   p.stage2_bytes = h->stage2_bytes;
   p.eps = c.rms_eps;
+  p.timeline = h->timeline;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -723,6 +726,12 @@ extern "C" int cf_ffn_launch_info(const cf_ffn_handle* h, int32_t* blocks, int32
   if (blocks) *blocks = h->blocks;
   if (rows_per_stage) *rows_per_stage = h->R;
   if (stages) *stages = h->stages;
+  return CF_OK;
+}
+
+extern "C" int cf_ffn_set_timeline(cf_ffn_handle* h, unsigned long long* stamps) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  h->timeline = stamps;
   return CF_OK;
 }
 

@@ -45,6 +45,9 @@
 namespace cf {
 
 constexpr int kFfnTcMaxStages = 8;
+// Copies of the rows' sums of squares that kernel 1's blocks add into (block
+// k into copy k % 8), so no word takes more than ~1/8 of the blocks' atomics.
+constexpr int kFfnSsqCopies = 8;
 
 struct FfnTcParams {
   CUtensorMap tm_wg;   // W_gate [I, H], box {64, UB}, 128-byte swizzle
@@ -56,7 +59,7 @@ struct FfnTcParams {
   const void* h;       // hidden [B, H] (residual)
   const void* g2;      // ln_weight [H]
   void* n;             // [2*BP, H] 16-bit
-  float* ssq;          // [BP] rows' sums of squares, zero between calls
+  float* ssq;          // [kFfnSsqCopies][BP] rows' sums of squares, zero between calls
   int* grid_count;     // arrivals at kernel 1's grid barrier, zero between calls
   int* grid_gen;       // generations of that barrier (only ever increases)
   void* a_hi;          // [B, Ip] 16-bit
@@ -72,7 +75,15 @@ struct FfnTcParams {
   int S;               // kernel 2: splits of the units
   int nsl2, stages2, stage2_bytes;  // kernel 2: 64-unit slabs per stage, ring
   float eps;
+  unsigned long long* timeline;  // optional [grid][kFfnTlSlots] globaltimer stamps of
+                                 // kernel 1 (NULL = off)
 };
+
+// Stamps of kernel 1's optional timeline (per block): start, the consumers'
+// dependency wait done, phase 0 done, grid barrier passed, stage st landed at
+// the issuer (slot 4 + st, st < 48), every MMA complete, epilogue done.
+constexpr int kFfnTlSlots = 56;
+constexpr int kFfnTlMaxStages = 48;
 
 // Bounded wait until the grid-barrier generation differs from `gen0` (every
 // block of this fully resident grid has arrived).  On expiry it records
@@ -134,6 +145,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // advances once every block of this launch has arrived)
   const int gen0 = *reinterpret_cast<volatile int*>(p.grid_gen);
 
+  auto stamp = [&](int slot) {
+    if (p.timeline != nullptr && tid == 0)
+      p.timeline[(size_t)blockIdx.x * kFfnTlSlots + slot] = globaltimer_ns();
+  };
+  stamp(0);
   if (tid == 0) {
     for (int s = 0; s < p.stages1; ++s) {
       mbar_init(&full[s], 1);
@@ -199,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // h comes from the previous kernel; n, a and the row sums are reused
     // across calls, so nothing is written before this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    stamp(1);
     // ---- Phase 0: this block's columns of n = h * g2 as 16-bit hi rows
     // 0..BP-1 and lo rows BP..2BP-1 of n [2*BP, H], and the rows' sums of
     // squares over them [LNA §三 stage 1] -------------------------------------
@@ -208,40 +225,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       T* n = static_cast<T*>(p.n);
       const int H8 = p.H / 8;
       const int c0 = (int)((long long)blockIdx.x * H8 / G);
-      const int c1 = (int)((long long)(blockIdx.x + 1) * H8 / G);
-      float ssl[BP / kConsumerWarps];
-#pragma unroll
-      for (int i = 0; i < BP / kConsumerWarps; ++i) ssl[i] = 0.f;
-      // warp w: rows w, w + 8, ...; lanes over 8-element column groups
-      for (int c = c0 + lane; c < c1; c += 32) {
-        float g[8];
+      const int nc = (int)((long long)(blockIdx.x + 1) * H8 / G) - c0;
+      // the block's (row, 8-column group) items spread over all consumer
+      // threads, so their loads are in flight together; the rows' sums of
+      // squares meet in shared memory (rinv holds them until the barrier)
+      if (tid < BP) rinv[tid] = 0.f;
+      named_sync(kBarConsumers, kConsumers);
+      for (int item = tid; item < BP * nc; item += kConsumers) {
+        const int b = item / nc, c = c0 + item % nc;
+        float g[8], x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         load_cvt<T, 8>(g2 + 8 * c, g);
+        if (b < p.B) load_cvt<T, 8>(hid + (size_t)b * p.H + 8 * c, x);
+        float ss = 0.f;
+        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int i = 0; i < BP / kConsumerWarps; ++i) {
-          const int b = warp + i * kConsumerWarps;
-          float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (b < p.B) load_cvt<T, 8>(hid + (size_t)b * p.H + 8 * c, x);
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            ssl[i] = fmaf(x[2 * e], x[2 * e], fmaf(x[2 * e + 1], x[2 * e + 1], ssl[i]));
-            MK::split2(x[2 * e] * g[2 * e], x[2 * e + 1] * g[2 * e + 1], hi[e], lo[e]);
-          }
-          *reinterpret_cast<uint4*>(n + (size_t)b * p.H + 8 * c) =
-              make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(n + (size_t)(BP + b) * p.H + 8 * c) =
-              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int e = 0; e < 4; ++e) {
+          ss = fmaf(x[2 * e], x[2 * e], fmaf(x[2 * e + 1], x[2 * e + 1], ss));
+          MK::split2(x[2 * e] * g[2 * e], x[2 * e + 1] * g[2 * e + 1], hi[e], lo[e]);
         }
+        *reinterpret_cast<uint4*>(n + (size_t)b * p.H + 8 * c) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(n + (size_t)(BP + b) * p.H + 8 * c) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (ss != 0.f) atomicAdd(&rinv[b], ss);
       }
-#pragma unroll
-      for (int i = 0; i < BP / kConsumerWarps; ++i) {
-        const float v = warp_sum(ssl[i]);
-        const int b = warp + i * kConsumerWarps;
-        if (lane == 0 && b < p.B && v != 0.f) atomicAdd(p.ssq + b, v);
-      }
+      named_sync(kBarConsumers, kConsumers);
+      if (tid < p.B && tid < BP && rinv[tid] != 0.f)
+        atomicAdd(p.ssq + (blockIdx.x % kFfnSsqCopies) * BP + tid, rinv[tid]);
       // grid barrier: every block's n columns and row sums are published
       __threadfence();
       named_sync(kBarConsumers, kConsumers);
+      stamp(2);
       if (tid == 0) {
         if (atomicAdd(p.grid_count, 1) == G - 1) {
           *reinterpret_cast<volatile int*>(p.grid_count) = 0;
@@ -253,9 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
       }
       named_sync(kBarConsumers, kConsumers);
+      stamp(3);
     }
-    if (tid < BP)
-      rinv[tid] = tid < p.B ? 1.0f / sqrtf(__ldcg(p.ssq + tid) / (float)p.H + p.eps) : 0.f;
+    if (tid < BP) {
+      float t = 0.f;
+#pragma unroll
+      for (int k = 0; k < kFfnSsqCopies; ++k) t += __ldcg(p.ssq + k * BP + tid);
+      rinv[tid] = tid < p.B ? 1.0f / sqrtf(t / (float)p.H + p.eps) : 0.f;
+    }
     // ---- gate and up: one thread issues each stage's MMAs as it lands ----
     const uint32_t tmem = *s_tmem;
     const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, false);
@@ -263,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < nst; ++st) {
         const int s = st % p.stages1;
         mbar_wait(&full[s], (st / p.stages1) & 1, p.errflag);
+        if (st < kFfnTlMaxStages) stamp(4 + st);
         tc05_fence_after();
         const int ns = min(p.nsl1, nslab - st * p.nsl1);
         uint8_t* base = ring + (size_t)s * p.stage1_bytes;
@@ -286,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     named_sync(kBarConsumers, kConsumers);  // rinv
     mbar_wait(done, 0, p.errflag);
+    stamp(4 + kFfnTlMaxStages);
     tc05_fence_after();
     // a = silu(gate) * up: warp w reads units 32 (w % 4) + lane (its TMEM
     // lane quarter) for rows [h * BP/2, (h+1) * BP/2), h = w / 4
@@ -294,19 +315,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qd = warp & 3, hrow = (warp >> 2) * (BP / 2);
     const int unit = i0 + 32 * qd + lane;
     const uint32_t dq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)hrow;
+    // 16 rows at a time: the four loads share one wait
 #pragma unroll
-    for (int r8 = 0; r8 < BP / 2; r8 += 8) {
-      float gh[8], gl[8], uh[8], ul[8];
-      tmem_ld_32x32b_x8(dq + (uint32_t)r8, gh);
-      tmem_ld_32x32b_x8(dq + (uint32_t)(BP + r8), gl);
-      tmem_ld_32x32b_x8(dq + (uint32_t)(N5 + r8), uh);
-      tmem_ld_32x32b_x8(dq + (uint32_t)(N5 + BP + r8), ul);
+    for (int r16 = 0; r16 < BP / 2; r16 += 16) {
+      uint32_t gh[16], gl[16], uh[16], ul[16];
+      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)r16, gh);
+      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)(BP + r16), gl);
+      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)(N5 + r16), uh);
+      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)(N5 + BP + r16), ul);
+      tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int b = hrow + r8 + e;
+      for (int e = 0; e < 16; ++e) {
+        const int b = hrow + r16 + e;
         if (b < p.B && unit < i1) {
-          const float z = (gh[e] + gl[e]) * rinv[b];
-          const float u = (uh[e] + ul[e]) * rinv[b];
+          const float z = (__uint_as_float(gh[e]) + __uint_as_float(gl[e])) * rinv[b];
+          const float u = (__uint_as_float(uh[e]) + __uint_as_float(ul[e])) * rinv[b];
           const float a = z / (1.0f + expf(-z)) * u;
           T hi, lo;
           split1<T>(a, hi, lo);
@@ -316,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  stamp(5 + kFfnTlMaxStages);
   tc05_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -418,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================ consumers ========
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // kernel 1 of this call is complete: clear its row sums for the next call
-    if (blockIdx.x == 0 && tid < BP) p.ssq[tid] = 0.f;
+    if (blockIdx.x == 0)
+      for (int i = tid; i < kFfnSsqCopies * BP; i += kConsumers) p.ssq[i] = 0.f;
     const uint32_t tmem = *s_tmem;
     const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, true);
     if (tid == 0) {

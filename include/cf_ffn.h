@@ -88,6 +88,14 @@ int cf_ffn_get_status(cf_ffn_handle* h);
 int cf_ffn_launch_info(const cf_ffn_handle* h, int32_t* blocks, int32_t* rows_per_stage,
                        int32_t* stages);
 
+/* Optional timeline of the tensor-core pair's gate/up kernel (diagnostics):
+ * stamps is a device array of blocks1 x 56 unsigned 64-bit globaltimer
+ * values (ns) per block -- [0] start, [1] the dependency wait done, [2] its
+ * share of the normalized rows written, [3] the grid barrier passed, [4 + st]
+ * stage st (< 48) landed at the MMA issuer, [52] every MMA complete, [53]
+ * epilogue done -- or NULL (off, the default).  Other slots stay untouched. */
+int cf_ffn_set_timeline(cf_ffn_handle* h, unsigned long long* stamps);
+
 /* Kernels a call of `batch` rows launches: returns 1 (the one- and two-row
  * kernel, *blocks1 its grid, *blocks2 = 0) or 2 (the tensor-core pair, their
  * grids), or CF_ERR_INVALID_ARG.  Either pointer may be NULL. */
