@@ -69,6 +69,41 @@ def test_create_rejects_bad_config_before_cuda(kw, code):
     assert not h
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(hidden=0), binding.CF_ERR_INVALID_ARG),
+    (dict(hidden=100), binding.CF_ERR_INVALID_ARG),        # not a multiple of 8
+    (dict(intermediate=0), binding.CF_ERR_INVALID_ARG),
+    (dict(max_batch=0), binding.CF_ERR_INVALID_ARG),
+    (dict(dtype=7), binding.CF_ERR_INVALID_ARG),
+    (dict(rms_eps=float("nan")), binding.CF_ERR_INVALID_ARG),
+    (dict(stage_bytes=-1), binding.CF_ERR_INVALID_ARG),
+    (dict(hidden=8192), binding.CF_ERR_UNSUPPORTED),       # above the registers' 4096
+    (dict(max_batch=65), binding.CF_ERR_UNSUPPORTED),      # the pair's tile is 64 rows
+    (dict(max_batch=3, dtype=binding.CF_F32), binding.CF_ERR_UNSUPPORTED),
+    (dict(max_batch=16, hidden=320), binding.CF_ERR_UNSUPPORTED),  # not 128 | H
+])
+def test_ffn_create_rejects_bad_config_before_cuda(kw, code):
+    base = dict(hidden=4096, intermediate=11008, max_batch=1, rms_eps=1e-6,
+                dtype=binding.CF_F16, stage_bytes=0)
+    base.update(kw)
+    c = binding.CfFfnConfig(base["hidden"], base["intermediate"], base["max_batch"],
+                            base["rms_eps"], base["dtype"], base["stage_bytes"])
+    h = binding._vp()
+    assert binding.lib().cf_ffn_create(ctypes.byref(c), ctypes.byref(h)) == code
+    assert not h.value
+
+
+def test_ffn_null_arguments():
+    L = binding.lib()
+    assert L.cf_ffn_create(None, None) == binding.CF_ERR_INVALID_ARG
+    assert L.cf_ffn_forward(None, 1, *([None] * 7)) == binding.CF_ERR_INVALID_ARG
+    assert L.cf_ffn_get_status(None) == binding.CF_ERR_INVALID_ARG
+    assert L.cf_ffn_launch_info(None, None, None, None) == binding.CF_ERR_INVALID_ARG
+    assert L.cf_ffn_kernels(None, 1, None, None) == binding.CF_ERR_INVALID_ARG
+    assert L.cf_ffn_set_timeline(None, None) == binding.CF_ERR_INVALID_ARG
+    L.cf_ffn_destroy(None)  # NULL-safe
+
+
 def test_null_arguments():
     rc, _ = binding.cf_create_rc(None)
     assert rc == binding.CF_ERR_INVALID_ARG
