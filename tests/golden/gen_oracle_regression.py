@@ -1,7 +1,10 @@
-"""Write tiny_oracle_regression.txt from the float64 oracle (oracle/ only).
+"""Write tiny_oracle_regression.txt and tiny_ffn_oracle_regression.txt from
+the float64 oracle (oracle/ only).
 
 Inputs: the tiny workload (hidden 256, 4x64 MHA, batch 1, position 128,
-float32 storage) drawn on the CPU with seed 0 by the shared input module.
+float32 storage) and the tiny FFN workload (hidden 256, intermediate 688,
+batch 1, float32 storage), each drawn on the CPU with seed 0 by the shared
+input module.
 """
 import os
 import sys
@@ -25,6 +28,14 @@ def compute():
     return r
 
 
+def compute_ffn():
+    w = synth.FFN_WORKLOADS[synth.TINY_FFN]
+    t = synth.make_ffn(w, seed=0, device="cpu")
+    f = {k: synth.to_f64(v) for k, v in t.items()}
+    return oracle.ffn(f["hidden"], f["ln_weight"], f["w_gate"], f["w_up"], f["w_down"],
+                      w.rms_eps)
+
+
 if __name__ == "__main__":
     r = compute()
     path = os.path.join(HERE, "tiny_oracle_regression.txt")
@@ -32,4 +43,10 @@ if __name__ == "__main__":
         fh.write("# oracle output for the tiny workload, seed 0 (see README.md)\n")
         for key in ("out", "o"):
             fh.write(key + " " + " ".join(repr(float(v)) for v in r[key][0]) + "\n")
+    print("wrote", path)
+    rf = compute_ffn()
+    path = os.path.join(HERE, "tiny_ffn_oracle_regression.txt")
+    with open(path, "w") as fh:
+        fh.write("# FFN oracle output for the tiny FFN workload, seed 0 (see README.md)\n")
+        fh.write("out " + " ".join(repr(float(v)) for v in rf["out"][0]) + "\n")
     print("wrote", path)

@@ -334,6 +334,20 @@ def test_oracle_regression_fixture():
     np.testing.assert_allclose(r["o"][0], stored["o"], rtol=1e-12, atol=1e-13)
 
 
+def test_ffn_oracle_regression_fixture():
+    # The same guard for the FFN oracle (tiny FFN workload, seed 0).
+    import os
+    import sys
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    import gen_oracle_regression as gen
+    r = gen.compute_ffn()
+    with open(os.path.join(here, "tiny_ffn_oracle_regression.txt")) as fh:
+        rows = [ln.split() for ln in fh if not ln.startswith("#")]
+    stored = {row[0]: np.array([float(v) for v in row[1:]]) for row in rows}
+    np.testing.assert_allclose(r["out"][0], stored["out"], rtol=1e-12, atol=1e-13)
+
+
 # --------------------------------------------- second RMSNorm + SwiGLU FFN --
 # [LNA §一] puts "第二个 RMS Norm、FFN" after the residual of the attention block
 # of the LLaMA architecture; the FFN is read as LLaMA's gated form
