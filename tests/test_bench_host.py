@@ -26,6 +26,17 @@ def test_algorithmic_bytes_counts_each_rows_own_positions():
     assert b - a == 2 * 1024 * 32 * 64 * 2
 
 
+def test_ffn_algorithmic_bytes():
+    # W_gate, W_up, W_down [I, H] + the second norm's weight [H] + the rows
+    # read and written [B, H], all 16-bit; the batched pair's internal a and
+    # n round trips are not algorithmic bytes.
+    w = synth.FFN_WORKLOADS[synth.LLAMA3_FFN_B16]
+    expect = (3 * 14336 * 4096 + 4096 + 2 * 16 * 4096) * 2
+    assert bench.ffn_bytes(w) == expect == 352_591_872
+    w64 = synth.FFN_WORKLOADS[synth.B64_FFN]
+    assert bench.ffn_bytes(w64) == (3 * 5632 * 2048 + 2048 + 2 * 64 * 2048) * 2 == 69_734_400
+
+
 def test_parse_clocks():
     lines = [
         "0, 1965 MHz, 2070 MHz, 900.12 W, 0x0, Not Active, Not Active, Not Active, Not Active",
