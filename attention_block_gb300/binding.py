@@ -76,12 +76,11 @@ SIGNATURES = {
                                                       _vp, _vp]),
     "cf_test_cluster_gather": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp]),
     "cf_test_tc05_gemm": (ctypes.c_int, [ctypes.c_int] * 4 + [_vp] * 5),
+    "cf_test_lost_transfer": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_longlong,
+                                             _vp, _vp, _vp, _vp]),
     "cf_bench_cluster_collective": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    _vp, _vp, _vp, _vp, _vp]),
     "cf_set_timeline": (ctypes.c_int, [_vp, _vp]),
-    "cf_bench_tma_stream": (ctypes.c_int, [ctypes.c_int] * 8 + [_vp, _vp, _vp]),
-    "cf_bench_kv_stream": (ctypes.c_int, [ctypes.c_int] * 10 + [_vp] * 4),
-    "cf_bench_box_stream": (ctypes.c_int, [_vp] + [ctypes.c_int] * 10 + [_vp, _vp]),
     "cf_ffn_create": (ctypes.c_int, [ctypes.POINTER(CfFfnConfig), ctypes.POINTER(_vp)]),
     "cf_ffn_forward": (ctypes.c_int, [_vp, ctypes.c_int32] + [_vp] * 7),
     "cf_ffn_get_status": (ctypes.c_int, [_vp]),
@@ -89,7 +88,6 @@ SIGNATURES = {
     "cf_ffn_destroy": (None, [_vp]),
     "cf_ffn_kernels": (ctypes.c_int, [_vp, ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 2),
     "cf_ffn_set_timeline": (ctypes.c_int, [_vp, _vp]),
-    "cf_bench_contig_stream": (ctypes.c_int, [_vp, ctypes.c_longlong, ctypes.c_longlong] + [ctypes.c_int] * 5 + [_vp, _vp]),
     "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
                                      + [_vp] * 9),
 }
@@ -100,6 +98,8 @@ TIMELINE_NAMES = ["start", "norm", "proj", "reduce_scatter", "gather", "attn", "
                   "proj_loop_last_warp", "rinv", "attn_first_tile", "oproj_first_tile",
                   "oproj_loop", "ticket", "oproj_tile1", "oproj_tile2", "oproj_tile3",
                   "attn_loop", "attn_warps"]
+# Timeline slot holding the block's SM id (a value, not a time).
+TIMELINE_SMID = 26
 
 
 def lib_path() -> str:
@@ -247,6 +247,11 @@ def cf_test_cluster_reduce_scatter(cluster_size, n, inp, out, errflag, stream=No
 def cf_test_cluster_gather(cluster_size, n, inp, out, errflag, stream=None) -> int:
     return lib().cf_test_cluster_gather(int(cluster_size), int(n), _ptr(inp), _ptr(out),
                                         _ptr(errflag), _stream(stream))
+
+
+def cf_test_lost_transfer(n, drop_rank, limit_cycles, inp, out, errflag, stream=None) -> int:
+    return lib().cf_test_lost_transfer(int(n), int(drop_rank), int(limit_cycles), _ptr(inp),
+                                       _ptr(out), _ptr(errflag), _stream(stream))
 
 
 def cf_test_tc05_gemm(dtype, n, k, a, b, d, errflag, stream=None, a_mn=False) -> int:

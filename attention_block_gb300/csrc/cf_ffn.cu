@@ -433,7 +433,7 @@ bool plan_ffn_tc(cf_ffn_handle* h, int sms, int budget) {
   h->UB = (umax + 7) / 8 * 8;
   if (h->UB > 128) return false;
   const int slab1 = (2 * h->UB + N5) * 128;  // gate box | up box | n box
-  int extras1 = (2 * kFfnTcMaxStages + 1) * 8 + BP * 4 + 16;  // barriers, rinv, TMEM word
+  int extras1 = (2 * kFfnTcMaxStages + 2) * 8 + BP * 4 + 16;  // barriers, rinv, TMEM word
   // the M = 128 operand reads of a slab's gate and up boxes run up to 16 KB
   // past the box start: keep that much shared memory after the ring
   extras1 = std::max(extras1, 16384 - (h->UB + N5) * 128);

@@ -132,7 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + kFfnTcMaxStages;
   uint64_t* done = bars + 2 * kFfnTcMaxStages;
-  float* rinv = reinterpret_cast<float*>(bars + 2 * kFfnTcMaxStages + 1);  // [BP]
+  // consumer thread 0 arrives here once the grid barrier has passed, i.e.
+  // once every block's columns of n are published
+  uint64_t* n_ready = bars + 2 * kFfnTcMaxStages + 1;
+  float* rinv = reinterpret_cast<float*>(bars + 2 * kFfnTcMaxStages + 2);  // [BP]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(rinv + BP);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -141,9 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i1 = (int)((long long)(blockIdx.x + 1) * p.I / G);
   const int nslab = p.H / 64;
   const int nst = (nslab + p.nsl1 - 1) / p.nsl1;  // stages of the stream
-  // generation of the grid barrier before this launch arrives (it only
-  // advances once every block of this launch has arrived)
-  const int gen0 = *reinterpret_cast<volatile int*>(p.grid_gen);
 
   auto stamp = [&](int slot) {
     if (p.timeline != nullptr && tid == 0)
@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], kConsumerWarps);
     }
     mbar_init(done, 1);
+    mbar_init(n_ready, 1);
     fence_mbar_init_cluster();
   }
   if (warp == 0) {
@@ -191,14 +192,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                       &full[st % p.stages1], pol_n);
       };
       // The weights need nothing from this launch or the previous kernel:
-      // the first stages' weight boxes go out at once, their n boxes after
-      // the grid barrier that publishes n.
+      // the first stages' weight boxes go out at once, their n boxes once
+      // consumer thread 0 reports that the grid barrier publishing n has
+      // passed.  The barrier's words are read by that consumer only, after
+      // its dependency wait: with programmatic dependent launch an earlier
+      // launch of this kernel (the previous layer's) may still be inside its
+      // own barrier while this one starts.
       const int fill = min(p.stages1, nst);
       for (int st = 0; st < fill; ++st) {
         mbar_arrive_expect_tx(&full[st], (uint32_t)(stage_slabs(st) * slab1));
         load_w(st);
       }
-      wait_generation(p.grid_gen, gen0, p.errflag);
+      mbar_wait(n_ready, 0, p.errflag);
       fence_proxy_async_global();  // n was written by other blocks' threads
       for (int st = 0; st < fill; ++st) load_n(st);
       for (int st = fill; st < nst; ++st) {
@@ -212,9 +217,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================================================ consumers ========
-    // h comes from the previous kernel; n, a and the row sums are reused
-    // across calls, so nothing is written before this wait.
+    // h comes from the previous kernel; n, a, the row sums and the grid
+    // barrier's words are reused across calls, so none of them is read or
+    // written before this wait.  Once it returns, every earlier kernel of the
+    // stream has completed: each launch in the chain waits for its own
+    // predecessor before it can complete.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // generation of the grid barrier before this block arrives: it cannot
+    // advance until every block of this launch, this one included, has
+    // arrived
+    const int gen0 = tid == 0 ? *reinterpret_cast<volatile int*>(p.grid_gen) : 0;
     stamp(1);
     // ---- Phase 0: this block's columns of n = h * g2 as 16-bit hi rows
     // 0..BP-1 and lo rows BP..2BP-1 of n [2*BP, H], and the rows' sums of
@@ -265,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_generation(p.grid_gen, gen0, p.errflag);
         }
         __threadfence();
+        mbar_arrive(n_ready);  // the producer may now load n (also after a timeout)
       }
       named_sync(kBarConsumers, kConsumers);
       stamp(3);

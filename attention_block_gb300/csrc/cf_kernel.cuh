@@ -170,6 +170,8 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
       atomicMax(&p.timeline[blockIdx.x * kTimelineSlots + slot], globaltimer_ns());
   };
   stamp(kTlStart);
+  if (p.timeline != nullptr && tid == 0)
+    p.timeline[blockIdx.x * kTimelineSlots + kTlSmid] = sm_id();
 
   const int nkt = Hc / p.Rw;
   const int ncb = Hc / p.Co;

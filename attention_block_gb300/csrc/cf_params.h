@@ -57,6 +57,7 @@ enum TimelineSlot {
   kTlOprojTile1 = 21, // W_o tiles 1..3 in hand (slots 21..23)
   kTlAttnLoop = 24,   // last K/V tile and the new token consumed (row 0)
   kTlAttnWarps = 25,  // warp states written (row 0)
+  kTlSmid = 26,       // not a time: the SM the block ran on
   kTimelineSlots = 32
 };
 

@@ -20,6 +20,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -95,12 +101,13 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar,
   return done != 0;
 }
 
-// Bounded wait for the phase with the given parity.  On expiry it records
-// kDevErrTimeout and returns false; once any CTA has recorded a timeout the
-// other waits give up quickly, so the whole grid drains instead of hanging.
+// Bounded wait for the phase with the given parity.  On expiry (after
+// `limit` SM cycles) it records kDevErrTimeout and returns false; once any
+// CTA has recorded a timeout the other waits give up quickly, so the whole
+// grid drains instead of hanging.
 template <bool kCluster>
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                            int* errflag) {
+                                            int* errflag, long long limit) {
   const long long t0 = clock64();
   for (uint32_t spins = 1;; ++spins) {
     bool ok = kCluster ? mbar_try_wait_cluster(bar, parity)
@@ -108,7 +115,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
     if (ok) return true;
     if ((spins & 1023u) == 0) {
       if (*reinterpret_cast<volatile int*>(errflag) & kDevErrTimeout) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         atomicOr(errflag, kDevErrTimeout);
         return false;
       }
@@ -120,14 +127,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           int* errflag) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait_cta(a, parity)) return true;
-  return mbar_wait_slow<false>(a, parity, errflag);
+  return mbar_wait_slow<false>(a, parity, errflag, kWaitLimitCycles);
 }
 
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
-                                                  int* errflag) {
+                                                  int* errflag,
+                                                  long long limit = kWaitLimitCycles) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait_cluster(a, parity)) return true;
-  return mbar_wait_slow<true>(a, parity, errflag);
+  return mbar_wait_slow<true>(a, parity, errflag, limit);
 }
 
 // Bounded wait until the global counter reaches `target` (blocks of the same,

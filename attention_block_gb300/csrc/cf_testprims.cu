@@ -86,6 +86,38 @@ __global__ void __launch_bounds__(kNT) prim_kernel(int kind, int n, const float*
   cluster_sync_all();
 }
 
+// A lost transfer and the bounded wait that catches it: one exchange of the
+// all-reduce between the two blocks of a 2-block cluster in which block
+// `drop_rank` (0 or 1; -1 for none) does not send.  Its partner's wait gives
+// up after `limit` SM cycles and records kDevErrTimeout; the dropping block
+// still receives, so no remote write is in flight when the blocks leave.
+// out[r] = in[r] + whatever block r received (nothing: zeros).
+__global__ void __launch_bounds__(kNT) lost_send_kernel(int n, int drop_rank, long long limit,
+                                                        const float* __restrict__ in,
+                                                        float* __restrict__ out, int* errflag) {
+  extern __shared__ __align__(16) float smem[];
+  const int rank = (int)cluster_ctarank();
+  const int tid = threadIdx.x;
+  float* data = smem;
+  float* rb = smem + n;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * n);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init_cluster();
+    mbar_arrive_expect_tx(bar, allreduce_round_bytes(n));
+  }
+  for (int i = tid; i < n; i += kNT) {
+    data[i] = in[(size_t)rank * n + i];
+    rb[i] = 0.f;
+  }
+  __syncthreads();
+  cluster_sync_all();
+  if (rank != drop_rank) push_to_peer<kNT>(data, rb, n, bar, (uint32_t)(rank ^ 1), tid);
+  mbar_wait_cluster(bar, 0, errflag, limit);
+  for (int i = tid; i < n; i += kNT) out[(size_t)rank * n + i] = data[i] + rb[i];
+  cluster_sync_all();
+}
+
 int run(int kind, int N, int n, const float* in, float* out, int* errflag, long long* cycles,
         void* stream) {
   if (!(N == 1 || N == 2 || N == 4 || N == 8 || N == 16)) return CF_ERR_INVALID_ARG;
@@ -138,6 +170,35 @@ int cf_test_cluster_reduce_scatter(int cluster_size, int n, const float* in, flo
 int cf_test_cluster_gather(int cluster_size, int n, const float* in, float* out, int* errflag,
                            void* stream) {
   return run(kGather, cluster_size, n, in, out, errflag, nullptr, stream);
+}
+
+int cf_test_lost_transfer(int n, int drop_rank, long long limit_cycles, const float* in,
+                          float* out, int* errflag, void* stream) {
+  if (n <= 0 || n % 4 != 0 || n > 16384 || drop_rank < -1 || drop_rank > 1 ||
+      limit_cycles <= 0 || in == nullptr || out == nullptr || errflag == nullptr)
+    return CF_ERR_INVALID_ARG;
+  const size_t smem = (size_t)2 * n * 4 + 16;
+  if (cudaFuncSetAttribute(lost_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return CF_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.gridDim = dim3(2, 1, 1);
+  lc.blockDim = dim3(kNT, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = static_cast<cudaStream_t>(stream);
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, lost_send_kernel, n, drop_rank, limit_cycles, in, out, errflag) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return CF_ERR_CUDA;
+  }
+  return CF_OK;
 }
 
 int cf_bench_cluster_collective(int kind, int cluster_size, int n, const float* in, float* out,

@@ -37,58 +37,23 @@ int cf_test_cluster_reduce_scatter(int cluster_size, int n, const float* in, flo
 int cf_test_cluster_gather(int cluster_size, int n, const float* in, float* out, int* errflag,
                            void* stream);
 
+/* Failure detection of the bounded in-kernel waits [CF §4.3 典型性能问题排查]:
+ * one exchange of the sum all-reduce between the two blocks of a 2-block
+ * cluster in which block drop_rank (0 or 1; -1 = none) does not send, as if
+ * its transfer were lost.  The partner's wait gives up after limit_cycles SM
+ * cycles (the decode kernels use about one second) and ORs bit 2 (timeout)
+ * into *errflag; the launch then finishes normally and the context stays
+ * usable.  in, out [2][n] (n a multiple of 4, <= 16384): out row r = in row
+ * r + the row block r received (zeros when nothing arrived).
+ * Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
+int cf_test_lost_transfer(int n, int drop_rank, long long limit_cycles, const float* in,
+                          float* out, int* errflag, void* stream);
+
 /* Same collectives (kind 0 sum all-reduce, 1 max all-reduce, 2 reduce-scatter,
  * 3 gather) with the SM cycles each block spent inside the collective written
  * to cycles[cluster_size] (device long long).  Buffer shapes as above. */
 int cf_bench_cluster_collective(int kind, int cluster_size, int n, const float* in, float* out,
                                 int* errflag, long long* cycles, void* stream);
-
-/* Bare TMA streaming rate of the decode kernel's W_qkv access pattern: one
- * launch of cluster_size * n_kv_heads blocks (no cluster attribute; any
- * cluster_size dividing hidden), each streaming its K band of the three
- * head_dim-wide column slices of head g of the fp16 matrix w [hidden,
- * (nq+2nkv)*head_dim] in tiles of rows_per_tile rows through `stages`
- * shared-memory stages, with shared memory padded so that ctas_per_sm blocks
- * fit per SM.  No compute.  Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
-int cf_bench_tma_stream(int hidden, int n_q_heads, int n_kv_heads, int head_dim,
-                        int cluster_size, int rows_per_tile, int stages, int ctas_per_sm,
-                        const void* w, int* errflag, void* stream);
-
-/* Bare TMA streaming rate of the batched kernel's K/V access pattern: one
- * launch of n_kv_heads * batch / rows_per_block blocks; block i streams, for
- * KV head i % n_kv_heads and each of its rows_per_block batch rows, positions
- * [0, len) of the fp16 caches k_cache, v_cache [batch, s_max, n_kv_heads,
- * head_dim] in tiles of pos_per_tile positions (one K and one V box per
- * stage) through `stages` stages, shared memory padded so that ctas_per_sm
- * blocks fit per SM.  No compute.  Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
-int cf_bench_kv_stream(int batch, int s_max, int n_kv_heads, int head_dim, int elem_bytes,
-                       int len, int rows_per_block, int pos_per_tile, int stages,
-                       int ctas_per_sm, const void* k_cache, const void* v_cache, int* errflag,
-                       void* stream);
-
-/* Bare TMA streaming rate of weight-band tile shapes: `blocks` blocks, block i
- * streaming band_rows x band_cols of the row-major fp16 [rows, cols] matrix w
- * (band i mod cols/band_cols, row block i / (cols/band_cols) mod
- * rows/band_rows) as tiles of `bps` boxes {box_cols, box_rows} side by side,
- * through `stages` stages.  No compute.  flags: bit 0 the 128-byte swizzle;
- * bits 1-2 the L2 promotion (0: 256 B, 1: 128 B, 2: none, 3: 64 B); bit 3
- * launch with only the shared memory the ring needs (several blocks per SM),
- * else with the full opt-in amount (one block per SM); bit 4 walk the band's
- * tiles down its rows first (column groups outer).  Errors:
- * CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
-int cf_bench_box_stream(const void* w, int rows, int cols, int box_cols, int box_rows,
-                        int flags, int bps, int band_rows, int band_cols, int stages,
-                        int blocks, int* errflag, void* stream);
-
-/* Bare streaming rate of contiguous per-block regions: `blocks` blocks, block
- * i streaming bytes [(i mod n) * region_bytes, +region_bytes) of w (n =
- * min(blocks, total_bytes / region_bytes)) in stages of stage_bytes (a
- * multiple of 1024), each filled by `pieces` equal bulk copies, through
- * `stages` stages; shared_sm != 0 launches with only the shared memory the
- * ring needs.  No compute.  Errors: CF_ERR_INVALID_ARG, CF_ERR_CUDA. */
-int cf_bench_contig_stream(const void* w, long long total_bytes, long long region_bytes,
-                           int stage_bytes, int pieces, int stages, int blocks, int shared_sm,
-                           int* errflag, void* stream);
 
 /* Phase timeline of later cf_decode_attn_block calls of handle h (a tuning
  * aid): when `stamps` is a zeroed device buffer of grid_blocks * 32 unsigned

@@ -86,3 +86,55 @@ def test_bad_arguments_rejected_without_launch():
     assert binding.cf_test_cluster_allreduce(3, 0, 4, x, x, err) == binding.CF_ERR_INVALID_ARG
     assert binding.cf_test_cluster_allreduce(2, 0, 6, x, x, err) == binding.CF_ERR_INVALID_ARG
     assert binding.cf_test_cluster_gather(2, 4, None, x, err) == binding.CF_ERR_INVALID_ARG
+
+
+# SM cycles after which the lost-transfer test's wait gives up (~50 us at
+# 2 GHz; the decode kernels wait about one second).
+SHORT_LIMIT = 100_000
+TIMEOUT_BIT = 2  # the device bit the host reports as CF_ERR_DEVICE_TIMEOUT
+
+
+@pytest.mark.parametrize("drop", [1, 0])
+def test_lost_transfer_times_out_reports_and_leaves_the_context_usable(drop):
+    """A block whose partner never sends: the bounded wait gives up after the
+    short limit, the launch finishes by itself with the timeout bit set, the
+    partner's side of the exchange is intact, and ordinary launches work
+    afterwards (no fault, trap or hang is involved)."""
+    n = 256
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = _ints((2, n), 99 + drop)
+    out = torch.full_like(x, float("nan"))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    assert binding.cf_test_lost_transfer(n, drop, SHORT_LIMIT, x, out, err) == binding.CF_OK
+    t1.record()
+    torch.cuda.synchronize()
+    assert int(err.item()) & TIMEOUT_BIT
+    keep = 1 - drop  # did not receive: its row is its own input
+    assert torch.equal(out[keep], x[keep])
+    assert torch.equal(out[drop], x.sum(0))  # received its partner's row
+    assert t0.elapsed_time(t1) < 1000.0  # ms: ended by the short limit, not the default
+    # the same exchange with nothing dropped, then a plain collective
+    err.zero_()
+    out.fill_(float("nan"))
+    assert binding.cf_test_lost_transfer(n, -1, SHORT_LIMIT, x, out, err) == binding.CF_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out[0], x.sum(0)) and torch.equal(out[1], x.sum(0))
+    y = _ints((4, 64), 5)
+    out4 = torch.empty_like(y)
+    assert binding.cf_test_cluster_allreduce(4, 0, 64, y, out4, err) == binding.CF_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for r in range(4):
+        assert torch.equal(out4[r], y.sum(0))
+
+
+def test_lost_transfer_bad_arguments_rejected_without_launch():
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = torch.zeros(2, 64, device="cuda")
+    f = binding.cf_test_lost_transfer
+    assert f(6, 1, SHORT_LIMIT, x, x, err) == binding.CF_ERR_INVALID_ARG
+    assert f(64, 2, SHORT_LIMIT, x, x, err) == binding.CF_ERR_INVALID_ARG
+    assert f(64, 1, 0, x, x, err) == binding.CF_ERR_INVALID_ARG
+    assert f(64, 1, SHORT_LIMIT, x, x, None) == binding.CF_ERR_INVALID_ARG

@@ -246,3 +246,61 @@ def test_whole_decoder_layer_attention_then_ffn(B):
                        synth.to_f64(tf["w_gate"]), synth.to_f64(tf["w_up"]),
                        synth.to_f64(tf["w_down"]), wf.rms_eps)
     check(out.double().cpu().numpy(), round_to(ref_h["out"], "f16"), "ffn on the GPU's h")
+
+
+# Decoder layers chained through ONE attention handle and ONE FFN handle:
+# dtype, H, nq, nkv, d, position, I, batch
+CHAIN_SHAPES = [
+    # fewer FFN units than SMs: the gate/up grid leaves SMs free, so the next
+    # layer's kernels can become resident while this layer's FFN still runs
+    ("bf16", 4096, 32, 8, 128, 200, 100, 9),
+    # the Llama-3 layer's FFN at 16 rows (one gate/up block per SM)
+    ("bf16", 4096, 32, 8, 128, 256, 14336, 16),
+]
+
+
+@pytest.mark.parametrize("shape", CHAIN_SHAPES,
+                         ids=lambda s: f"{s[0]}-H{s[1]}-I{s[6]}-B{s[7]}")
+def test_decoder_layers_chained_under_programmatic_dependent_launch(shape):
+    """Three decoder layers back to back on one stream, each the attention
+    block then the FFN, with no host synchronization between launches and
+    programmatic dependent launch on (the default): a kernel may become
+    resident while earlier ones still run, including the previous layer's
+    FFN with its grid barrier.  Every layer's attention output and FFN
+    output is checked, all rows, against the oracle fed that layer's actual
+    GPU input, so errors do not compound."""
+    dt, H, nq, nkv, d, pos, I, B = shape
+    layers = 3
+    w = synth.custom(name="chain", hidden=H, n_q_heads=nq, n_kv_heads=nkv, head_dim=d, batch=B,
+                     s_max=pos + 1, dtype=dt, rope_theta=5e5, positions=f"fixed:{pos}")
+    wf = synth.custom_ffn(name="chain_ffn", hidden=H, intermediate=I, batch=B, dtype=dt)
+    ts = [synth.make_layer(w, 30 + l, device="cuda") for l in range(layers)]
+    tfs = [synth.make_ffn(wf, 60 + l, device="cuda") for l in range(layers)]
+    attn = make_block(w)
+    ffn = make_ffn_block(wf)
+    assert ffn.kernels(B)["kernels"] == 2
+    mids = [torch.full_like(ts[0]["hidden"], float("nan")) for _ in range(layers)]
+    outs = [torch.full_like(ts[0]["hidden"], float("nan")) for _ in range(layers)]
+    caches = [(t["k_cache"].clone(), t["v_cache"].clone()) for t in ts]
+    x = ts[0]["hidden"]
+    for l in range(layers):
+        t, tf = ts[l], tfs[l]
+        attn(B, x, t["ln_weight"], t["w_qkv"], t["w_o"], caches[l][0], caches[l][1],
+             t["positions"], mids[l])
+        ffn(B, mids[l], tf["ln_weight"], tf["w_gate"], tf["w_up"], tf["w_down"], outs[l])
+        x = outs[l]
+    torch.cuda.synchronize()
+    assert attn.status() == binding.CF_OK
+    assert ffn.status() == binding.CF_OK
+    for l in range(layers):
+        t, tf = ts[l], tfs[l]
+        x_in = ts[0]["hidden"] if l == 0 else outs[l - 1]
+        ref_a = run_oracle(w, t, hidden=x_in)
+        check(mids[l].double().cpu().numpy(), round_to(ref_a["out"], dt), f"layer {l} attention")
+        ref_f = oracle.ffn(synth.to_f64(mids[l]), synth.to_f64(tf["ln_weight"]),
+                           synth.to_f64(tf["w_gate"]), synth.to_f64(tf["w_up"]),
+                           synth.to_f64(tf["w_down"]), wf.rms_eps)
+        got = outs[l].double().cpu().numpy()
+        check(got, round_to(ref_f["out"], dt), f"layer {l} FFN")
+        h = synth.to_f64(mids[l])
+        check(got - h, round_to(ref_f["out"], dt) - h, f"layer {l} FFN - its input")
