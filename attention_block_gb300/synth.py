@@ -80,6 +80,24 @@ def custom(name: str = "custom", **kw) -> Workload:
     return Workload(name=name, **base)
 
 
+def workload(spec: str) -> Workload:
+    """A named workload, or an ad-hoc one written as
+    ``custom:hidden=H,q=NQ,kv=NKV,d=D,batch=B,pos=P[,dtype=T][,theta=X][,layers=L]``
+    (every row at position P, cache capacity P + 1; dtype f16 by default)."""
+    if not spec.startswith("custom:"):
+        return WORKLOADS[spec]
+    kv = dict(item.split("=", 1) for item in spec[len("custom:"):].split(",") if item)
+    known = {"hidden", "q", "kv", "d", "batch", "pos", "dtype", "theta", "layers"}
+    unknown = set(kv) - known
+    if unknown:
+        raise ValueError(f"unknown workload keys {sorted(unknown)} in {spec!r}")
+    pos = int(kv["pos"])
+    return Workload(spec, int(kv["hidden"]), int(kv["q"]), int(kv["kv"]), int(kv["d"]),
+                    int(kv["batch"]), pos + 1, kv.get("dtype", "f16"),
+                    float(kv.get("theta", 1e4)), 1e-6, f"fixed:{pos}",
+                    layers=int(kv.get("layers", 1)))
+
+
 def _positions(w: Workload, gen: torch.Generator, device) -> torch.Tensor:
     kind, *args = w.positions.split(":")
     if kind == "fixed":
@@ -181,6 +199,86 @@ def make_ffn(w: FfnWorkload, seed: int = 0, device="cpu", hidden=None) -> dict:
     out["w_gate"] = randn(I, H, std=0.02)
     out["w_up"] = randn(I, H, std=0.02)
     out["w_down"] = randn(I, H, std=0.02)
+    return out
+
+
+@dataclasses.dataclass(frozen=True)
+class MlaWorkload:
+    """The DeepSeek multi-head latent attention (MLA) variant of the block."""
+    name: str
+    hidden: int
+    n_heads: int
+    d_nope: int
+    d_rope: int
+    d_v: int
+    d_latent: int
+    batch: int
+    s_max: int
+    dtype: str
+    rope_theta: float
+    rms_eps: float
+    positions: str
+
+    def oracle_cfg(self) -> dict:
+        return dict(hidden=self.hidden, n_heads=self.n_heads, d_nope=self.d_nope,
+                    d_rope=self.d_rope, d_v=self.d_v, d_latent=self.d_latent, s_max=self.s_max,
+                    rope_theta=self.rope_theta, rms_eps=self.rms_eps)
+
+
+# MLA layers shaped like DeepSeek-V2-Lite's attention (hidden 2048, 16 heads,
+# 128 + 64 query/key dims, 128 value dims, a 512-dim latent), at the two
+# sequence lengths the pages measure MLA at (4K and 16K), and a tiny layer
+# with the same head dims.
+MLA_WORKLOADS = {w.name: w for w in [
+    MlaWorkload("deepseek_v2_lite_mla_b1_p4096_bf16", 2048, 16, 128, 64, 128, 512, 1, 4097,
+                "bf16", 1e4, 1e-6, "fixed:4096"),
+    MlaWorkload("deepseek_v2_lite_mla_b1_p16384_bf16", 2048, 16, 128, 64, 128, 512, 1, 16385,
+                "bf16", 1e4, 1e-6, "fixed:16384"),
+    MlaWorkload("tiny_mla_h512_h8_b1_p128_bf16", 512, 8, 128, 64, 128, 512, 1, 129, "bf16",
+                1e4, 1e-6, "fixed:128"),
+]}
+MLA_4K = "deepseek_v2_lite_mla_b1_p4096_bf16"
+MLA_16K = "deepseek_v2_lite_mla_b1_p16384_bf16"
+MLA_TINY = "tiny_mla_h512_h8_b1_p128_bf16"
+
+
+def custom_mla(name: str = "custom_mla", **kw) -> MlaWorkload:
+    base = dict(hidden=512, n_heads=8, d_nope=128, d_rope=64, d_v=128, d_latent=512, batch=1,
+                s_max=129, dtype="bf16", rope_theta=1e4, rms_eps=1e-6, positions="fixed:128")
+    base.update(kw)
+    return MlaWorkload(name=name, **base)
+
+
+def make_mla_layer(w: MlaWorkload, seed: int = 0, device="cpu") -> dict:
+    """Draw one MLA layer's tensors (storage dtype) on ``device``, in the order
+    hidden, ln_weight, w_q, w_dkv, kv_norm_weight, w_ukv, w_o, latent cache,
+    positions.  Laws as for the attention block: hidden ~ N(0,1), norm
+    weights ~ 1 + N(0, 0.1), weights ~ N(0, 0.02), the latent cache ~ N(0,1)
+    over its whole capacity."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    dt = DTYPES[w.dtype]
+    B, H, S, nh = w.batch, w.hidden, w.s_max, w.n_heads
+    dn, dr, dv, dc = w.d_nope, w.d_rope, w.d_v, w.d_latent
+
+    def randn(*shape, std=1.0, mean=0.0):
+        t = torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        if mean != 0.0:
+            t.add_(mean)
+        return t.to(dt)
+
+    out = {}
+    out["hidden"] = randn(B, H)
+    out["ln_weight"] = randn(H, std=0.1, mean=1.0)
+    out["w_q"] = randn(H, nh * (dn + dr), std=0.02)
+    out["w_dkv"] = randn(H, dc + dr, std=0.02)
+    out["kv_norm_weight"] = randn(dc, std=0.1, mean=1.0)
+    out["w_ukv"] = randn(dc, nh * (dn + dv), std=0.02)
+    out["w_o"] = randn(nh * dv, H, std=0.02)
+    out["latent_cache"] = randn(B, S, dc + dr)
+    out["positions"] = _positions(w, gen, device)
     return out
 
 

@@ -42,6 +42,20 @@ class OrcConfig(ctypes.Structure):
     ]
 
 
+class OrcMlaConfig(ctypes.Structure):
+    _fields_ = [
+        ("hidden", ctypes.c_int),
+        ("n_heads", ctypes.c_int),
+        ("d_nope", ctypes.c_int),
+        ("d_rope", ctypes.c_int),
+        ("d_v", ctypes.c_int),
+        ("d_latent", ctypes.c_int),
+        ("s_max", ctypes.c_int),
+        ("rope_theta", ctypes.c_double),
+        ("rms_eps", ctypes.c_double),
+    ]
+
+
 def build(force: bool = False) -> str:
     """Compile liboracle.so with gcc (no fast-math, no FMA contraction)."""
     stale = (not os.path.exists(_LIB)) or any(
@@ -78,6 +92,9 @@ def _load():
             lib.orc_silu.restype = ctypes.c_double
             lib.orc_ffn_row.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double] + [_dp] * 9
             lib.orc_ffn_row.restype = ctypes.c_int
+            lib.orc_mla_row.argtypes = [ctypes.POINTER(OrcMlaConfig)] + [_dp] * 8 + [
+                ctypes.c_int] + [_dp] * 5
+            lib.orc_mla_row.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -197,3 +214,28 @@ def ffn(Hs, g2, wg, wu, wd, eps: float, rows=None):
     rows = range(Hs.shape[0]) if rows is None else rows
     outs = [ffn_row(Hs[b], g2, wg, wu, wd, eps) for b in rows]
     return {k: np.stack([o[k] for o in outs]) for k in outs[0]}
+
+
+def mla_row(cfg: dict, x, g, wq, wdkv, g_kv, wukv, wo, lc, pos: int):
+    """One batch row of the MLA decode block (oracle.h, orc_mla_row).  lc is
+    this row's latent cache, a float64 [S, dc+dr] array updated in place.
+
+    cfg keys: hidden, n_heads, d_nope, d_rope, d_v, d_latent, s_max,
+    rope_theta, rms_eps.  Returns a dict with out, q, lat, o, proj.
+    """
+    c = OrcMlaConfig(*(int(cfg[k]) for k in ("hidden", "n_heads", "d_nope", "d_rope", "d_v",
+                                              "d_latent", "s_max")),
+                     float(cfg["rope_theta"]), float(cfg["rms_eps"]))
+    H, nh, dn, dr, dv, dc = c.hidden, c.n_heads, c.d_nope, c.d_rope, c.d_v, c.d_latent
+    x, g, wq, wdkv, g_kv, wukv, wo = (_f64(a) for a in (x, g, wq, wdkv, g_kv, wukv, wo))
+    assert wq.shape == (H, nh * (dn + dr)) and wdkv.shape == (H, dc + dr)
+    assert wukv.shape == (dc, nh * (dn + dv)) and wo.shape == (nh * dv, H)
+    assert lc.dtype == np.float64 and lc.flags.c_contiguous and lc.shape == (c.s_max, dc + dr)
+    res = {k: np.empty(n, dtype=np.float64) for k, n in (
+        ("out", H), ("q", nh * (dn + dr)), ("lat", dc + dr), ("o", nh * dv), ("proj", H))}
+    rc = _load().orc_mla_row(ctypes.byref(c), _p(x), _p(g), _p(wq), _p(wdkv), _p(g_kv),
+                             _p(wukv), _p(wo), _p(lc), int(pos), _p(res["out"]), _p(res["q"]),
+                             _p(res["lat"]), _p(res["o"]), _p(res["proj"]))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the MLA row (pos={pos}, cfg={cfg})")
+    return res

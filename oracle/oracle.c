@@ -238,3 +238,101 @@ int orc_ffn_row(int H, int I, double eps, const double* h, const double* g2,
   free(proj);
   return 0;
 }
+
+/* MLA decode row [CF §5.2], projections as DeepSeek's MLA (see oracle.h). */
+int orc_mla_row(const orc_mla_config* c, const double* x, const double* g,
+                const double* wq, const double* wdkv, const double* g_kv,
+                const double* wukv, const double* wo, double* lc, int pos,
+                double* out, double* dbg_q, double* dbg_lat, double* dbg_o,
+                double* dbg_proj) {
+  const int H = c->hidden, nh = c->n_heads, dn = c->d_nope, dr = c->d_rope;
+  const int dv = c->d_v, dc = c->d_latent, S = c->s_max;
+  if (H <= 0 || nh <= 0 || dn <= 0 || dr <= 0 || (dr % 2) != 0 || dv <= 0 ||
+      dc <= 0 || S <= 0)
+    return -1;
+  if (pos < 0 || pos >= S) return -1;
+  const int dq = dn + dr, dl = dc + dr, ntok = pos + 1;
+  const int wcols = nh * (dn + dv);
+
+  double* n = (double*)malloc(sizeof(double) * (size_t)H);
+  double* q = (double*)malloc(sizeof(double) * (size_t)nh * dq);
+  double* a = (double*)malloc(sizeof(double) * (size_t)dl);
+  double* k = (double*)malloc(sizeof(double) * (size_t)ntok * dq);
+  double* v = (double*)malloc(sizeof(double) * (size_t)ntok * dv);
+  double* s = (double*)malloc(sizeof(double) * (size_t)ntok);
+  double* o = (double*)malloc(sizeof(double) * (size_t)nh * dv);
+  double* proj = (double*)malloc(sizeof(double) * (size_t)H);
+
+  /* 1. RMSNorm of the hidden row [LNA §三 stage 1]. */
+  orc_rmsnorm(H, x, g, c->rms_eps, n);
+  /* 2. Query and latent projections. */
+  orc_matvec(H, nh * dq, n, wq, q);
+  orc_matvec(H, dl, n, wdkv, a);
+  /* 3. RMSNorm of the compressed part, RoPE of the position parts. */
+  orc_rmsnorm(dc, a, g_kv, c->rms_eps, a);
+  orc_rope(dr, c->rope_theta, pos, a + dc);
+  for (int h = 0; h < nh; ++h) orc_rope(dr, c->rope_theta, pos, q + (size_t)h * dq + dn);
+  /* 4. Append the latent row at slot pos. */
+  for (int i = 0; i < dl; ++i) lc[(size_t)pos * dl + i] = a[i];
+  /* 5. Per head: keys and values of every position from the latent cache,
+   *    then two-pass softmax attention. */
+  const double scale = 1.0 / sqrt((double)dq);
+  for (int h = 0; h < nh; ++h) {
+    const double* wk = wukv + (size_t)h * (dn + dv);  /* column offset of k part */
+    const double* wvv = wk + dn;                      /* column offset of v part */
+    for (int t = 0; t < ntok; ++t) {
+      const double* lt = lc + (size_t)t * dl;
+      double* kt = k + (size_t)t * dq;
+      double* vt = v + (size_t)t * dv;
+      for (int j = 0; j < dn; ++j) kt[j] = 0.0;
+      for (int j = 0; j < dv; ++j) vt[j] = 0.0;
+      for (int i = 0; i < dc; ++i) {
+        const double li = lt[i];
+        const double* row = wk + (size_t)i * wcols;
+        const double* vrow = wvv + (size_t)i * wcols;
+        for (int j = 0; j < dn; ++j) kt[j] += li * row[j];
+        for (int j = 0; j < dv; ++j) vt[j] += li * vrow[j];
+      }
+      for (int j = 0; j < dr; ++j) kt[dn + j] = lt[dc + j];
+    }
+    const double* qh = q + (size_t)h * dq;
+    double m = -INFINITY;
+    for (int t = 0; t < ntok; ++t) {
+      s[t] = dot(dq, qh, k + (size_t)t * dq) * scale;
+      if (s[t] > m) m = s[t];
+    }
+    double sum = 0.0;
+    for (int t = 0; t < ntok; ++t) {
+      s[t] = exp(s[t] - m);
+      sum += s[t];
+    }
+    double* oh = o + (size_t)h * dv;
+    for (int j = 0; j < dv; ++j) oh[j] = 0.0;
+    for (int t = 0; t < ntok; ++t) {
+      const double wt = s[t] / sum;
+      const double* vt = v + (size_t)t * dv;
+      for (int j = 0; j < dv; ++j) oh[j] += wt * vt[j];
+    }
+  }
+  /* 6. Output projection and residual [LNA §一]. */
+  orc_matvec(nh * dv, H, o, wo, proj);
+  for (int i = 0; i < H; ++i) out[i] = x[i] + proj[i];
+
+  if (dbg_q)
+    for (int i = 0; i < nh * dq; ++i) dbg_q[i] = q[i];
+  if (dbg_lat)
+    for (int i = 0; i < dl; ++i) dbg_lat[i] = a[i];
+  if (dbg_o)
+    for (int i = 0; i < nh * dv; ++i) dbg_o[i] = o[i];
+  if (dbg_proj)
+    for (int i = 0; i < H; ++i) dbg_proj[i] = proj[i];
+  free(n);
+  free(q);
+  free(a);
+  free(k);
+  free(v);
+  free(s);
+  free(o);
+  free(proj);
+  return 0;
+}

@@ -115,6 +115,48 @@ int orc_ffn_row(int H, int I, double eps, const double* h, const double* g2,
                 const double* wg, const double* wu, const double* wd,
                 double* out, double* dbg_n, double* dbg_a, double* dbg_proj);
 
+/* The DeepSeek multi-head latent attention (MLA) variant of the decode block
+ * [CF §5.2 DeepSeek-MLA特殊处理].  The page gives only the kernel-side
+ * adaptation (the latent key/value cache partitioned across clusters, a
+ * sparse ClusterReduce); the projections are read as DeepSeek's published MLA
+ * with an uncompressed query (the DeepSeek-V2-Lite form):
+ *   n     = RMSNorm(x; g)
+ *   q     = n . Wq             Wq [H, nh*(dn+dr)]; head h = [q_nope (dn) | q_rope (dr)]
+ *   a     = n . Wdkv           Wdkv [H, dc+dr];   a = [c (dc) | kr (dr)]
+ *   c'    = RMSNorm(c; g_kv)   (same eps)
+ *   q_rope_h <- RoPE(q_rope_h, pos), kr <- RoPE(kr, pos)  (rotate-half over dr)
+ *   L[pos] = [c' | kr]         the latent cache row, dc + dr values
+ *   for each head h and position t in 0..pos, with Wukv [dc, nh*(dn+dv)]
+ *   (head h's columns = [k part (dn) | v part (dv)]):
+ *     k_{t,h} = [ L[t, :dc] . Wukv[:, k part of h] | L[t, dc:] ]   (dn + dr)
+ *     v_{t,h} =   L[t, :dc] . Wukv[:, v part of h]                 (dv)
+ *     o_h     = softmax_t( q_h . k_{t,h} / sqrt(dn + dr) ) . v_{t,h}
+ *   out   = x + concat_h(o_h) . Wo                Wo [nh*dv, H]
+ * The keys and values are formed per position exactly as defined (no
+ * absorption of Wukv into the query or the output).                       */
+typedef struct {
+  int hidden;      /* H  */
+  int n_heads;     /* nh */
+  int d_nope;      /* dn: query/key dims without position encoding */
+  int d_rope;      /* dr: query/key dims with RoPE (even); the key part is shared by all heads */
+  int d_v;         /* dv: value dims per head */
+  int d_latent;    /* dc: compressed key/value dims */
+  int s_max;       /* S: latent cache capacity per row */
+  double rope_theta;
+  double rms_eps;
+} orc_mla_config;
+
+/* One batch row of the MLA decode block (definition above).  lc [S, dc+dr] is
+ * this row's latent cache, updated in place at slot pos only.  The dbg_*
+ * outputs may each be NULL: dbg_q [nh*(dn+dr)] (rope parts rotated),
+ * dbg_lat [dc+dr] (the new latent row), dbg_o [nh*dv], dbg_proj [H].
+ * Returns 0, or -1 if pos is outside [0, S) or the config is invalid.      */
+int orc_mla_row(const orc_mla_config* c, const double* x, const double* g,
+                const double* wq, const double* wdkv, const double* g_kv,
+                const double* wukv, const double* wo, double* lc, int pos,
+                double* out, double* dbg_q, double* dbg_lat, double* dbg_o,
+                double* dbg_proj);
+
 #ifdef __cplusplus
 }
 #endif

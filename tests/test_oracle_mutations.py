@@ -41,6 +41,21 @@ MUTATIONS = {
     "ffn_down_transposed": ("orc_matvec(I, H, a, wd, proj);",
                             "for (int j = 0; j < H; ++j) {\n    proj[j] = 0.0;\n    "
                             "for (int i = 0; i < I; ++i) proj[j] += a[i] * wd[(size_t)j * (size_t)I + i];\n  }"),
+    "mla_value_from_key_columns": ("const double* wvv = wk + dn;", "const double* wvv = wk;"),
+    "mla_scale_without_rope_dims": ("const double scale = 1.0 / sqrt((double)dq);",
+                                    "const double scale = 1.0 / sqrt((double)dn);"),
+    "mla_no_latent_norm": ("orc_rmsnorm(dc, a, g_kv, c->rms_eps, a);", ""),
+    "mla_rope_on_nope_part": ("orc_rope(dr, c->rope_theta, pos, q + (size_t)h * dq + dn);",
+                              "orc_rope(dr, c->rope_theta, pos, q + (size_t)h * dq);"),
+    "mla_no_rope_on_shared_key": ("orc_rope(dr, c->rope_theta, pos, a + dc);", ""),
+    "mla_drop_new_token": ("const int dq = dn + dr, dl = dc + dr, ntok = pos + 1;",
+                           "const int dq = dn + dr, dl = dc + dr, ntok = pos;"),
+    "mla_head_stride_without_value": ("const double* wk = wukv + (size_t)h * (dn + dv);",
+                                      "const double* wk = wukv + (size_t)h * dn;"),
+    "mla_key_rope_part_from_latent_head": ("for (int j = 0; j < dr; ++j) kt[dn + j] = lt[dc + j];",
+                                           "for (int j = 0; j < dr; ++j) kt[dn + j] = lt[j];"),
+    "mla_drop_residual": ("for (int i = 0; i < H; ++i) out[i] = x[i] + proj[i];\n\n  if (dbg_q)",
+                          "for (int i = 0; i < H; ++i) out[i] = proj[i];\n\n  if (dbg_q)"),
     "transposed_weight": (
         "const double* row = W + (size_t)i * (size_t)N;\n    for (int j = 0; j < N; ++j) y[j] += xi * row[j];",
         "for (int j = 0; j < N; ++j) y[j] += xi * W[(size_t)j * (size_t)K + i];"),

@@ -348,6 +348,21 @@ def test_ffn_oracle_regression_fixture():
     np.testing.assert_allclose(r["out"][0], stored["out"], rtol=1e-12, atol=1e-13)
 
 
+def test_mla_oracle_regression_fixture():
+    # The same guard for the MLA oracle (tiny MLA workload, seed 0).
+    import os
+    import sys
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    import gen_oracle_regression as gen
+    r = gen.compute_mla()
+    with open(os.path.join(here, "tiny_mla_oracle_regression.txt")) as fh:
+        rows = [ln.split() for ln in fh if not ln.startswith("#")]
+    stored = {row[0]: np.array([float(v) for v in row[1:]]) for row in rows}
+    np.testing.assert_allclose(r["out"], stored["out"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["o"], stored["o"], rtol=1e-12, atol=1e-13)
+
+
 # --------------------------------------------- second RMSNorm + SwiGLU FFN --
 # [LNA §一] puts "第二个 RMS Norm、FFN" after the residual of the attention block
 # of the LLaMA architecture; the FFN is read as LLaMA's gated form
@@ -452,3 +467,169 @@ def test_ffn_single_unit_one_hot_weights_transpose_check():
     expect = h.copy()
     expect[4] += 2.0 * (n1 / (1.0 + math.exp(-n1))) * n1
     np.testing.assert_allclose(r["out"], expect, rtol=1e-14, atol=1e-15)
+
+
+# -------------------------------------------------------- MLA variant --
+# [CF §5.2 DeepSeek-MLA特殊处理]; projections read as DeepSeek's MLA with an
+# uncompressed query (oracle.h).  Pins: pure-Python brute force of the
+# definition, the weight-absorbed form (a different association of the same
+# products, as the GPU computes it), one cached token, uniform attention,
+# a closed form of the latent RMSNorm, RoPE on the position parts only, and
+# the cache write.
+def _mla_cfg(H=16, nh=3, dn=4, dr=4, dv=3, dc=6, S=7, theta=1e4, eps=1e-6):
+    return dict(hidden=H, n_heads=nh, d_nope=dn, d_rope=dr, d_v=dv, d_latent=dc, s_max=S,
+                rope_theta=theta, rms_eps=eps)
+
+
+def _mla_inputs(cfg, seed=5, std=0.3):
+    r = np.random.default_rng(seed)
+    H, nh, dn, dr, dv, dc, S = (cfg[k] for k in ("hidden", "n_heads", "d_nope", "d_rope", "d_v",
+                                                 "d_latent", "s_max"))
+    return dict(x=r.normal(size=H), g=1 + 0.1 * r.normal(size=H),
+                wq=std * r.normal(size=(H, nh * (dn + dr))),
+                wdkv=std * r.normal(size=(H, dc + dr)), g_kv=1 + 0.1 * r.normal(size=dc),
+                wukv=std * r.normal(size=(dc, nh * (dn + dv))),
+                wo=std * r.normal(size=(nh * dv, H)), lc=r.normal(size=(S, dc + dr)))
+
+
+def _mla(cfg, t, pos, lc=None):
+    lc = t["lc"].copy() if lc is None else lc
+    res = oracle.mla_row(cfg, t["x"], t["g"], t["wq"], t["wdkv"], t["g_kv"], t["wukv"],
+                         t["wo"], lc, pos)
+    return res, lc
+
+
+def test_mla_brute_force_python_loops():
+    cfg = _mla_cfg(H=6, nh=2, dn=2, dr=2, dv=3, dc=3, S=4, theta=100.0, eps=1e-3)
+    t = _mla_inputs(cfg, seed=8, std=0.5)
+    pos = 2
+    res, lc = _mla(cfg, t, pos)
+    H, nh, dn, dr, dv, dc = 6, 2, 2, 2, 3, 3
+    x, g = list(t["x"]), list(t["g"])
+    ms = sum(v * v for v in x) / H
+    n = [x[i] / math.sqrt(ms + 1e-3) * g[i] for i in range(H)]
+    q = [sum(n[i] * t["wq"][i][j] for i in range(H)) for j in range(nh * (dn + dr))]
+    a = [sum(n[i] * t["wdkv"][i][j] for i in range(H)) for j in range(dc + dr)]
+    msc = sum(a[i] * a[i] for i in range(dc)) / dc
+    lat = [a[i] / math.sqrt(msc + 1e-3) * t["g_kv"][i] for i in range(dc)]
+    # rotate-half over dr = 2: one pair (0, 1), angle pos * 100^0 = pos
+    ang = float(pos)
+
+    def rot(u0, u1):
+        return u0 * math.cos(ang) - u1 * math.sin(ang), u1 * math.cos(ang) + u0 * math.sin(ang)
+
+    lat += list(rot(a[dc], a[dc + 1]))
+    for h in range(nh):
+        b = h * (dn + dr) + dn
+        q[b], q[b + 1] = rot(q[b], q[b + 1])
+    rows = [list(t["lc"][s]) for s in range(pos)] + [lat]
+    o = []
+    for h in range(nh):
+        qh = q[h * (dn + dr):(h + 1) * (dn + dr)]
+        scores, vals = [], []
+        for row in rows:
+            k = [sum(row[i] * t["wukv"][i][h * (dn + dv) + j] for i in range(dc))
+                 for j in range(dn)] + row[dc:]
+            v = [sum(row[i] * t["wukv"][i][h * (dn + dv) + dn + j] for i in range(dc))
+                 for j in range(dv)]
+            scores.append(sum(qh[j] * k[j] for j in range(dn + dr)) / math.sqrt(dn + dr))
+            vals.append(v)
+        mx = max(scores)
+        e = [math.exp(s - mx) for s in scores]
+        o += [sum(e[t_] * vals[t_][j] for t_ in range(len(rows))) / sum(e) for j in range(dv)]
+    out = [x[i] + sum(o[k] * t["wo"][k][i] for k in range(nh * dv)) for i in range(H)]
+    np.testing.assert_allclose(res["lat"], lat, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["q"], q, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["o"], o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["out"], out, rtol=1e-12, atol=1e-13)
+
+
+def test_mla_weight_absorbed_form_matches():
+    # The GPU's association: q_lat_h = Wuk_h q_nope_h (dc values), scores
+    # against the latent rows directly, o_lat_h = sum_t w_t L[t,:dc], then
+    # o_h = o_lat_h . Wuv_h.  Same products, different order.
+    cfg = _mla_cfg(H=24, nh=4, dn=8, dr=6, dv=5, dc=10, S=9)
+    t = _mla_inputs(cfg)
+    pos = 7
+    res, lc = _mla(cfg, t, pos)
+    nh, dn, dr, dv, dc = 4, 8, 6, 5, 10
+    W = t["wukv"].reshape(dc, nh, dn + dv)
+    L = lc[:pos + 1]
+    o = np.empty((nh, dv))
+    for h in range(nh):
+        qh = res["q"][h * (dn + dr):(h + 1) * (dn + dr)]
+        q_lat = W[:, h, :dn] @ qh[:dn]
+        s = (L[:, :dc] @ q_lat + L[:, dc:] @ qh[dn:]) / math.sqrt(dn + dr)
+        w = np.exp(s - s.max())
+        w /= w.sum()
+        o[h] = (w @ L[:, :dc]) @ W[:, h, dn:]
+    np.testing.assert_allclose(res["o"], o.reshape(-1), rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(res["proj"], o.reshape(-1) @ t["wo"], rtol=1e-11, atol=1e-13)
+
+
+def test_mla_one_token_attends_to_its_own_value():
+    cfg = _mla_cfg()
+    t = _mla_inputs(cfg, seed=9)
+    res, lc = _mla(cfg, t, 0)
+    nh, dn, dv, dc = 3, 4, 3, 6
+    W = t["wukv"].reshape(dc, nh, dn + dv)
+    v0 = np.concatenate([res["lat"][:dc] @ W[:, h, dn:] for h in range(nh)])
+    np.testing.assert_allclose(res["o"], v0, rtol=1e-12, atol=1e-14)
+
+
+def test_mla_zero_query_gives_uniform_attention():
+    cfg = _mla_cfg()
+    t = _mla_inputs(cfg, seed=10)
+    t["wq"][:] = 0.0
+    pos = 5
+    res, lc = _mla(cfg, t, pos)
+    nh, dn, dv, dc = 3, 4, 3, 6
+    W = t["wukv"].reshape(dc, nh, dn + dv)
+    mean_lat = lc[:pos + 1, :dc].mean(axis=0)  # includes the new row
+    want = np.concatenate([mean_lat @ W[:, h, dn:] for h in range(nh)])
+    np.testing.assert_allclose(res["o"], want, rtol=1e-12, atol=1e-14)
+
+
+def test_mla_latent_norm_closed_form():
+    # Every compressed column of Wdkv the same vector w: c_i = n . w = kappa
+    # for all i, so RMSNorm gives c'_i = g_kv_i kappa / sqrt(kappa^2 + eps).
+    cfg = _mla_cfg(eps=0.04)
+    t = _mla_inputs(cfg, seed=11)
+    dc = 6
+    t["wdkv"][:, :dc] = t["wdkv"][:, :1]
+    res, _ = _mla(cfg, t, 3)
+    n = oracle.rmsnorm(t["x"], t["g"], 0.04)
+    kappa = n @ t["wdkv"][:, 0]
+    np.testing.assert_allclose(res["lat"][:dc], t["g_kv"] * kappa / math.sqrt(kappa ** 2 + 0.04),
+                               rtol=1e-12)
+
+
+def test_mla_rope_only_on_position_parts_and_only_slot_pos_written():
+    cfg = _mla_cfg()
+    t = _mla_inputs(cfg, seed=12)
+    nh, dn, dr, dc = 3, 4, 4, 6
+    n = oracle.rmsnorm(t["x"], t["g"], 1e-6)
+    q_lin = (n @ t["wq"]).reshape(nh, dn + dr)
+    a_lin = n @ t["wdkv"]
+    for pos in (0, 4):
+        res, lc = _mla(cfg, t, pos)
+        q = res["q"].reshape(nh, dn + dr)
+        np.testing.assert_allclose(q[:, :dn], q_lin[:, :dn], rtol=1e-13)  # never rotated
+        for h in range(nh):
+            np.testing.assert_allclose(q[h, dn:], oracle.rope(q_lin[h, dn:], pos, 1e4),
+                                       rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(res["lat"][dc:], oracle.rope(a_lin[dc:], pos, 1e4),
+                                   rtol=1e-12, atol=1e-14)
+        if pos == 0:
+            np.testing.assert_allclose(q, q_lin, rtol=1e-13)  # RoPE at 0 is the identity
+        changed = np.any(lc != t["lc"], axis=1)
+        assert list(np.nonzero(changed)[0]) == [pos]
+        np.testing.assert_array_equal(lc[pos], res["lat"])
+
+
+def test_mla_rejects_bad_position():
+    cfg = _mla_cfg()
+    t = _mla_inputs(cfg)
+    for pos in (-1, cfg["s_max"]):
+        with pytest.raises(ValueError):
+            _mla(cfg, t, pos)
