@@ -41,6 +41,12 @@ class CfFfnConfig(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("stage_bytes", ctypes.c_int32)]
 
 
+class CfMlaConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "hidden", "n_heads", "d_nope", "d_rope", "d_v", "d_latent", "max_batch", "s_max")] + [
+        ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
 class CfLaunchInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "cluster_size", "batch_tile", "group", "rows_per_wtile", "pos_per_ktile",
@@ -90,6 +96,12 @@ SIGNATURES = {
     "cf_ffn_set_timeline": (ctypes.c_int, [_vp, _vp]),
     "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
                                      + [_vp] * 9),
+    "cf_noalloc_get_status": (ctypes.c_int, []),
+    "cf_mla_create": (ctypes.c_int, [ctypes.POINTER(CfMlaConfig), ctypes.POINTER(_vp)]),
+    "cf_mla_decode": (ctypes.c_int, [_vp, ctypes.c_int32] + [_vp] * 11),
+    "cf_mla_get_status": (ctypes.c_int, [_vp]),
+    "cf_mla_launch_info": (ctypes.c_int, [_vp] + [ctypes.POINTER(ctypes.c_int32)] * 5),
+    "cf_mla_destroy": (None, [_vp]),
 }
 
 TIMELINE_SLOTS = 32
@@ -200,6 +212,11 @@ def cf_decode_attn_block_noalloc(cfg: CfConfig, batch, hidden_states, ln_weight,
     return lib().cf_decode_attn_block_noalloc(
         ctypes.byref(cfg), int(batch), _ptr(hidden_states), _ptr(ln_weight), _ptr(w_qkv),
         _ptr(w_o), _ptr(k_cache), _ptr(v_cache), _ptr(positions), _ptr(out), _stream(stream))
+
+
+def cf_noalloc_get_status() -> int:
+    """Read and clear the error word of the allocation-free calls (current device)."""
+    return lib().cf_noalloc_get_status()
 
 
 def cf_get_status(handle) -> int:
@@ -379,6 +396,70 @@ class FfnBlock:
     def close(self) -> None:
         if getattr(self, "handle", None):
             lib().cf_ffn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------- MLA --
+def cf_mla_create_rc(cfg: CfMlaConfig | None) -> tuple[int, int | None]:
+    """Return code and handle without raising (boundary tests)."""
+    h = _vp()
+    rc = lib().cf_mla_create(ctypes.byref(cfg) if cfg is not None else None, ctypes.byref(h))
+    return rc, h.value
+
+
+def cf_mla_decode(handle, batch, hidden, ln_weight, w_q, w_dkv, kv_norm_weight, w_ukv, w_o,
+                  latent_cache, positions, out, stream=None) -> int:
+    return lib().cf_mla_decode(handle, int(batch), _ptr(hidden), _ptr(ln_weight), _ptr(w_q),
+                               _ptr(w_dkv), _ptr(kv_norm_weight), _ptr(w_ukv), _ptr(w_o),
+                               _ptr(latent_cache), _ptr(positions), _ptr(out), _stream(stream))
+
+
+class MlaBlock:
+    """Owns one cf_mla_handle; calling it enqueues one MLA decode step
+    (include/cf_mla.h).  Raises CfError on any non-zero return code."""
+
+    def __init__(self, hidden, n_heads, max_batch, s_max, rope_theta=1e4, rms_eps=1e-6,
+                 dtype=CF_BF16, d_nope=128, d_rope=64, d_v=128, d_latent=512):
+        if isinstance(dtype, str):
+            dtype = {"f32": CF_F32, "f16": CF_F16, "bf16": CF_BF16}[dtype]
+        self.cfg = CfMlaConfig(int(hidden), int(n_heads), int(d_nope), int(d_rope), int(d_v),
+                               int(d_latent), int(max_batch), int(s_max), float(rope_theta),
+                               float(rms_eps), int(dtype))
+        rc, h = cf_mla_create_rc(self.cfg)
+        if rc != CF_OK:
+            raise CfError(rc, "cf_mla_create")
+        self.handle = h
+
+    def __call__(self, batch, hidden, ln_weight, w_q, w_dkv, kv_norm_weight, w_ukv, w_o,
+                 latent_cache, positions, out, stream=None):
+        rc = cf_mla_decode(self.handle, batch, hidden, ln_weight, w_q, w_dkv, kv_norm_weight,
+                           w_ukv, w_o, latent_cache, positions, out, stream)
+        if rc != CF_OK:
+            raise CfError(rc, "cf_mla_decode")
+        return out
+
+    def launch_info(self) -> dict:
+        v = [ctypes.c_int32() for _ in range(5)]
+        rc = lib().cf_mla_launch_info(self.handle, *[ctypes.byref(x) for x in v])
+        if rc != CF_OK:
+            raise CfError(rc, "cf_mla_launch_info")
+        return dict(zip(("clusters", "cluster_size", "stages", "stage_bytes", "smem_bytes"),
+                        (x.value for x in v)))
+
+    def status(self) -> int:
+        import torch
+        torch.cuda.synchronize()
+        return lib().cf_mla_get_status(self.handle)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            lib().cf_mla_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -421,13 +421,16 @@ const KernelEntry* pick_rows_entry(const cf_config& c, int stage_req, const cuda
                                    Plan& pl) {
   if (!wants_rows(c)) return nullptr;
   const int D = c.head_dim, G = c.n_q_heads / c.n_kv_heads;
-  const KernelEntry* e = nullptr;
-  const int n = registry_rows(&e);
+  const KernelEntry* e0 = nullptr;
+  const KernelEntry* e1 = nullptr;
+  const int n0 = registry_rows(&e0);
+  const int n = n0 + registry_rows_sweep(&e1);
   const KernelEntry* best = nullptr;
   long long best_waves = 0, best_blocks = 0;
   for (int i = 0; i < n; ++i) {
-    const KernelEntry& k = e[i];
+    const KernelEntry& k = i < n0 ? e0[i] : e1[i - n0];
     if (k.dtype != c.dtype || k.D != D || k.G != G) continue;
+    if (k.explicit_only && !(c.batch_tile == k.BT && c.rows_per_block == k.RPC)) continue;
     if (c.batch_tile > 0 && k.BT != c.batch_tile) continue;
     if (c.rows_per_block > 0 && k.RPC != c.rows_per_block) continue;
     if (c.batch_tile == 0 && k.BT > std::max(4, c.max_batch)) continue;
@@ -485,29 +488,41 @@ int plan_handle(const cf_config& c, cf_handle& h) {
     ke = find_entry(c.dtype, D, G, BT);
     if (ke == nullptr) return CF_ERR_UNSUPPORTED;
     // Cluster size: requested, else the smallest power of two >= 2 that gives
-    // about two blocks per SM over the whole grid (capped by head_dim/4 and by
-    // the hidden size's 16-byte column bands).
+    // about two blocks per SM over the whole grid (capped by head_dim/4, by
+    // the hidden size's 16-byte column bands and by a K band of at least 64
+    // rows per block), then halved while the grid's clusters would not all be
+    // resident at once (measured: a second wave costs more than a smaller
+    // cluster -- the GQA layer at batch 1 runs 1.3x faster with 8 clusters of
+    // 8 than with 8 clusters of 16, of which only 7 fit).
     const int clusters = c.n_kv_heads * ((c.max_batch + BT - 1) / BT);
     int N = c.cluster_size;
     if (N == 0) {
       N = 2;
       while (N < 16 && N * 2 <= D / 4 && ((c.hidden / (N * 2)) * esize(c.dtype)) % 16 == 0 &&
+             c.hidden / (N * 2) >= 64 &&
              (long long)clusters * N * 2 <= 2LL * prop.multiProcessorCount)
         N *= 2;
     }
     if (N > D / 4 || ((c.hidden / N) * esize(c.dtype)) % 16 != 0) return CF_ERR_INVALID_ARG;
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, ke->fn) != cudaSuccess) return CF_ERR_CUDA;
-    int cps = c.ctas_per_sm;
-    if (cps == 0) {
-      // registers are allocated per thread in multiples of 8
-      const int regs = (fa.numRegs + 7) / 8 * 8;
-      const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
-      cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
+    for (;;) {
+      int cps = c.ctas_per_sm;
+      if (cps == 0) {
+        // registers are allocated per thread in multiples of 8
+        const int regs = (fa.numRegs + 7) / 8 * 8;
+        const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
+        cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
+      }
+      if (!make_plan(c, N, BT, stage_req, cps, prop, pl) &&
+          !(cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)))
+        return CF_ERR_UNSUPPORTED;
+      if (c.cluster_size != 0 || N <= 2) break;
+      const int rc = prepare_function(ke->fn, pl.L.total, N);
+      if (rc != CF_OK) return rc;
+      if (resident_clusters(ke->fn, N, pl.L.total) >= clusters) break;
+      N /= 2;
     }
-    if (!make_plan(c, N, BT, stage_req, cps, prop, pl) &&
-        !(cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)))
-      return CF_ERR_UNSUPPORTED;
   }
   const int N = pl.N;
   {
@@ -1020,16 +1035,35 @@ extern "C" int cf_decode_attn_block_noalloc(const cf_config* cfg, int32_t batch,
   }
   // The kernel leaves the accumulator and counters at zero, but the array
   // keeps whatever the previous call left (e.g. one stopped by an error), so
-  // the regions this call uses are cleared first, on the same stream.
+  // the regions this call uses are cleared first, on the same stream.  The
+  // error word is not: it collects the device-detected errors of every call
+  // until cf_noalloc_get_status reads and clears it.
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t acc_bytes = (size_t)batch * cfg->hidden * sizeof(float);
   const size_t cnt_bytes = counter_slots(s.h.main().plan, batch) * sizeof(int);
   if (cudaMemsetAsync(s.h.acc, 0, acc_bytes, st) != cudaSuccess ||
-      cudaMemsetAsync(s.h.counters, 0, cnt_bytes, st) != cudaSuccess ||
-      cudaMemsetAsync(s.h.errflag, 0, sizeof(int), st) != cudaSuccess) {
+      cudaMemsetAsync(s.h.counters, 0, cnt_bytes, st) != cudaSuccess) {
     cudaGetLastError();
     return CF_ERR_CUDA;
   }
   return cf_decode_attn_block(&s.h, batch, hidden_states, ln_weight, w_qkv, w_o, k_cache, v_cache,
                               positions, out, stream);
+}
+
+extern "C" int cf_noalloc_get_status(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CF_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return CF_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocSlot& s = g_noalloc[dev];
+  if (!s.ready) return CF_OK;  // no call has run on this device
+  int* flag_dev =
+      reinterpret_cast<int*>(s.scratch + kNoAllocAccFloats * 4 + kNoAllocCounters * 4);
+  int flag = 0;
+  if (cudaMemcpy(&flag, flag_dev, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CF_ERR_CUDA;
+  if (flag != 0 && cudaMemset(flag_dev, 0, sizeof(int)) != cudaSuccess) return CF_ERR_CUDA;
+  if (flag & kDevErrTimeout) return CF_ERR_DEVICE_TIMEOUT;
+  if (flag & kDevErrPosRange) return CF_ERR_DEVICE_POS_RANGE;
+  return CF_OK;
 }

@@ -15,6 +15,9 @@ struct KernelEntry {
   const void* fn;  // __global__ function
   int mode = 0;
   int RPC = 0;     // rows per block (mode 1)
+  // Only chosen when the caller asks for exactly this batch tile and rows per
+  // block (instances kept to measure other cluster sizes, N = BT / RPC).
+  bool explicit_only = false;
 };
 
 // Each instantiation unit (cf_inst_*.cu) defines one of these.
@@ -22,5 +25,6 @@ int registry_f32(const KernelEntry** out);
 int registry_f16(const KernelEntry** out);
 int registry_bf16(const KernelEntry** out);
 int registry_rows(const KernelEntry** out);
+int registry_rows_sweep(const KernelEntry** out);
 
 }  // namespace cf

@@ -33,7 +33,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode attention-block µs/step and achieved HBM GB/s (fraction of GB300 peak)"
-DEFAULT_WORKLOAD = "llama2_7b_layer_b1_p1024_f16"
+# The largest single-GPU workload: the Llama-2-7B-shaped layer at 16384 cached
+# positions, 32 independently seeded layers chained in one CUDA graph.
+DEFAULT_WORKLOAD = "llama2_7b_layer_b1_p16384_f16_x32"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_L2_BYTES = 129 * 1024 * 1024
 # The fused kernel's name by launch mode (cf_launch_info.mode): 0 the
@@ -93,20 +95,37 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# Sources of the fused decode kernels and their launch planning (not the
-# measurement probes, the test primitives or the unfused baseline).
-FUSED_KERNEL_SOURCES = ("cf_api.cu", "cf_attention.cuh", "cf_attention_tc.cuh", "cf_cluster.cuh",
-                        "cf_common.cuh", "cf_inst_bf16.cu", "cf_inst_f16.cu", "cf_inst_f32.cu",
-                        "cf_inst_rows.cu", "cf_kernel.cuh", "cf_kernel_rows.cuh", "cf_mma.cuh",
-                        "cf_params.h", "cf_ptx.cuh", "cf_registry.h")
+# Translation units of the fused decode kernels and their launch planning; the
+# hash covers them and every header they include (found by following the
+# #include "..." lines), so a change to any of them invalidates a recorded
+# ncu traffic figure.
+FUSED_KERNEL_ROOTS = ("cf_api.cu", "cf_inst_bf16.cu", "cf_inst_f16.cu", "cf_inst_f32.cu",
+                      "cf_inst_rows.cu", "cf_inst_rows_sweep.cu")
+
+
+def fused_kernel_sources() -> list[str]:
+    import re
+    dirs = [os.path.join(ROOT, "attention_block_gb300", "csrc"), os.path.join(ROOT, "include")]
+    seen, todo = {}, list(FUSED_KERNEL_ROOTS)
+    while todo:
+        name = todo.pop()
+        if name in seen:
+            continue
+        for d in dirs:
+            path = os.path.join(d, name)
+            if os.path.exists(path):
+                seen[name] = path
+                with open(path, encoding="utf-8") as fh:
+                    todo += re.findall(r'^\s*#\s*include\s+"([^"]+)"', fh.read(), re.M)
+                break
+    return [seen[n] for n in sorted(seen)]
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "attention_block_gb300", "csrc")
-    for name in FUSED_KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(name.encode() + fh.read())
+    for path in fused_kernel_sources():
+        with open(path, "rb") as fh:
+            h.update(os.path.basename(path).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -165,7 +184,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader", "-lms", "50"],
+                 "--format=csv,noheader", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -350,9 +369,15 @@ def main(argv=None):
                     help="--impl reference: seconds of oracle work per step (0 = the run's "
                          "~150 s spread over its steps)")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--collectives", action="store_true",
+                    help="instead of the decode step: time the DSMEM collectives "
+                         "(ClusterReduce all-reduce / reduce-scatter, ClusterGather) for "
+                         "cluster sizes 2-16 in SM cycles, one JSON line each")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.collectives:
+        return run_collectives(args)
 
     import torch
 
@@ -361,7 +386,12 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    w = synth.WORKLOADS[args.workload]
+    if args.workload in synth.MLA_WORKLOADS:
+        wm = synth.MLA_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            return run_mla_reference(args, wm, rank, world)
+        return run_mla(args, wm, rank, world, local)
+    w = synth.workload(args.workload)
 
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
@@ -666,7 +696,8 @@ def main(argv=None):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32",
+            "dtype": w.dtype,
+            "accumulate": "f32",
             "data": "synthetic",
             "config": {
                 "workload": w.name + (f"+ffn_i{args.ffn}" if wf else ""),
@@ -717,6 +748,326 @@ def main(argv=None):
     blk.close()
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+# ------------------------------------------------------------- MLA variant --
+MLA_TENSORS = ("hidden", "ln_weight", "w_q", "w_dkv", "kv_norm_weight", "w_ukv", "w_o")
+
+
+def mla_bytes(w, positions) -> int:
+    """Bytes one MLA decode step must move at minimum: every weight once, the
+    latent cache rows [0, p_b) of every row, the new latent row written,
+    hidden read, out written, positions."""
+    es = 4 if w.dtype == "f32" else 2
+    nh, dn, dr, dv, dc, H = w.n_heads, w.d_nope, w.d_rope, w.d_v, w.d_latent, w.hidden
+    weights = (H * nh * (dn + dr) + H * (dc + dr) + dc * nh * (dn + dv) + nh * dv * H + H
+               + dc) * es
+    cache = sum(int(p) * (dc + dr) * es for p in positions) + w.batch * (dc + dr) * es
+    return weights + cache + 2 * w.batch * H * es + 4 * w.batch
+
+
+def run_mla(args, w, rank, world, local):
+    """The MLA variant's decode step (cf_mla_decode), timed like the attention
+    block: graph replays over replicas spanning >= 4x L2, CUDA events on the
+    launching stream, max over ranks; e2e with host buffers; the float64
+    oracle as the CPU baseline."""
+    import torch
+    import torch.distributed as dist
+
+    from attention_block_gb300 import binding, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or FALLBACK_L2_BYTES
+    layer0 = synth.make_mla_layer(w, seed=0, device=dev)
+    pos0 = layer0["positions"].tolist()
+    step_bytes = mla_bytes(w, pos0)
+    n_rep = max(1, -(-4 * l2 // step_bytes))
+    reps = [layer0] + [synth.make_mla_layer(w, seed=r, device=dev) for r in range(1, n_rep)]
+    R = len(reps)
+    footprint = sum(tensor_bytes(L) for L in reps)
+    blk = binding.MlaBlock(w.hidden, w.n_heads, w.batch, w.s_max, w.rope_theta, w.rms_eps,
+                           w.dtype, w.d_nope, w.d_rope, w.d_v, w.d_latent)
+    info = blk.launch_info()
+    outs = [torch.empty_like(L["hidden"]) for L in reps]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(r, x=None, pos=None, ev=None):
+        L = reps[r]
+        args_ = [L[k] for k in MLA_TENSORS]
+        if x is not None:
+            args_[0] = x
+        if ev:
+            ev[0].record(stream)
+        blk(w.batch, *args_, L["latent_cache"], L["positions"] if pos is None else pos, outs[r],
+            stream)
+        if ev:
+            ev[1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i % R)
+    stream.synchronize()
+    if blk.status() != binding.CF_OK:
+        raise RuntimeError("MLA device status after warm-up")
+    n_lat = min(args.steps, 4 * R)
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(n_lat)]
+    with torch.cuda.stream(stream):
+        for i in range(n_lat):
+            step(i % R, ev=evs[i])
+    stream.synchronize()
+    launch_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    use_graph = not args.no_graph
+    single, full = [], None
+    if use_graph:
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(r)
+            single.append(g)
+        full = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(full, stream=stream):
+            for r in range(R):
+                step(r)
+        with torch.cuda.stream(stream):
+            for _ in range(-(-args.warmup // R)):
+                full.replay()
+        stream.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        h0 = time.time()
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            if use_graph:
+                for _ in range(args.steps // R):
+                    full.replay()
+                for r in range(args.steps % R):
+                    single[r].replay()
+            else:
+                for i in range(args.steps):
+                    step(i % R)
+            t_end.record(stream)
+        stream.synchronize()
+        clk.mark(h0, time.time())
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    elapsed_s = t_start.elapsed_time(t_end) / 1e3
+    if blk.status() != binding.CF_OK:
+        raise RuntimeError("MLA device status after timed steps")
+    # end to end: hidden rows and positions from pinned host memory, out back
+    h_in = [L["hidden"].cpu().pin_memory() for L in reps]
+    p_in = [L["positions"].cpu().pin_memory() for L in reps]
+    h_out = torch.empty_like(h_in[0]).pin_memory()
+    x_dev = [torch.empty_like(L["hidden"]) for L in reps]
+    p_dev = [torch.empty_like(L["positions"]) for L in reps]
+
+    def e2e_step(i):
+        r = i % R
+        x_dev[r].copy_(h_in[r], non_blocking=True)
+        p_dev[r].copy_(p_in[r], non_blocking=True)
+        step(r, x=x_dev[r], pos=p_dev[r])
+        h_out.copy_(outs[r], non_blocking=True)
+
+    e2e_steps = max(args.e2e_steps, 3)
+    e2e_graphs = []
+    if use_graph:
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                e2e_step(r)
+            e2e_graphs.append(g)
+    run = (lambda i: e2e_graphs[i % R].replay()) if e2e_graphs else e2e_step
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            run(i)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            run(i)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    rows = allgather_rows([float(step_bytes * args.steps), elapsed_s, float(args.steps),
+                           float(step_bytes * e2e_steps), e2e_s, float(e2e_steps)], world, dev)
+    agg = aggregate([r[:3] for r in rows])
+    agg_e2e = aggregate([r[3:] for r in rows])
+    if rank == 0:
+        peak, peak_kind = measured_peak_hbm()
+        launch_s = elapsed_s / args.steps
+        achieved = step_bytes / launch_s / 1e9
+        cpu = None
+        if world == 1:
+            cpu = time_mla_oracle(w, reps[0], args.cpu_budget)
+        B, H = w.batch, w.hidden
+        line = {
+            "metric": METRIC, "value": round(agg["gbs"], 2), "unit": "GB/s",
+            "us_per_step": round(elapsed_s / args.steps * 1e6, 3), "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_s / args.steps * 1e3, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "accumulate": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "variant": "DeepSeek MLA (latent KV cache)",
+                       "hidden": H, "heads": w.n_heads, "d_nope": w.d_nope, "d_rope": w.d_rope,
+                       "d_v": w.d_v, "d_latent": w.d_latent, "batch": B,
+                       "positions": w.positions, "storage_dtype": w.dtype,
+                       "algorithmic_bytes_per_step": step_bytes,
+                       "l2_defeat": (f"inputs larger than L2: {R} independently seeded "
+                                     f"replica(s) rotated, {footprint / 1e9:.2f} GB resident vs "
+                                     f"L2 {l2 / 1e6:.0f} MB"),
+                       "cuda_graph": use_graph, "parallelism": f"replicas x{world}",
+                       "launch": info},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "traffic": None, "kernel": "cf_mla_kernel",
+                         "launch_us_avg": round(launch_s * 1e6, 3),
+                         "launch_timing": "timed region (graph replays) / launches",
+                         "isolated_launch_us_avg": round(sum(launch_ms) / len(launch_ms) * 1e3, 3),
+                         "bytes_per_launch": step_bytes,
+                         "frac_of_nominal_7_9TBs": round(achieved / 7900.0, 4)},
+            "e2e": {"value": round(agg_e2e["gbs"], 2), "unit": "GB/s",
+                    "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
+                    "h2d_bytes_per_step": B * H * h_in[0].element_size() + 4 * B,
+                    "d2h_bytes_per_step": B * H * h_out.element_size(),
+                    "steps": e2e_steps, "cuda_graph": bool(e2e_graphs)},
+            "gpu_launches": args.steps,
+            "clocks": clk.result(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    blk.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def time_mla_oracle(w, layer, budget_s: float):
+    """The float64 MLA oracle on one host core over batch rows of one step
+    until budget_s is spent (at least one row), scaled to a full step."""
+    import oracle
+    from attention_block_gb300 import synth
+
+    f = {k: synth.to_f64(layer[k]) for k in MLA_TENSORS}
+    pos = layer["positions"].tolist()
+    rows, t_rows, b = 0, 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        lc = synth.to_f64(layer["latent_cache"][b]).copy()
+        s = time.perf_counter()
+        oracle.mla_row(w.oracle_cfg(), f["hidden"][b], f["ln_weight"], f["w_q"], f["w_dkv"],
+                       f["kv_norm_weight"], f["w_ukv"], f["w_o"], lc, int(pos[b]))
+        t_rows += time.perf_counter() - s
+        rows += 1
+        b = (b + 1) % w.batch
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    t_step = t_rows / rows * w.batch
+    return {"value": mla_bytes(w, pos) / t_step / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "us_per_step": t_step * 1e6,
+            "sample": (f"{rows} batch row(s) of one layer through the float64 single-threaded "
+                       f"C MLA oracle; per-step time = per-row time x {w.batch} rows"),
+            "host_cpus": os.cpu_count()}
+
+
+def run_mla_reference(args, w, rank, world):
+    """The float64 MLA oracle as the reference arm, host cores, rank 0 only."""
+    if rank != 0:
+        return 0
+    from attention_block_gb300 import synth
+
+    layer = synth.make_mla_layer(w, seed=0, device="cpu")
+    budget = (args.ref_budget if args.ref_budget > 0
+              else max(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    times = [time_mla_oracle(w, layer, budget)["us_per_step"] for _ in range(args.steps)]
+    t = sum(times) / len(times) / 1e6
+    step_bytes = mla_bytes(w, layer["positions"].tolist())
+    val = step_bytes / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+            "us_per_step": round(t * 1e6, 1), "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "variant": "DeepSeek MLA (latent KV cache)",
+                       "batch": w.batch, "positions": w.positions,
+                       "algorithmic_bytes_per_step": step_bytes},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"each step: rows of one layer through the float64 MLA "
+                                       f"oracle for ~{budget:.1f} s, scaled to {w.batch} rows",
+                             "host_cpus": os.cpu_count()},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# The collectives timed by --collectives: (name, kind of cf_bench_cluster_collective,
+# floats per block for a given total payload and cluster size).  The totals
+# follow the 128 KB payload of the pages' primitive latency table: for the
+# all-reduce the blocks' contributions sum to it, for the gather it is what
+# every block ends up holding, for the reduce-scatter it is each block's input
+# (64 KB: the receive buffers must fit next to it in shared memory).
+COLLECTIVES = (
+    ("allreduce_sum", 0, lambda total, N: total // (4 * N)),
+    ("allreduce_max", 1, lambda total, N: total // (4 * N)),
+    ("reduce_scatter", 2, lambda total, N: total // 2 // (4 * N)),
+    ("gather", 3, lambda total, N: total // (4 * N)),
+)
+
+
+def run_collectives(args):
+    """Median over repeats of the slowest block's SM cycles inside one
+    collective, and that time in microseconds at the sampled SM clock."""
+    import torch
+
+    from attention_block_gb300 import binding
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    total = 128 * 1024
+    reps = max(5, min(args.steps, 50))
+    with ClockSampler(dev.index) as clk:
+        rows = []
+        for name, kind, per_block in COLLECTIVES:
+            for N in (2, 4, 8, 16):
+                n = per_block(total, N)
+                length = N * n if kind >= 2 else n
+                x = torch.randn(N, length, device=dev)
+                out = torch.empty(N, N * n if kind == 3 else (n if kind == 2 else length),
+                                  device=dev)
+                err = torch.zeros(1, dtype=torch.int32, device=dev)
+                cyc = torch.zeros(N, dtype=torch.int64, device=dev)
+                got = []
+                for i in range(args.warmup + reps):
+                    rc = binding.cf_bench_cluster_collective(kind, N, n, x, out, err, cyc)
+                    if rc != binding.CF_OK:
+                        raise RuntimeError(f"{name} N={N}: {binding.strerror(rc)}")
+                    torch.cuda.synchronize()
+                    if i >= args.warmup:
+                        got.append(int(cyc.max().item()))
+                if int(err.item()) != 0:
+                    raise RuntimeError(f"{name} N={N}: device error {int(err.item())}")
+                rows.append((name, N, n, statistics.median(got)))
+    clocks = clk.result()
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0
+    for name, N, n, cyc in rows:
+        payload = (N * n if name != "reduce_scatter" else N * n) * 4
+        print(json.dumps({"collective": name, "cluster_size": N, "floats_per_block": n,
+                          "payload_bytes": payload, "cycles": cyc,
+                          "us": round(cyc / mhz, 3), "sm_mhz": mhz,
+                          "rounds": (N - 1).bit_length(), "clocks": clocks}), flush=True)
     return 0
 
 

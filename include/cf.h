@@ -199,13 +199,22 @@ void cf_destroy(cf_handle* h);
  * array it uses.  All calls share the one array: calls whose work overlaps
  * on the GPU (different streams, or different host threads) race and give
  * wrong results -- serialize them.  Device-detected errors (out-of-range
- * positions) are not reported (there is no handle to read them from); such
- * rows are left as described for cf_decode_attn_block.  Arguments, layouts
- * and other return codes are those of cf_create + cf_decode_attn_block. */
+ * positions, an in-kernel wait that timed out) accumulate in one word of the
+ * array until cf_noalloc_get_status reads and clears it; out-of-range rows
+ * are left as described for cf_decode_attn_block.  Arguments, layouts and
+ * other return codes are those of cf_create + cf_decode_attn_block. */
 int cf_decode_attn_block_noalloc(const cf_config* cfg, int32_t batch, const void* hidden_states,
                                  const void* ln_weight, const void* w_qkv, const void* w_o,
                                  void* k_cache, void* v_cache, const int32_t* positions,
                                  void* out, void* stream);
+
+/* Read and clear the device-side error word that the allocation-free calls
+ * on the current device share (synchronize their stream first).  Allocates
+ * nothing.  Returns CF_OK (also when no such call has run on this device),
+ * CF_ERR_DEVICE_POS_RANGE, CF_ERR_DEVICE_TIMEOUT, CF_ERR_UNSUPPORTED (device
+ * index beyond the library's table) or CF_ERR_CUDA.  Like the calls whose
+ * errors it reports, it has no counterpart on the pages. */
+int cf_noalloc_get_status(void);
 
 #ifdef __cplusplus
 }

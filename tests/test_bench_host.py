@@ -104,3 +104,19 @@ def test_reference_arm_prints_the_contract_line_on_the_host():
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "tiny_h256_mha4x64_b1_p128_f32"
+
+
+def test_kernel_hash_covers_every_included_source():
+    """The traffic record is keyed by a hash of the fused kernels' sources;
+    it must cover every header they include (e.g. the tcgen05 helpers)."""
+    names = {os.path.basename(p) for p in bench.fused_kernel_sources()}
+    assert {"cf_api.cu", "cf_kernel.cuh", "cf_kernel_rows.cuh", "cf_tc05.cuh", "cf_ptx.cuh",
+            "cf_attention.cuh", "cf_attention_tc.cuh", "cf_cluster.cuh", "cf_params.h"} <= names
+
+
+def test_default_workload_is_the_largest_single_gpu_one():
+    from attention_block_gb300 import synth
+    w = synth.WORKLOADS[bench.DEFAULT_WORKLOAD]
+    sizes = {n: bench.algorithmic_bytes(x, [int(x.positions.split(":")[1])] * x.batch) * x.layers
+             for n, x in synth.WORKLOADS.items() if x.positions.startswith("fixed")}
+    assert w.layers == 32 and bench.DEFAULT_WORKLOAD == max(sizes, key=sizes.get)

@@ -122,3 +122,40 @@ def test_package_import_loads_no_library_and_fails_loudly_when_missing(tmp_path,
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(RuntimeError):
         binding.lib(build_if_missing=False)
+
+
+MLA_BASE = dict(hidden=2048, n_heads=16, d_nope=128, d_rope=64, d_v=128, d_latent=512,
+                max_batch=1, s_max=4097, rope_theta=1e4, rms_eps=1e-6, dtype=binding.CF_BF16)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hidden=0), binding.CF_ERR_INVALID_ARG),
+    (dict(s_max=0), binding.CF_ERR_INVALID_ARG),
+    (dict(rope_theta=0.0), binding.CF_ERR_INVALID_ARG),
+    (dict(rms_eps=-1.0), binding.CF_ERR_INVALID_ARG),
+    (dict(dtype=7), binding.CF_ERR_INVALID_ARG),
+    (dict(d_latent=256), binding.CF_ERR_UNSUPPORTED),
+    (dict(d_rope=32), binding.CF_ERR_UNSUPPORTED),
+    (dict(dtype=binding.CF_F32), binding.CF_ERR_UNSUPPORTED),
+    (dict(n_heads=12), binding.CF_ERR_UNSUPPORTED),
+    (dict(n_heads=64), binding.CF_ERR_UNSUPPORTED),
+    (dict(hidden=2000), binding.CF_ERR_UNSUPPORTED),
+    (dict(hidden=32768), binding.CF_ERR_UNSUPPORTED),
+    (dict(max_batch=5), binding.CF_ERR_UNSUPPORTED),
+])
+def test_mla_create_rejects_bad_config_before_cuda(kw, code):
+    cfg = dict(MLA_BASE)
+    cfg.update(kw)
+    c = binding.CfMlaConfig(*(cfg[k] for k in ("hidden", "n_heads", "d_nope", "d_rope", "d_v",
+                                               "d_latent", "max_batch", "s_max", "rope_theta",
+                                               "rms_eps", "dtype")))
+    rc, h = binding.cf_mla_create_rc(c)
+    assert rc == code and not h
+
+
+def test_mla_null_arguments():
+    assert binding.cf_mla_create_rc(None)[0] == binding.CF_ERR_INVALID_ARG
+    lib = binding.lib()
+    assert lib.cf_mla_decode(None, 1, *([None] * 11)) == binding.CF_ERR_INVALID_ARG
+    assert lib.cf_mla_get_status(None) == binding.CF_ERR_INVALID_ARG
+    lib.cf_mla_destroy(None)
