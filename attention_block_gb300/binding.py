@@ -102,6 +102,7 @@ SIGNATURES = {
     "cf_mla_get_status": (ctypes.c_int, [_vp]),
     "cf_mla_launch_info": (ctypes.c_int, [_vp] + [ctypes.POINTER(ctypes.c_int32)] * 5),
     "cf_mla_destroy": (None, [_vp]),
+    "cf_mla_set_timeline": (ctypes.c_int, [_vp, _vp]),
 }
 
 TIMELINE_SLOTS = 32
@@ -110,6 +111,9 @@ TIMELINE_NAMES = ["start", "norm", "proj", "reduce_scatter", "gather", "attn", "
                   "proj_loop_last_warp", "rinv", "attn_first_tile", "oproj_first_tile",
                   "oproj_loop", "ticket", "oproj_tile1", "oproj_tile2", "oproj_tile3",
                   "attn_loop", "attn_warps"]
+MLA_TIMELINE_NAMES = ["start", "norm", "A", "bar1", "B", "bar2", "C_first_tile", "C_tiles",
+                      "C_merged", "bar3", "D_wuv", "D_allreduce", "D_wo", "end", "prod_A",
+                      "prod_C", "prod_D"]
 # Timeline slot holding the block's SM id (a value, not a time).
 TIMELINE_SMID = 26
 
@@ -443,6 +447,11 @@ class MlaBlock:
         if rc != CF_OK:
             raise CfError(rc, "cf_mla_decode")
         return out
+
+    def set_timeline(self, stamps) -> None:
+        rc = lib().cf_mla_set_timeline(self.handle, _ptr(stamps))
+        if rc != CF_OK:
+            raise CfError(rc, "cf_mla_set_timeline")
 
     def launch_info(self) -> dict:
         v = [ctypes.c_int32() for _ in range(5)]

@@ -56,6 +56,7 @@
 #include "cf_mla.h"
 #include "cf_params.h"
 #include "cf_ptx.cuh"
+#include "cf_test.h"
 #include "cf_tmap.h"
 
 namespace cf {
@@ -76,6 +77,7 @@ constexpr int GW = DQ;          // columns per projection group (192)
 constexpr int RT = 32;          // latent rows per cache tile
 constexpr int REC = DC + 4;     // state record: o_lat[512], m, l, 2 pad
 constexpr int MAX_STAGES = 8;
+constexpr int kMaxClusters = 64;  // resident clusters the phase-D merge handles
 constexpr int STAGE_BYTES = RT * DL * 2;  // 36,864: the largest item (a cache tile)
 static_assert(KT * GW * 2 <= STAGE_BYTES && DC % KT == 0 && DCB % KT == 0, "stage plan");
 
@@ -98,12 +100,13 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   int* bar;             // [0] arrivals, [1] generation of the grid barrier
   int* tickets;         // [NCLU] per column band, zero between launches
   int* errflag;
+  unsigned long long* timeline;  // optional [grid][kMlaTlSlots] globaltimer stamps (NULL = off)
   int B, H, nh, S;
   int ncl, nb;          // clusters, blocks
   int ncr_max;          // clusters per row, rounded up
   int stages;
   int wob;              // W_o box width (64 or 128)
-  int off_bars, off_xs, off_scr, off_misc;
+  int off_bars, off_xs, off_scr, off_misc, off_sc;
   float eps;
   float qk_scale_log2;  // log2(e) / sqrt(DQ)
   float turn_hi[DR / 2], turn_lo[DR / 2];  // RoPE turn rates theta^(-2i/DR) / (2 pi)
@@ -111,12 +114,41 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
 
 __host__ __device__ inline int c1_cols(int nh) { return nh * DQ + DL; }
 
+// Phase stamps of the optional timeline (a tuning aid; one row per block).
+enum MlaTimelineSlot {
+  kMlaTlStart = 0,      // after the start-up cluster barrier
+  kMlaTlNorm = 1,       // consumers: dependency wait and x * ln_weight done
+  kMlaTlA = 2,          // projection tiles consumed and flushed
+  kMlaTlBar1 = 3,       // grid barrier 1 passed
+  kMlaTlB = 4,          // absorption / latent row done
+  kMlaTlBar2 = 5,       // grid barrier 2 passed
+  kMlaTlC0 = 6,         // first cache tile in hand (or no tile)
+  kMlaTlC1 = 7,         // cache tiles and the new row folded in
+  kMlaTlC2 = 8,         // sparse ClusterReduce merged and written
+  kMlaTlBar3 = 9,       // grid barrier 3 passed
+  kMlaTlD0 = 10,        // w_uv product done
+  kMlaTlD1 = 11,        // DSMEM all-reduce of o_h done
+  kMlaTlD2 = 12,        // w_o product and atomics done
+  kMlaTlEnd = 13,       // before the final cluster barrier
+  kMlaTlProdA = 14,     // producer: projection tiles issued
+  kMlaTlProdC = 15,     // producer: cache tiles issued
+  kMlaTlProdD = 16,     // producer: everything issued
+  kMlaTlSlots = 32
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Bounded wait until *word != old (written by other blocks of this fully
-// resident grid).  On expiry it records kDevErrTimeout and returns false.
+// resident grid), with acquire semantics.  On expiry it records
+// kDevErrTimeout and returns false.
 static __device__ __noinline__ bool wait_word_changes(const int* word, int old, int* errflag) {
   const long long t0 = clock64();
   for (uint32_t spins = 1;; ++spins) {
-    if (*reinterpret_cast<const volatile int*>(word) != old) return true;
+    if (ld_acquire_gpu(word) != old) return true;
     if ((spins & 255u) == 0) {
       if (*reinterpret_cast<volatile int*>(errflag) & kDevErrTimeout) return false;
       if (clock64() - t0 > kWaitLimitCycles) {
@@ -129,19 +161,23 @@ static __device__ __noinline__ bool wait_word_changes(const int* word, int old, 
 }
 
 // Grid-wide barrier of the consumer threads (thread 0 of each block takes
-// part).  `gen` is the generation this block last saw (thread 0 only).
+// part, after a block barrier, so its release covers the block's writes).
+// The arrival is an acquire-release add; the last arrival resets the count
+// and publishes a new generation with a release add; the others wait for it
+// with acquire loads.  `gen` is the generation this block last saw (thread 0
+// only).
 __device__ __forceinline__ void grid_sync(const Params& p, int& gen, int tid) {
   named_sync(kBarConsumers, kConsumers);
   if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&p.bar[0], 1) == p.nb - 1) {
-      atomicExch(&p.bar[0], 0);
-      __threadfence();
-      atomicAdd(&p.bar[1], 1);
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(old) : "l"(&p.bar[0]) : "memory");
+    if (old == p.nb - 1) {
+      asm volatile("st.relaxed.gpu.global.s32 [%0], 0;" ::"l"(&p.bar[0]) : "memory");
+      asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(&p.bar[1]) : "memory");
     } else {
       wait_word_changes(&p.bar[1], gen, p.errflag);
     }
-    __threadfence();
     ++gen;
   }
   named_sync(kBarConsumers, kConsumers);
@@ -206,6 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
   float* s_red = reinterpret_cast<float*>(s_flag + 4);    // [8] block reductions
   const Plan pl = plan_of(p, blk);
   const int ab = p.B * DV;  // floats of the phase-D all-reduce
+  auto stamp = [&](int slot) {
+    if (p.timeline != nullptr && (tid == 0 || (slot >= kMlaTlProdA && lane == 0)))
+      p.timeline[(size_t)blk * kMlaTlSlots + slot] = globaltimer_ns();
+  };
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
@@ -227,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
   }
   __syncthreads();
   cluster_sync_all();  // peers' barriers exist before any DSMEM traffic
+  stamp(kMlaTlStart);
 
   const int KTN = H / KT;
   if (warp == kConsumerWarps) {
@@ -256,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
         uint8_t* dst = slot(KT * DN * 2, bar);
         tma_load_2d(dst, &p.tm_wukv, h * (DN + DV), ib * KT, bar, pol);
       }
+      stamp(kMlaTlProdA);
       // C: this block's cached latent rows (written by earlier steps)
       asm volatile("griddepcontrol.wait;" ::: "memory");
       {
@@ -270,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
           bulk_load_1d(dst, base + (size_t)t * DL, (uint32_t)(n * DL * 2), bar, pol);
         }
       }
+      stamp(kMlaTlProdC);
       // D: w_uv rows of this block's latent band, then w_o of its column
       // band, box by box (both 64-row halves of each)
       for (int h = cl; h < nh; h += p.ncl) {
@@ -284,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
             tma_load_2d(dst, &p.tm_wo, rank * cb + cx * p.wob, h * DV + rb * KT, bar, pol);
           }
       }
+      stamp(kMlaTlProdD);
     }
     __syncwarp();
   } else {
@@ -329,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
         named_sync(kBarConsumers, kConsumers);
       }
     }
+    stamp(kMlaTlNorm);
     int it = 0;
     // ---- A: projection partial sums ---------------------------------------
     {
@@ -387,7 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       }
       if (cur >= 0) flush(cur);
     }
+    stamp(kMlaTlA);
     grid_sync(p, gen, tid);
+    stamp(kMlaTlBar1);
 
     // ---- B: absorption, query RoPE, the latent row ------------------------
     for (int item = blk; item < nh * (DC / KT); item += p.nb, ++it) {
@@ -473,7 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       }
       named_sync(kBarConsumers, kConsumers);
     }
+    stamp(kMlaTlB);
     grid_sync(p, gen, tid);
+    stamp(kMlaTlBar2);
 
     // ---- C: attention over this block's share of the latent cache ---------
     {
@@ -485,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       sub_range(pos >= 0 ? pos : 0, pl.sidx, pl.nsub, t0, t1);
       const bool fold_new = pos >= 0 && pl.sidx == pl.nsub - 1;
       // this warp's heads h = warp + 8k; query parts of the lane's dims,
-      // pre-scaled into log2 units
+      // pre-scaled into log2 units (16-byte loads)
       float qc[HPW][16], qr[HPW][2];
       float m[HPW], l[HPW], o[HPW][16];
 #pragma unroll
@@ -496,43 +545,94 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
         for (int e = 0; e < 16; ++e) o[k][e] = 0.f;
         const float* qh = p.qf + ((size_t)b * nh + warp + kConsumerWarps * k) * DL;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) qc[k][e] = __ldcg(qh + 16 * lane + e) * p.qk_scale_log2;
-        qr[k][0] = __ldcg(qh + DC + 2 * lane) * p.qk_scale_log2;
-        qr[k][1] = __ldcg(qh + DC + 2 * lane + 1) * p.qk_scale_log2;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(qh + 16 * lane) + q4);
+          qc[k][4 * q4] = v.x * p.qk_scale_log2;
+          qc[k][4 * q4 + 1] = v.y * p.qk_scale_log2;
+          qc[k][4 * q4 + 2] = v.z * p.qk_scale_log2;
+          qc[k][4 * q4 + 3] = v.w * p.qk_scale_log2;
+        }
+        const float2 r2 = __ldcg(reinterpret_cast<const float2*>(qh + DC) + lane);
+        qr[k][0] = r2.x * p.qk_scale_log2;
+        qr[k][1] = r2.y * p.qk_scale_log2;
       }
-      // One group of n <= 32 latent rows: scores by a transposed reduction
-      // (lane t ends with row t's score), online-softmax update, o += p c.
-      auto group = [&](auto&& row_c, auto&& row_r, int n) {
+      float* sbuf = reinterpret_cast<float*>(sm + p.off_sc) + warp * HPW * RT;  // [HPW][RT]
+      // n <= RT rows: (1) scores, two rows at a time (HPW * 2 independent
+      // dot products per lane, reduced over the warp by one transposed
+      // shuffle reduction) into sbuf; (2) per head the tile's online-softmax
+      // update, probabilities back into sbuf; (3) o += p c, rows reloaded.
+      auto attend_rows = [&](auto&& row_c, auto&& row_r, int n) {
+        constexpr int PB = 2, NV = HPW * PB;
+        for (int t0r = 0; t0r < n; t0r += PB) {
+          float cf[PB][16], rf[PB][2];
 #pragma unroll
-        for (int k = 0; k < HPW; ++k) {
-          float v[32];
+          for (int j = 0; j < PB; ++j) {
+            if (t0r + j < n) {
+              row_c(t0r + j, cf[j]);
+              row_r(t0r + j, rf[j]);
+            } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            float a = 0.f;
-            if (t < n) {
-              float c[16], rr[2];
-              row_c(t, c);
-              row_r(t, rr);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) a = fmaf(qc[k][e], c[e], a);
-              a = fmaf(qr[k][0], rr[0], fmaf(qr[k][1], rr[1], a));
+              for (int e = 0; e < 16; ++e) cf[j][e] = 0.f;
+              rf[j][0] = rf[j][1] = 0.f;
             }
-            v[t] = a;
           }
+          float v[NV];
+#pragma unroll
+          for (int k = 0; k < HPW; ++k)
+#pragma unroll
+            for (int j = 0; j < PB; ++j) {
+              float a0 = qr[k][0] * rf[j][0], a1 = qr[k][1] * rf[j][1];
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                a0 = fmaf(qc[k][e], cf[j][e], a0);
+                a1 = fmaf(qc[k][e + 1], cf[j][e + 1], a1);
+              }
+              v[k * PB + j] = a0 + a1;
+            }
+          // transposed reduction: after the halving rounds lane l holds value
+          // index idx(l) (bits from lane bits 4, 3, ... down), the remaining
+          // rounds complete the sum within each lane group
+          int cnt = NV;
 #pragma unroll
           for (int w = 16; w >= 1; w >>= 1) {
-            const bool upper = (lane & w) != 0;
+            if (cnt > 1) {
+              const bool upper = (lane & w) != 0;
+              const int half = cnt / 2;
 #pragma unroll
-            for (int i = 0; i < w; ++i) {
-              const float send = upper ? v[i] : v[i + w];
-              const float keep = upper ? v[i + w] : v[i];
-              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+              for (int i = 0; i < NV / 2; ++i) {
+                if (i < half) {
+                  const float send = upper ? v[i] : v[i + half];
+                  const float keep = upper ? v[i + half] : v[i];
+                  v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                }
+              }
+              cnt = half;
+            } else {
+              v[0] += __shfl_xor_sync(0xffffffffu, v[0], w);
             }
           }
-          const float sc = lane < n ? v[0] : -INFINITY;  // lane t: score of row t
+          // idx = sum over the halving rounds of (lane bit set ? half : 0)
+          int idx = 0, lowmask = 0;
+          {
+            int c2 = NV, w = 16;
+            while (c2 > 1) {
+              c2 /= 2;
+              if (lane & w) idx += c2;
+              w >>= 1;
+            }
+            lowmask = 2 * w - 1;  // lanes below the last halving bit share the value
+          }
+          const int k = idx / PB, j = idx % PB;
+          if ((lane & lowmask) == 0 && t0r + j < n) sbuf[k * RT + t0r + j] = v[0];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < HPW; ++k) {
+          const float sc = lane < n ? sbuf[k * RT + lane] : -INFINITY;
           float mt = sc;
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+          for (int off = 16; off >= 1; off >>= 1)
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
           const float mn = fmaxf(m[k], mt);
           const float alpha = exp2f(m[k] - mn);  // m = -inf, mn finite: 0
           const float pr = lane < n ? exp2f(sc - mn) : 0.f;
@@ -543,40 +643,57 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
           m[k] = mn;
 #pragma unroll
           for (int e = 0; e < 16; ++e) o[k][e] *= alpha;
-          for (int t = 0; t < n; ++t) {
-            const float pt = __shfl_sync(0xffffffffu, pr, t);
-            float c[16];
-            row_c(t, c);
+          __syncwarp();
+          if (lane < n) sbuf[k * RT + lane] = pr;
+        }
+        __syncwarp();
+        for (int t = 0; t < n; t += 2) {
+          float c0[16], c1[16];
+          row_c(t, c0);
+          if (t + 1 < n) row_c(t + 1, c1);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[k][e] = fmaf(pt, c[e], o[k][e]);
+          for (int k = 0; k < HPW; ++k) {
+            const float p0 = sbuf[k * RT + t];
+            const float p1 = t + 1 < n ? sbuf[k * RT + t + 1] : 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              o[k][e] = fmaf(p0, c0[e], t + 1 < n ? fmaf(p1, c1[e], o[k][e]) : o[k][e]);
           }
         }
+        __syncwarp();
       };
       for (int tt = t0; tt < t1; tt += RT, ++it) {
         const int n = min(RT, t1 - tt);
         const int s = it % p.stages;
         mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        if (tt == t0) stamp(kMlaTlC0);
         const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
-        group(
+        attend_rows(
             [&](int t, float* c) {
               const uint4* q4 = reinterpret_cast<const uint4*>(tile + t * DL + 16 * lane);
               cvt8<T>(q4[0], c);
               cvt8<T>(q4[1], c + 8);
             },
             [&](int t, float* r2) { load_cvt<T, 2>(tile + t * DL + DC + 2 * lane, r2); }, n);
-        __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       if (fold_new) {
         const float* nl = p.lat + (size_t)b * DL;
-        group(
+        attend_rows(
             [&](int, float* c) {
 #pragma unroll
-              for (int e = 0; e < 16; ++e) c[e] = __ldcg(nl + 16 * lane + e);
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(nl + 16 * lane) + q4);
+                c[4 * q4] = v.x;
+                c[4 * q4 + 1] = v.y;
+                c[4 * q4 + 2] = v.z;
+                c[4 * q4 + 3] = v.w;
+              }
             },
             [&](int, float* r2) {
-              r2[0] = __ldcg(nl + DC + 2 * lane);
-              r2[1] = __ldcg(nl + DC + 2 * lane + 1);
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(nl + DC) + lane);
+              r2[0] = v.x;
+              r2[1] = v.y;
             },
             1);
       }
@@ -598,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
                         rbar);
           if (lane == 0) st_async_v4(raddr + 4u * DC, make_float4(m[k], l[k], 0.f, 0.f), rbar);
         }
+        stamp(kMlaTlC1);
         mbar_wait_cluster(rx, 0, p.errflag);
         // merge the NCLU states of each owned head: slot j = (w / NCLU) * HPW
         // + k holds head h = w + 8k of warp w = rank + NCLU * (j / HPW)
@@ -624,7 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
         }
       }
     }
+    stamp(kMlaTlC2);
     grid_sync(p, gen, tid);
+    stamp(kMlaTlBar3);
 
     // ---- D: per head: merge, w_uv, w_o, residual --------------------------
     {
@@ -635,22 +755,53 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       float* rb = ov + BMAX * DV;               // [log2 NCLU][B][DV] all-reduce receive
       const int cpl = p.wob / 32;               // w_o columns per lane (2 or 4)
       for (int h = cl; h < nh; h += p.ncl) {
-        // merge of the row's cluster partials for this block's DCB latent rows
+        // merge of the row's cluster partials: warp b computes row b's
+        // per-cluster factors 2^(m_c - M) / L into s_mf, then every thread
+        // sums its latent rows over the clusters with independent loads
+        float* s_mf = s_red + 8;  // [BMAX][kMaxClusters]
+        if (warp < B) {
+          const int b = warp;
+          const int ncr = (p.ncl - b + B - 1) / B;
+          float mc[kMaxClusters / 32], lc[kMaxClusters / 32];
+          float mm = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kMaxClusters / 32; ++q) {
+            const int c = lane + 32 * q;
+            const float* ps = p.part + (((size_t)b * p.ncr_max + c) * nh + h) * REC;
+            mc[q] = c < ncr ? __ldcg(ps + DC) : -INFINITY;
+            lc[q] = c < ncr ? __ldcg(ps + DC + 1) : 0.f;
+            mm = fmaxf(mm, mc[q]);
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+          float L = 0.f, f[kMaxClusters / 32];
+#pragma unroll
+          for (int q = 0; q < kMaxClusters / 32; ++q) {
+            f[q] = mm == -INFINITY ? 0.f : exp2f(mc[q] - mm);
+            L = fmaf(lc[q], f[q], L);
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+#pragma unroll
+          for (int q = 0; q < kMaxClusters / 32; ++q)
+            s_mf[b * kMaxClusters + lane + 32 * q] = L > 0.f ? f[q] / L : 0.f;
+        }
+        named_sync(kBarConsumers, kConsumers);
         for (int idx = tid; idx < B * DCB; idx += kConsumers) {
           const int b = idx / DCB, i = rank * DCB + idx % DCB;
           const int ncr = (p.ncl - b + B - 1) / B;
-          float mm = -INFINITY;
-          for (int c = 0; c < ncr; ++c)
-            mm = fmaxf(mm, __ldcg(p.part + (((size_t)b * p.ncr_max + c) * nh + h) * REC + DC));
-          float L = 0.f, v = 0.f;
-          if (mm != -INFINITY)
-            for (int c = 0; c < ncr; ++c) {
-              const float* ps = p.part + (((size_t)b * p.ncr_max + c) * nh + h) * REC;
-              const float sc = exp2f(__ldcg(ps + DC) - mm);
-              L = fmaf(__ldcg(ps + DC + 1), sc, L);
-              v = fmaf(__ldcg(ps + i), sc, v);
-            }
-          ol[idx] = L > 0.f ? v / L : 0.f;
+          const float* ps = p.part + ((size_t)b * p.ncr_max * nh + h) * REC + i;
+          const size_t cstride = (size_t)nh * REC;
+          float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
+          int c = 0;
+          for (; c + 4 <= ncr; c += 4) {
+            v0 = fmaf(__ldcg(ps + c * cstride), s_mf[b * kMaxClusters + c], v0);
+            v1 = fmaf(__ldcg(ps + (c + 1) * cstride), s_mf[b * kMaxClusters + c + 1], v1);
+            v2 = fmaf(__ldcg(ps + (c + 2) * cstride), s_mf[b * kMaxClusters + c + 2], v2);
+            v3 = fmaf(__ldcg(ps + (c + 3) * cstride), s_mf[b * kMaxClusters + c + 3], v3);
+          }
+          for (; c < ncr; ++c) v0 = fmaf(__ldcg(ps + c * cstride), s_mf[b * kMaxClusters + c], v0);
+          ol[idx] = (v0 + v1) + (v2 + v3);
         }
         named_sync(kBarConsumers, kConsumers);
         // o_h partial over the block's latent rows, 64 per w_uv box: warp w
@@ -694,9 +845,11 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
           }
           named_sync(kBarConsumers, kConsumers);
         }
+        stamp(kMlaTlD0);
         // o_h = sum over the cluster's latent bands [CF §3.1.1]
         cluster_allreduce<OpSum, kConsumers, kBarConsumers>(ov, ab, rb, ga, rank, NCLU, tid,
                                                             p.errflag);
+        stamp(kMlaTlD1);
         // w_o rows h*DV.. of this block's column band, one box of wob columns
         // at a time (both 64-row halves), then its cross-warp sum and fp32
         // atomics into the accumulator [CF §3.2 原子写合并]
@@ -742,6 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
           }
           named_sync(kBarConsumers, kConsumers);
         }
+        stamp(kMlaTlD2);
         __threadfence();
         named_sync(kBarConsumers, kConsumers);
         if (tid == 0) {
@@ -770,6 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       }
     }
   }
+  stamp(kMlaTlEnd);
   // no block leaves while a peer may still write into its shared memory
   __syncwarp();
   cluster_sync_all();
@@ -777,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
 
 // Dynamic shared memory of a plan (bytes past the 1024-aligned base).
 struct Layout {
-  int bars, xs, scr, misc, total;
+  int bars, xs, scr, misc, sc, total;
 };
 inline Layout layout_for(int stages, int max_batch, int H, int nh) {
   auto r128 = [](int v) { return (v + 127) / 128 * 128; };
@@ -797,7 +952,9 @@ inline Layout layout_for(int stages, int max_batch, int H, int nh) {
                    3 * BMAX * DV;
   off += r128(4 * std::max(scrA, std::max(scrC, scrD)));
   L.misc = off;
-  off += r128(4 * (2 * BMAX + 4 + 8));
+  off += r128(4 * (2 * BMAX + 4 + 8 + BMAX * kMaxClusters));
+  L.sc = off;
+  off += r128(4 * kConsumerWarps * hpw * RT);
   L.total = off + 1024;
   return L;
 }
@@ -817,6 +974,7 @@ struct cf_mla_handle {
   void* ws = nullptr;
   float *y = nullptr, *qf = nullptr, *lat = nullptr, *part = nullptr, *acc = nullptr;
   int *bar = nullptr, *tickets = nullptr, *errflag = nullptr;
+  unsigned long long* timeline = nullptr;
   float turn_hi[DR / 2], turn_lo[DR / 2];
   struct MapSlot {
     const void* ptr = nullptr;
@@ -926,6 +1084,7 @@ int cf_mla_create(const cf_mla_config* cfg, cf_mla_handle** out) {
   h->ncl = resident_mla_clusters(h->fn, h->L.total);
   // one cluster per head in the last phase, at least one per batch row
   if (h->ncl < c.n_heads || h->ncl < c.max_batch) return fail(CF_ERR_CLUSTER);
+  h->ncl = std::min(h->ncl, kMaxClusters);
   h->nb = h->ncl * NCLU;
   // rows share the clusters (row b gets ceil((ncl - b) / batch)); sized for
   // a one-row call, which gives one row every cluster
@@ -1013,6 +1172,7 @@ int cf_mla_decode(cf_mla_handle* h, int32_t batch, const void* hidden_states,
   p.bar = h->bar;
   p.tickets = h->tickets;
   p.errflag = h->errflag;
+  p.timeline = h->timeline;
   p.B = batch;
   p.H = H;
   p.nh = nh;
@@ -1026,6 +1186,7 @@ int cf_mla_decode(cf_mla_handle* h, int32_t batch, const void* hidden_states,
   p.off_xs = h->L.xs;
   p.off_scr = h->L.scr;
   p.off_misc = h->L.misc;
+  p.off_sc = h->L.sc;
   p.eps = c.rms_eps;
   p.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)DQ));
   for (int i = 0; i < DR / 2; ++i) {
@@ -1075,6 +1236,12 @@ int cf_mla_launch_info(const cf_mla_handle* h, int32_t* clusters, int32_t* clust
   *stages = h->stages;
   *stage_bytes = STAGE_BYTES;
   *smem_bytes = h->L.total;
+  return CF_OK;
+}
+
+int cf_mla_set_timeline(cf_mla_handle* h, unsigned long long* stamps) {
+  if (h == nullptr) return CF_ERR_INVALID_ARG;
+  h->timeline = stamps;
   return CF_OK;
 }
 

@@ -65,6 +65,15 @@ int cf_bench_cluster_collective(int kind, int cluster_size, int n, const float* 
 struct cf_handle;
 int cf_set_timeline(struct cf_handle* h, unsigned long long* stamps);
 
+/* Phase timeline of later cf_mla_decode calls of handle h (a tuning aid):
+ * when `stamps` is a zeroed device buffer of clusters * 4 * 32 unsigned
+ * 64-bit values, every block writes %globaltimer (ns) at its phase boundaries
+ * into its row of 32 slots (slot meanings: the MlaTimelineSlot enum of the
+ * kernel source, listed in order by the Python binding).  NULL turns it off.
+ * Returns CF_OK or CF_ERR_INVALID_ARG. */
+struct cf_mla_handle;
+int cf_mla_set_timeline(struct cf_mla_handle* h, unsigned long long* stamps);
+
 /* One fifth-generation tensor-core product by one block:
  * d[128, n] = A . b[n, k]^T with fp32 accumulation, where A = a as a [128, k]
  * row-major array (a_mn = 0, K-major operand) or A = a^T with a a [k, 128]
