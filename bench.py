@@ -101,12 +101,14 @@ def measured_peak_hbm():
 # ncu traffic figure.
 FUSED_KERNEL_ROOTS = ("cf_api.cu", "cf_inst_bf16.cu", "cf_inst_f16.cu", "cf_inst_f32.cu",
                       "cf_inst_rows.cu", "cf_inst_rows_sweep.cu")
+# The MLA variant's translation unit.
+MLA_KERNEL_ROOTS = ("cf_mla.cu",)
 
 
-def fused_kernel_sources() -> list[str]:
+def fused_kernel_sources(roots=FUSED_KERNEL_ROOTS) -> list[str]:
     import re
     dirs = [os.path.join(ROOT, "attention_block_gb300", "csrc"), os.path.join(ROOT, "include")]
-    seen, todo = {}, list(FUSED_KERNEL_ROOTS)
+    seen, todo = {}, list(roots)
     while todo:
         name = todo.pop()
         if name in seen:
@@ -121,15 +123,15 @@ def fused_kernel_sources() -> list[str]:
     return [seen[n] for n in sorted(seen)]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(roots=FUSED_KERNEL_ROOTS) -> str:
     h = hashlib.sha256()
-    for path in fused_kernel_sources():
+    for path in fused_kernel_sources(roots):
         with open(path, "rb") as fh:
             h.update(os.path.basename(path).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, roots=FUSED_KERNEL_ROOTS):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -137,7 +139,7 @@ def recorded_traffic(workload: str):
         with open(path) as fh:
             rec = json.load(fh)
         ent = rec.get(workload)
-        if ent and ent.get("kernel_src_sha") == kernel_source_hash():
+        if ent and ent.get("kernel_src_sha") == kernel_source_hash(roots):
             return int(ent["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -931,7 +933,8 @@ def run_mla(args, w, rank, world, local):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "traffic": None, "kernel": "cf_mla_kernel",
+                         "traffic": recorded_traffic(w.name, MLA_KERNEL_ROOTS),
+                         "kernel": "cf_mla_kernel",
                          "launch_us_avg": round(launch_s * 1e6, 3),
                          "launch_timing": "timed region (graph replays) / launches",
                          "isolated_launch_us_avg": round(sum(launch_ms) / len(launch_ms) * 1e3, 3),
