@@ -31,8 +31,7 @@ class CfConfig(ctypes.Structure):
         ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)] + [
         (n, ctypes.c_int32) for n in (
             "dtype", "cluster_size", "batch_tile", "stage_bytes", "ctas_per_sm",
-            "prefetch_ahead", "prefetch_late", "pdl", "max_stages", "rows_per_block",
-            "kv_prefetch", "adaptive")]
+            "pdl", "max_stages", "rows_per_block", "adaptive")]
 
 
 class CfFfnConfig(ctypes.Structure):
@@ -94,6 +93,7 @@ SIGNATURES = {
     "cf_ffn_destroy": (None, [_vp]),
     "cf_ffn_kernels": (ctypes.c_int, [_vp, ctypes.c_int32] + [ctypes.POINTER(ctypes.c_int32)] * 2),
     "cf_ffn_set_timeline": (ctypes.c_int, [_vp, _vp]),
+    "cf_ffn_debug_a": (ctypes.c_int, [_vp, ctypes.c_int32, _vp]),
     "cf_decode_attn_block_noalloc": (ctypes.c_int, [ctypes.POINTER(CfConfig), ctypes.c_int32]
                                      + [_vp] * 9),
     "cf_noalloc_get_status": (ctypes.c_int, []),
@@ -168,15 +168,14 @@ def strerror(code: int) -> str:
 
 def make_config(hidden, n_q_heads, n_kv_heads, head_dim, max_batch, s_max, rope_theta=1e4,
                 rms_eps=1e-6, dtype=CF_F16, cluster_size=0, batch_tile=0, stage_bytes=0,
-                ctas_per_sm=0, prefetch_ahead=0, prefetch_late=0, pdl=0,
-                max_stages=0, rows_per_block=0, kv_prefetch=0, adaptive=0) -> CfConfig:
+                ctas_per_sm=0, pdl=0, max_stages=0, rows_per_block=0,
+                adaptive=0) -> CfConfig:
     if isinstance(dtype, str):
         dtype = {"f32": CF_F32, "f16": CF_F16, "bf16": CF_BF16}[dtype]
     return CfConfig(int(hidden), int(n_q_heads), int(n_kv_heads), int(head_dim),
                     int(max_batch), int(s_max), float(rope_theta), float(rms_eps), int(dtype),
                     int(cluster_size), int(batch_tile), int(stage_bytes), int(ctas_per_sm),
-                    int(prefetch_ahead), int(prefetch_late), int(pdl), int(max_stages),
-                    int(rows_per_block), int(kv_prefetch), int(adaptive))
+                    int(pdl), int(max_stages), int(rows_per_block), int(adaptive))
 
 
 def cf_create(cfg: CfConfig) -> int:
@@ -391,6 +390,16 @@ class FfnBlock:
         if n < 0:
             raise CfError(n, "cf_ffn_kernels")
         return {"kernels": n, "blocks1": b1.value, "blocks2": b2.value}
+
+    def debug_a(self, batch):
+        """The last call's intermediate activations [batch, I] (tensor-core
+        pair only), read back from the device as a float64 numpy array."""
+        import numpy as np
+        a = np.empty((int(batch), int(self.cfg.intermediate)), dtype=np.float32)
+        rc = lib().cf_ffn_debug_a(self.handle, int(batch), a.ctypes.data)
+        if rc != CF_OK:
+            raise CfError(rc, "cf_ffn_debug_a")
+        return a.astype(np.float64)
 
     def status(self) -> int:
         import torch

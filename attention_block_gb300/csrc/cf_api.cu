@@ -303,7 +303,6 @@ struct cf_handle {
   int* errflag = nullptr;
   float* dbg = nullptr;
   unsigned long long* timeline = nullptr;
-  int prefetch_ahead = 0, prefetch_late = 0, kv_prefetch = 0;
   bool pdl = true;
   float turn_hi[64], turn_lo[64];  // RoPE turn rates as float pairs (see KParams)
   // three-kernel (unfused) path: HBM intermediates and counters
@@ -332,9 +331,6 @@ int validate_config(const cf_config* c) {
   if (c->stage_bytes != 0 && (c->stage_bytes < 2048 || c->stage_bytes > 131072))
     return CF_ERR_INVALID_ARG;
   if (c->ctas_per_sm < 0 || c->ctas_per_sm > 2) return CF_ERR_INVALID_ARG;
-  if (c->prefetch_ahead < -1 || c->prefetch_ahead > 64) return CF_ERR_INVALID_ARG;
-  if (c->prefetch_late < -1 || c->prefetch_late > 3) return CF_ERR_INVALID_ARG;
-  if (c->kv_prefetch < -1 || c->kv_prefetch > 64) return CF_ERR_INVALID_ARG;
   if (c->adaptive < -1 || c->adaptive > 1) return CF_ERR_INVALID_ARG;
   if (c->pdl < -1 || c->pdl > 1) return CF_ERR_INVALID_ARG;
   if (c->max_stages < 0 || c->max_stages == 1 || c->max_stages > kMaxStages)
@@ -540,11 +536,6 @@ int plan_handle(const cf_config& c, cf_handle& h) {
   h.slots[0].plan = pl;
   h.slots[0].fn = ke->fn;
   h.slots[0].max_active_clusters = nclusters;
-  // Both L2 prefetches measured slower on the B = 1 Llama2 layer (they compete
-  // with the W_qkv stream), so they are off unless asked for.
-  h.prefetch_ahead = std::max(0, c.prefetch_ahead);
-  h.prefetch_late = std::max(0, c.prefetch_late);
-  h.kv_prefetch = c.kv_prefetch < 0 ? 0 : (c.kv_prefetch > 0 ? c.kv_prefetch : kDefaultKvPrefetch);
   h.pdl = c.pdl != -1;
   for (int i = 0; i < 64; ++i) {
     // turns per position: theta^(-2i/d) / (2 pi), split into hi + lo floats
@@ -772,9 +763,6 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
   kp.errflag = h->errflag;
   kp.dbg = h->dbg;
   kp.timeline = h->timeline;
-  kp.prefetch_ahead = h->prefetch_ahead;
-  kp.prefetch_late = h->prefetch_late;
-  kp.kv_prefetch = h->kv_prefetch;
   // The last min(4, nkv) blocks of a (tile, band) share its finalize when the
   // whole grid is resident at once (the earlier ones wait for the later).
   const long long grid_clusters = (long long)nkv * ((batch + pl.BT - 1) / pl.BT);

@@ -48,6 +48,7 @@
 #include "cf_ffn_tc.cuh"
 #include "cf_params.h"
 #include "cf_ptx.cuh"
+#include "cf_test.h"
 #include "cf_tmap.h"
 
 namespace cf {
@@ -742,6 +743,32 @@ extern "C" int cf_ffn_kernels(const cf_ffn_handle* h, int32_t batch, int32_t* bl
   if (blocks1) *blocks1 = tc ? h->blocks1 : h->blocks;
   if (blocks2) *blocks2 = tc ? h->blocks2 : 0;
   return tc ? 2 : 1;
+}
+
+extern "C" int cf_ffn_debug_a(const cf_ffn_handle* h, int32_t batch, float* a_out) {
+  if (h == nullptr || a_out == nullptr || batch < 1 || batch > h->cfg.max_batch)
+    return CF_ERR_INVALID_ARG;
+  if (!h->tc) return CF_ERR_UNSUPPORTED;
+  const int I = h->cfg.intermediate, Ip = h->Ip;
+  const size_t n = (size_t)batch * Ip;
+  uint16_t* hi = new (std::nothrow) uint16_t[2 * n];
+  if (hi == nullptr) return CF_ERR_CUDA;
+  uint16_t* lo = hi + n;
+  const bool ok = cudaMemcpy(hi, h->a_hi, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess &&
+                  cudaMemcpy(lo, h->a_lo, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (ok) {
+    const bool bf = h->cfg.dtype == CF_BF16;
+    for (int b = 0; b < batch; ++b)
+      for (int i = 0; i < I; ++i) {
+        const size_t k = (size_t)b * Ip + i;
+        a_out[(size_t)b * I + i] = (bf ? __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&hi[k]))
+                                       : __half2float(*reinterpret_cast<__half*>(&hi[k]))) +
+                                   (bf ? __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&lo[k]))
+                                       : __half2float(*reinterpret_cast<__half*>(&lo[k])));
+      }
+  }
+  delete[] hi;
+  return ok ? CF_OK : CF_ERR_CUDA;
 }
 
 extern "C" void cf_ffn_destroy(cf_ffn_handle* h) {

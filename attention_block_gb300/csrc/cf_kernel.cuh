@@ -181,7 +181,6 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
     // ============================================== TMA producer warp ====
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();
       int it = 0;
       auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
         const int s = it % p.stages;
@@ -190,37 +189,10 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
         mbar_arrive_expect_tx(bar, bytes);
         return ring + (size_t)s * p.stage_bytes;
       };
-      // L2 prefetch of the K/V and W_o boxes this block will need after its
-      // cluster exchanges, so HBM streams them while the block is still in
-      // the projection (the later TMA loads then hit L2).
-      auto prefetch_late = [&]() {
-        for (int bb = 0; bb < BT; ++bb) {
-          int t0, t1;
-          kv_tile_range(s_pos[bb], p.Rt, rank, N, t0, t1);
-          for (int t = t0; t < t1; ++t) {
-            tma_prefetch_4d(&p.tm_k, 0, g, t * p.Rt, b0 + bb, pol_keep);
-            tma_prefetch_4d(&p.tm_v, 0, g, t * p.Rt, b0 + bb, pol_keep);
-          }
-        }
-        for (int cb = 0; cb < ncb; ++cb)
-          for (int rt = 0; rt < nrt; ++rt)
-            tma_prefetch_2d(&p.tm_wo, k0 + cb * p.Co, g * G * D + rt * p.Ro, pol_keep);
-      };
-      auto prefetch_w = [&](int kt) {
-        const int y = k0 + kt * p.Rw;
-        for (int j = 0; j < G; ++j) tma_prefetch_2d(&p.tm_wqkv, (g * G + j) * D, y, pol);
-        tma_prefetch_2d(&p.tm_wqkv, (p.nq + g) * D, y, pol);
-        tma_prefetch_2d(&p.tm_wqkv, (p.nq + p.nkv + g) * D, y, pol);
-      };
       // Phase 1: W_qkv row tiles of this block's K band, G+2 head slices each
       // (the first `fill` were requested before the dependency wait).
       for (int kt = 0; kt < nkt; ++kt, ++it) {
-        if (kt < fill) {
-          if (kt == fill - 1 && p.prefetch_ahead > 0)
-            for (int k2 = fill; k2 < min(nkt, fill + p.prefetch_ahead); ++k2) prefetch_w(k2);
-          if (kt == fill - 1 && p.prefetch_late == 2) prefetch_late();
-          continue;
-        }
+        if (kt < fill) continue;
         uint64_t* bar;
         uint8_t* dst = slot(NSEG * seg_bytes, bar);
         const int y = k0 + kt * p.Rw;
@@ -228,18 +200,7 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
           tma_load_2d(dst + j * seg_bytes, &p.tm_wqkv, (g * G + j) * D, y, bar, pol);
         tma_load_2d(dst + G * seg_bytes, &p.tm_wqkv, (p.nq + g) * D, y, bar, pol);
         tma_load_2d(dst + (G + 1) * seg_bytes, &p.tm_wqkv, (p.nq + p.nkv + g) * D, y, bar, pol);
-        if (p.prefetch_ahead > 0) {
-          // keep a window of prefetch_ahead tiles beyond the ring in flight
-          if (kt == fill - 1)
-            for (int k2 = fill; k2 < min(nkt, fill + p.prefetch_ahead); ++k2) prefetch_w(k2);
-          else if (kt >= fill && kt + p.prefetch_ahead < nkt)
-            prefetch_w(kt + p.prefetch_ahead);
-        }
-        if (kt == fill - 1 && p.prefetch_late == 2) prefetch_late();
       }
-      // Default: queue the late prefetches behind the whole W_qkv stream, so
-      // they fill HBM's idle time during the cluster exchanges.
-      if (p.prefetch_late == 1) prefetch_late();
       if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdW] = globaltimer_ns();
       // Phase 2: K and V tiles of this block's share of each row's positions.
       const uint32_t kv_bytes = (uint32_t)(p.Rt * D * sizeof(T));
@@ -411,14 +372,6 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
         fence_proxy_async_smem();  // our stores into the stage precede the next TMA write
         named_sync(kBarConsumers, kConsumers);
         if (lane == 0) mbar_arrive(&empty[s_last]);  // hand the stage back
-      }
-      // Optional: pull this block's W_o band into L2 now that its own W_qkv
-      // stream is done, so the O-projection tiles later come from L2.
-      if (p.prefetch_late == 3 && tid == 0) {
-        const uint64_t keep = policy_evict_last();
-        for (int cb = 0; cb < ncb; ++cb)
-          for (int rt = 0; rt < nrt; ++rt)
-            tma_prefetch_2d(&p.tm_wo, k0 + cb * p.Co, g * G * D + rt * p.Ro, keep);
       }
       stamp(kTlRinv);
     }

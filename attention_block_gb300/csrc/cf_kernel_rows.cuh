@@ -216,30 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
         mbar_arrive_expect_tx(bar, bytes);
         return ring + (size_t)s * p.stage_bytes;
       };
-      // L2 prefetch of kv_prefetch K/V tiles of each owned row, spread over
-      // its sequence, issued in step with the W_qkv stream: the weights come
-      // mostly from L2 (the head's batch tiles share them), so DRAM has room
-      // for these, and the attention later mixes L2 hits into its DRAM stream.
-      const int npf = p.kv_prefetch;
-      const uint64_t pol_pf = policy_evict_normal();
-      const int nunits = RPC * npf, nwst = nkt * NCG;
-      int unit = 0;
-      auto prefetch_units = [&](int upto) {
-        for (; unit < upto && unit < nunits; ++unit) {
-          const int r = unit % RPC, j = unit / RPC;
-          int t0, t1;
-          kv_tile_range(s_pos[r0 + r], p.Rt, 0, 1, t0, t1);
-          if (j >= t1 - t0) continue;
-          const int n = min(npf, t1 - t0);
-          if (j >= n) continue;
-          const int t = t0 + (int)(((2LL * j + 1) * (t1 - t0)) / (2 * n));
-#pragma unroll
-          for (int bx = 0; bx < D / 64; ++bx) {
-            tma_prefetch_4d(&p.tm_k, bx * 64, g, t * p.Rt, b0 + r0 + r, pol_pf);
-            tma_prefetch_4d(&p.tm_v, bx * 64, g, t * p.Rt, b0 + r0 + r, pol_pf);
-          }
-        }
-      };
       // Phase 1: W_qkv tiles of the K band.  Each slice of Rw rows comes as
       // NCG stages of CB 64-column swizzled boxes (the G+2 head slices' NC
       // columns in order); the first stage of a slice also carries the
@@ -247,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       for (int kt = 0; kt < nkt; ++kt) {
         const int y = k0 + kt * p.Rw;
         for (int cg = 0; cg < NCG; ++cg, ++it) {
-          if (nunits > 0) prefetch_units((int)((long long)(kt * NCG + cg) * nunits / nwst));
           uint64_t* bar;
           uint8_t* dst = slot(CB * wbox_bytes + (cg == 0 ? x_bytes : 0u), bar);
           for (int bx = 0; bx < CB; ++bx) {
@@ -260,7 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           if (cg == 0) tma_load_2d(dst + CB * wbox_bytes, &p.tm_x, y, b0, bar, pol_w);
         }
       }
-      prefetch_units(nunits);
       if (p.timeline) p.timeline[blockIdx.x * kTimelineSlots + kTlProdW] = globaltimer_ns();
       // Phase 2: K/V tiles of the owned rows, whole sequence each, as
       // 64-column swizzled boxes: K [D/64][Rt][64] then V.

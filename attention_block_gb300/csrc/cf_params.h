@@ -17,10 +17,6 @@ constexpr int kThreads = kConsumers + 32;         // + one TMA producer warp
 constexpr int kMaxCluster = 16;
 constexpr int kMaxRounds = 4;                     // log2(kMaxCluster)
 constexpr int kMaxStages = 32;
-// Batched kernel: default number of K/V tiles per owned row prefetched into L2
-// while the QKV projection streams (its DRAM use is low: the head's batch
-// tiles share the weights through L2).
-constexpr int kDefaultKvPrefetch = 0;
 
 // Batched kernel: 64-column boxes per W_qkv stage.  The head group's NC
 // projection columns come in NC/64/CB stages per slice of Rw hidden rows.  A
@@ -110,11 +106,6 @@ struct KParams {  // 128-byte aligned through its CUtensorMap members
   int* errflag;          // device error bits
   float* dbg;            // optional intermediate dump (NULL = off)
   unsigned long long* timeline;  // optional [grid][kTimelineSlots] globaltimer stamps (NULL = off)
-  int prefetch_ahead;    // W_qkv tiles prefetched into L2 ahead of the ring (0 = off)
-  int prefetch_late;     // L2 prefetch of the block's K/V and W_o boxes: 0 off,
-                         // 1 after the last W_qkv tile is issued, 2 at the start
-  int kv_prefetch;       // batched kernel: K/V tiles per owned row prefetched into
-                         // L2 during the QKV projection (0 = none)
   int fin_split;         // batched kernel: blocks sharing the finalize of a
                          // (tile, band) (<= 1: the last block alone)
   int B, H, nq, nkv, S;

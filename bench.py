@@ -345,17 +345,11 @@ def main(argv=None):
     ap.add_argument("--batch-tile", type=int, default=int(os.environ.get("CF_BATCH_TILE", 0)))
     ap.add_argument("--stage-bytes", type=int, default=int(os.environ.get("CF_STAGE_BYTES", 0)))
     ap.add_argument("--ctas-per-sm", type=int, default=int(os.environ.get("CF_CTAS_PER_SM", 0)))
-    ap.add_argument("--prefetch-ahead", type=int,
-                    default=int(os.environ.get("CF_PREFETCH_AHEAD", 0)))
-    ap.add_argument("--prefetch-late", type=int, default=int(os.environ.get("CF_PREFETCH_LATE", 0)))
     ap.add_argument("--max-stages", type=int, default=int(os.environ.get("CF_MAX_STAGES", 0)))
     ap.add_argument("--ffn", type=int, default=0,
                     help="intermediate size of the gated FFN that follows the attention block "
                          "in every layer (a whole decoder layer per step); 0 = the attention "
                          "block alone")
-    ap.add_argument("--kv-prefetch", type=int, default=int(os.environ.get("CF_KV_PREFETCH", 0)),
-                    help="batched kernel: K/V tiles per owned row prefetched into L2 during "
-                         "the QKV projection (0 default, -1 none)")
     ap.add_argument("--rows-per-block", type=int,
                     default=int(os.environ.get("CF_ROWS_PER_BLOCK", 0)))
     ap.add_argument("--pdl", type=int, default=int(os.environ.get("CF_PDL", 0)),
@@ -437,9 +431,7 @@ def main(argv=None):
         max_batch=w.batch, s_max=w.s_max, rope_theta=w.rope_theta, rms_eps=w.rms_eps,
         dtype=w.dtype, cluster_size=args.cluster_size, batch_tile=args.batch_tile,
         stage_bytes=args.stage_bytes, ctas_per_sm=args.ctas_per_sm,
-        prefetch_ahead=args.prefetch_ahead, prefetch_late=args.prefetch_late, pdl=args.pdl,
-        max_stages=args.max_stages, rows_per_block=args.rows_per_block,
-        kv_prefetch=args.kv_prefetch)
+        pdl=args.pdl, max_stages=args.max_stages, rows_per_block=args.rows_per_block)
     info = blk.launch_info()
     step_fn = blk.unfused if args.unfused else blk
     kernels_per_layer = 3 if args.unfused else 1

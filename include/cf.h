@@ -69,23 +69,12 @@ typedef struct cf_config {
   int32_t batch_tile;   /* 0 = default, else batch rows per cluster           */
   int32_t stage_bytes;  /* 0 = default, else bytes per shared-memory stage    */
   int32_t ctas_per_sm;  /* 0 = default, else 1 or 2 (shared-memory split)    */
-  int32_t prefetch_ahead; /* W_qkv tiles prefetched into L2 beyond the ring:
-                             0 or -1 = none (default), else that many        */
-  int32_t prefetch_late;  /* L2 prefetch of each block's later tiles:
-                             0 or -1 = off (default); K/V and W_o tiles
-                             1 = after the block's last W_qkv tile is issued,
-                             2 = at kernel start; W_o tiles only 3 = once the
-                             block's projection is complete                   */
   int32_t pdl;            /* programmatic dependent launch: 0 = default (on),
                              -1 = off                                         */
   int32_t max_stages;     /* 0 = as many ring stages as fit, else at most this
                              many (>= 2)                                      */
   int32_t rows_per_block; /* batched mode (batch_tile >= 16, fp16/bf16): batch
                              rows each block of a cluster owns; 0 = default  */
-  int32_t kv_prefetch;    /* batched mode: K/V tiles of each owned row that are
-                             prefetched into L2 while the QKV projection
-                             streams (spread over the sequence); 0 = default,
-                             -1 = none, else at most that many (<= 64)       */
   int32_t adaptive;       /* 0 or 1 = default: for MHA (nq == nkv), besides the
                              max_batch plan, plan for batch caps 1, 2, 4 and 8
                              and give each call the smallest one that holds

@@ -17,6 +17,8 @@
 #ifndef CF_TEST_H
 #define CF_TEST_H
 
+#include <stdint.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -73,6 +75,16 @@ int cf_set_timeline(struct cf_handle* h, unsigned long long* stamps);
  * Returns CF_OK or CF_ERR_INVALID_ARG. */
 struct cf_mla_handle;
 int cf_mla_set_timeline(struct cf_mla_handle* h, unsigned long long* stamps);
+
+/* The intermediate activations a = silu(gate) * up of the last
+ * cf_ffn_forward call of handle h with `batch` rows on the tensor-core pair
+ * (batches of 3 or more rows): the kernel keeps a as 16-bit hi + lo pairs,
+ * which this reads back (synchronously) and writes summed into the host
+ * array a_out [batch, intermediate].  A test aid.  Errors:
+ * CF_ERR_INVALID_ARG, CF_ERR_UNSUPPORTED (a handle without the pair),
+ * CF_ERR_CUDA. */
+struct cf_ffn_handle;
+int cf_ffn_debug_a(const struct cf_ffn_handle* h, int32_t batch, float* a_out);
 
 /* One fifth-generation tensor-core product by one block:
  * d[128, n] = A . b[n, k]^T with fp32 accumulation, where A = a as a [128, k]

@@ -100,30 +100,6 @@ def test_llama3_gqa_layer_full_batched(bt, rpc):
     full_check(synth.WORKLOADS[synth.LLAMA3_GQA], batch_tile=bt, rows_per_block=rpc)
 
 
-@pytest.mark.parametrize("name,npf", [(synth.LLAMA3_GQA, 1), (synth.LLAMA3_GQA, 12),
-                                      (synth.LLAMA3_GQA, 64), (synth.SMALL_HEAD_B64, 4)])
-def test_kv_l2_prefetch_leaves_results_bit_identical(name, npf):
-    """The K/V L2 prefetch during the projection moves no data the kernel
-    computes with: the cache writes equal those without it bit for bit, the
-    outputs agree up to the order of the fp32 atomics that merge the KV heads
-    (the 64-tile count exceeds every row's tiles), and both match the oracle."""
-    w = synth.WORKLOADS[name]
-    t = synth.make_layer(w, 4, device="cuda")
-    outs = []
-    for kv_prefetch in (-1, npf):
-        blk = make_block(w, kv_prefetch=kv_prefetch)
-        assert blk.launch_info()["mode"] == 1
-        out, kc, vc, _, st = run_gpu(w, t, block=blk)
-        assert st == binding.CF_OK
-        outs.append((out, kc, vc))
-    assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][2], outs[1][2])
-    check(outs[1][0].double().cpu().numpy(), outs[0][0].double().cpu().numpy(),
-          "with vs without prefetch", mean_rel=1e-5)
-    rows = [0, 5, w.batch - 1]
-    ref = run_oracle(w, t, rows=rows)
-    check(outs[1][0][rows].double().cpu().numpy(), round_to(ref["out"], w.dtype), "out")
-
-
 def test_batched_workloads_on_sequence_split_kernel():
     w = synth.WORKLOADS[synth.SMALL_HEAD_B64]
     t = synth.make_layer(w, 0, device="cuda")

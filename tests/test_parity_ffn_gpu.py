@@ -102,13 +102,15 @@ def test_tensor_core_pair_scaled_shapes(shape):
     assert blk.kernels(B)["kernels"] == 2 and blk.kernels(2)["kernels"] == 1
     out, st = run_ffn(w, t, blk)
     assert st == binding.CF_OK
-    rows = sorted({0, B // 2, B - 1})
+    rows = list(range(B))  # every row
     ref = oracle_ffn(w, t, rows)
     got = out[rows].double().cpu().numpy()
     want = round_to(ref["out"], w.dtype)
     check(got, want, "out")
     x = synth.to_f64(t["hidden"][rows])
     check(got - x, want - x, "out - hidden")
+    # the intermediate activations the pair hands from one kernel to the next
+    check(blk.debug_a(B), ref["a"], "a = silu(gate) * up")
 
 
 def test_tensor_core_pair_small_batches_and_repeats_on_one_handle():
