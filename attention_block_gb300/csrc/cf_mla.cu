@@ -79,13 +79,15 @@ constexpr int REC = DC + 4;     // state record: o_lat[512], m, l, 2 pad
 constexpr int MAX_STAGES = 8;
 constexpr int kMaxClusters = 64;  // resident clusters the phase-D merge handles
 constexpr int STAGE_BYTES = RT * DL * 2;  // 36,864: the largest item (a cache tile)
-static_assert(KT * GW * 2 <= STAGE_BYTES && DC % KT == 0 && DCB % KT == 0, "stage plan");
+static_assert(KT * GW * 2 <= STAGE_BYTES && DC % KT == 0 && DCB * DV * 2 <= STAGE_BYTES &&
+                  DV * 128 * 2 <= STAGE_BYTES && DCB % kConsumerWarps == 0, "stage plan");
 
 struct Params {  // 128-byte aligned through its CUtensorMap members
   CUtensorMap tm_wq;    // [H, nh*DQ],  box {192, 64}
   CUtensorMap tm_wdkv;  // [H, DL],     box {192, 64}
-  CUtensorMap tm_wukv;  // [DC, nh*(DN+DV)], box {128, 64}
-  CUtensorMap tm_wo;    // [nh*DV, H],  box {wob, 64}
+  CUtensorMap tm_wukv;  // [DC, nh*(DN+DV)], box {128, 64}   (phase B: k parts)
+  CUtensorMap tm_wuv;   // [DC, nh*(DN+DV)], box {128, DCB}  (phase D: v parts)
+  CUtensorMap tm_wo;    // [nh*DV, H],  box {wob, DV}
   const void* hidden;   // [B, H]
   const void* ln_w;     // [H]
   const void* g_kv;     // [DC]
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
     prefetch_tensormap(&p.tm_wq);
     prefetch_tensormap(&p.tm_wdkv);
     prefetch_tensormap(&p.tm_wukv);
+    prefetch_tensormap(&p.tm_wuv);
     prefetch_tensormap(&p.tm_wo);
   }
   __syncthreads();
@@ -316,16 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       // D: w_uv rows of this block's latent band, then w_o of its column
       // band, box by box (both 64-row halves of each)
       for (int h = cl; h < nh; h += p.ncl) {
-        for (int ri = 0; ri < DCB / KT; ++ri) {
-          uint8_t* dst = slot(KT * DV * 2, bar);
-          tma_load_2d(dst, &p.tm_wukv, h * (DN + DV) + DN, rank * DCB + ri * KT, bar, pol);
-        }
+        uint8_t* dst = slot(DCB * DV * 2, bar);
+        tma_load_2d(dst, &p.tm_wuv, h * (DN + DV) + DN, rank * DCB, bar, pol);
         const int cb = H / NCLU;
-        for (int cx = 0; cx < cb / p.wob; ++cx)
-          for (int rb = 0; rb < DV / KT; ++rb) {
-            uint8_t* dst = slot((uint32_t)(KT * p.wob * 2), bar);
-            tma_load_2d(dst, &p.tm_wo, rank * cb + cx * p.wob, h * DV + rb * KT, bar, pol);
-          }
+        for (int cx = 0; cx < cb / p.wob; ++cx) {
+          dst = slot((uint32_t)(DV * p.wob * 2), bar);
+          tma_load_2d(dst, &p.tm_wo, rank * cb + cx * p.wob, h * DV, bar, pol);
+        }
       }
       stamp(kMlaTlProdD);
     }
@@ -812,25 +812,26 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
           for (int b = 0; b < BMAX; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) a4[b][e] = 0.f;
-          for (int ri = 0; ri < DCB / KT; ++ri, ++it) {
+          {
             const int s = it % p.stages;
             mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
             const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
-#pragma unroll
-            for (int rr = 0; rr < KT / kConsumerWarps; ++rr) {
-              const int i = warp * (KT / kConsumerWarps) + rr;
+#pragma unroll 4
+            for (int rr = 0; rr < DCB / kConsumerWarps; ++rr) {
+              const int i = warp * (DCB / kConsumerWarps) + rr;
               float w4[4];
               load_cvt<T, 4>(tile + i * DV + 4 * lane, w4);
 #pragma unroll
               for (int b = 0; b < BMAX; ++b) {
                 if (b >= B) continue;
-                const float ov1 = ol[b * DCB + ri * KT + i];
+                const float ov1 = ol[b * DCB + i];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) a4[b][e] = fmaf(ov1, w4[e], a4[b][e]);
               }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            ++it;
           }
 #pragma unroll
           for (int b = 0; b < BMAX; ++b)
@@ -859,26 +860,27 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
           for (int b = 0; b < BMAX; ++b)
 #pragma unroll
             for (int e = 0; e < 4; ++e) a[b][e] = 0.f;
-          for (int rbx = 0; rbx < DV / KT; ++rbx, ++it) {
+          {
             const int s = it % p.stages;
             mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
             const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
-#pragma unroll
-            for (int rr = 0; rr < KT / kConsumerWarps; ++rr) {
-              const int j = warp * (KT / kConsumerWarps) + rr;
+#pragma unroll 4
+            for (int rr = 0; rr < DV / kConsumerWarps; ++rr) {
+              const int j = warp * (DV / kConsumerWarps) + rr;
               float w[4] = {0.f, 0.f, 0.f, 0.f};
               if (cpl == 4) load_cvt<T, 4>(tile + j * p.wob + 4 * lane, w);
               else load_cvt<T, 2>(tile + j * p.wob + 2 * lane, w);
 #pragma unroll
               for (int b = 0; b < BMAX; ++b) {
                 if (b >= B) continue;
-                const float ovj = ov[b * DV + rbx * KT + j];
+                const float ovj = ov[b * DV + j];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) a[b][e] = fmaf(ovj, w[e], a[b][e]);
               }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            ++it;
           }
 #pragma unroll
           for (int b = 0; b < BMAX; ++b)
@@ -979,7 +981,7 @@ struct cf_mla_handle {
   struct MapSlot {
     const void* ptr = nullptr;
     CUtensorMap map;
-  } m_wq, m_wdkv, m_wukv, m_wo;
+  } m_wq, m_wdkv, m_wukv, m_wuv, m_wo;
 };
 
 namespace {
@@ -1152,11 +1154,13 @@ int cf_mla_decode(cf_mla_handle* h, int32_t batch, const void* hidden_states,
   const CUtensorMap* m1 = mla_map(h->m_wq, c.dtype, w_q, (uint64_t)nh * DQ, H, GW, KT);
   const CUtensorMap* m2 = mla_map(h->m_wdkv, c.dtype, w_dkv, DL, H, GW, KT);
   const CUtensorMap* m3 = mla_map(h->m_wukv, c.dtype, w_ukv, (uint64_t)nh * (DN + DV), DC, 128, KT);
-  const CUtensorMap* m4 = mla_map(h->m_wo, c.dtype, w_o, H, (uint64_t)nh * DV, h->wob, KT);
-  if (!m1 || !m2 || !m3 || !m4) return CF_ERR_CUDA;
+  const CUtensorMap* m5 = mla_map(h->m_wuv, c.dtype, w_ukv, (uint64_t)nh * (DN + DV), DC, 128, DCB);
+  const CUtensorMap* m4 = mla_map(h->m_wo, c.dtype, w_o, H, (uint64_t)nh * DV, h->wob, DV);
+  if (!m1 || !m2 || !m3 || !m4 || !m5) return CF_ERR_CUDA;
   p.tm_wq = *m1;
   p.tm_wdkv = *m2;
   p.tm_wukv = *m3;
+  p.tm_wuv = *m5;
   p.tm_wo = *m4;
   p.hidden = hidden_states;
   p.ln_w = ln_weight;

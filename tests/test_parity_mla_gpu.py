@@ -163,6 +163,38 @@ def test_repeats_smaller_batches_and_graph_replay_leave_the_workspace_clean():
     check(out.double().cpu().numpy(), first.double().cpu().numpy(), "graph", mean_rel=1e-5)
 
 
+def test_back_to_back_launches_on_one_cache_agree():
+    """Launches that follow one another with nothing in between (each may
+    start while the previous one drains) and graph replays separated by
+    host synchronizations, all on the cache the first launch appended to,
+    give the first launch's output."""
+    w = synth.custom_mla(name="mla_b2b", hidden=1024, n_heads=16, batch=4, s_max=200,
+                         positions="list:199,3,77,150")
+    t = synth.make_mla_layer(w, 5, device="cuda")
+    blk = make_mla(w)
+    first, lc, st = run_mla(w, t, blk)
+    assert st == binding.CF_OK
+    ref = first.double().cpu().numpy()
+    outs = [torch.full_like(first, float("nan")) for _ in range(6)]
+    for o in outs:
+        blk(w.batch, *[t[k] for k in ARGS], lc, t["positions"], o)
+    torch.cuda.synchronize()
+    assert blk.status() == binding.CF_OK
+    for i, o in enumerate(outs):
+        check(o.double().cpu().numpy(), ref, f"launch {i}", mean_rel=1e-5)
+    out = torch.full_like(first, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        blk(w.batch, *[t[k] for k in ARGS], lc, t["positions"], out, s)
+    for i in range(4):
+        g.replay()
+        torch.cuda.synchronize()
+        check(out.double().cpu().numpy(), ref, f"replay {i}", mean_rel=1e-5)
+    assert blk.status() == binding.CF_OK
+
+
 def test_layers_chained_on_one_handle_under_programmatic_dependent_launch():
     """Four layers back to back on one stream and one handle (each launch may
     start while the previous one drains; the grid barrier's words are read
