@@ -407,14 +407,17 @@ struct cf_ffn_handle {
   int BP = 0, Ip = 0;
   FfnTcFn fn_gu = nullptr, fn_down = nullptr;
   int blocks1 = 0, UB = 0, nsl1 = 0, stages1 = 0, stage1_bytes = 0, smem1 = 0;
+  bool stacked = false;
   int blocks2 = 0, S = 0, nsl2 = 0, stages2 = 0, stage2_bytes = 0, smem2 = 0;
   void* a_hi = nullptr;
   void* a_lo = nullptr;
-  void* n = nullptr;      // [2 * BP, H] 16-bit: h * g2 as hi rows, then lo rows
+  void* n = nullptr;      // [NR, H] 16-bit: h * g2 (fp16 rows, or bf16 hi rows then lo rows)
   float* ssq = nullptr;   // [8][BP] rows' sums of squares (copies)
   int* grid = nullptr;    // kernel 1's grid barrier: [0] arrivals, [1] generation
   TmapSlot m_wg, m_wu, m_wd;
-  unsigned long long* timeline = nullptr;  // optional stamps of kernel 1
+  int acc_batch = 0;      // batch the accumulator's tensor map was encoded for
+  CUtensorMap m_acc;      // acc [acc_batch, H] fp32: kernel 2's reduction target
+  unsigned long long* timeline = nullptr;  // optional stamps of both kernels
   CUtensorMap m_ahi, m_alo, m_n;
 };
 
@@ -426,13 +429,15 @@ bool plan_ffn_tc(cf_ffn_handle* h, int sms, int budget) {
   const cf_ffn_config& c = h->cfg;
   const int H = c.hidden, I = c.intermediate;
   h->BP = c.max_batch <= 16 ? 16 : (c.max_batch <= 32 ? 32 : 64);
-  const int BP = h->BP, N5 = 2 * BP;
+  // activations (h * g2, a) as one fp16 value each, or as bf16 hi + lo pairs
+  const int BP = h->BP, N5 = c.dtype == CF_BF16 ? 2 * BP : BP;
   h->Ip = (I + 7) / 8 * 8;
   // kernel 1: one block per SM, each at most UB (multiple of 8) units
   h->blocks1 = std::min(sms, I);
   const int umax = (I + h->blocks1 - 1) / h->blocks1;
   h->UB = (umax + 7) / 8 * 8;
   if (h->UB > 128) return false;
+  h->stacked = 2 * h->UB <= 128;
   const int slab1 = (2 * h->UB + N5) * 128;  // gate box | up box | n box
   int extras1 = (2 * kFfnTcMaxStages + 2) * 8 + BP * 4 + 16;  // barriers, rinv, TMEM word
   // the M = 128 operand reads of a slab's gate and up boxes run up to 16 KB
@@ -447,6 +452,8 @@ bool plan_ffn_tc(cf_ffn_handle* h, int sms, int budget) {
   }
   if (h->stages1 < 2) return false;
   h->smem1 = h->stages1 * h->stage1_bytes + extras1 + 1024;
+  // the stacked epilogue stages the fp32 sums [BP][128] in the idle ring
+  if (h->stacked && BP * 128 * (int)sizeof(float) > h->stages1 * h->stage1_bytes) return false;
   // kernel 2: H / 128 column tiles x S splits of the 64-unit slabs
   const int tiles = H / 128, slabs = (I + 63) / 64;
   h->S = std::max(1, std::min(slabs, sms / tiles));
@@ -456,7 +463,8 @@ bool plan_ffn_tc(cf_ffn_handle* h, int sms, int budget) {
   h->nsl2 = std::max(1, std::min((slabs + h->S - 1) / h->S, 65536 / slab2));
   h->stage2_bytes = h->nsl2 * slab2;
   h->stages2 = std::min(kFfnTcMaxStages, (budget - extras2) / h->stage2_bytes);
-  if (h->stages2 < 2) return false;
+  // the epilogue stages the fp32 partial tile [BP][128] in the idle ring
+  if (h->stages2 < 2 || BP * 128 * (int)sizeof(float) > h->stage2_bytes) return false;
   h->smem2 = h->stages2 * h->stage2_bytes + extras2 + 1024;
   ffn_tc_entries(c.dtype, BP, h->fn_gu, h->fn_down);
   if (!raise_smem(reinterpret_cast<const void*>(h->fn_gu), h->smem1) ||
@@ -545,7 +553,8 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
   // barrier [2]) | row sums [8][64] | a_hi | a_lo | n
   const size_t acc_bytes = (size_t)c.max_batch * c.hidden * sizeof(float);
   const size_t a_bytes = h->tc ? (size_t)c.max_batch * h->Ip * 2 : 0;
-  const size_t n_bytes = h->tc ? (size_t)2 * h->BP * c.hidden * 2 : 0;
+  const int n_rows = c.dtype == CF_BF16 ? 2 * h->BP : h->BP;
+  const size_t n_bytes = h->tc ? (size_t)n_rows * c.hidden * 2 : 0;
   const size_t ssq_bytes = (size_t)kFfnSsqCopies * 64 * sizeof(float);
   const size_t total = acc_bytes + 512 + ssq_bytes + 2 * a_bytes + n_bytes;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
@@ -567,8 +576,8 @@ extern "C" int cf_ffn_create(const cf_ffn_config* cfg, cf_ffn_handle** out) {
     h->a_hi = static_cast<char*>(h->ws) + acc_bytes + 512 + ssq_bytes;
     h->a_lo = static_cast<char*>(h->a_hi) + a_bytes;
     h->n = static_cast<char*>(h->a_lo) + a_bytes;
-    if (!encode_tmap_2d(&h->m_n, c.dtype, h->n, c.hidden, 2 * h->BP, (uint64_t)c.hidden * 2, 64,
-                        2 * h->BP, true)) {
+    if (!encode_tmap_2d(&h->m_n, c.dtype, h->n, c.hidden, n_rows, (uint64_t)c.hidden * 2, 64,
+                        n_rows, true)) {
       cudaFree(h->ws);
       delete h;
       return CF_ERR_CUDA;
@@ -599,6 +608,15 @@ int ffn_forward_tc(cf_ffn_handle* h, int batch, const void* hidden, const void* 
   const CUtensorMap* mu = cached_map(h->m_wu, c.dtype, w_up, H, I, h->UB);
   const CUtensorMap* md = cached_map(h->m_wd, c.dtype, w_down, H, I, 64);
   if (!mg || !mu || !md) return CF_ERR_CUDA;
+  if (h->acc_batch != batch) {
+    // box = exactly the call's rows, so the reduction never leaves the tensor
+    if (!encode_tmap_2d(&h->m_acc, CF_F32, h->acc, H, (uint64_t)batch, H * sizeof(float), 128,
+                        (uint32_t)batch, false)) {
+      h->acc_batch = 0;
+      return CF_ERR_CUDA;
+    }
+    h->acc_batch = batch;
+  }
   FfnTcParams p;
   std::memset(&p, 0, sizeof(p));
   p.tm_wg = *mg;
@@ -608,6 +626,7 @@ int ffn_forward_tc(cf_ffn_handle* h, int batch, const void* hidden, const void* 
   p.ssq = h->ssq;
   p.grid_count = h->grid;
   p.grid_gen = h->grid + 1;
+  p.tm_acc = h->m_acc;
   p.tm_wd = *md;
   p.tm_ahi = h->m_ahi;
   p.tm_alo = h->m_alo;
@@ -624,6 +643,7 @@ int ffn_forward_tc(cf_ffn_handle* h, int batch, const void* hidden, const void* 
   p.I = c.intermediate;
   p.Ip = h->Ip;
   p.UB = h->UB;
+  p.stacked = h->stacked ? 1 : 0;
   p.nsl1 = h->nsl1;
   p.stages1 = h->stages1;
   p.stage1_bytes = h->stage1_bytes;
@@ -631,6 +651,7 @@ int ffn_forward_tc(cf_ffn_handle* h, int batch, const void* hidden, const void* 
   p.nsl2 = h->nsl2;
   p.stages2 = h->stages2;
   p.stage2_bytes = h->stage2_bytes;
+  p.grid1 = h->blocks1;
   p.eps = c.rms_eps;
   p.timeline = h->timeline;
   cudaLaunchAttribute attr[1];
@@ -757,14 +778,15 @@ extern "C" int cf_ffn_debug_a(const cf_ffn_handle* h, int32_t batch, float* a_ou
   const bool ok = cudaMemcpy(hi, h->a_hi, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess &&
                   cudaMemcpy(lo, h->a_lo, n * 2, cudaMemcpyDeviceToHost) == cudaSuccess;
   if (ok) {
+    // bf16: a = hi + lo; fp16: a = hi alone
     const bool bf = h->cfg.dtype == CF_BF16;
     for (int b = 0; b < batch; ++b)
       for (int i = 0; i < I; ++i) {
         const size_t k = (size_t)b * Ip + i;
-        a_out[(size_t)b * I + i] = (bf ? __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&hi[k]))
-                                       : __half2float(*reinterpret_cast<__half*>(&hi[k]))) +
-                                   (bf ? __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&lo[k]))
-                                       : __half2float(*reinterpret_cast<__half*>(&lo[k])));
+        a_out[(size_t)b * I + i] =
+            bf ? __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&hi[k])) +
+                     __bfloat162float(*reinterpret_cast<__nv_bfloat16*>(&lo[k]))
+               : __half2float(*reinterpret_cast<__half*>(&hi[k]));
       }
   }
   delete[] hi;

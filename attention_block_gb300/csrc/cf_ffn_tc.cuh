@@ -17,19 +17,26 @@
 // [i0, i1) (at most UB <= 128 of them).  Both products run transposed:
 // M = 128 unit rows of W_gate / W_up (one TMA box of the block's rows, the
 // [I, H] layout read as a K-major operand; the rows past the block's units
-// are not used), N = 2 * BP (the rows' h * g2 as 16-bit hi halves, then lo
-// halves), K = the hidden dimension in 64-column slabs.  The norm scale rinv
-// is applied in the epilogue (each block sees every column of h, so it sums
-// h^2 while staging).  The epilogue writes a as 16-bit hi and lo arrays
-// [B, I], exactly the operand layout kernel 2 loads.
+// are not used), N = the rows of n = h * g2 as 16-bit values -- one fp16 row
+// per batch row, or for bf16 (8 significant bits) a hi row and a lo row, so
+// that hi + lo carries about fp32 accuracy -- and K = the hidden dimension
+// in 64-column slabs.  When 2 UB <= 128 the gate box and the up box, which
+// lie next to each other in shared memory, form one M = 128 operand and one
+// MMA serves both.  Phase 0 writes each block's share of the columns of n
+// to a workspace and a grid barrier publishes it; every block then streams
+// n with its weight boxes.  The norm scale rinv is applied in the epilogue
+// (the rows' sums of squares are added up in phase 0).  The epilogue writes
+// a in the operand layout kernel 2 loads: fp16 [B, I], or bf16 hi and lo
+// arrays [B, I].
 //
 // Kernel 2 (down): (H / 128) column tiles x S splits of the units.  Each
 // block computes out^T[128 columns, rows] = Wd^T a^T over its units: M = 128
 // output columns (two swizzled 64-column TMA boxes of Wd, an M-major
-// operand), N = 2 * BP (a's hi and lo rows, loaded by TMA straight into a
-// K-major slab), K = units.  Partial sums meet in an fp32 accumulator by
-// atomics; the last split of a column tile adds the residual, writes `out`
-// and clears the accumulator.
+// operand), N = a's rows (fp16, or bf16 hi rows then lo rows, loaded by TMA
+// straight into a K-major slab), K = units.  The block's partial tile goes
+// through shared memory to one bulk tensor reduction (add) into an fp32
+// accumulator; the last split of a column tile adds the residual, writes
+// `out` and clears the accumulator.
 #pragma once
 
 #include <cuda.h>
@@ -45,6 +52,7 @@
 namespace cf {
 
 constexpr int kFfnTcMaxStages = 8;
+
 // Copies of the rows' sums of squares that kernel 1's blocks add into (block
 // k into copy k % 8), so no word takes more than ~1/8 of the blocks' atomics.
 constexpr int kFfnSsqCopies = 8;
@@ -52,13 +60,14 @@ constexpr int kFfnSsqCopies = 8;
 struct FfnTcParams {
   CUtensorMap tm_wg;   // W_gate [I, H], box {64, UB}, 128-byte swizzle
   CUtensorMap tm_wu;   // W_up   [I, H], box {64, UB}
-  CUtensorMap tm_n;    // n [2*BP, H] (h * g2 as hi rows, then lo rows), box {64, 2*BP}
+  CUtensorMap tm_n;    // n [NR, H] (h * g2: fp16 rows, or bf16 hi rows then lo rows), box {64, NR}
   CUtensorMap tm_wd;   // W_down [I, H], box {64, 64}
   CUtensorMap tm_ahi;  // a hi   [B, I], box {64, BP}
   CUtensorMap tm_alo;  // a lo   [B, I], box {64, BP}
+  CUtensorMap tm_acc;  // acc    [B, H] fp32, box {128, B}, no swizzle (reduction target)
   const void* h;       // hidden [B, H] (residual)
   const void* g2;      // ln_weight [H]
-  void* n;             // [2*BP, H] 16-bit
+  void* n;             // [NR, H] 16-bit
   float* ssq;          // [kFfnSsqCopies][BP] rows' sums of squares, zero between calls
   int* grid_count;     // arrivals at kernel 1's grid barrier, zero between calls
   int* grid_gen;       // generations of that barrier (only ever increases)
@@ -71,17 +80,22 @@ struct FfnTcParams {
   int B, H, I;
   int Ip;              // row stride of a_hi / a_lo (I rounded up to 8)
   int UB;              // kernel 1: unit rows per box (multiple of 8, <= 128)
+  int stacked;         // kernel 1: 2 UB <= 128, gate and up boxes as one M = 128 operand
   int nsl1, stages1, stage1_bytes;  // kernel 1: 64-column slabs per stage, ring
   int S;               // kernel 2: splits of the units
   int nsl2, stages2, stage2_bytes;  // kernel 2: 64-unit slabs per stage, ring
+  int grid1;           // kernel 1's blocks (kernel 2's timeline rows follow them)
   float eps;
-  unsigned long long* timeline;  // optional [grid][kFfnTlSlots] globaltimer stamps of
-                                 // kernel 1 (NULL = off)
+  unsigned long long* timeline;  // optional [grid1 + grid2][kFfnTlSlots] globaltimer
+                                 // stamps (NULL = off)
 };
 
-// Stamps of kernel 1's optional timeline (per block): start, the consumers'
-// dependency wait done, phase 0 done, grid barrier passed, stage st landed at
-// the issuer (slot 4 + st, st < 48), every MMA complete, epilogue done.
+// Stamps of the optional timeline, one row per block.  Kernel 1: start, the
+// consumers' dependency wait done, phase 0 done, grid barrier passed, stage
+// st landed at the MMA issuer (slot 4 + st, st < 48), every MMA complete
+// (52), epilogue done (53).  Kernel 2: start, the consumers' dependency wait
+// done, stage st landed (slot 4 + st), every MMA complete (52), partial tile
+// reduced into the accumulator (53), done (54).
 constexpr int kFfnTlSlots = 56;
 constexpr int kFfnTlMaxStages = 48;
 
@@ -103,12 +117,6 @@ static __device__ __noinline__ bool wait_generation(const int* gen, int gen0, in
   }
 }
 
-// Orders global writes this thread has observed (by the generic proxy) before
-// its later bulk-tensor (async proxy) reads of them.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // 16-bit hi + lo split of one fp32 value (hi = round(v), lo = round(v - hi)).
 template <typename T>
 __device__ __forceinline__ void split1(float v, T& hi, T& lo) {
@@ -120,13 +128,14 @@ __device__ __forceinline__ void split1(float v, T& hi, T& lo) {
 template <typename T, int BP>
 __global__ void __launch_bounds__(kThreads, 1)
     cf_ffn_gu_kernel(const __grid_constant__ FfnTcParams p) {
-  constexpr int N5 = 2 * BP;
-  constexpr int TCOLS = tmem_cols_for(2 * N5);  // gate and up accumulators
   using MK = MmaKind<T>;
+  constexpr bool kHiLo = MK::kAttnHiLo;   // bf16: n as hi + lo rows
+  constexpr int NR = kHiLo ? 2 * BP : BP;  // rows of n (the MMA's N)
+  constexpr int TCOLS = tmem_cols_for(2 * NR);  // gate and up accumulators
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const int slab1 = (2 * p.UB + N5) * 128;  // gate box | up box | n box
+  const int slab1 = (2 * p.UB + NR) * 128;  // gate box | up box | n box
   uint8_t* ring = sm;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + (size_t)p.stages1 * p.stage1_bytes);
   uint64_t* full = bars;
@@ -144,6 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i1 = (int)((long long)(blockIdx.x + 1) * p.I / G);
   const int nslab = p.H / 64;
   const int nst = (nslab + p.nsl1 - 1) / p.nsl1;  // stages of the stream
+  // 2 UB <= 128: one M = 128 MMA covers the gate box (rows 0..UB-1) and the
+  // up box right after it (rows UB..2UB-1), so gate unit u accumulates in
+  // TMEM lane u and up unit u in lane UB + u
+  const bool stacked = p.stacked != 0;
 
   auto stamp = [&](int slot) {
     if (p.timeline != nullptr && tid == 0)
@@ -228,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // arrived
     const int gen0 = tid == 0 ? *reinterpret_cast<volatile int*>(p.grid_gen) : 0;
     stamp(1);
-    // ---- Phase 0: this block's columns of n = h * g2 as 16-bit hi rows
-    // 0..BP-1 and lo rows BP..2BP-1 of n [2*BP, H], and the rows' sums of
-    // squares over them [LNA §三 stage 1] -------------------------------------
+    // ---- Phase 0: this block's columns of n = h * g2 (fp16: one row per
+    // batch row; bf16: hi rows 0..BP-1, lo rows BP..2BP-1 of n [NR, H]), and
+    // the rows' sums of squares over them [LNA §三 stage 1] ------------------
     {
       const T* __restrict__ hid = static_cast<const T*>(p.h);
       const T* __restrict__ g2 = static_cast<const T*>(p.g2);
@@ -257,8 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *reinterpret_cast<uint4*>(n + (size_t)b * p.H + 8 * c) =
             make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(n + (size_t)(BP + b) * p.H + 8 * c) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if constexpr (kHiLo)
+          *reinterpret_cast<uint4*>(n + (size_t)(BP + b) * p.H + 8 * c) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
         if (ss != 0.f) atomicAdd(&rinv[b], ss);
       }
       named_sync(kBarConsumers, kConsumers);
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- gate and up: one thread issues each stage's MMAs as it lands ----
     const uint32_t tmem = *s_tmem;
-    const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, false);
+    const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, NR, false);
     if (tid == 0) {
       for (int st = 0; st < nst; ++st) {
         const int s = st % p.stages1;
@@ -307,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool acc = st > 0 || j > 0 || ks > 0;
             const uint64_t bd = smem_desc_k_sw128(bn + ks * 32u, 1024);
             tc05_mma_f16(tmem, smem_desc_k_sw128(ag + ks * 32u, 1024), bd, idesc, acc);
-            tc05_mma_f16(tmem + (uint32_t)N5, smem_desc_k_sw128(au + ks * 32u, 1024), bd, idesc,
-                         acc);
+            if (!stacked)
+              tc05_mma_f16(tmem + (uint32_t)NR, smem_desc_k_sw128(au + ks * 32u, 1024), bd, idesc,
+                           acc);
           }
         }
         mbar_arrive_cnt(&empty[s], kConsumerWarps - 1);
@@ -321,33 +336,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(done, 0, p.errflag);
     stamp(4 + kFfnTlMaxStages);
     tc05_fence_after();
-    // a = silu(gate) * up: warp w reads units 32 (w % 4) + lane (its TMEM
-    // lane quarter) for rows [h * BP/2, (h+1) * BP/2), h = w / 4
-    T* ahi = static_cast<T*>(p.a_hi);
-    T* alo = static_cast<T*>(p.a_lo);
+    // a = silu(gate) * up.  Warp w reads TMEM lane quarter w % 4 (lanes
+    // 32 (w % 4) + lane) for rows [h BP/2, (h+1) BP/2), h = w / 4; the hi
+    // and lo columns of a row are summed and scaled by the row's rinv.
+    T* __restrict__ ahi = static_cast<T*>(p.a_hi);
+    T* __restrict__ alo = static_cast<T*>(p.a_lo);
     const int qd = warp & 3, hrow = (warp >> 2) * (BP / 2);
-    const int unit = i0 + 32 * qd + lane;
+    const int tl = 32 * qd + lane;  // this thread's TMEM lane
     const uint32_t dq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)hrow;
-    // 16 rows at a time: the four loads share one wait
+    constexpr int RB = BP / 2 < 16 ? BP / 2 : 16;  // rows per TMEM load batch
+    if (stacked) {
+      // gate (lanes < UB) and up (lanes UB..2UB-1) of a unit sit in different
+      // lanes: every lane's scaled sums go to shared memory (the ring is idle
+      // once every MMA is complete) as S[row][lane], then each (row, unit)
+      // pair is finished from there
+      float* S = reinterpret_cast<float*>(ring);
+      if (32 * qd < 2 * p.UB) {
 #pragma unroll
-    for (int r16 = 0; r16 < BP / 2; r16 += 16) {
-      uint32_t gh[16], gl[16], uh[16], ul[16];
-      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)r16, gh);
-      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)(BP + r16), gl);
-      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)(N5 + r16), uh);
-      tmem_ld_32x32b_x16_nowait(dq + (uint32_t)(N5 + BP + r16), ul);
-      tmem_wait_ld();
+        for (int r0 = 0; r0 < BP / 2; r0 += RB) {
+          uint32_t vh[RB], vl[RB];
+          tmem_ld_32x32b_nowait<RB>(dq + (uint32_t)r0, vh);
+          if constexpr (kHiLo) tmem_ld_32x32b_nowait<RB>(dq + (uint32_t)(BP + r0), vl);
+          tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int b = hrow + r16 + e;
-        if (b < p.B && unit < i1) {
-          const float z = (__uint_as_float(gh[e]) + __uint_as_float(gl[e])) * rinv[b];
-          const float u = (__uint_as_float(uh[e]) + __uint_as_float(ul[e])) * rinv[b];
-          const float a = z / (1.0f + expf(-z)) * u;
-          T hi, lo;
-          split1<T>(a, hi, lo);
-          ahi[(size_t)b * p.Ip + unit] = hi;
-          alo[(size_t)b * p.Ip + unit] = lo;
+          for (int e = 0; e < RB; ++e) {
+            const int b = hrow + r0 + e;
+            float v = __uint_as_float(vh[e]);
+            if constexpr (kHiLo) v += __uint_as_float(vl[e]);
+            S[b * 128 + tl] = v * rinv[b];
+          }
+        }
+      }
+      named_sync(kBarConsumers, kConsumers);
+      const int nu = i1 - i0;
+      for (int idx = tid; idx < p.B * nu; idx += kConsumers) {
+        const int b = idx / nu, u = idx % nu;
+        const float z = S[b * 128 + u], up = S[b * 128 + p.UB + u];
+        T hi, lo;
+        split1<T>(z * __frcp_rn(1.0f + __expf(-z)) * up, hi, lo);
+        ahi[(size_t)b * p.Ip + i0 + u] = hi;
+        if constexpr (kHiLo) alo[(size_t)b * p.Ip + i0 + u] = lo;
+      }
+    } else if (i0 + 32 * qd < i1) {
+      // gate in columns [0, NR), up in [NR, 2 NR) of the same lane (unit)
+      const int unit = i0 + tl;
+      const bool own = unit < i1;
+#pragma unroll
+      for (int r0 = 0; r0 < BP / 2; r0 += RB) {
+        float rv[RB];
+#pragma unroll
+        for (int e = 0; e < RB; ++e) rv[e] = rinv[hrow + r0 + e];
+        uint32_t gh[RB], gl[RB], uh[RB], ul[RB];
+        tmem_ld_32x32b_nowait<RB>(dq + (uint32_t)r0, gh);
+        tmem_ld_32x32b_nowait<RB>(dq + (uint32_t)(NR + r0), uh);
+        if constexpr (kHiLo) {
+          tmem_ld_32x32b_nowait<RB>(dq + (uint32_t)(BP + r0), gl);
+          tmem_ld_32x32b_nowait<RB>(dq + (uint32_t)(NR + BP + r0), ul);
+        }
+        tmem_wait_ld();
+        T hv[RB], lv[RB];
+#pragma unroll
+        for (int e = 0; e < RB; ++e) {
+          float z = __uint_as_float(gh[e]), u = __uint_as_float(uh[e]);
+          if constexpr (kHiLo) {
+            z += __uint_as_float(gl[e]);
+            u += __uint_as_float(ul[e]);
+          }
+          z *= rv[e];
+          u *= rv[e];
+          split1<T>(z * __frcp_rn(1.0f + __expf(-z)) * u, hv[e], lv[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < RB; ++e) {
+          const int b = hrow + r0 + e;
+          if (b < p.B && own) {
+            ahi[(size_t)b * p.Ip + unit] = hv[e];
+            if constexpr (kHiLo) alo[(size_t)b * p.Ip + unit] = lv[e];
+          }
         }
       }
     }
@@ -361,13 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
 // ------------------------------------------------------------ kernel 2 ---
 template <typename T, int BP>
 __global__ void __launch_bounds__(kThreads, 1)
     cf_ffn_down_kernel(const __grid_constant__ FfnTcParams p) {
-  constexpr int N5 = 2 * BP;
-  constexpr int TCOLS = tmem_cols_for(N5);
   using MK = MmaKind<T>;
+  constexpr bool kHiLo = MK::kAttnHiLo;   // bf16: a as hi + lo rows
+  constexpr int N5 = kHiLo ? 2 * BP : BP;  // rows of the B operand (the MMA's N)
+  constexpr int TCOLS = tmem_cols_for(N5);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -391,6 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nslab = sl1 - sl0;
   const int nst = (nslab + p.nsl2 - 1) / p.nsl2;
 
+  auto stamp = [&](int slot) {
+    if (p.timeline != nullptr && tid == 0)
+      p.timeline[(size_t)(p.grid1 + blockIdx.x) * kFfnTlSlots + slot] = globaltimer_ns();
+  };
+  stamp(0);
   if (tid == 0) {
     for (int s = 0; s < p.stages2; ++s) {
       mbar_init(&full[s], 1);
@@ -414,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&p.tm_wd);
       prefetch_tensormap(&p.tm_ahi);
       prefetch_tensormap(&p.tm_alo);
+      prefetch_tensormap(&p.tm_acc);
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_normal();
       auto stage_slabs = [&](int st) { return min(p.nsl2, nslab - st * p.nsl2); };
       auto load_w = [&](int st) {
@@ -431,8 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int u = (sl0 + st * p.nsl2 + j) * 64;
           tma_load_2d(base + j * kSlab + 2 * kWBox, &p.tm_ahi, u, 0, &full[st % p.stages2],
                       pol_a);
-          tma_load_2d(base + j * kSlab + 2 * kWBox + BP * 128, &p.tm_alo, u, 0,
-                      &full[st % p.stages2], pol_a);
+          if constexpr (kHiLo)
+            tma_load_2d(base + j * kSlab + 2 * kWBox + BP * 128, &p.tm_alo, u, 0,
+                        &full[st % p.stages2], pol_a);
         }
       };
       const int fill = min(p.stages2, nst);
@@ -454,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================ consumers ========
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    stamp(1);
     // kernel 1 of this call is complete: clear its row sums for the next call
     if (blockIdx.x == 0)
       for (int i = tid; i < kFfnSsqCopies * BP; i += kConsumers) p.ssq[i] = 0.f;
@@ -463,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int st = 0; st < nst; ++st) {
         const int s = st % p.stages2;
         mbar_wait(&full[s], (st / p.stages2) & 1, p.errflag);
+        if (st < kFfnTlMaxStages) stamp(4 + st);
         tc05_fence_after();
         const int ns = min(p.nsl2, nslab - st * p.nsl2);
         uint8_t* base = ring + (size_t)s * p.stage2_bytes;
@@ -481,28 +557,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     mbar_wait(done, 0, p.errflag);
+    stamp(4 + kFfnTlMaxStages);
     tc05_fence_after();
-    // lane = output column j0 + 32 (w % 4) + lane; rows [h BP/2, (h+1) BP/2)
+    // The partial tile [rows][128 columns] (hi + lo products summed) goes to
+    // shared memory -- the ring is idle once every MMA is complete -- and
+    // from there to one bulk tensor reduction (add) into the accumulator of
+    // the call's B rows (the box is B rows high: rows B.. of the tile are not
+    // read).  Lane = output column j0 + 32 (w % 4) + lane; rows
+    // [h BP/2, (h+1) BP/2), h = w / 4.
+    float* tile = reinterpret_cast<float*>(ring);
     const int qd = warp & 3, hrow = (warp >> 2) * (BP / 2);
-    const int col = j0 + 32 * qd + lane;
+    const int cl = 32 * qd + lane;
     const uint32_t dq = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)hrow;
     if (nslab > 0) {
 #pragma unroll
       for (int r8 = 0; r8 < BP / 2; r8 += 8) {
-        float vh[8], vl[8];
+        float vh[8], vl[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         tmem_ld_32x32b_x8(dq + (uint32_t)r8, vh);
-        tmem_ld_32x32b_x8(dq + (uint32_t)(BP + r8), vl);
+        if constexpr (kHiLo) tmem_ld_32x32b_x8(dq + (uint32_t)(BP + r8), vl);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int b = hrow + r8 + e;
-          if (b < p.B) atomicAdd(p.acc + (size_t)b * p.H + col, vh[e] + vl[e]);
-        }
+        for (int e = 0; e < 8; ++e) tile[(hrow + r8 + e) * 128 + cl] = vh[e] + vl[e];
       }
+      fence_proxy_async_smem();
     }
     tc05_fence_before();
-    __threadfence();
     named_sync(kBarConsumers, kConsumers);
     if (tid == 0) {
+      if (nslab > 0) {
+        tma_reduce_add_2d(&p.tm_acc, j0, 0, tile);
+        bulk_commit_group();
+        bulk_wait_group_0();          // the reduction's writes are performed
+        fence_proxy_async_global();   // ... and ordered before the ticket below
+      }
+      stamp(5 + kFfnTlMaxStages);
+      __threadfence();
       const int last = atomicAdd(&p.counters[jt], 1) == p.S - 1;
       if (last) __threadfence();
       s_flag[0] = last;
@@ -524,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (tid == 0) p.counters[jt] = 0;
     }
+    stamp(6 + kFfnTlMaxStages);
   }
   tc05_fence_before();
   __syncthreads();

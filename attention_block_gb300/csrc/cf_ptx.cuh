@@ -162,6 +162,36 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's async-proxy global-memory accesses (bulk copies and
+// reductions it has waited for) with its later generic-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Tiled tensor reduction (add, in the tensor map's element type) of a box in
+// this CTA's shared memory into global memory, tracked by the issuing
+// thread's bulk async-group.  Both coordinates are non-negative and the
+// innermost one is a multiple of 16 bytes (host-checked layouts); elements
+// outside the tensor map are not written.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, int x, int y,
+                                                  const void* src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];"
+      ::"l"(tm), "r"(x), "r"(y), "r"(smem_u32(src))
+      : "memory");
+}
+
+// Closes this thread's current bulk async-group.
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every bulk async-group of this thread is complete (the writes
+// to global memory performed, not only the shared-memory reads).
+__device__ __forceinline__ void bulk_wait_group_0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ------------------------------------------------------------ TMA loads --
 // Contiguous bulk copy global -> this CTA's shared memory of `bytes` bytes
 // (both addresses 16-byte aligned, bytes a multiple of 16), completing on

@@ -141,6 +141,23 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16_nowait(uint32_t taddr, uint32
         "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
+// 8 consecutive fp32 columns of the warp's 32 TMEM lanes, without waiting.
+__device__ __forceinline__ void tmem_ld_32x32b_x8_nowait(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "r"(taddr));
+}
+// N (8 or 16) consecutive fp32 columns, without waiting.
+template <int N>
+__device__ __forceinline__ void tmem_ld_32x32b_nowait(uint32_t taddr, uint32_t (&v)[N]) {
+  static_assert(N == 8 || N == 16, "8 or 16 columns");
+  if constexpr (N == 16)
+    tmem_ld_32x32b_x16_nowait(taddr, v);
+  else
+    tmem_ld_32x32b_x8_nowait(taddr, v);
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -88,12 +88,16 @@ int cf_ffn_get_status(cf_ffn_handle* h);
 int cf_ffn_launch_info(const cf_ffn_handle* h, int32_t* blocks, int32_t* rows_per_stage,
                        int32_t* stages);
 
-/* Optional timeline of the tensor-core pair's gate/up kernel (diagnostics):
- * stamps is a device array of blocks1 x 56 unsigned 64-bit globaltimer
- * values (ns) per block -- [0] start, [1] the dependency wait done, [2] its
+/* Optional timeline of the tensor-core pair (diagnostics): stamps is a device
+ * array of (blocks1 + blocks2) x 56 unsigned 64-bit globaltimer values (ns),
+ * one row per block of the gate/up kernel, then one per block of the down
+ * kernel.  Gate/up rows: [0] start, [1] the dependency wait done, [2] its
  * share of the normalized rows written, [3] the grid barrier passed, [4 + st]
  * stage st (< 48) landed at the MMA issuer, [52] every MMA complete, [53]
- * epilogue done -- or NULL (off, the default).  Other slots stay untouched. */
+ * epilogue done.  Down rows: [0] start, [1] the dependency wait done,
+ * [4 + st] stage st landed at the MMA issuer, [52] every MMA complete, [53]
+ * the partial tile reduced into the accumulator, [54] done.  NULL turns it
+ * off (the default).  Other slots stay untouched. */
 int cf_ffn_set_timeline(cf_ffn_handle* h, unsigned long long* stamps);
 
 /* Kernels a call of `batch` rows launches: returns 1 (the one- and two-row
