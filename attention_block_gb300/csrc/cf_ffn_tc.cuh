@@ -368,14 +368,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       named_sync(kBarConsumers, kConsumers);
-      const int nu = i1 - i0;
-      for (int idx = tid; idx < p.B * nu; idx += kConsumers) {
-        const int b = idx / nu, u = idx % nu;
-        const float z = S[b * 128 + u], up = S[b * 128 + p.UB + u];
-        T hi, lo;
-        split1<T>(z * __frcp_rn(1.0f + __expf(-z)) * up, hi, lo);
-        ahi[(size_t)b * p.Ip + i0 + u] = hi;
-        if constexpr (kHiLo) alo[(size_t)b * p.Ip + i0 + u] = lo;
+      // four independent (row, unit) pairs per pass, so their shared-memory
+      // reads and arithmetic overlap
+      const int nu = i1 - i0, total = p.B * nu;
+      for (int i = tid; i < total; i += 4 * kConsumers) {
+        float z[4], up[4];
+        int off[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int idx = min(i + k * kConsumers, total - 1);
+          const int b = idx / nu, u = idx - b * nu;
+          z[k] = S[b * 128 + u];
+          up[k] = S[b * 128 + p.UB + u];
+          off[k] = b * p.Ip + i0 + u;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          T hi, lo;
+          split1<T>(z[k] * __frcp_rn(1.0f + __expf(-z[k])) * up[k], hi, lo);
+          if (i + k * kConsumers < total) {
+            ahi[off[k]] = hi;
+            if constexpr (kHiLo) alo[off[k]] = lo;
+          }
+        }
       }
     } else if (i0 + 32 * qd < i1) {
       // gate in columns [0, NR), up in [NR, 2 NR) of the same lane (unit)
