@@ -53,6 +53,7 @@
 #include "cf.h"
 #include "cf_cluster.cuh"
 #include "cf_common.cuh"
+#include "cf_mma.cuh"
 #include "cf_mla.h"
 #include "cf_params.h"
 #include "cf_ptx.cuh"
@@ -79,6 +80,7 @@ constexpr int REC = DC + 4;     // state record: o_lat[512], m, l, 2 pad
 constexpr int MAX_STAGES = 8;
 constexpr int kMaxClusters = 64;  // resident clusters the phase-D merge handles
 constexpr int STAGE_BYTES = RT * DL * 2;  // 36,864: the largest item (a cache tile)
+static_assert(STAGE_BYTES == (DL / 64) * RT * 128 && RT % 16 == 0 && RT <= 32, "cache tile = nine swizzled boxes");
 static_assert(KT * GW * 2 <= STAGE_BYTES && DC % KT == 0 && DCB * DV * 2 <= STAGE_BYTES &&
                   DV * 128 * 2 <= STAGE_BYTES && DCB % kConsumerWarps == 0, "stage plan");
 
@@ -88,6 +90,7 @@ struct Params {  // 128-byte aligned through its CUtensorMap members
   CUtensorMap tm_wukv;  // [DC, nh*(DN+DV)], box {128, 64}   (phase B: k parts)
   CUtensorMap tm_wuv;   // [DC, nh*(DN+DV)], box {128, DCB}  (phase D: v parts)
   CUtensorMap tm_wo;    // [nh*DV, H],  box {wob, DV}
+  CUtensorMap tm_cache; // [B*S, DL] latent cache, box {64, RT}, 128-byte swizzle
   const void* hidden;   // [B, H]
   const void* ln_w;     // [H]
   const void* g_kv;     // [DC]
@@ -211,11 +214,6 @@ __device__ __forceinline__ void sub_range(int pos, int sidx, int nsub, int& t0, 
   t1 = (int)((long long)(sidx + 1) * n / nsub);
 }
 
-template <typename T>
-__device__ __forceinline__ void cvt8(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-  Elem<T>::words(w, 4, f);
-}
 
 // ------------------------------------------------------------------ kernel --
 // HPW: query heads per consumer warp (n_heads = 8 * HPW).
@@ -267,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
     prefetch_tensormap(&p.tm_wukv);
     prefetch_tensormap(&p.tm_wuv);
     prefetch_tensormap(&p.tm_wo);
+    prefetch_tensormap(&p.tm_cache);
   }
   __syncthreads();
   cluster_sync_all();  // peers' barriers exist before any DSMEM traffic
@@ -308,11 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
         const int posv = (pos >= 0 && pos < p.S) ? pos : 0;
         int t0, t1;
         sub_range(posv, pl.sidx, pl.nsub, t0, t1);
-        const T* base = static_cast<const T*>(p.cache) + (size_t)pl.row * p.S * DL;
+        // each tile: RT rows as nine 64-column boxes with the 128-byte
+        // swizzle (rows past the range arrive too and are zeroed by the
+        // consumers; rows past the tensor read as zero)
         for (int t = t0; t < t1; t += RT) {
-          const int n = min(RT, t1 - t);
-          uint8_t* dst = slot((uint32_t)(n * DL * 2), bar);
-          bulk_load_1d(dst, base + (size_t)t * DL, (uint32_t)(n * DL * 2), bar, pol);
+          uint8_t* dst = slot((uint32_t)STAGE_BYTES, bar);
+          for (int i = 0; i < DL / 64; ++i)
+            tma_load_2d(dst + i * RT * 128, &p.tm_cache, 64 * i, pl.row * p.S + t, bar, pol);
         }
       }
       stamp(kMlaTlProdC);
@@ -533,187 +534,227 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       int t0, t1;
       sub_range(pos >= 0 ? pos : 0, pl.sidx, pl.nsub, t0, t1);
       const bool fold_new = pos >= 0 && pl.sidx == pl.nsub - 1;
-      // this warp's heads h = warp + 8k; query parts of the lane's dims,
-      // pre-scaled into log2 units (16-byte loads)
-      float qc[HPW][16], qr[HPW][2];
-      float m[HPW], l[HPW], o[HPW][16];
+      // Tensor-core form of the latent attention [CF §5.2].  The 16 query
+      // rows (heads; rows nh..15 zero) are the MMAs' M side.  Warp w owns the
+      // latent dims [64 w, 64 w + 64) -- slab w of a cache tile -- and, for
+      // w < 4, the position dims [512 + 16 w, 512 + 16 w + 16) of slab 8:
+      // (1) its partial scores q[:, its dims] c[t, its dims]^T for the RT
+      // positions of a tile (A = the scaled query as 16-bit fragments held in
+      // registers for the whole phase, B = the tile's rows), summed over the
+      // warps in shared memory; (2) warp w's heads 2w, 2w+1 take the
+      // online-softmax step (lane = position) and write p and the factor of
+      // the running sums; (3) o[:, its dims] = alpha o + p c (A = p, B = slab
+      // w, transposed by ldmatrix).  The query and p enter as one fp16 value
+      // or as bf16 hi + lo pairs (about fp32 accuracy).
+      using MK = MmaKind<T>;
+      constexpr bool kHiLo = MK::kAttnHiLo;
+      const int nks = warp < 4 ? 5 : 4;  // k-steps of this warp's share of the scores
+      const int g = lane >> 2, cq = 2 * (lane & 3);
+      uint32_t qh[5][4], ql[5][4];
+      {
+        const float* qb = p.qf + (size_t)b * nh * DL;
 #pragma unroll
-      for (int k = 0; k < HPW; ++k) {
-        m[k] = -INFINITY;
-        l[k] = 0.f;
+        for (int ks = 0; ks < 5; ++ks) {
+          const int k0 = ks < 4 ? 64 * warp + 16 * ks : DC + 16 * warp;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[k][e] = 0.f;
-        const float* qh = p.qf + ((size_t)b * nh + warp + kConsumerWarps * k) * DL;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(qh + 16 * lane) + q4);
-          qc[k][4 * q4] = v.x * p.qk_scale_log2;
-          qc[k][4 * q4 + 1] = v.y * p.qk_scale_log2;
-          qc[k][4 * q4 + 2] = v.z * p.qk_scale_log2;
-          qc[k][4 * q4 + 3] = v.w * p.qk_scale_log2;
+          for (int e = 0; e < 4; ++e) {
+            // fragment register e: row g (+8 for odd e), columns k0 + cq (+8 for e >= 2)
+            const int r = g + 8 * (e & 1), k = k0 + cq + 8 * (e >> 1);
+            float v0 = 0.f, v1 = 0.f;
+            if (ks < nks && r < nh) {
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(qb + (size_t)r * DL + k));
+              v0 = v.x * p.qk_scale_log2;
+              v1 = v.y * p.qk_scale_log2;
+            }
+            MK::split2(v0, v1, qh[ks][e], ql[ks][e]);
+          }
         }
-        const float2 r2 = __ldcg(reinterpret_cast<const float2*>(qh + DC) + lane);
-        qr[k][0] = r2.x * p.qk_scale_log2;
-        qr[k][1] = r2.y * p.qk_scale_log2;
       }
-      float* sbuf = reinterpret_cast<float*>(sm + p.off_sc) + warp * HPW * RT;  // [HPW][RT]
-      // n <= RT rows: (1) scores, two rows at a time (HPW * 2 independent
-      // dot products per lane, reduced over the warp by one transposed
-      // shuffle reduction) into sbuf; (2) per head the tile's online-softmax
-      // update, probabilities back into sbuf; (3) o += p c, rows reloaded.
-      auto attend_rows = [&](auto&& row_c, auto&& row_r, int n) {
-        constexpr int PB = 2, NV = HPW * PB;
-        for (int t0r = 0; t0r < n; t0r += PB) {
-          float cf[PB][16], rf[PB][2];
+      float o[8][4];
 #pragma unroll
-          for (int j = 0; j < PB; ++j) {
-            if (t0r + j < n) {
-              row_c(t0r + j, cf[j]);
-              row_r(t0r + j, rf[j]);
-            } else {
+      for (int nb = 0; nb < 8; ++nb)
 #pragma unroll
-              for (int e = 0; e < 16; ++e) cf[j][e] = 0.f;
-              rf[j][0] = rf[j][1] = 0.f;
-            }
-          }
-          float v[NV];
-#pragma unroll
-          for (int k = 0; k < HPW; ++k)
-#pragma unroll
-            for (int j = 0; j < PB; ++j) {
-              float a0 = qr[k][0] * rf[j][0], a1 = qr[k][1] * rf[j][1];
-#pragma unroll
-              for (int e = 0; e < 16; e += 2) {
-                a0 = fmaf(qc[k][e], cf[j][e], a0);
-                a1 = fmaf(qc[k][e + 1], cf[j][e + 1], a1);
-              }
-              v[k * PB + j] = a0 + a1;
-            }
-          // transposed reduction: after the halving rounds lane l holds value
-          // index idx(l) (bits from lane bits 4, 3, ... down), the remaining
-          // rounds complete the sum within each lane group
-          int cnt = NV;
-#pragma unroll
-          for (int w = 16; w >= 1; w >>= 1) {
-            if (cnt > 1) {
-              const bool upper = (lane & w) != 0;
-              const int half = cnt / 2;
-#pragma unroll
-              for (int i = 0; i < NV / 2; ++i) {
-                if (i < half) {
-                  const float send = upper ? v[i] : v[i + half];
-                  const float keep = upper ? v[i + half] : v[i];
-                  v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-                }
-              }
-              cnt = half;
-            } else {
-              v[0] += __shfl_xor_sync(0xffffffffu, v[0], w);
-            }
-          }
-          // idx = sum over the halving rounds of (lane bit set ? half : 0)
-          int idx = 0, lowmask = 0;
-          {
-            int c2 = NV, w = 16;
-            while (c2 > 1) {
-              c2 /= 2;
-              if (lane & w) idx += c2;
-              w >>= 1;
-            }
-            lowmask = 2 * w - 1;  // lanes below the last halving bit share the value
-          }
-          const int k = idx / PB, j = idx % PB;
-          if ((lane & lowmask) == 0 && t0r + j < n) sbuf[k * RT + t0r + j] = v[0];
-        }
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < HPW; ++k) {
-          const float sc = lane < n ? sbuf[k * RT + lane] : -INFINITY;
-          float mt = sc;
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1)
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-          const float mn = fmaxf(m[k], mt);
-          const float alpha = exp2f(m[k] - mn);  // m = -inf, mn finite: 0
-          const float pr = lane < n ? exp2f(sc - mn) : 0.f;
-          float ps = pr;
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-          l[k] = l[k] * alpha + ps;
-          m[k] = mn;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[k][e] *= alpha;
-          __syncwarp();
-          if (lane < n) sbuf[k * RT + lane] = pr;
-        }
-        __syncwarp();
-        for (int t = 0; t < n; t += 2) {
-          float c0[16], c1[16];
-          row_c(t, c0);
-          if (t + 1 < n) row_c(t + 1, c1);
-#pragma unroll
-          for (int k = 0; k < HPW; ++k) {
-            const float p0 = sbuf[k * RT + t];
-            const float p1 = t + 1 < n ? sbuf[k * RT + t + 1] : 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              o[k][e] = fmaf(p0, c0[e], t + 1 < n ? fmaf(p1, c1[e], o[k][e]) : o[k][e]);
-          }
-        }
-        __syncwarp();
-      };
+        for (int e = 0; e < 4; ++e) o[nb][e] = 0.f;
+      float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};  // heads 2 warp + j
+      float* sS = reinterpret_cast<float*>(sm + p.off_sc);         // [8][16][RT] partial scores
+      T* sPh = reinterpret_cast<T*>(sS + kConsumerWarps * 16 * RT);  // [16][RT + 8] p (hi)
+      T* sPl = sPh + 16 * (RT + 8);                                  // [16][RT + 8] p (lo)
+      float* sAl = reinterpret_cast<float*>(sPl + 16 * (RT + 8));     // [16] factors
+      float* sPn = sAl + 16;                                          // [16] p of the new row
+      constexpr int PP = (RT + 8) * 2;  // p row pitch in bytes (not a multiple of 128)
       for (int tt = t0; tt < t1; tt += RT, ++it) {
         const int n = min(RT, t1 - tt);
         const int s = it % p.stages;
         mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
         if (tt == t0) stamp(kMlaTlC0);
-        const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
-        attend_rows(
-            [&](int t, float* c) {
-              const uint4* q4 = reinterpret_cast<const uint4*>(tile + t * DL + 16 * lane);
-              cvt8<T>(q4[0], c);
-              cvt8<T>(q4[1], c + 8);
-            },
-            [&](int t, float* r2) { load_cvt<T, 2>(tile + t * DL + DC + 2 * lane, r2); }, n);
+        uint8_t* tile = ring + (size_t)s * STAGE_BYTES;  // [DL / 64][RT][64], 128-byte swizzle
+        if (n < RT) {
+          // rows past the range (later positions, another row's cache or the
+          // zero fill) must not reach the sums: zero them
+          const int zr = (RT - n) * 8;  // 16-byte chunks per slab
+          for (int i = tid; i < (DL / 64) * zr; i += kConsumers) {
+            const int sl = i / zr, w = i - sl * zr;
+            *reinterpret_cast<uint4*>(tile + sl * RT * 128 + (n + w / 8) * 128 + (w % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // before the stage goes back to the TMA writes
+          named_sync(kBarConsumers, kConsumers);
+        }
+        // (1) partial scores of this warp's dims
+        {
+          float acc[4][4];
+#pragma unroll
+          for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 5; ++ks) {
+            if (ks < nks) {
+              const uint8_t* slab = tile + (ks < 4 ? warp : DC / 64) * (RT * 128);
+              const int k0 = ks < 4 ? 16 * ks : 16 * warp;  // column within the slab
+#pragma unroll
+              for (int nb = 0; nb < RT / 8; ++nb) {
+                uint32_t b0, b1;
+                ldmatrix_bt_sw128(b0, b1, slab, 8 * nb, k0, lane);
+                MK::mma(acc[nb], qh[ks], b0, b1);
+                if constexpr (kHiLo) MK::mma(acc[nb], ql[ks], b0, b1);
+              }
+            }
+          }
+          float* dst = sS + warp * 16 * RT;
+#pragma unroll
+          for (int nb = 0; nb < RT / 8; ++nb) {
+            *reinterpret_cast<float2*>(dst + g * RT + 8 * nb + cq) = make_float2(acc[nb][0], acc[nb][1]);
+            *reinterpret_cast<float2*>(dst + (g + 8) * RT + 8 * nb + cq) =
+                make_float2(acc[nb][2], acc[nb][3]);
+          }
+        }
+        named_sync(kBarConsumers, kConsumers);
+        // (2) online softmax of heads 2 warp + j over the tile
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int h = 2 * warp + j;
+          float sc = -INFINITY;
+          if (h < nh && lane < n) {
+            sc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) sc += sS[(w * 16 + h) * RT + lane];
+          }
+          float mt = sc;
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+          const float mn = fmaxf(m2[j], mt);
+          const float alpha = mn == -INFINITY ? 1.f : exp2f(m2[j] - mn);
+          const float pr = sc == -INFINITY ? 0.f : exp2f(sc - mn);
+          float ps = pr;
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+          l2[j] = l2[j] * alpha + ps;
+          m2[j] = mn;
+          const T phv = Elem<T>::from_f(pr);
+          sPh[h * (RT + 8) + lane] = phv;
+          if constexpr (kHiLo) sPl[h * (RT + 8) + lane] = Elem<T>::from_f(pr - Elem<T>::to_f(phv));
+          if (lane == 0) sAl[h] = alpha;
+        }
+        named_sync(kBarConsumers, kConsumers);
+        // (3) o = alpha o + p c over this warp's 64 latent dims
+        {
+          const float a0 = sAl[g], a1 = sAl[g + 8];
+#pragma unroll
+          for (int nb = 0; nb < 8; ++nb) {
+            o[nb][0] *= a0;
+            o[nb][1] *= a0;
+            o[nb][2] *= a1;
+            o[nb][3] *= a1;
+          }
+          const uint8_t* slab = tile + warp * (RT * 128);
+#pragma unroll
+          for (int ks = 0; ks < RT / 16; ++ks) {
+            uint32_t pa[4], pb[4];
+            ldmatrix_a(pa, sPh + 16 * ks, PP, lane);
+            if constexpr (kHiLo) ldmatrix_a(pb, sPl + 16 * ks, PP, lane);
+#pragma unroll
+            for (int nb = 0; nb < 8; ++nb) {
+              uint32_t b0, b1;
+              ldmatrix_b_sw128(b0, b1, slab, 16 * ks, 8 * nb, lane);
+              MK::mma(o[nb], pa, b0, b1);
+              if constexpr (kHiLo) MK::mma(o[nb], pb, b0, b1);
+            }
+          }
+        }
+        __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       if (fold_new) {
+        // the new row (fp32, not yet rounded): its scores, the softmax step
+        // and its term in o, on the CUDA cores
+        named_sync(kBarConsumers, kConsumers);  // every warp is done with sAl
         const float* nl = p.lat + (size_t)b * DL;
-        attend_rows(
-            [&](int, float* c) {
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(nl + 16 * lane) + q4);
-                c[4 * q4] = v.x;
-                c[4 * q4 + 1] = v.y;
-                c[4 * q4 + 2] = v.z;
-                c[4 * q4 + 3] = v.w;
-              }
-            },
-            [&](int, float* r2) {
-              const float2 v = __ldcg(reinterpret_cast<const float2*>(nl + DC) + lane);
-              r2[0] = v.x;
-              r2[1] = v.y;
-            },
-            1);
+        for (int j = 0; j < 2; ++j) {
+          const int h = 2 * warp + j;
+          float sc = 0.f;
+          if (h < nh) {
+            const float* qr = p.qf + ((size_t)b * nh + h) * DL;
+            for (int d = lane; d < DL; d += 32) sc = fmaf(__ldcg(qr + d), __ldcg(nl + d), sc);
+          }
+          sc = warp_sum(sc) * p.qk_scale_log2;
+          float alpha = 1.f, pn = 0.f;
+          if (h < nh) {
+            const float mn = fmaxf(m2[j], sc);
+            alpha = exp2f(m2[j] - mn);
+            pn = exp2f(sc - mn);
+            l2[j] = l2[j] * alpha + pn;
+            m2[j] = mn;
+          }
+          if (lane == 0) {
+            sAl[h] = alpha;
+            sPn[h] = pn;
+          }
+        }
+        named_sync(kBarConsumers, kConsumers);
+        const float a0 = sAl[g], a1 = sAl[g + 8], p0 = sPn[g], p1 = sPn[g + 8];
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+          const float2 c2 = __ldcg(reinterpret_cast<const float2*>(nl + 64 * warp + 8 * nb + cq));
+          o[nb][0] = fmaf(p0, c2.x, o[nb][0] * a0);
+          o[nb][1] = fmaf(p0, c2.y, o[nb][1] * a0);
+          o[nb][2] = fmaf(p1, c2.x, o[nb][2] * a1);
+          o[nb][3] = fmaf(p1, c2.y, o[nb][3] * a1);
+        }
       }
       // sparse ClusterReduce: head h's state goes only to the cluster block
-      // that owns it -- warp w's heads h = w + 8k all belong to block
-      // w % NCLU -- into slot [rank][(w / NCLU) * HPW + k] there
+      // that owns it, block (h % 8) % NCLU, into slot
+      // [rank][((h % 8) / NCLU) * HPW + h / 8] there; each warp sends its 64
+      // dims of every head, lane 0 of warp w the (m, l) of heads 2w, 2w+1
       {
         float* rbuf = scr;  // [NCLU][WPO * HPW][REC]
-        const uint32_t owner = (uint32_t)(warp % NCLU);
-        const uint32_t rbar = mapa(smem_u32(rx), owner);
+        auto record = [&](int h, uint32_t& raddr, uint32_t& rbar) {
+          const uint32_t owner = (uint32_t)((h % kConsumerWarps) % NCLU);
+          const int j = ((h % kConsumerWarps) / NCLU) * HPW + h / kConsumerWarps;
+          raddr = mapa(smem_u32(rbuf + ((size_t)rank * WPO * HPW + j) * REC), owner);
+          rbar = mapa(smem_u32(rx), owner);
+        };
 #pragma unroll
-        for (int k = 0; k < HPW; ++k) {
-          float* dst = rbuf + ((size_t)rank * WPO * HPW + (warp / NCLU) * HPW + k) * REC;
-          const uint32_t raddr = mapa(smem_u32(dst), owner);
+        for (int hf = 0; hf < 2; ++hf) {
+          const int h = g + 8 * hf;
+          if (h < nh) {
+            uint32_t raddr, rbar;
+            record(h, raddr, rbar);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_async_v4(raddr + 4u * (16 * lane + 4 * q),
-                        make_float4(o[k][4 * q], o[k][4 * q + 1], o[k][4 * q + 2], o[k][4 * q + 3]),
-                        rbar);
-          if (lane == 0) st_async_v4(raddr + 4u * DC, make_float4(m[k], l[k], 0.f, 0.f), rbar);
+            for (int nb = 0; nb < 8; ++nb)
+              st_async_v2(raddr + 4u * (64 * warp + 8 * nb + cq),
+                          make_float2(o[nb][2 * hf], o[nb][2 * hf + 1]), rbar);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int h = 2 * warp + j;
+          if (h < nh && lane == 0) {
+            uint32_t raddr, rbar;
+            record(h, raddr, rbar);
+            st_async_v4(raddr + 4u * DC, make_float4(m2[j], l2[j], 0.f, 0.f), rbar);
+          }
         }
         stamp(kMlaTlC1);
         mbar_wait_cluster(rx, 0, p.errflag);
@@ -956,7 +997,8 @@ inline Layout layout_for(int stages, int max_batch, int H, int nh) {
   L.misc = off;
   off += r128(4 * (2 * BMAX + 4 + 8 + BMAX * kMaxClusters));
   L.sc = off;
-  off += r128(4 * kConsumerWarps * hpw * RT);
+  // phase C: partial scores [8][16][RT] fp32, p hi and lo [16][RT + 8], factors [16], new-row p [16]
+  off += r128(4 * kConsumerWarps * 16 * RT + 2 * 2 * 16 * (RT + 8) + 2 * 16 * 4);
   L.total = off + 1024;
   return L;
 }
@@ -982,6 +1024,9 @@ struct cf_mla_handle {
     const void* ptr = nullptr;
     CUtensorMap map;
   } m_wq, m_wdkv, m_wukv, m_wuv, m_wo;
+  // latent cache [batch * S, DL] with the 128-byte swizzle, for the batch it was encoded for
+  MapSlot m_cache;
+  int cache_batch = 0;
 };
 
 namespace {
@@ -1162,6 +1207,15 @@ int cf_mla_decode(cf_mla_handle* h, int32_t batch, const void* hidden_states,
   p.tm_wukv = *m3;
   p.tm_wuv = *m5;
   p.tm_wo = *m4;
+  if (h->m_cache.ptr != latent_cache || h->cache_batch != batch) {
+    h->m_cache.ptr = nullptr;
+    if (!encode_tmap_2d(&h->m_cache.map, c.dtype, latent_cache, DL, (uint64_t)batch * S, DL * 2,
+                        64, RT, true))
+      return CF_ERR_CUDA;
+    h->m_cache.ptr = latent_cache;
+    h->cache_batch = batch;
+  }
+  p.tm_cache = h->m_cache.map;
   p.hidden = hidden_states;
   p.ln_w = ln_weight;
   p.g_kv = kv_norm_weight;

@@ -106,6 +106,20 @@ __device__ __forceinline__ void ldmatrix_b_sw128(uint32_t& b0, uint32_t& b1, con
                : "r"(addr));
 }
 
+// B fragment (16 k-columns x 8 n-rows) whose columns are rows of a TMA box
+// written with the 128-byte swizzle: B[k][n] = box[n0 + n][k0 + k] (box rows
+// of 64 16-bit elements, base 1024-byte aligned; n0 a multiple of 8, k0 of
+// 16 below 64).  Matrix i of the pair holds columns k0 + 8 i .. k0 + 8 i + 7.
+__device__ __forceinline__ void ldmatrix_bt_sw128(uint32_t& b0, uint32_t& b1, const void* box,
+                                                  int n0, int k0, int lane) {
+  const int r = n0 + (lane & 7);
+  const int chunk = ((k0 >> 3) + ((lane >> 3) & 1)) ^ (r & 7);
+  const uint32_t addr = smem_u32(box) + r * 128 + chunk * 16;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(b0), "=r"(b1)
+               : "r"(addr));
+}
+
 // A fragment (16 m-rows x 16 k-columns) of the TRANSPOSE of a TMA box written
 // with the 128-byte swizzle: A[m][k] = box[k0 + k][m0 + m], i.e. the 8x8
 // blocks (k0..7, m0..7), (k0..7, m8..15), (k8..15, m0..7), (k8..15, m8..15)

@@ -282,8 +282,15 @@ __device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
   return r;
 }
 
-// Asynchronous 16-byte store into a remote CTA's shared memory that signals
-// the remote mbarrier `rbar` with complete_tx(16).
+// Asynchronous 8- or 16-byte store into a remote CTA's shared memory that
+// signals the remote mbarrier `rbar` with complete_tx of its byte count.
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, float2 v, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+          raddr),
+      "f"(v.x), "f"(v.y), "r"(rbar)
+      : "memory");
+}
 __device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
   asm volatile(
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
