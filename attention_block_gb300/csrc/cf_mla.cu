@@ -759,23 +759,31 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
         stamp(kMlaTlC1);
         mbar_wait_cluster(rx, 0, p.errflag);
         // merge the NCLU states of each owned head: slot j = (w / NCLU) * HPW
-        // + k holds head h = w + 8k of warp w = rank + NCLU * (j / HPW)
+        // + k holds head h = w + 8k of warp w = rank + NCLU * (j / HPW); the
+        // slot's maximum and the sources' factors 2^(m_src - max) first
         const int ci = pl.sidx / NCLU;
         constexpr int JPB = WPO * HPW;
-        for (int idx = tid; idx < JPB * (DC + 2); idx += kConsumers) {
-          const int j = idx / (DC + 2), e = idx % (DC + 2);
+        float* sf = sS;  // [JPB][NCLU + 1]: factors, then the maximum
+        if (tid < JPB) {
           float mm = -INFINITY;
           for (int src = 0; src < NCLU; ++src)
-            mm = fmaxf(mm, rbuf[((size_t)src * JPB + j) * REC + DC]);
+            mm = fmaxf(mm, rbuf[((size_t)src * JPB + tid) * REC + DC]);
+          for (int src = 0; src < NCLU; ++src)
+            sf[tid * (NCLU + 1) + src] =
+                mm == -INFINITY ? 0.f : exp2f(rbuf[((size_t)src * JPB + tid) * REC + DC] - mm);
+          sf[tid * (NCLU + 1) + NCLU] = mm;
+        }
+        named_sync(kBarConsumers, kConsumers);
+        for (int idx = tid; idx < JPB * (DC + 2); idx += kConsumers) {
+          const int j = idx / (DC + 2), e = idx % (DC + 2);
           float v = 0.f;
           if (e == DC) {
-            v = mm;
+            v = sf[j * (NCLU + 1) + NCLU];
           } else {
-            for (int src = 0; src < NCLU; ++src) {
-              const float* rs = rbuf + ((size_t)src * JPB + j) * REC;
-              const float sc = (mm == -INFINITY) ? 0.f : exp2f(rs[DC] - mm);
-              v = fmaf(e < DC ? rs[e] : rs[DC + 1], sc, v);
-            }
+            const int ee = e < DC ? e : DC + 1;
+#pragma unroll
+            for (int src = 0; src < NCLU; ++src)
+              v = fmaf(rbuf[((size_t)src * JPB + j) * REC + ee], sf[j * (NCLU + 1) + src], v);
           }
           const int h = rank + NCLU * (j / HPW) + kConsumerWarps * (j % HPW);
           float* dst = p.part + (((size_t)b * p.ncr_max + ci) * nh + h) * REC;
@@ -828,21 +836,44 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
             s_mf[b * kMaxClusters + lane + 32 * q] = L > 0.f ? f[q] / L : 0.f;
         }
         named_sync(kBarConsumers, kConsumers);
-        for (int idx = tid; idx < B * DCB; idx += kConsumers) {
-          const int b = idx / DCB, i = rank * DCB + idx % DCB;
-          const int ncr = (p.ncl - b + B - 1) / B;
-          const float* ps = p.part + ((size_t)b * p.ncr_max * nh + h) * REC + i;
-          const size_t cstride = (size_t)nh * REC;
-          float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-          int c = 0;
-          for (; c + 4 <= ncr; c += 4) {
-            v0 = fmaf(__ldcg(ps + c * cstride), s_mf[b * kMaxClusters + c], v0);
-            v1 = fmaf(__ldcg(ps + (c + 1) * cstride), s_mf[b * kMaxClusters + c + 1], v1);
-            v2 = fmaf(__ldcg(ps + (c + 2) * cstride), s_mf[b * kMaxClusters + c + 2], v2);
-            v3 = fmaf(__ldcg(ps + (c + 3) * cstride), s_mf[b * kMaxClusters + c + 3], v3);
+        {
+          // with fewer (row, latent row) items than threads, SP threads share
+          // an item's clusters; eight loads in flight per thread
+          const int items = B * DCB;
+          const int SP = items >= kConsumers ? 1 : kConsumers / items;
+          float* half = red;  // [SP][items] partial sums
+          for (int t = tid; t < items * SP; t += kConsumers) {
+            const int idx = t % items, sp = t / items;
+            const int b = idx / DCB, i = rank * DCB + idx % DCB;
+            const int ncr = (p.ncl - b + B - 1) / B;
+            const float* ps = p.part + ((size_t)b * p.ncr_max * nh + h) * REC + i;
+            const size_t cstride = (size_t)nh * REC;
+            float v0 = 0.f, v1 = 0.f;
+            for (int c0 = sp; c0 < ncr; c0 += 8 * SP) {
+              float x[8], f[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int c = c0 + k * SP;
+                x[k] = c < ncr ? __ldcg(ps + c * cstride) : 0.f;
+                f[k] = c < ncr ? s_mf[b * kMaxClusters + c] : 0.f;
+              }
+#pragma unroll
+              for (int k = 0; k < 8; k += 2) {
+                v0 = fmaf(x[k], f[k], v0);
+                v1 = fmaf(x[k + 1], f[k + 1], v1);
+              }
+            }
+            if (SP == 1) ol[idx] = v0 + v1;
+            else half[sp * items + idx] = v0 + v1;
           }
-          for (; c < ncr; ++c) v0 = fmaf(__ldcg(ps + c * cstride), s_mf[b * kMaxClusters + c], v0);
-          ol[idx] = (v0 + v1) + (v2 + v3);
+          if (SP > 1) {
+            named_sync(kBarConsumers, kConsumers);
+            for (int idx = tid; idx < items; idx += kConsumers) {
+              float v = 0.f;
+              for (int sp = 0; sp < SP; ++sp) v += half[sp * items + idx];
+              ol[idx] = v;
+            }
+          }
         }
         named_sync(kBarConsumers, kConsumers);
         // o_h partial over the block's latent rows, 64 per w_uv box: warp w
