@@ -63,6 +63,11 @@ __device__ void cluster_allreduce(float* data, int n, float* rbuf, uint64_t* rba
   for (int s = 1; s < N; s <<= 1, ++r) {
     float* rb = rbuf + r * n;
     push_to_peer<NT>(data, rb, n, &rbar[r], rank ^ s, tid);
+    // Every thread has read its share of data for the push before any thread
+    // overwrites data below: the threads that push nothing (n / 4 < NT) or
+    // finish first would otherwise update chunks another thread has yet to
+    // send, and the partner would add its own contribution twice.
+    named_sync(kBar, NT);
     mbar_wait_cluster(&rbar[r], 0, err);
     for (int i = tid; i < n; i += NT) data[i] = Op::apply(data[i], rb[i]);
     named_sync(kBar, NT);

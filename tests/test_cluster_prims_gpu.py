@@ -40,6 +40,25 @@ def test_allreduce_sum_and_max(N, n):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("N", [2, 4, 8])
+def test_allreduce_with_threads_that_push_nothing_repeated(N):
+    """n = 512 floats: only half of the threads push a chunk, all of them
+    combine, so the combine must wait until every chunk has been read for the
+    push.  Many launches back to back vary the timing."""
+    n, reps = 512, 200
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = _ints((N, n), 7 * N)
+    ref = x.sum(0)
+    outs = [torch.full_like(x, float("nan")) for _ in range(reps)]
+    for out in outs:
+        assert binding.cf_test_cluster_allreduce(N, 0, n, x, out, err) == binding.CF_OK
+    torch.cuda.synchronize()
+    for i, out in enumerate(outs):
+        for r in range(N):
+            assert torch.equal(out[r], ref), (N, i, r)
+    assert int(err.item()) == 0
+
+
 def test_allreduce_max_with_ties_and_negative_infinity():
     N, n = 8, 8
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
