@@ -28,13 +28,26 @@ def round_to(ref: np.ndarray, dtype: str) -> np.ndarray:
     return t.to(torch.float64).numpy()
 
 
-def check(gpu, ref, what: str, mean_rel: float = MEAN_REL):
+def storage_ulp(values: np.ndarray, dtype: str) -> float:
+    """One unit in the last place of the storage type at the largest
+    magnitude of `values` (0 for fp32 storage)."""
+    bits = {"f16": 10, "bf16": 7}.get(dtype)
+    m = float(np.max(np.abs(values))) if np.size(values) else 0.0
+    if bits is None or m == 0.0:
+        return 0.0
+    return 2.0 ** (np.floor(np.log2(m)) - bits)
+
+
+def check(gpu, ref, what: str, mean_rel: float = MEAN_REL, floor: float = 0.0):
+    """`floor` widens the max bound for differences of values that were each
+    rounded to the storage type (e.g. out - hidden): one rounding flip of
+    the output moves such a difference by one storage ulp of the output."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
     assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU values"
     err = np.abs(gpu - ref)
-    bound = MAX_ABS_REL * np.max(np.abs(ref)) + MAX_ABS_ADD
+    bound = MAX_ABS_REL * np.max(np.abs(ref)) + MAX_ABS_ADD + floor
     mre = err.sum() / max(np.abs(ref).sum(), 1e-300)
     assert err.max() <= bound, f"{what}: max|err| {err.max():.3e} > {bound:.3e}"
     assert mre <= mean_rel, f"{what}: mean rel err {mre:.3e} > {mean_rel:.1e}"

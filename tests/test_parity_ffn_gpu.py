@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from attention_block_gb300 import binding, synth
-from parity_util import check, make_block, round_to, run_gpu, run_oracle
+from parity_util import check, make_block, round_to, run_gpu, run_oracle, storage_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,7 @@ def full_ffn_check(w, seed=0, rows=None, **kw):
     # the FFN's own contribution, unmasked by the residual (both sides carry
     # the output's rounding to the storage type)
     x = synth.to_f64(t["hidden"][rows])
-    check(got - x, want - x, "out - hidden")
+    check(got - x, want - x, "out - hidden", floor=storage_ulp(want, w.dtype))
     return out, ref
 
 
@@ -108,7 +108,7 @@ def test_tensor_core_pair_scaled_shapes(shape):
     want = round_to(ref["out"], w.dtype)
     check(got, want, "out")
     x = synth.to_f64(t["hidden"][rows])
-    check(got - x, want - x, "out - hidden")
+    check(got - x, want - x, "out - hidden", floor=storage_ulp(want, w.dtype))
     # the intermediate activations the pair hands from one kernel to the next
     check(blk.debug_a(B), ref["a"], "a = silu(gate) * up")
 
@@ -126,7 +126,12 @@ def test_tensor_core_pair_small_batches_and_repeats_on_one_handle():
         assert blk.status() == binding.CF_OK
         assert torch.isnan(out[B:]).all()
         if B in firsts:
-            check(out[:B].double().cpu().numpy(), firsts[B], f"repeat B={B}", mean_rel=1e-5)
+            # The row sums of squares meet by fp32 atomics in any order, so a
+            # repeat may round a few single-fp16 activations one ulp apart,
+            # which moves outputs by about one fp16 ulp: bound the mean
+            # relative difference at 1e-4 (stale workspace state would show
+            # as errors of the order of the values themselves).
+            check(out[:B].double().cpu().numpy(), firsts[B], f"repeat B={B}", mean_rel=1e-4)
             continue
         firsts[B] = out[:B].double().cpu().numpy()
         rows = sorted({0, B - 1})
@@ -305,4 +310,5 @@ def test_decoder_layers_chained_under_programmatic_dependent_launch(shape):
         got = outs[l].double().cpu().numpy()
         check(got, round_to(ref_f["out"], dt), f"layer {l} FFN")
         h = synth.to_f64(mids[l])
-        check(got - h, round_to(ref_f["out"], dt) - h, f"layer {l} FFN - its input")
+        want = round_to(ref_f["out"], dt)
+        check(got - h, want - h, f"layer {l} FFN - its input", floor=storage_ulp(want, dt))
