@@ -613,17 +613,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_sync(kBarConsumers, kConsumers);
     if (s_flag[0]) {
       // residual of the column tile [LNA §一]
-      const T* hid = static_cast<const T*>(p.h);
-      T* out = static_cast<T*>(p.out);
-      for (int idx = tid; idx < p.B * 32; idx += kConsumers) {
-        const int b = idx / 32, c4 = idx % 32;
-        const size_t off = (size_t)b * p.H + j0 + 4 * c4;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
-        float x[4];
-        load_cvt<T, 4>(hid + off, x);
-        const float r4[4] = {x[0] + v.x, x[1] + v.y, x[2] + v.z, x[3] + v.w};
-        store4<T>(out + off, r4);
-        __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
+      // eight (row, 4-column) items per thread and pass (all 64 rows in one
+      // pass), all loads first
+      constexpr int U = 8;
+      const T* __restrict__ hid = static_cast<const T*>(p.h);
+      T* __restrict__ out = static_cast<T*>(p.out);
+      const int items = p.B * 32;
+      for (int i0 = tid; i0 < items; i0 += U * kConsumers) {
+        float4 v[U];
+        float x[U][4];
+        size_t off[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int idx = i0 + k * kConsumers;
+          off[k] = (size_t)(idx < items ? idx / 32 : 0) * p.H + j0 + 4 * (idx % 32);
+          if (idx < items) {
+            v[k] = __ldcg(reinterpret_cast<const float4*>(p.acc + off[k]));
+            load_cvt<T, 4>(hid + off[k], x[k]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          if (i0 + k * kConsumers < items) {
+            const float r4[4] = {x[k][0] + v[k].x, x[k][1] + v[k].y, x[k][2] + v[k].z,
+                                 x[k][3] + v[k].w};
+            store4<T>(out + off[k], r4);
+            __stcg(reinterpret_cast<float4*>(p.acc + off[k]), make_float4(0.f, 0.f, 0.f, 0.f));
+          }
+        }
       }
       if (tid == 0) p.counters[jt] = 0;
     }
