@@ -179,9 +179,15 @@ bool make_plan_rows(const cf_config& c, int BT, int RPC, int stage_req, const cu
   budget -= 1024;
   int stages = std::min((budget - extras) / pl.stage_bytes, kMaxStages);
   if (c.max_stages > 0) stages = std::min(stages, c.max_stages);
-  if (stages < 2) {
-    // a default stage size larger than 32 KB that leaves fewer than two
-    // stages: retry with 32 KB
+  // On tcgen05 only the MMA-issuing thread waits for every W_qkv stage; the
+  // other consumers wait for the first stage of each K slice only, NC/64/CB
+  // ring slots after the previous one.  The ring must hold a whole slice's
+  // stages, or that wait could meet a slot whose earlier fill is still
+  // pending and take its parity as complete.
+  const int min_stages = tc5 ? std::max(2, NC / 64 / CB) : 2;
+  if (stages < min_stages) {
+    // a default stage size larger than 32 KB that leaves too few stages:
+    // retry with 32 KB
     if (c.stage_bytes == 0 && stage_req > 32768)
       return make_plan_rows(c, BT, RPC, 32768, prop, pl);
     return false;
