@@ -55,6 +55,7 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
   constexpr int KS = D / 16;  // k steps of S^T = K Q^T
   constexpr int MD = D / 16;  // 16-row tiles of O^T
   constexpr int NB = D / 64;  // swizzled boxes per K (or V) tile
+  constexpr int NA = MK::kAttnHiLo ? 2 : 4;  // S^T accumulators per 16-row tile (per product)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int h0 = 2 * tq;  // this lane's two head columns h0, h0 + 1
@@ -103,15 +104,23 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
   const int lch = lane >> 4;
   int t0, t1;
   kv_tile_range(pos, p.Rt, 0, 1, t0, t1);
-  for (int t = t0; t < t1; ++t, ++it) {
+  // ring slot of tile t and the group that owns it, advanced by counting
+  RingPos rp(it, p.stages);
+  int gsel = 0;
+  auto next = [&]() {
+    ++it;
+    rp.next(p.stages);
+    if (++gsel == GROUPS) gsel = 0;
+  };
+  for (int t = t0; t < t1; ++t, next()) {
     // Every warp waits for every tile, in ring order, and arrives once on its
     // release: a warp never waits on a stage whose earlier phase is still
     // pending (its parity would read as complete).  Only the owning group
     // computes on the tile.
-    const int s = it % p.stages;
-    mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+    const int s = rp.slot;
+    mbar_wait(&full[s], rp.phase, p.errflag);
     if (t == t0) stamp(kTlAttnFirst);
-    if ((t - t0) % GROUPS != my_group) {
+    if (gsel != my_group) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       continue;
@@ -135,24 +144,30 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
         wrote = true;
         __syncwarp();
       }
-      // ---- S^T for positions cb..cb+31 (two 16-row tiles), hi and lo
-      // products in separate accumulators (independent chains)
-      float sa[2][4], sb[2][4];
+      // ---- S^T for positions cb..cb+31 (two 16-row tiles).  A dependent
+      // mma.sync waits for the full latency of the one before it, so the k
+      // steps rotate over NA accumulators per tile and the hi and lo products
+      // go to separate ones: consecutive MMAs are independent.
+      float sa[2][NA][4], sb[2][NA][4];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sa[mt][e] = sb[mt][e] = 0.f;
+        for (int j = 0; j < NA; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sa[mt][j][e] = sb[mt][j][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint4 f = qf[ks * 32 + lane];
         const int ch = ks * 2 + lch;
+        uint32_t a[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          ldsm_x4(a[mt][0], a[mt][1], a[mt][2], a[mt][3],
+                  kbase + (ch >> 3) * box_bytes + sw128(cb + mt * 16 + lrow, ch & 7));
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-          uint32_t a[4];
-          ldsm_x4(a[0], a[1], a[2], a[3],
-                  kbase + (ch >> 3) * box_bytes + sw128(cb + mt * 16 + lrow, ch & 7));
-          MK::mma(sa[mt], a, f.x, f.y);
-          if constexpr (MK::kAttnHiLo) MK::mma(sb[mt], a, f.z, f.w);
+          MK::mma(sa[mt][ks % NA], a[mt], f.x, f.y);
+          if constexpr (MK::kAttnHiLo) MK::mma(sb[mt][ks % NA], a[mt], f.z, f.w);
         }
       }
       // ---- online softmax per head column (positions are spread over gq)
@@ -163,7 +178,9 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int pp = cb + mt * 16 + gq + ((e >> 1) << 3);
-          const float v = sa[mt][e] + sb[mt][e];
+          float v = 0.f;
+#pragma unroll
+          for (int j = 0; j < NA; ++j) v += MK::kAttnHiLo ? sa[mt][j][e] + sb[mt][j][e] : sa[mt][j][e];
           sc[mt][e] = (pp < lim) ? v : -INFINITY;
         }
 #pragma unroll
@@ -194,13 +211,6 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
       }
       l[0] = fmaf(l[0], al0, ps0);
       l[1] = fmaf(l[1], al1, ps1);
-#pragma unroll
-      for (int md = 0; md < MD; ++md) {
-        o[md][0] *= al0;
-        o[md][2] *= al0;
-        o[md][1] *= al1;
-        o[md][3] *= al1;
-      }
       // ---- P^T as B fragments: (positions 2tq.., head gq) per 8-position
       // half, from the S^T layout (position gq, heads 2tq..) by transposing
       uint32_t bh[2][2], bl[2][2];
@@ -216,18 +226,34 @@ __device__ void attend_row_tc(const KParams& p, const float* q_in, const float* 
           bl[mt][1] = movmatrix_trans(l23);
         }
       }
-      // ---- O^T += V^T P^T: k = 32 positions in two steps
+      // ---- O^T += V^T P^T: k = 32 positions in two steps, into fresh
+      // accumulators, the dimension tiles interleaved so that consecutive
+      // MMAs are independent (the lo products in a second pass over V^T);
+      // the running O^T is rescaled and the chunk added once
+      float pa[MD][4];
+#pragma unroll
+      for (int md = 0; md < MD; ++md)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pa[md][e] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hl = 0; hl < (MK::kAttnHiLo ? 2 : 1); ++hl)
+#pragma unroll
+          for (int md = 0; md < MD; ++md) {
+            const int ch = md * 2 + lch;
+            uint32_t a[4];
+            ldsm_x4_trans(a[0], a[2], a[1], a[3],
+                          vbase + (ch >> 3) * box_bytes + sw128(cb + mt * 16 + lrow, ch & 7));
+            if (hl == 0) MK::mma(pa[md], a, bh[mt][0], bh[mt][1]);
+            else MK::mma(pa[md], a, bl[mt][0], bl[mt][1]);
+          }
 #pragma unroll
       for (int md = 0; md < MD; ++md) {
-        const int ch = md * 2 + lch;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          uint32_t a[4];
-          ldsm_x4_trans(a[0], a[2], a[1], a[3],
-                        vbase + (ch >> 3) * box_bytes + sw128(cb + mt * 16 + lrow, ch & 7));
-          MK::mma(o[md], a, bh[mt][0], bh[mt][1]);
-          if constexpr (MK::kAttnHiLo) MK::mma(o[md], a, bl[mt][0], bl[mt][1]);
-        }
+        o[md][0] = fmaf(o[md][0], al0, pa[md][0]);
+        o[md][1] = fmaf(o[md][1], al1, pa[md][1]);
+        o[md][2] = fmaf(o[md][2], al0, pa[md][2]);
+        o[md][3] = fmaf(o[md][3], al1, pa[md][3]);
       }
     }
     // Generic-proxy writes into the stage must be ordered before the TMA

@@ -85,6 +85,23 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Position in a ring of n mbarrier-guarded slots: the slot of use `it` and
+// the parity of its pass (the k-th fill of a slot completes the barrier's
+// phase k), advanced by counting: a division by a runtime divisor is a long
+// dependent instruction chain, paid per stage otherwise.
+struct RingPos {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ RingPos(int it, int n)
+      : slot(it % n), phase((uint32_t)(it / n) & 1u) {}
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // Position tiles [t0, t1) of the cached keys 0..pos-1 handled by block `rank`
 // (balanced split of ceil(pos/Rt) tiles over N blocks).  pos < 0 marks an
 // invalid row; pos == 0 has no cached key (only the new token).

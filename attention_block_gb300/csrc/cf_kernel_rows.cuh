@@ -209,9 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       const uint64_t pol_w = p.nbt > 1 ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_kv = policy_evict_first();
       int it = 0;
+      RingPos rp(0, p.stages);
       auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
-        const int s = it % p.stages;
-        if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+        const int s = rp.slot;
+        if (it >= p.stages) mbar_wait(&empty[s], rp.phase ^ 1u, p.errflag);
+        rp.next(p.stages);
         bar = &full[s];
         mbar_arrive_expect_tx(bar, bytes);
         return ring + (size_t)s * p.stage_bytes;
@@ -300,13 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       float ss[NRW];
 #pragma unroll
       for (int i = 0; i < NRW; ++i) ss[i] = 0.f;
+      RingPos rp(it, p.stages);
       for (int kt = 0; kt < nkt; ++kt) {
         uint8_t* xs = un + (size_t)(kt & 1) * xbuf;
-        for (int cg = 0; cg < NCG; ++cg, ++it) {
-          const int s = it % p.stages;
+        for (int cg = 0; cg < NCG; ++cg, ++it, rp.next(p.stages)) {
+          const int s = rp.slot;
           uint8_t* st = ring + (size_t)s * p.stage_bytes;
           if (cg == 0) {
-            mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+            mbar_wait(&full[s], rp.phase, p.errflag);
             // the MMAs of slice kt - 2 read this buffer
             if (kt >= 2) mbar_wait(&tc_bar[kt & 1], ((kt - 2) >> 1) & 1, p.errflag);
             const T* xt = reinterpret_cast<const T*>(st + CB * wbox_bytes);  // [BT][Rw]
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
             named_sync(kBarConsumers, kConsumers);
           }
           if (tid == 0) {
-            if (cg != 0) mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+            if (cg != 0) mbar_wait(&full[s], rp.phase, p.errflag);
             tc05_fence_after();
 #pragma unroll
             for (int t = 0; t < NT5; ++t) {
@@ -414,14 +417,15 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       float ss[NRW];
 #pragma unroll
       for (int i = 0; i < NRW; ++i) ss[i] = 0.f;
+      RingPos rp(it, p.stages);
       for (int kt = 0; kt < nkt; ++kt) {
         // x * g of this K slice as hi + lo 16-bit pairs (double-buffered)
         uint8_t* ahi = un + (size_t)(kt & 1) * 2 * abytes;
         uint8_t* alo = ahi + abytes;
 #pragma unroll
-        for (int cg = 0; cg < NCG; ++cg, ++it) {
-          const int s = it % p.stages;
-          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        for (int cg = 0; cg < NCG; ++cg, ++it, rp.next(p.stages)) {
+          const int s = rp.slot;
+          mbar_wait(&full[s], rp.phase, p.errflag);
           uint8_t* st = ring + (size_t)s * p.stage_bytes;
           if (cg == 0) {
             // stage the slice's x * g; warp w stages rows w, w+8, ...
@@ -670,13 +674,14 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, true);
       const int it0 = it;
       const int qd = warp & 3, hrow = (warp >> 2) * (BT / 2);
+      RingPos rp(it0, p.stages);  // advanced by the issuing thread only
       for (int cb = 0; cb <= ncb; ++cb) {
         if (cb < ncb && tid == 0) {
           tc05_fence_after();
           const uint32_t dbuf = tmem + (uint32_t)((cb & 1) * 2 * N5);
-          for (int rt = 0; rt < nrt; ++rt) {
-            const int i = it0 + cb * nrt + rt, s = i % p.stages;
-            mbar_wait(&full[s], (i / p.stages) & 1, p.errflag);
+          for (int rt = 0; rt < nrt; ++rt, rp.next(p.stages)) {
+            const int s = rp.slot;
+            mbar_wait(&full[s], rp.phase, p.errflag);
             if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
             uint8_t* st = ring + (size_t)s * p.stage_bytes;
             for (int tt = 0; tt < ntl; ++tt) {
@@ -736,15 +741,16 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
       const int mtiles = p.Co / 16;
       const int gq = lane >> 2, tq = lane & 3;
       const bool even = (gq & 1) == 0;
+      RingPos rp(it, p.stages);
       for (int cb = 0; cb < ncb; ++cb) {
         float acc[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-        for (int rt = 0; rt < nrt; ++rt, ++it) {
-          const int s = it % p.stages;
-          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        for (int rt = 0; rt < nrt; ++rt, ++it, rp.next(p.stages)) {
+          const int s = rp.slot;
+          mbar_wait(&full[s], rp.phase, p.errflag);
           if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
           uint8_t* st = ring + (size_t)s * p.stage_bytes;
           for (int ks = 0; ks < p.Ro / 16; ++ks) {
@@ -792,6 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
     } else {
       const int ntiles = p.Co / 8;
       const int gq = lane >> 2, tq = lane & 3;
+      RingPos rp(it, p.stages);
       for (int cb = 0; cb < ncb; ++cb) {
         float acc[MT][4][4];  // up to 4 n-tiles per warp per box (Co <= 256)
 #pragma unroll
@@ -800,9 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
           for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mt][j][e] = 0.f;
-        for (int rt = 0; rt < nrt; ++rt, ++it) {
-          const int s = it % p.stages;
-          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        for (int rt = 0; rt < nrt; ++rt, ++it, rp.next(p.stages)) {
+          const int s = rp.slot;
+          mbar_wait(&full[s], rp.phase, p.errflag);
           if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
           uint8_t* st = ring + (size_t)s * p.stage_bytes;
           for (int ks = 0; ks < p.Ro / 16; ++ks) {
