@@ -113,9 +113,10 @@ __device__ void attend_row(const KParams& p, const float* q_in, const float* kn,
   int t0, t1;
   kv_tile_range(pos, p.Rt, seq_rank, seq_n, t0, t1);
   constexpr int kStep = kConsumerWarps * NGRP;  // positions per warp-wide pass
-  for (int t = t0; t < t1; ++t, ++it) {
-    const int s = it % p.stages;
-    mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+  RingPos rp(it, p.stages);
+  for (int t = t0; t < t1; ++t, ++it, rp.next(p.stages)) {
+    const int s = rp.slot;
+    mbar_wait(&full[s], rp.phase, p.errflag);
     if (t == t0) stamp(kTlAttnFirst);
     const T* Kt = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
     const T* Vt = Kt + (size_t)p.Rt * D;

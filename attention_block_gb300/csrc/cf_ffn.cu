@@ -147,14 +147,15 @@ __global__ void __launch_bounds__(kThreads, 1) cf_ffn_kernel(const __grid_consta
                                 static_cast<const uint8_t*>(p.wu),
                                 static_cast<const uint8_t*>(p.wd)};
       int it = 0;
+      RingPos rp(0, p.stages);
       // gate and up rows of every group, then the down rows
       for (int pass = 0; pass < 2; ++pass)
         for (int c = 0; c < nchunk; ++c) {
           const int r0 = i0 + c * p.R;
           const uint32_t bytes = (uint32_t)(min(p.R, i1 - r0) * row_bytes);
-          for (int m = pass * 2; m < (pass ? 3 : 2); ++m, ++it) {
-            const int s = it % p.stages;
-            if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+          for (int m = pass * 2; m < (pass ? 3 : 2); ++m, ++it, rp.next(p.stages)) {
+            const int s = rp.slot;
+            if (it >= p.stages) mbar_wait(&empty[s], rp.phase ^ 1u, p.errflag);
             mbar_arrive_expect_tx(&full[s], bytes);
             bulk_load_1d(ring + (size_t)s * p.stage_bytes, mats[m] + (size_t)r0 * row_bytes,
                          bytes, &full[s], pol);
@@ -218,12 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1) cf_ffn_kernel(const __grid_consta
   // its own shuffle-reduced sums (no block barrier while the stream runs) --
   const int nunits = i1 - i0;
   int it = 0;
+  RingPos rp(0, p.stages);
   for (int c = 0; c < nchunk; ++c) {
     const int rc = min(p.R, nunits - c * p.R);
 #pragma unroll
-    for (int m = 0; m < 2; ++m, ++it) {
-      const int s = it % p.stages;
-      mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+    for (int m = 0; m < 2; ++m, ++it, rp.next(p.stages)) {
+      const int s = rp.slot;
+      mbar_wait(&full[s], rp.phase, p.errflag);
       const uint8_t* st = ring + (size_t)s * p.stage_bytes;
       constexpr int V = kFfnMaxR * BMAX;  // (row, batch row) partials per thread
       float part[V];
@@ -276,10 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_ffn_kernel(const __grid_consta
     for (int b = 0; b < BMAX; ++b)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[j][b][e] = 0.f;
-  for (int c = 0; c < nchunk; ++c, ++it) {
+  for (int c = 0; c < nchunk; ++c, ++it, rp.next(p.stages)) {
     const int rc = min(p.R, nunits - c * p.R);
-    const int s = it % p.stages;
-    mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+    const int s = rp.slot;
+    mbar_wait(&full[s], rp.phase, p.errflag);
     const uint8_t* st = ring + (size_t)s * p.stage_bytes;
     for (int r = 0; r < rc; ++r) {
       const T* row = reinterpret_cast<const T*>(st + (size_t)r * row_bytes);

@@ -189,20 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&p.tm_n);
       const uint64_t pol_w = policy_evict_first(), pol_n = policy_evict_normal();
       auto stage_slabs = [&](int st) { return min(p.nsl1, nslab - st * p.nsl1); };
-      auto load_w = [&](int st) {
-        uint8_t* base = ring + (size_t)(st % p.stages1) * p.stage1_bytes;
+      // stage st goes to ring slot s
+      auto load_w = [&](int st, int s) {
+        uint8_t* base = ring + (size_t)s * p.stage1_bytes;
         for (int j = 0; j < stage_slabs(st); ++j) {
           const int x = (st * p.nsl1 + j) * 64;
-          tma_load_2d(base + j * slab1, &p.tm_wg, x, i0, &full[st % p.stages1], pol_w);
-          tma_load_2d(base + j * slab1 + p.UB * 128, &p.tm_wu, x, i0, &full[st % p.stages1],
-                      pol_w);
+          tma_load_2d(base + j * slab1, &p.tm_wg, x, i0, &full[s], pol_w);
+          tma_load_2d(base + j * slab1 + p.UB * 128, &p.tm_wu, x, i0, &full[s], pol_w);
         }
       };
-      auto load_n = [&](int st) {
-        uint8_t* base = ring + (size_t)(st % p.stages1) * p.stage1_bytes;
+      auto load_n = [&](int st, int s) {
+        uint8_t* base = ring + (size_t)s * p.stage1_bytes;
         for (int j = 0; j < stage_slabs(st); ++j)
           tma_load_2d(base + j * slab1 + 2 * p.UB * 128, &p.tm_n, (st * p.nsl1 + j) * 64, 0,
-                      &full[st % p.stages1], pol_n);
+                      &full[s], pol_n);
       };
       // The weights need nothing from this launch or the previous kernel:
       // the first stages' weight boxes go out at once, their n boxes once
@@ -214,17 +214,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int fill = min(p.stages1, nst);
       for (int st = 0; st < fill; ++st) {
         mbar_arrive_expect_tx(&full[st], (uint32_t)(stage_slabs(st) * slab1));
-        load_w(st);
+        load_w(st, st);
       }
       mbar_wait(n_ready, 0, p.errflag);
       fence_proxy_async_global();  // n was written by other blocks' threads
-      for (int st = 0; st < fill; ++st) load_n(st);
-      for (int st = fill; st < nst; ++st) {
-        const int s = st % p.stages1;
-        mbar_wait(&empty[s], ((st / p.stages1) + 1) & 1, p.errflag);
+      for (int st = 0; st < fill; ++st) load_n(st, st);
+      RingPos rp(fill, p.stages1);
+      for (int st = fill; st < nst; ++st, rp.next(p.stages1)) {
+        const int s = rp.slot;
+        mbar_wait(&empty[s], rp.phase ^ 1u, p.errflag);
         mbar_arrive_expect_tx(&full[s], (uint32_t)(stage_slabs(st) * slab1));
-        load_w(st);
-        load_n(st);
+        load_w(st, s);
+        load_n(st, s);
       }
     }
     __syncwarp();
@@ -306,9 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *s_tmem;
     const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, NR, false);
     if (tid == 0) {
-      for (int st = 0; st < nst; ++st) {
-        const int s = st % p.stages1;
-        mbar_wait(&full[s], (st / p.stages1) & 1, p.errflag);
+      RingPos rp(0, p.stages1);
+      for (int st = 0; st < nst; ++st, rp.next(p.stages1)) {
+        const int s = rp.slot;
+        mbar_wait(&full[s], rp.phase, p.errflag);
         if (st < kFfnTlMaxStages) stamp(4 + st);
         tc05_fence_after();
         const int ns = min(p.nsl1, nslab - st * p.nsl1);
@@ -504,39 +506,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&p.tm_acc);
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_normal();
       auto stage_slabs = [&](int st) { return min(p.nsl2, nslab - st * p.nsl2); };
-      auto load_w = [&](int st) {
-        uint8_t* base = ring + (size_t)(st % p.stages2) * p.stage2_bytes;
+      // stage st goes to ring slot s
+      auto load_w = [&](int st, int s) {
+        uint8_t* base = ring + (size_t)s * p.stage2_bytes;
         for (int j = 0; j < stage_slabs(st); ++j) {
           const int u = (sl0 + st * p.nsl2 + j) * 64;
-          tma_load_2d(base + j * kSlab, &p.tm_wd, j0, u, &full[st % p.stages2], pol_w);
-          tma_load_2d(base + j * kSlab + kWBox, &p.tm_wd, j0 + 64, u, &full[st % p.stages2],
-                      pol_w);
+          tma_load_2d(base + j * kSlab, &p.tm_wd, j0, u, &full[s], pol_w);
+          tma_load_2d(base + j * kSlab + kWBox, &p.tm_wd, j0 + 64, u, &full[s], pol_w);
         }
       };
-      auto load_a = [&](int st) {
-        uint8_t* base = ring + (size_t)(st % p.stages2) * p.stage2_bytes;
+      auto load_a = [&](int st, int s) {
+        uint8_t* base = ring + (size_t)s * p.stage2_bytes;
         for (int j = 0; j < stage_slabs(st); ++j) {
           const int u = (sl0 + st * p.nsl2 + j) * 64;
-          tma_load_2d(base + j * kSlab + 2 * kWBox, &p.tm_ahi, u, 0, &full[st % p.stages2],
-                      pol_a);
+          tma_load_2d(base + j * kSlab + 2 * kWBox, &p.tm_ahi, u, 0, &full[s], pol_a);
           if constexpr (kHiLo)
-            tma_load_2d(base + j * kSlab + 2 * kWBox + BP * 128, &p.tm_alo, u, 0,
-                        &full[st % p.stages2], pol_a);
+            tma_load_2d(base + j * kSlab + 2 * kWBox + BP * 128, &p.tm_alo, u, 0, &full[s],
+                        pol_a);
         }
       };
       const int fill = min(p.stages2, nst);
       for (int st = 0; st < fill; ++st) {
         mbar_arrive_expect_tx(&full[st], (uint32_t)(stage_slabs(st) * kSlab));
-        load_w(st);
+        load_w(st, st);
       }
       asm volatile("griddepcontrol.wait;" ::: "memory");  // a comes from kernel 1
-      for (int st = 0; st < fill; ++st) load_a(st);
-      for (int st = fill; st < nst; ++st) {
-        const int s = st % p.stages2;
-        mbar_wait(&empty[s], ((st / p.stages2) + 1) & 1, p.errflag);
+      for (int st = 0; st < fill; ++st) load_a(st, st);
+      RingPos rp(fill, p.stages2);
+      for (int st = fill; st < nst; ++st, rp.next(p.stages2)) {
+        const int s = rp.slot;
+        mbar_wait(&empty[s], rp.phase ^ 1u, p.errflag);
         mbar_arrive_expect_tx(&full[s], (uint32_t)(stage_slabs(st) * kSlab));
-        load_w(st);
-        load_a(st);
+        load_w(st, s);
+        load_a(st, s);
       }
     }
     __syncwarp();
@@ -550,9 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *s_tmem;
     const uint32_t idesc = idesc_kind_f16(MK::kBf16, 128, N5, true);
     if (tid == 0) {
-      for (int st = 0; st < nst; ++st) {
-        const int s = st % p.stages2;
-        mbar_wait(&full[s], (st / p.stages2) & 1, p.errflag);
+      RingPos rp(0, p.stages2);
+      for (int st = 0; st < nst; ++st, rp.next(p.stages2)) {
+        const int s = rp.slot;
+        mbar_wait(&full[s], rp.phase, p.errflag);
         if (st < kFfnTlMaxStages) stamp(4 + st);
         tc05_fence_after();
         const int ns = min(p.nsl2, nslab - st * p.nsl2);

@@ -182,9 +182,11 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int it = 0;
+      RingPos rp(fill, p.stages);  // the prologue filled uses 0 .. fill-1
       auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
-        const int s = it % p.stages;
-        if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+        const int s = rp.slot;
+        if (it >= p.stages) mbar_wait(&empty[s], rp.phase ^ 1u, p.errflag);
+        rp.next(p.stages);
         bar = &full[s];
         mbar_arrive_expect_tx(bar, bytes);
         return ring + (size_t)s * p.stage_bytes;
@@ -288,9 +290,10 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
         for (int sg = 0; sg < NSEG; ++sg)
 #pragma unroll
           for (int e = 0; e < CPL; ++e) acc[bb][sg][e] = 0.f;
-      for (int kt = 0; kt < nkt; ++kt, ++it) {
-        const int s = it % p.stages;
-        mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+      RingPos rp(it, p.stages);
+      for (int kt = 0; kt < nkt; ++kt, ++it, rp.next(p.stages)) {
+        const int s = rp.slot;
+        mbar_wait(&full[s], rp.phase, p.errflag);
         const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
         for (int r = warp; r < p.Rw; r += kConsumerWarps) {
           float nv[BT];
@@ -492,15 +495,18 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
       const int RG = kConsumers / CC;
       const int cc = tid % CC, rg = tid / CC;
       const int CQ = p.Co / 4;
+      RingPos rp(it, p.stages);
       for (int cb = 0; cb < ncb; ++cb) {
         float a[BT][CW];
 #pragma unroll
         for (int bb = 0; bb < BT; ++bb)
 #pragma unroll
           for (int e = 0; e < CW; ++e) a[bb][e] = 0.f;
-        for (int rt = 0; rt < nrt; ++rt, ++it) {
-          const int s = it % p.stages;
-          mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        int s_last = 0;  // the box's last tile stage
+        for (int rt = 0; rt < nrt; ++rt, ++it, rp.next(p.stages)) {
+          const int s = rp.slot;
+          s_last = s;
+          mbar_wait(&full[s], rp.phase, p.errflag);
           if (cb == 0 && rt == 0) stamp(kTlOprojFirst);
           else if (cb * nrt + rt < 4) stamp(kTlOprojTile1 - 1 + cb * nrt + rt);
           const T* W = reinterpret_cast<const T*>(ring + (size_t)s * p.stage_bytes);
@@ -526,7 +532,6 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
         // Row-group partials [RG][BT][Co] into the held stage, then each
         // float4 of the box summed over the groups in a fixed order and added
         // to the accumulator with one vector atomic.
-        const int s_last = (it - 1) % p.stages;
         float* pb = reinterpret_cast<float*>(ring + (size_t)s_last * p.stage_bytes);
         named_sync(kBarConsumers, kConsumers);  // every warp is done reading the tile
         if (rg < RG)

@@ -277,12 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int it = 0;
+      RingPos rp(0, p.stages);
       auto slot = [&](uint32_t bytes, uint64_t*& bar) -> uint8_t* {
-        const int s = it % p.stages;
-        if (it >= p.stages) mbar_wait(&empty[s], ((it / p.stages) + 1) & 1, p.errflag);
+        const int s = rp.slot;
+        if (it >= p.stages) mbar_wait(&empty[s], rp.phase ^ 1u, p.errflag);
         bar = &full[s];
         mbar_arrive_expect_tx(bar, bytes);
         ++it;
+        rp.next(p.stages);
         return ring + (size_t)s * STAGE_BYTES;
       };
       uint64_t* bar;
@@ -376,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
     }
     stamp(kMlaTlNorm);
     int it = 0;
+    RingPos rc(0, p.stages);  // ring slot and parity of use `it`
     // ---- A: projection partial sums ---------------------------------------
     {
       float acc[BMAX][6];
@@ -406,12 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       };
       zero();
       int cur = -1;
-      for (int t = pl.ta0; t < pl.ta1; ++t, ++it) {
+      for (int t = pl.ta0; t < pl.ta1; ++t, ++it, rc.next(p.stages)) {
         const int g = t / KTN, kt = t % KTN;
         if (g != cur && cur >= 0) flush(cur);
         cur = g;
-        const int s = it % p.stages;
-        mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        const int s = rc.slot;
+        mbar_wait(&full[s], rc.phase, p.errflag);
         const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
         for (int r = warp; r < KT; r += kConsumerWarps) {
           float nv[BMAX];
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
     stamp(kMlaTlBar1);
 
     // ---- B: absorption, query RoPE, the latent row ------------------------
-    for (int item = blk; item < nh * (DC / KT); item += p.nb, ++it) {
+    for (int item = blk; item < nh * (DC / KT); item += p.nb, ++it, rc.next(p.stages)) {
       const int h = item / (DC / KT), ib = item % (DC / KT);
       float qn[BMAX][4];
 #pragma unroll
@@ -446,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           qn[b][e] = b < B ? __ldcg(p.y + (size_t)b * C1 + h * DQ + 4 * lane + e) : 0.f;
-      const int s = it % p.stages;
-      mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+      const int s = rc.slot;
+      mbar_wait(&full[s], rc.phase, p.errflag);
       const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
 #pragma unroll
       for (int rr = 0; rr < KT / kConsumerWarps; ++rr) {
@@ -582,10 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
       float* sAl = reinterpret_cast<float*>(sPl + 16 * (RT + 8));     // [16] factors
       float* sPn = sAl + 16;                                          // [16] p of the new row
       constexpr int PP = (RT + 8) * 2;  // p row pitch in bytes (not a multiple of 128)
-      for (int tt = t0; tt < t1; tt += RT, ++it) {
+      for (int tt = t0; tt < t1; tt += RT, ++it, rc.next(p.stages)) {
         const int n = min(RT, t1 - tt);
-        const int s = it % p.stages;
-        mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+        const int s = rc.slot;
+        mbar_wait(&full[s], rc.phase, p.errflag);
         if (tt == t0) stamp(kMlaTlC0);
         uint8_t* tile = ring + (size_t)s * STAGE_BYTES;  // [DL / 64][RT][64], 128-byte swizzle
         if (n < RT) {
@@ -885,8 +888,8 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
 #pragma unroll
             for (int e = 0; e < 4; ++e) a4[b][e] = 0.f;
           {
-            const int s = it % p.stages;
-            mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+            const int s = rc.slot;
+            mbar_wait(&full[s], rc.phase, p.errflag);
             const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
 #pragma unroll 4
             for (int rr = 0; rr < DCB / kConsumerWarps; ++rr) {
@@ -904,6 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             ++it;
+            rc.next(p.stages);
           }
 #pragma unroll
           for (int b = 0; b < BMAX; ++b)
@@ -933,8 +937,8 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
 #pragma unroll
             for (int e = 0; e < 4; ++e) a[b][e] = 0.f;
           {
-            const int s = it % p.stages;
-            mbar_wait(&full[s], (it / p.stages) & 1, p.errflag);
+            const int s = rc.slot;
+            mbar_wait(&full[s], rc.phase, p.errflag);
             const T* tile = reinterpret_cast<const T*>(ring + (size_t)s * STAGE_BYTES);
 #pragma unroll 4
             for (int rr = 0; rr < DV / kConsumerWarps; ++rr) {
@@ -953,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             ++it;
+            rc.next(p.stages);
           }
 #pragma unroll
           for (int b = 0; b < BMAX; ++b)
