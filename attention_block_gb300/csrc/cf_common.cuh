@@ -104,16 +104,19 @@ struct RingPos {
 
 // Position tiles [t0, t1) of the cached keys 0..pos-1 handled by block `rank`
 // (balanced split of ceil(pos/Rt) tiles over N blocks).  pos < 0 marks an
-// invalid row; pos == 0 has no cached key (only the new token).
+// invalid row; pos == 0 has no cached key (only the new token).  Rt and N are
+// powers of two (the plans make them so), so the split takes shifts and a
+// 64-bit product, not divisions.
 __device__ __forceinline__ void kv_tile_range(int pos, int Rt, int rank, int N, int& t0,
                                               int& t1) {
   if (pos <= 0) {
     t0 = t1 = 0;
     return;
   }
-  const int nt = (pos + Rt - 1) / Rt;
-  t0 = (int)(((long long)rank * nt) / N);
-  t1 = (int)(((long long)(rank + 1) * nt) / N);
+  const int lr = __ffs(Rt) - 1, ln = __ffs(N) - 1;
+  const unsigned nt = ((unsigned)pos + (unsigned)(Rt - 1)) >> lr;
+  t0 = (int)(((unsigned long long)rank * nt) >> ln);
+  t1 = (int)(((unsigned long long)(rank + 1) * nt) >> ln);
 }
 
 // cos and sin of the RoPE angle pos * theta^(-2i/d) [LNA §三] without FP64

@@ -71,6 +71,9 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
   const int bt = cid % p.nbt; // batch tile
   const int b0 = bt * BT;
   const int P = D / (2 * N);            // RoPE pairs per head-dim slice
+  // P is a power of two: index splits by shift and mask (a division by a
+  // runtime divisor is a long dependent chain on the exchange path)
+  const int lP = 31 - __clz(P);
   const int SE = BT * NSEG * 2 * P;     // floats per slice
   const int Hc = p.H / N;               // K band rows == O-proj column band
   const int k0 = rank * Hc;
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
       }
       // cos/sin of this block's own RoPE pairs
       for (int idx = tid; idx < BT * P; idx += kConsumers) {
-        const int bb = idx / P, j = idx % P;
+        const int bb = idx >> lP, j = idx & (P - 1);
         const int pos = s_pos[bb];
         float c = 1.f, sn = 0.f;
         if (pos >= 0) rope_cos_sin(pos, p.turn_hi[rank * P + j], p.turn_lo[rank * P + j], c, sn);
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
             for (int e = 0; e < CPL; ++e) {
               const int col = lane * CPL + e;
               const int hi = col / (D / 2), il = col % (D / 2);
-              const int c = il / P, j = il % P;
+              const int c = il >> lP, j = il & (P - 1);
 #pragma unroll
               for (int bb = 0; bb < BT; ++bb)
                 red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j] = acc[bb][sg][e] * s_rinv[bb];
@@ -391,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
       T* kc = reinterpret_cast<T*>(p.k_cache);
       T* vc = reinterpret_cast<T*>(p.v_cache);
       for (int idx = tid; idx < BT * NSEG * P; idx += kConsumers) {
-        const int bb = idx / (NSEG * P), rem = idx % (NSEG * P);
-        const int sg = rem / P, j = rem % P;
+        const int q = idx >> lP, j = idx & (P - 1);
+        const int bb = q / NSEG, sg = q % NSEG;
         const int pos = s_pos[bb];
         if (pos < 0) continue;
         float* lo = my + ((bb * NSEG + sg) * 2) * P + j;
@@ -425,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
       const int bb = idx / (NSEG * D), rem = idx % (NSEG * D);
       const int sg = rem / D, dim = rem % D;
       const int hi = dim / (D / 2), il = dim % (D / 2);
-      const int c = il / P, j = il % P;
+      const int c = il >> lP, j = il & (P - 1);
       qkv[idx] = red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j];
     }
     named_sync(kBarConsumers, kConsumers);
