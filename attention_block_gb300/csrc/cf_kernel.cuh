@@ -545,21 +545,22 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
               *reinterpret_cast<float4*>(pb + ((size_t)rg * BT + bb) * p.Co + cc * CW + e4) =
                   make_float4(a[bb][e4], a[bb][e4 + 1], a[bb][e4 + 2], a[bb][e4 + 3]);
         named_sync(kBarConsumers, kConsumers);
-        for (int i4 = tid; i4 < BT * CQ; i4 += kConsumers) {
-          const int bb = i4 / CQ, cq = i4 % CQ;
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int gq = 0; gq < RG; ++gq) {
-            const float4 u =
-                *reinterpret_cast<const float4*>(pb + ((size_t)gq * BT + bb) * p.Co + cq * 4);
-            v.x += u.x;
-            v.y += u.y;
-            v.z += u.z;
-            v.w += u.w;
-          }
+        for (int bb = 0; bb < BT; ++bb) {
           const int b = b0 + bb;
-          if (b < p.B && s_pos[bb] >= 0)
-            atomicAdd(reinterpret_cast<float4*>(p.acc + (size_t)b * p.H + k0 + cb * p.Co + cq * 4),
-                      v);
+          for (int cq = tid; cq < CQ; cq += kConsumers) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int gq = 0; gq < RG; ++gq) {
+              const float4 u =
+                  *reinterpret_cast<const float4*>(pb + ((size_t)gq * BT + bb) * p.Co + cq * 4);
+              v.x += u.x;
+              v.y += u.y;
+              v.z += u.z;
+              v.w += u.w;
+            }
+            if (b < p.B && s_pos[bb] >= 0)
+              atomicAdd(
+                  reinterpret_cast<float4*>(p.acc + (size_t)b * p.H + k0 + cb * p.Co + cq * 4), v);
+          }
         }
         fence_proxy_async_smem();  // our stores into the stage precede the next TMA write
         named_sync(kBarConsumers, kConsumers);
@@ -583,22 +584,23 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
       T* out = reinterpret_cast<T*>(p.out);
       float* dproj = p.dbg ? p.dbg + (size_t)p.B * (2 * p.nq + 2 * p.nkv) * D : nullptr;
       const int C4 = Hc / 4;
-      for (int i4 = tid; i4 < BT * C4; i4 += kConsumers) {
-        const int bb = i4 / C4, c4 = i4 % C4;
+      for (int bb = 0; bb < BT; ++bb) {
         const int b = b0 + bb;
         if (b >= p.B) continue;
-        const size_t off = (size_t)b * p.H + k0 + c4 * 4;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
-        __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
-        float xf[4];
-        load_cvt<T, 4>(hidden + off, xf);
-        const float r[4] = {xf[0] + v.x, xf[1] + v.y, xf[2] + v.z, xf[3] + v.w};
-        store4<T>(out + off, r);
-        if (dproj) {
-          dproj[off + 0] = v.x;
-          dproj[off + 1] = v.y;
-          dproj[off + 2] = v.z;
-          dproj[off + 3] = v.w;
+        for (int c4 = tid; c4 < C4; c4 += kConsumers) {
+          const size_t off = (size_t)b * p.H + k0 + c4 * 4;
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(p.acc + off));
+          __stcg(reinterpret_cast<float4*>(p.acc + off), make_float4(0.f, 0.f, 0.f, 0.f));
+          float xf[4];
+          load_cvt<T, 4>(hidden + off, xf);
+          const float r[4] = {xf[0] + v.x, xf[1] + v.y, xf[2] + v.z, xf[3] + v.w};
+          store4<T>(out + off, r);
+          if (dproj) {
+            dproj[off + 0] = v.x;
+            dproj[off + 1] = v.y;
+            dproj[off + 2] = v.z;
+            dproj[off + 3] = v.w;
+          }
         }
       }
       if (tid == 0) p.counters[bt * N + rank] = 0;
