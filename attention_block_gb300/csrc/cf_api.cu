@@ -769,11 +769,11 @@ int cf_decode_attn_block(cf_handle* h, int32_t batch, const void* hidden_states,
   kp.errflag = h->errflag;
   kp.dbg = h->dbg;
   kp.timeline = h->timeline;
-  // The last min(4, nkv) blocks of a (tile, band) share its finalize when the
+  // The last min(8, nkv) blocks of a (tile, band) share its finalize when the
   // whole grid is resident at once (the earlier ones wait for the later).
   const long long grid_clusters = (long long)nkv * ((batch + pl.BT - 1) / pl.BT);
   kp.fin_split =
-      (rows && pl.BT >= 16 && grid_clusters <= ps.max_active_clusters) ? std::min(4, nkv) : 1;
+      (rows && pl.BT >= 16 && grid_clusters <= ps.max_active_clusters) ? std::min(8, nkv) : 1;
   kp.B = batch;
   kp.H = H;
   kp.nq = nq;
