@@ -308,6 +308,22 @@ __device__ __forceinline__ void mbar_remote_arrive(uint32_t rbar) {
                : "memory");
 }
 
+// Release fence at cluster scope restricted to shared::cta accesses: orders
+// this thread's earlier shared-memory writes, and those it has observed
+// through a CTA barrier, before its later relaxed arrivals on peers'
+// mbarriers (an acquiring wait on such a barrier then sees the writes).
+// The unrestricted release also waits for the thread's other memory traffic.
+__device__ __forceinline__ void fence_release_smem_cluster() {
+  asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
+}
+
+// Relaxed arrival on the mbarrier at cluster shared address `rbar`; pair with
+// fence_release_smem_cluster() for release ordering.
+__device__ __forceinline__ void mbar_remote_arrive_relaxed(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
+               : "memory");
+}
+
 // 16-byte loads from (possibly another CTA's) shared memory at a cluster
 // shared address.
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
