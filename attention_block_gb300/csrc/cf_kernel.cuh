@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
   stamp(kTlFinal);
   // No block leaves while a peer may still write into its shared memory.
   __syncwarp();
-  cluster_sync_all();
+  cluster_sync_exit();
   stamp(kTlEnd);
 }
 

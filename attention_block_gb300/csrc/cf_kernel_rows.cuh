@@ -940,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_rows_kernel(const __grid_const
   __syncwarp();
   // Peers may still read this block's shared memory (reduce-scatter slices,
   // the A operand rows) until they pass this barrier.
-  cluster_sync_all();
+  cluster_sync_exit();
   stamp(kTlEnd);
 }
 

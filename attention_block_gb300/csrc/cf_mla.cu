@@ -1006,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1) cf_mla_kernel(const __grid_consta
   stamp(kMlaTlEnd);
   // no block leaves while a peer may still write into its shared memory
   __syncwarp();
-  cluster_sync_all();
+  cluster_sync_exit();
 }
 
 // Dynamic shared memory of a plan (bytes past the 1024-aligned base).

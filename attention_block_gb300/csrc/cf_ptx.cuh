@@ -40,6 +40,17 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Cluster barrier before the CTAs exit: no CTA leaves while a peer may still
+// access its shared memory.  Every remote access has completed by then (each
+// pushed store was waited for by its receiver, each pulled load was consumed
+// by its issuer before the issuer arrives), so the arrival needs no release
+// ordering, which would wait for the thread's outstanding global stores.
+__device__ __forceinline__ void cluster_sync_exit() {
+  asm volatile(
+      "barrier.cluster.arrive.relaxed.aligned;\n\t"
+      "barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Named barrier among `nthreads` threads (a multiple of 32) with id `id`.
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
