@@ -326,58 +326,89 @@ __global__ void __launch_bounds__(kThreads, MINB) cf_decode_kernel(const __grid_
         for (int w = 0; w < kConsumerWarps; ++w) tot += wred[w * BT + tid];
         s_rinv[tid] = (b0 + tid < p.B) ? 1.0f / sqrtf(tot / (float)p.H + p.eps) : 0.f;
       }
-      // Tree sum of the 8 warps' partials (8 -> 4 -> 2 -> 1) through the held
-      // stage, [slot][value][lane] so every access is conflict-free; no
-      // atomics, and the summation order is fixed.
+      // Sum of the 8 warps' partials through the held stage, [warp][value]
+      // [lane] so every access is conflict-free; no atomics, and the
+      // summation order is fixed.  When all 8 warps' partials fit the stage
+      // they are written at once and every thread sums the 8 copies of its
+      // values (one barrier); otherwise a tree (8 -> 4 -> 2 -> 1).
       {
         const int s_last = (it - 1) % p.stages;
         float* tb = reinterpret_cast<float*>(ring + (size_t)s_last * p.stage_bytes);
         constexpr int PW = BT * NSEG * CPL;
-        const bool disjoint = 7 * PW * 32 * 4 <= p.stage_bytes;  // one region per step
-        int base = 0;
+        constexpr int NV = PW * 32;  // values per warp
         named_sync(kBarConsumers, kConsumers);  // every warp is done reading the tile
-        for (int half = kConsumerWarps / 2; half >= 1; half >>= 1) {
-          if (warp >= half && warp < 2 * half) {
-            float* dst = tb + (base + warp - half) * PW * 32 + lane;
+        if (kConsumerWarps * NV * 4 <= p.stage_bytes) {
+          float* dst = tb + warp * NV + lane;
 #pragma unroll
-            for (int bb = 0; bb < BT; ++bb)
+          for (int bb = 0; bb < BT; ++bb)
 #pragma unroll
-              for (int sg = 0; sg < NSEG; ++sg)
+            for (int sg = 0; sg < NSEG; ++sg)
 #pragma unroll
-                for (int e = 0; e < CPL; ++e) dst[((bb * NSEG + sg) * CPL + e) * 32] = acc[bb][sg][e];
-          }
+              for (int e = 0; e < CPL; ++e) dst[((bb * NSEG + sg) * CPL + e) * 32] = acc[bb][sg][e];
           named_sync(kBarConsumers, kConsumers);
-          if (warp < half) {
-            const float* src = tb + (base + warp) * PW * 32 + lane;
+          // value o = ((bb * NSEG + sg) * CPL + e) * 32 + lane: column lane * CPL + e of
+          // segment sg of row bb, stored scaled by r and slice-ordered as below
+          for (int o = tid; o < NV; o += kConsumers) {
+            float sum = 0.f;
 #pragma unroll
-            for (int bb = 0; bb < BT; ++bb)
-#pragma unroll
-              for (int sg = 0; sg < NSEG; ++sg)
-#pragma unroll
-                for (int e = 0; e < CPL; ++e) acc[bb][sg][e] += src[((bb * NSEG + sg) * CPL + e) * 32];
+            for (int w = 0; w < kConsumerWarps; ++w) sum += tb[w * NV + o];
+            const int v = o >> 5, e = v % CPL, bs = v / CPL, sg = bs % NSEG, bb = bs / NSEG;
+            const int col = (o & 31) * CPL + e;
+            const int hi = col / (D / 2), il = col % (D / 2);
+            const int c = il >> lP, j = il & (P - 1);
+            red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j] = sum * s_rinv[bb];
           }
-          if (disjoint) base += half;
-          else named_sync(kBarConsumers, kConsumers);
-        }
-        // Warp 0 holds the block's partial sums: scale by r and store them
-        // slice-ordered -- column i of a segment belongs to slice
-        // c = (i mod d/2) / P, so each RoPE pair (i, i + d/2) stays in one slice.
-        if (warp == 0) {
-#pragma unroll
-          for (int sg = 0; sg < NSEG; ++sg)
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) {
-              const int col = lane * CPL + e;
-              const int hi = col / (D / 2), il = col % (D / 2);
-              const int c = il >> lP, j = il & (P - 1);
+          fence_proxy_async_smem();  // our reads of the stage precede the next TMA write
+          named_sync(kBarConsumers, kConsumers);
+          if (lane == 0) mbar_arrive(&empty[s_last]);  // hand the stage back
+        } else {
+          const bool disjoint = 7 * PW * 32 * 4 <= p.stage_bytes;  // one region per step
+          int base = 0;
+          for (int half = kConsumerWarps / 2; half >= 1; half >>= 1) {
+            if (warp >= half && warp < 2 * half) {
+              float* dst = tb + (base + warp - half) * PW * 32 + lane;
 #pragma unroll
               for (int bb = 0; bb < BT; ++bb)
-                red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j] = acc[bb][sg][e] * s_rinv[bb];
+#pragma unroll
+                for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+                  for (int e = 0; e < CPL; ++e)
+                    dst[((bb * NSEG + sg) * CPL + e) * 32] = acc[bb][sg][e];
             }
+            named_sync(kBarConsumers, kConsumers);
+            if (warp < half) {
+              const float* src = tb + (base + warp) * PW * 32 + lane;
+#pragma unroll
+              for (int bb = 0; bb < BT; ++bb)
+#pragma unroll
+                for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+                  for (int e = 0; e < CPL; ++e)
+                    acc[bb][sg][e] += src[((bb * NSEG + sg) * CPL + e) * 32];
+            }
+            if (disjoint) base += half;
+            else named_sync(kBarConsumers, kConsumers);
+          }
+          // Warp 0 holds the block's partial sums: scale by r and store them
+          // slice-ordered -- column i of a segment belongs to slice
+          // c = (i mod d/2) / P, so each RoPE pair (i, i + d/2) stays in one slice.
+          if (warp == 0) {
+#pragma unroll
+            for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+              for (int e = 0; e < CPL; ++e) {
+                const int col = lane * CPL + e;
+                const int hi = col / (D / 2), il = col % (D / 2);
+                const int c = il >> lP, j = il & (P - 1);
+#pragma unroll
+                for (int bb = 0; bb < BT; ++bb)
+                  red[c * SE + ((bb * NSEG + sg) * 2 + hi) * P + j] = acc[bb][sg][e] * s_rinv[bb];
+              }
+          }
+          fence_proxy_async_smem();  // our stores into the stage precede the next TMA write
+          named_sync(kBarConsumers, kConsumers);
+          if (lane == 0) mbar_arrive(&empty[s_last]);  // hand the stage back
         }
-        fence_proxy_async_smem();  // our stores into the stage precede the next TMA write
-        named_sync(kBarConsumers, kConsumers);
-        if (lane == 0) mbar_arrive(&empty[s_last]);  // hand the stage back
       }
       stamp(kTlRinv);
     }
