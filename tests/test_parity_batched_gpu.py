@@ -76,6 +76,34 @@ def test_every_instance_scaled_shape(inst):
     full_check(w, seed=11, batch_tile=BT, rows_per_block=RPC)
 
 
+@pytest.mark.parametrize("inst,stages", [
+    (("f16", 64, 1, 16, 4), 2), (("f16", 64, 1, 16, 4), 3),
+    (("bf16", 128, 4, 4, 1), 2), (("bf16", 128, 4, 4, 1), 3),
+    (("bf16", 128, 4, 16, 4), 3), (("f16", 64, 1, 64, 16), 3)],
+    ids=lambda v: "-".join(map(str, v)) if isinstance(v, tuple) else f"stages{v}")
+def test_ring_depths(inst, stages):
+    # Ring slots and fill parities are advanced by counting in every loop
+    # (projection, attention tiles, O projection, producer); a shallow ring
+    # wraps many times per launch, so every slot reuses its barrier phases.
+    dt, d, G, BT, RPC = inst
+    w = _shape_for(*inst)
+    blk = make_block(w, batch_tile=BT, rows_per_block=RPC, max_stages=stages)
+    assert blk.launch_info()["stages"] == stages
+    full_check(w, seed=17, batch_tile=BT, rows_per_block=RPC, max_stages=stages)
+
+
+def test_tcgen05_ring_must_hold_a_k_slice():
+    # The 16-row bf16 GQA instance stages each K slice of W_qkv as 3 ring
+    # stages and only its MMA issuer waits for the second and third: a
+    # 2-stage ring is refused rather than run.
+    w = _shape_for("bf16", 128, 4, 16, 4)
+    cfg = binding.make_config(w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim, w.batch, w.s_max,
+                              w.rope_theta, w.rms_eps, w.dtype, batch_tile=16, rows_per_block=4,
+                              max_stages=2)
+    rc, h = binding.cf_create_rc(cfg)
+    assert rc == binding.CF_ERR_UNSUPPORTED and not h
+
+
 def test_default_picks_batched_kernel_for_batched_workloads():
     for name, bt in ((synth.SMALL_HEAD_B64, 64), (synth.LLAMA3_GQA, 4)):
         w = synth.WORKLOADS[name]
