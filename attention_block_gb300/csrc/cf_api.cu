@@ -516,8 +516,18 @@ int plan_handle(const cf_config& c, cf_handle& h) {
         const bool regs_ok = regs * kThreads * 2 <= prop.regsPerMultiprocessor;
         cps = (regs_ok && (long long)clusters * N > prop.multiProcessorCount) ? 2 : 1;
       }
-      if (!make_plan(c, N, BT, stage_req, cps, prop, pl) &&
-          !(cps == 2 && make_plan(c, N, BT, stage_req, 1, prop, pl)))
+      // When the weights dominate the stream (the cached K/V of every row at
+      // s_max below half the W_qkv bytes), 48 KB stages: the W_qkv phase then
+      // moves 64-row tiles, fewer stages through each SM's TMA unit, which
+      // bounds the SMs that hold two blocks; K/V and W_o tiles stay 32 KB.
+      // Measured: Llama-2 1K layer 32.78 -> 32.31 us; a 16K-position layer
+      // keeps 32 KB stages (48 KB: 2145 -> 2154 us per 32-layer step).
+      const bool weight_bound =
+          (long long)c.s_max * 2 * BT < (long long)c.hidden * (G + 2) / 2;
+      const int req = (c.stage_bytes == 0 && weight_bound) ? 49152 : stage_req;
+      if (!make_plan(c, N, BT, req, cps, prop, pl) &&
+          !(cps == 2 && make_plan(c, N, BT, req, 1, prop, pl)) &&
+          !(req != stage_req && make_plan(c, N, BT, stage_req, cps, prop, pl)))
         return CF_ERR_UNSUPPORTED;
       if (c.cluster_size != 0 || N <= 2) break;
       const int rc = prepare_function(ke->fn, pl.L.total, N);
